@@ -1,0 +1,390 @@
+/*
+ * agoq_oracle.c -- TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT PATH.
+ *
+ * A plain, slow, scalar CPU restatement of what the AGoQ element-wise
+ * quantization path computes, written to be checked against the method by eye.
+ * Only the tests, the smoke check and the bench's CPU-baseline leg load it;
+ * the library under gradient_quantization_gb300/ never calls it and shares no
+ * code, header, table or constant generator with it.
+ *
+ * Source of the method: "AGoQ: Activation and Gradient Quantization for
+ * Memory-Efficient Distributed Training of LLMs" (gist.science summary page),
+ * cited below as [AGoQ] with its section:
+ *   §2.A  Layer-Aware Activation Quantization (LAAQ): "Strategie" (4-bit
+ *         block-wise activations), "Herberekening versus Caching" (the stored
+ *         4-bit input is dequantized in the backward pass), "DBCA-PP" (5, 6 or
+ *         8 bits for pipeline stages with fewer in-flight batches).
+ *   §2.B  QuanGrad: "Lokale accumulatie" (dequantize the FP8 master gradient,
+ *         add the new micro-batch gradient, requantize to FP8) and
+ *         "Precision-Preserved All-Reduce" step 2 "Lokale reduce" (dequantize
+ *         the received shards to FP32, sum locally, requantize to FP8).
+ *   §2.C  Kernel Fusion (dequantization fused with the adjacent GEMM).
+ * The summary fixes no block size, scale format, rounding or bit layout.  This
+ * implementation fixes them as: blocks of 128 consecutive elements, one FP32
+ * scale per block equal to the block's absolute maximum divided by qmax, codes
+ * from round-to-nearest-even of the IEEE FP32 quotient x/scale, qmax =
+ * 2^(b-1)-1 for b-bit integer codes and 448 for FP8 E4M3, saturating E4M3.
+ * Every floating-point step below is a single IEEE binary32 operation in
+ * round-to-nearest-even; the file must be compiled with -ffp-contract=off and
+ * without fast-math so that no multiply-add is fused.
+ *
+ * Parity pins: every function here is pinned by tests under tests/ (codec
+ * sweeps against library casts, exact-rational brute force, closed forms and
+ * invariants).  No function in this file is "parity unpinned".
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define OR_BLOCK 128
+
+/* ------------------------------------------------------------------------- */
+/* BF16: the upper 16 bits of an IEEE binary32 (1 sign, 8 exponent, 7 fraction).
+ * Decoding is exact: the 16 bits become the high half of a binary32.          */
+float or_bf16_to_f32(uint16_t h)
+{
+    uint32_t u = (uint32_t)h << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return f;
+}
+
+/* Round a binary32 to BF16, to nearest with ties to even: the 16 discarded
+ * bits are compared with one half unit in the last kept place.  A carry out of
+ * the fraction correctly bumps the exponent (and reaches infinity on
+ * overflow).  NaN stays NaN (quiet bit set).                                  */
+uint16_t or_f32_to_bf16(float f)
+{
+    uint32_t u;
+    memcpy(&u, &f, sizeof u);
+    if ((u & 0x7F800000u) == 0x7F800000u) {
+        if (u & 0x007FFFFFu)
+            return (uint16_t)((u >> 16) | 0x0040u);
+        return (uint16_t)(u >> 16);
+    }
+    uint32_t kept = u >> 16;
+    uint32_t dropped = u & 0xFFFFu;
+    if (dropped > 0x8000u || (dropped == 0x8000u && (kept & 1u)))
+        kept += 1u;
+    return (uint16_t)kept;
+}
+
+/* ------------------------------------------------------------------------- */
+/* FP8 E4M3 in its "FN" form (OCP 8-bit floating point): 1 sign bit, 4 exponent
+ * bits with bias 7, 3 fraction bits; exponent field 0 is subnormal with value
+ * m * 2^-9; S.1111.111 is NaN; there is no infinity; the largest finite
+ * magnitude is 0x7E = 1.75 * 2^8 = 448.                                       */
+static double or_e4m3_magnitude(unsigned code7)
+{
+    unsigned e = (code7 >> 3) & 15u, m = code7 & 7u;
+    if (e == 0)
+        return ldexp((double)m, -9);
+    return ldexp(1.0 + (double)m / 8.0, (int)e - 7);
+}
+
+float or_e4m3_to_f32(uint8_t c)
+{
+    if ((c & 0x7Fu) == 0x7Fu)
+        return NAN;
+    double mag = or_e4m3_magnitude(c & 0x7Fu);
+    return (float)((c & 0x80u) ? -mag : mag); /* exact: at most 4 significant bits */
+}
+
+/* Round a finite binary32 to E4M3 to nearest, ties to even, saturating: any
+ * magnitude above 448 becomes 448.  The two neighbouring representable
+ * magnitudes are found by bisection over the 127 finite non-negative codes
+ * (their values increase with the code), and the nearer one wins; on an exact
+ * tie the code with a zero last fraction bit (an even code) wins.  The sign bit
+ * is kept, so a negative value that rounds to zero gives 0x80.                 */
+uint8_t or_f32_to_e4m3(float v)
+{
+    uint8_t sign = signbit(v) ? 0x80u : 0x00u;
+    double a = fabs((double)v);
+    if (a >= 448.0)
+        return (uint8_t)(sign | 0x7Eu);
+    unsigned lo = 0, hi = 0x7Eu; /* invariant: mag(lo) <= a < mag(hi) */
+    while (hi - lo > 1) {
+        unsigned mid = (lo + hi) / 2;
+        if (or_e4m3_magnitude(mid) <= a)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    double dlo = a - or_e4m3_magnitude(lo); /* exact in binary64 */
+    double dhi = or_e4m3_magnitude(hi) - a;
+    unsigned pick;
+    if (dlo < dhi)
+        pick = lo;
+    else if (dhi < dlo)
+        pick = hi;
+    else
+        pick = (lo & 1u) ? hi : lo;
+    return (uint8_t)(sign | pick);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Signed b-bit codes in a dense little-endian bit stream.  Within a block
+ * record of 16*b bytes, element j occupies bits [j*b, j*b+b); bit k of the
+ * record is bit (k mod 8) of byte floor(k/8).  The field holds the code in
+ * two's complement.  For b=4 this is "two codes per byte, low nibble first";
+ * for b=8 it is one int8 per byte.                                            */
+static void or_put_field(uint8_t *rec, int j, int bits, int32_t code)
+{
+    uint32_t field = (uint32_t)code & ((1u << bits) - 1u);
+    for (int k = 0; k < bits; ++k) {
+        int pos = j * bits + k;
+        if ((field >> k) & 1u)
+            rec[pos / 8] |= (uint8_t)(1u << (pos % 8));
+    }
+}
+
+static int32_t or_get_field(const uint8_t *rec, int j, int bits)
+{
+    uint32_t field = 0;
+    for (int k = 0; k < bits; ++k) {
+        int pos = j * bits + k;
+        field |= (uint32_t)((rec[pos / 8] >> (pos % 8)) & 1u) << k;
+    }
+    if (field & (1u << (bits - 1))) /* negative in two's complement */
+        return (int32_t)field - (int32_t)(1u << bits);
+    return (int32_t)field;
+}
+
+static int or_bits_ok(int bits)
+{
+    return bits == 4 || bits == 5 || bits == 6 || bits == 8;
+}
+
+/* Return codes of the oracle entry points. */
+#define OR_OK 0
+#define OR_BAD_ARG 1
+
+/* LAAQ block-wise activation quantization, [AGoQ] §2.A "Strategie" (4 bits)
+ * and "DBCA-PP" (5, 6, 8 bits).  Per block of 128 elements:
+ *   absmax = max |x_i|                        (exact)
+ *   s      = fl(absmax / qmax)                (binary32 division)
+ *   c_i    = clamp(rne_int(fl(x_i / s)), -qmax, qmax)
+ * An all-zero block stores s = +0 and all-zero codes (no 0/0).
+ * Output: codes, 16*bits bytes per block (dense bit stream), scales[n/128].  */
+int or_quant_act(const uint16_t *x, int64_t n, int bits, uint8_t *codes, float *scales)
+{
+    if (!or_bits_ok(bits) || n < 0 || n % OR_BLOCK)
+        return OR_BAD_ARG;
+    const int32_t qmax = (1 << (bits - 1)) - 1;
+    const int64_t rec_bytes = 16 * (int64_t)bits;
+    for (int64_t b = 0; b < n / OR_BLOCK; ++b) {
+        const uint16_t *xb = x + b * OR_BLOCK;
+        uint8_t *rec = codes + b * rec_bytes;
+        float absmax = 0.0f;
+        for (int i = 0; i < OR_BLOCK; ++i) {
+            float v = fabsf(or_bf16_to_f32(xb[i]));
+            if (v > absmax)
+                absmax = v;
+        }
+        float s = absmax / (float)qmax;
+        scales[b] = s; /* +0 when absmax is 0 */
+        memset(rec, 0, (size_t)rec_bytes);
+        for (int i = 0; i < OR_BLOCK; ++i) {
+            int32_t c = 0;
+            if (absmax != 0.0f) {
+                float q = or_bf16_to_f32(xb[i]) / s;
+                float r = rintf(q); /* ties to even in the default rounding mode */
+                if (r > (float)qmax)
+                    r = (float)qmax;
+                if (r < -(float)qmax)
+                    r = -(float)qmax;
+                c = (int32_t)r;
+            }
+            or_put_field(rec, i, bits, c);
+        }
+    }
+    return OR_OK;
+}
+
+/* LAAQ dequantization, [AGoQ] §2.A "Herberekening versus Caching": the
+ * backward pass reads the stored low-bit input back.  y_i = bf16_rne(fl(c_i*s)). */
+int or_dequant_act(const uint8_t *codes, const float *scales, int64_t n, int bits, uint16_t *y)
+{
+    if (!or_bits_ok(bits) || n < 0 || n % OR_BLOCK)
+        return OR_BAD_ARG;
+    const int64_t rec_bytes = 16 * (int64_t)bits;
+    for (int64_t b = 0; b < n / OR_BLOCK; ++b) {
+        const uint8_t *rec = codes + b * rec_bytes;
+        float s = scales[b];
+        for (int i = 0; i < OR_BLOCK; ++i) {
+            float prod = (float)or_get_field(rec, i, bits) * s;
+            y[b * OR_BLOCK + i] = or_f32_to_bf16(prod);
+        }
+    }
+    return OR_OK;
+}
+
+/* Requantize 128 binary32 values to E4M3 with a fresh block scale:
+ * s' = fl(absmax / 448); c_i = e4m3_rne_satfinite(fl(t_i / s')).
+ * An all-zero block (absmax 0, whatever the signs) stores s' = +0, codes 0x00. */
+static void or_requant_block(const float *t, uint8_t *out_codes, float *out_scale)
+{
+    float absmax = 0.0f;
+    for (int i = 0; i < OR_BLOCK; ++i) {
+        float v = fabsf(t[i]);
+        if (v > absmax)
+            absmax = v;
+    }
+    float s = absmax / 448.0f;
+    *out_scale = s;
+    for (int i = 0; i < OR_BLOCK; ++i)
+        out_codes[i] = (absmax == 0.0f) ? (uint8_t)0x00u : or_f32_to_e4m3(t[i] / s);
+}
+
+/* QuanGrad local accumulation, [AGoQ] §2.B "Lokale accumulatie", in place on
+ * the FP8 master gradient.  Per block:
+ *   m_i = fl(e4m3(c_i) * s)       t_i = fl(m_i + bf16(g_i))
+ *   then requantize t with a fresh block scale (or_requant_block).
+ * The summary names FP16/BF16 for the dequantized master; this implementation
+ * keeps the intermediate in binary32, which holds every FP16/BF16 value.      */
+int or_grad_accum_fp8(uint8_t *master, float *master_scales, const uint16_t *grad, int64_t n)
+{
+    if (n < 0 || n % OR_BLOCK)
+        return OR_BAD_ARG;
+    float t[OR_BLOCK];
+    for (int64_t b = 0; b < n / OR_BLOCK; ++b) {
+        uint8_t *cb = master + b * OR_BLOCK;
+        float s = master_scales[b];
+        for (int i = 0; i < OR_BLOCK; ++i) {
+            float m = or_e4m3_to_f32(cb[i]) * s;
+            t[i] = m + or_bf16_to_f32(grad[b * OR_BLOCK + i]);
+        }
+        or_requant_block(t, cb, &master_scales[b]);
+    }
+    return OR_OK;
+}
+
+/* Local reduce of the precision-preserved all-reduce, [AGoQ] §2.B
+ * "Precision-Preserved All-Reduce" step 2 ("Lokale reduce"), with the W
+ * received shards laid out shard-major: shard r's codes at shards[r*n ...],
+ * its scales at shard_scales[r*(n/128) ...].  Per element:
+ *   acc = +0;  for r = 0 .. W-1:  acc = fl(acc + fl(e4m3(c_r) * s_r))
+ * then requantize acc per block (or_requant_block).
+ *
+ * naive_overflow (may be NULL) receives the number of elements for which the
+ * naive FP8 all-reduce the page contrasts with overflows: the FP8 values are
+ * summed directly in rank order in the FP8 domain (all shards share one scale),
+ * acc = e4m3(c_0); for r = 1 .. W-1: t = acc + e4m3(c_r) (exact in binary32);
+ * if |t| > 448 the element has overflowed (counted once); otherwise
+ * acc = e4m3(rne(t)).                                                          */
+int or_reduce_fp8_shards(const uint8_t *shards, const float *shard_scales, int W, int64_t n,
+                         uint8_t *out, float *out_scales, uint64_t *naive_overflow)
+{
+    if (W < 1 || n < 0 || n % OR_BLOCK)
+        return OR_BAD_ARG;
+    const int64_t nb = n / OR_BLOCK;
+    uint64_t overflow = 0;
+    float acc[OR_BLOCK];
+    for (int64_t b = 0; b < nb; ++b) {
+        for (int i = 0; i < OR_BLOCK; ++i)
+            acc[i] = 0.0f;
+        for (int r = 0; r < W; ++r) {
+            const uint8_t *cb = shards + (int64_t)r * n + b * OR_BLOCK;
+            float s = shard_scales[(int64_t)r * nb + b];
+            for (int i = 0; i < OR_BLOCK; ++i) {
+                float v = or_e4m3_to_f32(cb[i]) * s;
+                acc[i] = acc[i] + v;
+            }
+        }
+        or_requant_block(acc, out + b * OR_BLOCK, &out_scales[b]);
+        if (naive_overflow) {
+            for (int i = 0; i < OR_BLOCK; ++i) {
+                float a = or_e4m3_to_f32(shards[b * OR_BLOCK + i]);
+                for (int r = 1; r < W; ++r) {
+                    float t = a + or_e4m3_to_f32(shards[(int64_t)r * n + b * OR_BLOCK + i]);
+                    if (fabsf(t) > 448.0f) {
+                        ++overflow;
+                        break;
+                    }
+                    a = or_e4m3_to_f32(or_f32_to_e4m3(t));
+                }
+            }
+        }
+    }
+    if (naive_overflow)
+        *naive_overflow = overflow;
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Weight-gradient product with an INT4 LAAQ operand, [AGoQ] §2.C "Kernel
+ * Fusion": dW = dY^T * Xhat, where dY is BF16 [K][M] row-major (K tokens),
+ * Xhat[k][j] is exactly the LAAQ 4-bit dequantization of X (or_dequant_act on
+ * row k: codes [K][N/2], scales [K][N/128]), and dW[i][j] = sum_k dY[k][i] *
+ * Xhat[k][j] is accumulated in binary64 in k order.  Output dW is binary64
+ * [M][N] row-major: the unrounded reference the GPU result is measured against. */
+static double or_xhat(const uint8_t *xc, const float *xs, int N, int64_t k, int64_t j)
+{
+    const uint8_t *rec = xc + k * (int64_t)(N / 2) + (j / OR_BLOCK) * 64;
+    int32_t c = or_get_field(rec, (int)(j % OR_BLOCK), 4);
+    float prod = (float)c * xs[k * (N / OR_BLOCK) + j / OR_BLOCK];
+    return (double)or_bf16_to_f32(or_f32_to_bf16(prod));
+}
+
+int or_wgrad_gemm_int4_f64(const uint16_t *dY, const uint8_t *xc, const float *xs, int M, int N,
+                           int K, double *dW)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || N % OR_BLOCK)
+        return OR_BAD_ARG;
+    double *xhat = (double *)malloc(sizeof(double) * (size_t)K * (size_t)N);
+    if (!xhat)
+        return OR_BAD_ARG;
+    for (int64_t k = 0; k < K; ++k)
+        for (int64_t j = 0; j < N; ++j)
+            xhat[k * N + j] = or_xhat(xc, xs, N, k, j);
+    for (int64_t i = 0; i < M; ++i)
+        for (int64_t j = 0; j < N; ++j) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)or_bf16_to_f32(dY[k * M + i]) * xhat[k * N + j];
+            dW[i * N + j] = acc;
+        }
+    free(xhat);
+    return OR_OK;
+}
+
+/* The same product for a list of entries (rows[e], cols[e]), one plain dot
+ * product each, for checking sampled entries of a full-size result.           */
+int or_wgrad_gemm_int4_f64_entries(const uint16_t *dY, const uint8_t *xc, const float *xs, int M,
+                                   int N, int K, const int32_t *rows, const int32_t *cols,
+                                   int64_t count, double *out)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || N % OR_BLOCK || count < 0)
+        return OR_BAD_ARG;
+    for (int64_t e = 0; e < count; ++e) {
+        int64_t i = rows[e], j = cols[e];
+        if (i < 0 || i >= M || j < 0 || j >= N)
+            return OR_BAD_ARG;
+        double acc = 0.0;
+        for (int64_t k = 0; k < K; ++k)
+            acc += (double)or_bf16_to_f32(dY[k * M + i]) * or_xhat(xc, xs, N, k, j);
+        out[e] = acc;
+    }
+    return OR_OK;
+}
+
+/* ------------------------------------------------------------------------- */
+/* Array forms of the codecs, for the codec sweeps in the tests.               */
+void or_f32_to_bf16_array(const float *src, uint16_t *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = or_f32_to_bf16(src[i]);
+}
+
+void or_f32_to_e4m3_array(const float *src, uint8_t *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = or_f32_to_e4m3(src[i]);
+}
+
+void or_e4m3_to_f32_array(const uint8_t *src, float *dst, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = or_e4m3_to_f32(src[i]);
+}

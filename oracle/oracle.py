@@ -1,0 +1,171 @@
+"""ctypes front end of the CPU oracle (TEST INFRASTRUCTURE, not the product).
+
+Only tests, ``__graft_entry__.smoke()`` and the bench's CPU-baseline leg import
+this module.  It builds ``libagoq_oracle.so`` from ``agoq_oracle.c`` on first
+use and exposes each oracle function over numpy arrays.  Arrays of BF16 values
+are carried as ``numpy.uint16`` bit patterns and FP8 E4M3 values as
+``numpy.uint8`` codes, so no library cast is involved on the oracle side.
+
+What each function computes, and the section of "AGoQ: Activation and Gradient
+Quantization for Memory-Efficient Distributed Training of LLMs" it restates, is
+documented in ``agoq_oracle.c``.
+"""
+import ctypes
+import os
+
+import numpy as np
+
+from . import build as _build
+
+BLOCK = 128
+
+_lib = None
+
+
+def lib():
+    """Load (building first if needed) the oracle shared library."""
+    global _lib
+    if _lib is None:
+        path = _build.build()
+        L = ctypes.CDLL(path)
+        vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+        L.or_quant_act.argtypes = [vp, i64, i32, vp, vp]
+        L.or_dequant_act.argtypes = [vp, vp, i64, i32, vp]
+        L.or_grad_accum_fp8.argtypes = [vp, vp, vp, i64]
+        L.or_reduce_fp8_shards.argtypes = [vp, vp, i32, i64, vp, vp, vp]
+        L.or_wgrad_gemm_int4_f64.argtypes = [vp, vp, vp, i32, i32, i32, vp]
+        L.or_wgrad_gemm_int4_f64_entries.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp]
+        L.or_f32_to_bf16_array.argtypes = [vp, vp, i64]
+        L.or_f32_to_e4m3_array.argtypes = [vp, vp, i64]
+        L.or_e4m3_to_f32_array.argtypes = [vp, vp, i64]
+        for name in ("or_quant_act", "or_dequant_act", "or_grad_accum_fp8",
+                     "or_reduce_fp8_shards", "or_wgrad_gemm_int4_f64",
+                     "or_wgrad_gemm_int4_f64_entries"):
+            getattr(L, name).restype = ctypes.c_int
+        for name in ("or_f32_to_bf16_array", "or_f32_to_e4m3_array", "or_e4m3_to_f32_array"):
+            getattr(L, name).restype = None
+        _lib = L
+    return _lib
+
+
+def _ptr(a):
+    return a.ctypes.data_as(ctypes.c_void_p)
+
+
+def _contig(a, dtype):
+    a = np.ascontiguousarray(a)
+    if a.dtype != dtype:
+        raise TypeError("expected %s, got %s" % (dtype, a.dtype))
+    return a
+
+
+def _check(rc, what):
+    if rc != 0:
+        raise ValueError("oracle %s rejected its arguments (code %d)" % (what, rc))
+
+
+def record_bytes(bits):
+    """Bytes of one packed block record of 128 b-bit codes."""
+    return 16 * bits
+
+
+# --- codecs --------------------------------------------------------------
+def f32_to_bf16(x):
+    x = _contig(np.asarray(x, dtype=np.float32), np.float32)
+    out = np.empty(x.shape, np.uint16)
+    lib().or_f32_to_bf16_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def bf16_to_f32(h):
+    h = _contig(h, np.uint16)
+    return (h.astype(np.uint32) << 16).view(np.float32)
+
+
+def f32_to_e4m3(x):
+    x = _contig(np.asarray(x, dtype=np.float32), np.float32)
+    out = np.empty(x.shape, np.uint8)
+    lib().or_f32_to_e4m3_array(_ptr(x), _ptr(out), x.size)
+    return out
+
+
+def e4m3_to_f32(c):
+    c = _contig(c, np.uint8)
+    out = np.empty(c.shape, np.float32)
+    lib().or_e4m3_to_f32_array(_ptr(c), _ptr(out), c.size)
+    return out
+
+
+# --- the path ------------------------------------------------------------
+def quant_act(x_bf16, bits):
+    """LAAQ quantize: BF16 bit patterns [n] -> (codes uint8 [n/128*16*bits], scales f32 [n/128])."""
+    x = _contig(x_bf16, np.uint16).reshape(-1)
+    n = x.size
+    codes = np.empty(n // BLOCK * record_bytes(bits), np.uint8)
+    scales = np.empty(n // BLOCK, np.float32)
+    _check(lib().or_quant_act(_ptr(x), n, bits, _ptr(codes), _ptr(scales)), "quant_act")
+    return codes, scales
+
+
+def dequant_act(codes, scales, n, bits):
+    """LAAQ dequantize: packed codes + scales -> BF16 bit patterns [n]."""
+    codes = _contig(codes, np.uint8).reshape(-1)
+    scales = _contig(scales, np.float32).reshape(-1)
+    if codes.size < n // BLOCK * record_bytes(bits) or scales.size < n // BLOCK:
+        raise ValueError("codes/scales too short for n")
+    y = np.empty(n, np.uint16)
+    _check(lib().or_dequant_act(_ptr(codes), _ptr(scales), n, bits, _ptr(y)), "dequant_act")
+    return y
+
+
+def grad_accum_fp8(master, master_scales, grad_bf16):
+    """QuanGrad local accumulation; returns new (master, scales), inputs untouched."""
+    m = _contig(master, np.uint8).reshape(-1).copy()
+    s = _contig(master_scales, np.float32).reshape(-1).copy()
+    g = _contig(grad_bf16, np.uint16).reshape(-1)
+    if g.size != m.size or s.size != m.size // BLOCK:
+        raise ValueError("shape mismatch")
+    _check(lib().or_grad_accum_fp8(_ptr(m), _ptr(s), _ptr(g), m.size), "grad_accum_fp8")
+    return m, s
+
+
+def reduce_fp8_shards(shards, shard_scales, W, n, count_naive=True):
+    """Local reduce over W shard-major shards; returns (codes, scales, naive_overflow or None)."""
+    sh = _contig(shards, np.uint8).reshape(-1)
+    ss = _contig(shard_scales, np.float32).reshape(-1)
+    if sh.size != W * n or ss.size != W * (n // BLOCK):
+        raise ValueError("shape mismatch")
+    out = np.empty(n, np.uint8)
+    outs = np.empty(n // BLOCK, np.float32)
+    cnt = np.zeros(1, np.uint64)
+    _check(lib().or_reduce_fp8_shards(_ptr(sh), _ptr(ss), W, n, _ptr(out), _ptr(outs),
+                                       _ptr(cnt) if count_naive else None),
+           "reduce_fp8_shards")
+    return out, outs, (int(cnt[0]) if count_naive else None)
+
+
+def wgrad_gemm_int4_f64(dY_bf16, x_codes, x_scales, M, N, K):
+    """Binary64 dW [M][N] = dY^T Xhat for dY BF16 [K][M] and LAAQ INT4 X [K][N]."""
+    dY = _contig(dY_bf16, np.uint16).reshape(-1)
+    xc = _contig(x_codes, np.uint8).reshape(-1)
+    xs = _contig(x_scales, np.float32).reshape(-1)
+    if dY.size != K * M or xc.size != K * N // 2 or xs.size != K * N // BLOCK:
+        raise ValueError("shape mismatch")
+    out = np.empty((M, N), np.float64)
+    _check(lib().or_wgrad_gemm_int4_f64(_ptr(dY), _ptr(xc), _ptr(xs), M, N, K, _ptr(out)),
+           "wgrad_gemm_int4_f64")
+    return out
+
+
+def wgrad_gemm_int4_f64_entries(dY_bf16, x_codes, x_scales, M, N, K, rows, cols):
+    """Binary64 entries dW[rows[e], cols[e]] of the same product."""
+    dY = _contig(dY_bf16, np.uint16).reshape(-1)
+    xc = _contig(x_codes, np.uint8).reshape(-1)
+    xs = _contig(x_scales, np.float32).reshape(-1)
+    r = _contig(np.asarray(rows, np.int32), np.int32)
+    c = _contig(np.asarray(cols, np.int32), np.int32)
+    out = np.empty(r.size, np.float64)
+    _check(lib().or_wgrad_gemm_int4_f64_entries(_ptr(dY), _ptr(xc), _ptr(xs), M, N, K,
+                                                _ptr(r), _ptr(c), r.size, _ptr(out)),
+           "wgrad_gemm_int4_f64_entries")
+    return out
