@@ -1,0 +1,538 @@
+#!/usr/bin/env python
+"""Throughput of the AGoQ element-wise quantization path on GB300.
+
+One step = the DBCA-PP activation workload (LLaMA-7B MLP shapes): the RMSNorm
+input BF16 [8192 x 4096] and the SiLU/gate input BF16 [8192 x 11008], Student-t
+(nu=4) values, each quantized at 4, 5, 6 and 8 bits and dequantized back: 16
+library calls (8 quantize, then 8 dequantize).  The metric is algorithmic HBM
+bytes per second (each call reads its input and writes its output once:
+n*(2 + bits/8 + 1/32) bytes) and input elements per second.
+
+Every kernel's inputs were last touched at least 247 MB of HBM traffic earlier
+(the 180 MB SiLU tensor sits between two uses of the 67 MB RMSNorm tensor) and
+one step moves 2.7 GB, so the L2 (126 MB) holds no input between uses.
+
+Also reported:
+  roofline      the dominant kernel's algorithmic GB/s (CUDA events around each
+                launch on the launching stream) against the measured HBM copy peak;
+  e2e           the same step with inputs copied from pinned host memory and all
+                outputs copied back inside the timed region;
+  cpu_baseline  the CPU oracle timed on a bounded sample of the same workload;
+  rows          each other kernel of the path on its own workload (QuanGrad
+                accumulation of 2^30 elements, FP8 shard reduce W=8/64 of 2^25,
+                INT4-fused weight-gradient GEMM 11008x4096x8192, the 2048x4096
+                4-bit round trip), L2 flushed before each timed launch.
+
+--impl reference times the CPU oracle (the plain restatement the kernels are
+checked against) on a bounded sample of the same workload.
+Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
+torch.distributed.run, one rank per GPU, each rank running the workload on its
+own GPU (weak scaling, no collective on the data path).
+"""
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+WIDTHS = (4, 5, 6, 8)
+METRIC = "HBM GB/s and Gelem/s per quant kernel; fraction of GB300 HBM/tensor peak"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel,
+# from the ncu capture summarised in profiles/; None until one is taken for the
+# current kernel build.
+DOMINANT_TRAFFIC_BYTES = {}
+
+
+def act_bytes(n, bits):
+    """Algorithmic bytes of one quantize or dequantize call on n elements."""
+    return n * 2 + n * bits // 8 + (n // 128) * 4
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])), "measured"
+    except (OSError, KeyError, ValueError):
+        return FALLBACK_HBM_GBS, FALLBACK_BF16_TFLOPS, 1700.0, "fallback"
+
+
+# ----------------------------------------------------------------------- distributed
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def dist_init(backend):
+    import torch.distributed as dist
+    world, rank, _ = dist_env()
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return world, rank
+
+
+def dist_barrier(device=None):
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        if device is not None and dist.get_backend() == "nccl":
+            dist.barrier(device_ids=[device.index])
+        else:
+            dist.barrier()
+
+
+def max_over_ranks(value, device=None):
+    """Maximum of a float over all ranks (the value itself without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value, device=None):
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()):
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+# ----------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi samples of this GPU's clocks and throttle reasons."""
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_uuid=None, period_ms=100):
+        self.rows = []
+        self.proc = None
+        cmd = ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+               "-lms", str(period_ms)]
+        if device_uuid:
+            cmd[1:1] = ["-i", device_uuid]
+        try:
+            self.proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL,
+                                         text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [c.strip() for c in line.split(",")]))
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        rows = [r for (t, r) in self.rows if t0 <= t <= t1] or [r for (_, r) in self.rows]
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unavailable"], "samples": 0}
+        sm = [float(r[0]) for r in rows if r[0].replace(".", "").isdigit()]
+        smax = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4)
+                          if len(r) > 4 + i and r[4 + i].lower() == "active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": reasons, "samples": len(rows)}
+
+
+# ----------------------------------------------------------------------- GPU arm
+def gpu_arm(args):
+    import torch
+    from gradient_quantization_gb300 import agoq, synthetic
+
+    world, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init("nccl")
+    hbm_peak, bf16_peak, bf16_sust, peak_kind = measured_peaks()
+
+    # ---- inputs resident in HBM
+    x1, x2 = synthetic.dbca_activations_torch(seed=1 + rank, device=device)
+    tensors = [("rmsnorm_in", x1), ("silu_in", x2)]
+    codes, scales, outs = {}, {}, {}
+    for name, x in tensors:
+        n = x.numel()
+        for b in WIDTHS:
+            codes[name, b] = torch.empty(n // 128 * 16 * b, dtype=torch.uint8, device=device)
+            scales[name, b] = torch.empty(n // 128, dtype=torch.float32, device=device)
+            outs[name, b] = torch.empty(n, dtype=torch.bfloat16, device=device)
+    calls = []   # (label, bytes, elems, fn)
+    for b in WIDTHS:
+        for name, x in tensors:
+            n = x.numel()
+            calls.append(("quant_b%d_%s" % (b, name), act_bytes(n, b), n,
+                          (lambda x=x, b=b, name=name: agoq.agoq_quant_act(x, b, codes[name, b], scales[name, b]))))
+    for b in WIDTHS:
+        for name, x in tensors:
+            n = x.numel()
+            calls.append(("dequant_b%d_%s" % (b, name), act_bytes(n, b), n,
+                          (lambda n=n, b=b, name=name: agoq.agoq_dequant_act(codes[name, b], scales[name, b], n, b, outs[name, b]))))
+    step_bytes = sum(c[1] for c in calls)
+    step_elems = sum(c[2] for c in calls)
+
+    def step():
+        for c in calls:
+            c[3]()
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    uuid = None
+    try:
+        uuid = "GPU-" + str(torch.cuda.get_device_properties(device).uuid)
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+
+    stream = torch.cuda.current_stream(device)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(len(calls) + 1)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(device)
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(stream)
+    for k in range(args.steps):
+        e = ev[k]
+        e[0].record(stream)
+        for i, c in enumerate(calls):
+            c[3]()
+            e[i + 1].record(stream)
+    stop.record(stream)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    dist_barrier(device)
+    elapsed_ms = start.elapsed_time(stop)
+    per_call = [0.0] * len(calls)
+    for k in range(args.steps):
+        for i in range(len(calls)):
+            per_call[i] += ev[k][i].elapsed_time(ev[k][i + 1])
+    per_call = [t / args.steps for t in per_call]
+    if sampler:
+        time.sleep(0.25)
+        sampler.stop()
+        clocks = sampler.summary(t_wall0 - 0.05, t_wall1 + 0.3)
+    max_ms = max_over_ranks(elapsed_ms, device)
+    total_bytes = sum_over_ranks(step_bytes * args.steps, device)
+    total_elems = sum_over_ranks(step_elems * args.steps, device)
+    value = total_bytes / (max_ms * 1e-3) / 1e9
+    gelem = total_elems / (max_ms * 1e-3) / 1e9
+
+    # ---- dominant kernel and its roofline
+    dom = max(range(len(calls)), key=lambda i: per_call[i])
+    dom_label, dom_bytes = calls[dom][0], calls[dom][1]
+    achieved = dom_bytes / (per_call[dom] * 1e-3) / 1e9
+    traffic = DOMINANT_TRAFFIC_BYTES.get(dom_label)
+    kernels = {c[0]: {"us": round(per_call[i] * 1e3, 2),
+                      "GB/s": round(c[1] / (per_call[i] * 1e-3) / 1e9, 1),
+                      "Gelem/s": round(c[2] / (per_call[i] * 1e-3) / 1e9, 2),
+                      "frac_of_measured_hbm": round(c[1] / (per_call[i] * 1e-3) / 1e9 / hbm_peak, 4)}
+               for i, c in enumerate(calls)}
+
+    # ---- end to end through host buffers
+    e2e = e2e_arm(args, tensors, codes, scales, outs, calls, device)
+
+    # ---- other rows of the path
+    rows = None
+    if rank == 0 and not args.no_rows:
+        rows = rows_arm(device, hbm_peak, bf16_peak)
+
+    # ---- CPU oracle baseline
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(max_ms / args.steps, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "gelem_per_s": round(gelem, 2),
+            "frac_of_measured_hbm": round(value / world / hbm_peak, 4),
+            "frac_of_nominal_hbm": round(value / world / NOMINAL_HBM_GBS, 4),
+            "config": {"workload": "DBCA-PP activations: RMSNorm in BF16[8192x4096] + SiLU in "
+                                   "BF16[8192x11008], Student-t nu=4, quantize+dequantize at 4/5/6/8 bits",
+                       "calls_per_step": len(calls), "bytes_per_step": step_bytes,
+                       "elems_per_step": step_elems,
+                       "l2": "inputs larger than L2: every kernel's inputs last touched >=247 MB of "
+                             "traffic earlier; 2.7 GB moved per step",
+                       "parallelism": "dp%d (independent replicas)" % world},
+            "roofline": {"kernel": dom_label, "bound": "hbm", "achieved": round(achieved, 1),
+                         "peak": hbm_peak, "unit": "GB/s",
+                         "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
+                         "bytes_per_launch": dom_bytes, "us_per_launch": round(per_call[dom] * 1e3, 2),
+                         "traffic": traffic},
+            "kernels": kernels,
+            "e2e": e2e,
+            "gpu_launches": len(calls) * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+        }
+        if rows is not None:
+            line["rows"] = rows
+        print(json.dumps(line), flush=True)
+
+
+def e2e_arm(args, tensors, codes, scales, outs, calls, device):
+    """The step with inputs copied from pinned host memory and every output
+    copied back to pinned host memory inside the timed region."""
+    import torch
+    host_in = {name: x.cpu().pin_memory() for name, x in tensors}
+    host_codes = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in codes.items()}
+    host_scales = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in scales.items()}
+    host_outs = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in outs.items()}
+    dev_in = {name: x for name, x in tensors}
+    h2d = sum(t.numel() * t.element_size() for t in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for d in (host_codes, host_scales, host_outs)
+              for t in d.values())
+    step_bytes = sum(c[1] for c in calls)
+    steps = max(1, min(args.steps, 20))
+
+    def one():
+        for name, h in host_in.items():
+            dev_in[name].copy_(h, non_blocking=True)
+        for c in calls:
+            c[3]()
+        for k in codes:
+            host_codes[k].copy_(codes[k], non_blocking=True)
+            host_scales[k].copy_(scales[k], non_blocking=True)
+            host_outs[k].copy_(outs[k], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(device)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    dist_barrier(device)
+    a.record(stream)
+    for _ in range(steps):
+        one()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = max_over_ranks(a.elapsed_time(b), device)
+    total = sum_over_ranks(step_bytes * steps, device)
+    return {"value": round(total / (ms * 1e-3) / 1e9, 1), "unit": "GB/s",
+            "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+            "ms_per_step": round(ms / steps, 3), "steps": steps}
+
+
+def _flush_l2(buf):
+    buf.add_(1)
+
+
+def _time_launch(fn, flush, reps=5, warm=2):
+    import torch
+    for _ in range(warm):
+        fn()
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(reps):
+        flush()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        b.synchronize()
+        ts.append(a.elapsed_time(b))
+    return statistics.median(ts)
+
+
+def rows_arm(device, hbm_peak, bf16_peak):
+    """Each other kernel of the path on its own workload, L2 flushed before each launch."""
+    import torch
+    from gradient_quantization_gb300 import agoq, synthetic
+    rows = {}
+    flushbuf = torch.zeros(256 << 20 >> 2, dtype=torch.float32, device=device)
+    flush = lambda: _flush_l2(flushbuf)   # noqa: E731
+
+    def row(name, nbytes, elems, ms, extra=None):
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        r = {"us": round(ms * 1e3, 2), "GB/s": round(gbs, 1),
+             "Gelem/s": round(elems / (ms * 1e-3) / 1e9, 2),
+             "frac_of_measured_hbm": round(gbs / hbm_peak, 4),
+             "frac_of_nominal_hbm": round(gbs / NOMINAL_HBM_GBS, 4)}
+        if extra:
+            r.update(extra)
+        rows[name] = r
+
+    # 4-bit round trip on the 2048 x 4096 activation
+    x = synthetic.laaq_activation_torch(seed=0, device=device)
+    n = x.numel()
+    c, s = agoq.agoq_quant_act(x, 4)
+    y = torch.empty_like(x)
+    row("laaq_int4_quant_2048x4096", act_bytes(n, 4), n,
+        _time_launch(lambda: agoq.agoq_quant_act(x, 4, c, s), flush))
+    row("laaq_int4_dequant_2048x4096", act_bytes(n, 4), n,
+        _time_launch(lambda: agoq.agoq_dequant_act(c, s, n, 4, y), flush))
+    del x, c, s, y
+
+    # QuanGrad accumulation, 2^30 elements
+    n = synthetic.QUANGRAD_N
+    m = torch.zeros(n, dtype=torch.uint8, device=device)
+    ms_ = torch.zeros(n // 128, dtype=torch.float32, device=device)
+    g = synthetic.quangrad_grad_torch(seed=2, step=0, device=device)
+    agoq.agoq_grad_accum_fp8(m, ms_, g)
+    nbytes = n * 4 + (n // 128) * 8
+    row("quangrad_accum_2^30", nbytes, n,
+        _time_launch(lambda: agoq.agoq_grad_accum_fp8(m, ms_, g), flush, reps=5, warm=1))
+    del m, ms_, g
+
+    # FP8 shard local reduce, 2^25 elements per shard
+    n = synthetic.REDUCE_N
+    for W in synthetic.REDUCE_WS:
+        sh = torch.randint(0, 126, (W, n), dtype=torch.uint8, device=device)
+        sh |= (torch.randint(0, 2, (W, n), dtype=torch.uint8, device=device) << 7)
+        ss = torch.rand((W, n // 128), device=device) * 1e-4
+        out = torch.empty(n, dtype=torch.uint8, device=device)
+        outs = torch.empty(n // 128, dtype=torch.float32, device=device)
+        cnt = torch.zeros(1, dtype=torch.int64, device=device)
+        nbytes = (W + 1) * (n + (n // 128) * 4)
+        row("reduce_W%d_2^25" % W, nbytes, W * n,
+            _time_launch(lambda: agoq.agoq_reduce_fp8_shards(sh, ss, W, n, out, outs, cnt), flush))
+        row("reduce_W%d_2^25_nocount" % W, nbytes, W * n,
+            _time_launch(lambda: agoq.agoq_reduce_fp8_shards(sh, ss, W, n, out, outs), flush))
+        del sh, ss, out, outs
+
+    # INT4-dequant-fused weight-gradient GEMM
+    M, N, K = synthetic.WGRAD_M, synthetic.WGRAD_N, synthetic.WGRAD_K
+    dy, xg = synthetic.wgrad_inputs_torch(seed=4, device=device)
+    xc, xs = agoq.agoq_quant_act(xg, 4)
+    dw = torch.empty((M, N), dtype=torch.bfloat16, device=device)
+    try:
+        ms = _time_launch(lambda: agoq.agoq_wgrad_gemm_int4(dy, xc, xs, M, N, K, dw), flush)
+        agoq.agoq_device_status()
+        tflops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        rows["wgrad_gemm_int4_11008x4096x8192"] = {
+            "us": round(ms * 1e3, 1), "TFLOP/s": round(tflops, 1),
+            "frac_of_measured_bf16": round(tflops / bf16_peak, 4),
+            "bytes": 2 * K * M + K * N // 2 + K * (N // 128) * 4 + 2 * M * N}
+        xh = agoq.agoq_dequant_act(xc, xs, K * N, 4).view(K, N)
+        ref_ms = _time_launch(lambda: torch.matmul(dy.t(), xh, out=dw), flush)
+        rows["wgrad_gemm_int4_11008x4096x8192"]["torch_matmul_bf16_predequantized_us"] = round(ref_ms * 1e3, 1)
+    except agoq.AgoqError as e:
+        rows["wgrad_gemm_int4_11008x4096x8192"] = {"unavailable": str(e)}
+    return rows
+
+
+# ----------------------------------------------------------------------- CPU oracle
+def _oracle_step(O, a, b):
+    for x in (a, b):
+        flat = x.reshape(-1)
+        for bits in WIDTHS:
+            c, s = O.quant_act(flat, bits)
+            O.dequant_act(c, s, flat.size, bits)
+
+
+def cpu_sample(target_s):
+    """The workload restricted to its first R token rows, R chosen for ~target_s of oracle work."""
+    from gradient_quantization_gb300 import synthetic
+    from oracle import oracle as O
+    O.lib()
+    rows = 16
+    a, b = synthetic.dbca_activations_np(seed=1, tokens=rows)
+    t0 = time.perf_counter()
+    _oracle_step(O, a, b)
+    dt = time.perf_counter() - t0
+    rows = int(max(16, min(8192, rows * target_s / max(dt, 1e-6))))
+    a, b = synthetic.dbca_activations_np(seed=1, tokens=rows)
+    nbytes = sum(2 * act_bytes(x.size, bits) for x in (a, b) for bits in WIDTHS)
+    nelems = sum(2 * x.size for x in (a, b) for _ in WIDTHS)
+    return O, a, b, rows, nbytes, nelems
+
+
+def cpu_baseline(target_s):
+    O, a, b, rows, nbytes, nelems = cpu_sample(target_s)
+    t0 = time.perf_counter()
+    _oracle_step(O, a, b)
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "gelem_per_s": round(nelems / dt / 1e9, 5), "seconds": round(dt, 2),
+            "sample": "first %d of 8192 token rows of both tensors, quantize+dequantize at 4/5/6/8 "
+                      "bits (single-threaded C oracle)" % rows}
+
+
+def reference_arm(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return
+    # keep the whole reference run within about three minutes of host time
+    per_step = min(args.ref_step_seconds, 180.0 / (args.steps + args.warmup))
+    O, a, b, rows, nbytes, nelems = cpu_sample(per_step)
+    for _ in range(args.warmup):
+        _oracle_step(O, a, b)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(O, a, b)
+    dt = time.perf_counter() - t0
+    value = nbytes * args.steps / dt / 1e9
+    sample = ("first %d of 8192 token rows of both tensors per step, quantize+dequantize at "
+              "4/5/6/8 bits (single-threaded C oracle)" % rows)
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "gelem_per_s": round(nelems * args.steps / dt / 1e9, 5),
+            "config": {"workload": "DBCA-PP activations: RMSNorm in BF16[8192x4096] + SiLU in "
+                                   "BF16[8192x11008], Student-t nu=4, quantize+dequantize at 4/5/6/8 bits",
+                       "sample_rows": rows, "parallelism": "single host thread"},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=("gb300", "reference"), default="gb300")
+    ap.add_argument("--no-rows", action="store_true", help="skip the other rows of the path")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="target CPU seconds of the oracle baseline sample")
+    ap.add_argument("--ref-step-seconds", type=float, default=4.0,
+                    help="target seconds of one reference-arm step")
+    args = ap.parse_args(argv)
+    args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
+    args.steps = max(1, args.steps)
+    if args.impl == "reference":
+        reference_arm(args)
+    else:
+        gpu_arm(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,44 @@
+// agoq_launch.h -- internal launchers behind the C ABI (not installed).
+#pragma once
+
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace agoq {
+
+constexpr int kMaxDevices = 64;
+constexpr int64_t kBlockElems = 128;   // elements per quantization block
+
+// Multiprocessor count of the current device (cached per device).
+int sm_count();
+
+// Resident CTAs per SM for `kernel` at `threads` threads and `smem` bytes of
+// dynamic shared memory; cached in `cache` (one slot per device, 0 = unknown).
+template <typename K>
+int resident_per_sm(K kernel, int threads, size_t smem, int *cache) {
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices) dev = 0;
+    if (cache[dev] == 0) {
+        int per_sm = 0;
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, threads, smem);
+        cache[dev] = per_sm > 0 ? per_sm : 1;
+    }
+    return cache[dev];
+}
+
+cudaError_t launch_laaq_quant(const void *x, int64_t n, int bits, void *codes, float *scales,
+                              cudaStream_t st);
+cudaError_t launch_laaq_dequant(const void *codes, const float *scales, int64_t n, int bits,
+                                void *y, cudaStream_t st);
+cudaError_t launch_grad_accum(void *master, float *master_scales, const void *grad, int64_t n,
+                              cudaStream_t st);
+cudaError_t launch_reduce_shards(const void *shards, const float *shard_scales, int W, int64_t n,
+                                 void *out, float *out_scales, unsigned long long *naive_count,
+                                 cudaStream_t st);
+cudaError_t launch_wgrad_gemm(const void *dY, const void *xc, const float *xs, int M, int N, int K,
+                              void *dW, bool f32_out, cudaStream_t st);
+// Synchronise `st`, read and clear the device status word (0 = no timeout).
+cudaError_t read_and_clear_device_status(cudaStream_t st, unsigned *status);
+
+}  // namespace agoq

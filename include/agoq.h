@@ -1,0 +1,160 @@
+/*
+ * agoq.h -- C ABI of libagoq.so: the AGoQ element-wise quantization kernels
+ * and the INT4-dequant-fused weight-gradient GEMM, for NVIDIA GB300 (sm_103a).
+ *
+ * Method: "AGoQ: Activation and Gradient Quantization for Memory-Efficient
+ * Distributed Training of LLMs" (gist.science summary page), sections
+ * 2.A (LAAQ, DBCA-PP), 2.B (QuanGrad: local accumulation, precision-preserved
+ * all-reduce) and 2.C (kernel fusion).  The page fixes no numeric format; this
+ * library fixes:
+ *   - blocks of 128 consecutive elements of the flat tensor;
+ *   - one FP32 scale per block = (block absmax) / qmax, rounded once (IEEE
+ *     binary32 division); an all-zero block stores scale +0 and zero codes;
+ *   - integer codes c = clamp(round_half_even(fl32(x / scale)), -qmax, qmax)
+ *     with qmax = 2^(bits-1) - 1, stored as two's-complement bit fields in a
+ *     dense little-endian stream: element j of a block occupies bits
+ *     [j*bits, j*bits+bits) of the block's 16*bits-byte record, bit k being
+ *     bit (k mod 8) of byte k/8 (for bits=4: two codes per byte, low nibble
+ *     first; for bits=8: one int8 per byte);
+ *   - FP8 codes are OCP E4M3 "FN" (bias 7, max 448, no infinity), produced by
+ *     round-to-nearest-even with saturation to +-448; qmax = 448;
+ *   - every intermediate is a separately rounded binary32 operation (no fused
+ *     multiply-add), so results are bit-identical to a plain scalar
+ *     implementation of the same steps.
+ *
+ * Conventions shared by every entry point:
+ *   - All data pointers are DEVICE pointers (memory the GPU can address) owned
+ *     by the caller.  The library allocates no memory and keeps no state
+ *     between calls.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls are asynchronous and stream-ordered: they return after
+ *     the launch; results are valid once the stream has been synchronised.
+ *   - Arguments are validated before anything is launched.  On any error the
+ *     call returns a non-zero status and touches no buffer.
+ *   - n counts elements; n must be a multiple of 128 (ragged tails are not
+ *     supported: AGOQ_ERR_SHAPE); n == 0 is a valid no-op.
+ *   - Data pointers must be 16-byte aligned (AGOQ_ERR_ALIGN); scale arrays 4-byte.
+ *   - Outputs must not overlap inputs (AGOQ_ERR_ALIAS), except where a call is
+ *     documented as in place.
+ *   - Inputs must be finite; NaN or infinite inputs give unspecified codes.
+ */
+#ifndef AGOQ_H
+#define AGOQ_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    AGOQ_OK = 0,
+    AGOQ_ERR_NULL = 1,    /* a required pointer is NULL */
+    AGOQ_ERR_SHAPE = 2,   /* n not a multiple of 128, negative size, or GEMM tile rule broken */
+    AGOQ_ERR_BITS = 3,    /* bits not in {4, 5, 6, 8} */
+    AGOQ_ERR_ALIGN = 4,   /* pointer not aligned as required */
+    AGOQ_ERR_ALIAS = 5,   /* an output overlaps an input */
+    AGOQ_ERR_CUDA = 6,    /* the CUDA runtime reported an error at launch */
+    AGOQ_ERR_TIMEOUT = 7  /* a GEMM pipeline wait gave up (see agoq_device_status) */
+} agoq_status;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *agoq_status_string(agoq_status status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+int agoq_version(void);
+
+/*
+ * LAAQ block-wise activation quantization (AGoQ section 2.A, "Strategie" for
+ * 4 bits; "Dynamic Bit-width Compensation (DBCA-PP)" for 5, 6 and 8 bits).
+ *   x_bf16 : in,  n BF16 values (the flattened activation, row-major).
+ *   n      : number of elements, multiple of 128.
+ *   bits   : 4, 5, 6 or 8.
+ *   codes  : out, (n/128) * 16 * bits bytes: one packed record per block.
+ *   scales : out, n/128 FP32 block scales.
+ */
+agoq_status agoq_quant_act(const void *x_bf16, int64_t n, int bits, void *codes, float *scales,
+                           void *stream);
+
+/*
+ * LAAQ dequantization (AGoQ section 2.A, "Herberekening versus Caching": the
+ * stored low-bit input is read back in the backward pass).
+ *   y_i = bf16_round_nearest_even(fl32(c_i * scale)).
+ *   codes, scales : in, as written by agoq_quant_act with the same n and bits.
+ *   y_bf16        : out, n BF16 values.
+ */
+agoq_status agoq_dequant_act(const void *codes, const float *scales, int64_t n, int bits,
+                             void *y_bf16, void *stream);
+
+/*
+ * QuanGrad local accumulation (AGoQ section 2.B, "Lokale accumulatie"), IN
+ * PLACE on an FP8 master gradient.  Per block of 128:
+ *   m_i = fl32(e4m3(c_i) * scale);  t_i = fl32(m_i + g_i);
+ *   scale' = fl32(absmax(t) / 448); c_i' = e4m3_rne_satfinite(fl32(t_i / scale')).
+ *   master_e4m3   : in/out, n E4M3 codes.  A zeroed buffer is a zero gradient.
+ *   master_scales : in/out, n/128 FP32 scales.
+ *   grad_bf16     : in, n BF16 micro-batch gradient values (must not overlap the master).
+ * The page dequantizes to FP16/BF16; this library keeps the sum in FP32.
+ */
+agoq_status agoq_grad_accum_fp8(void *master_e4m3, float *master_scales, const void *grad_bf16,
+                                int64_t n, void *stream);
+
+/*
+ * Local reduce of the precision-preserved all-reduce (AGoQ section 2.B,
+ * "Precision-Preserved All-Reduce", step 2 "Lokale reduce"): the W shards an
+ * all-to-all delivered, summed in FP32 in rank order and requantized to FP8.
+ *   shards_e4m3  : in, W * n E4M3 codes, shard-major ([W][n]).
+ *   shard_scales : in, W * (n/128) FP32 scales ([W][n/128]).
+ *   W            : number of shards, >= 1.
+ *   out_e4m3     : out, n codes;  out_scales : out, n/128 scales.
+ *   Per element acc = +0; for r = 0..W-1: acc = fl32(acc + fl32(e4m3(c_r) * s_r));
+ *   then the requantization of agoq_grad_accum_fp8.
+ *   naive_overflow_count : out (device pointer to one uint64) or NULL.  When
+ *     given, it is set (not accumulated) to the number of elements at which a
+ *     naive FP8 all-reduce -- the W FP8 values summed directly in rank order,
+ *     the running sum rounded back to E4M3 after each add -- exceeds 448.
+ *     The library zeroes it on `stream` before the reduce.
+ */
+agoq_status agoq_reduce_fp8_shards(const void *shards_e4m3, const float *shard_scales, int W,
+                                   int64_t n, void *out_e4m3, float *out_scales,
+                                   unsigned long long *naive_overflow_count, void *stream);
+
+/*
+ * Weight-gradient GEMM with the LAAQ 4-bit activation dequantized inside the
+ * kernel's operand path (AGoQ section 2.C, "Kernel Fusion"):
+ *   dW[M][N] = sum_k dY[k][m] * Xhat[k][n],
+ *   Xhat[k][n] = bf16_rne(fl32(c[k][n] * scale[k][n/128])), exactly what
+ *   agoq_dequant_act(bits=4) gives for row k;  FP32 accumulation in tensor
+ *   memory, BF16 round-to-nearest-even output.
+ *   dY_bf16  : in, BF16 [K][M] row-major (K tokens).
+ *   x_codes  : in, [K][N/2] bytes: row k is agoq_quant_act(bits=4) of X row k.
+ *   x_scales : in, FP32 [K][N/128].
+ *   dW_bf16  : out, BF16 [M][N] row-major.
+ *   M and N must be multiples of 256, K a multiple of 64, all > 0
+ *   (AGOQ_ERR_SHAPE otherwise).
+ */
+agoq_status agoq_wgrad_gemm_int4(const void *dY_bf16, const void *x_codes, const float *x_scales,
+                                 int M, int N, int K, void *dW_bf16, void *stream);
+
+/*
+ * The same GEMM with the FP32 accumulator written out unrounded
+ * (dW_f32 : out, FP32 [M][N] row-major).  For verification: it isolates the
+ * accumulation error from the BF16 output rounding.
+ */
+agoq_status agoq_wgrad_gemm_int4_f32out(const void *dY_bf16, const void *x_codes,
+                                        const float *x_scales, int M, int N, int K, float *dW_f32,
+                                        void *stream);
+
+/*
+ * Synchronise `stream`, then read and clear the library's device-side status
+ * word for the current device.  Returns AGOQ_ERR_TIMEOUT if a GEMM pipeline
+ * wait exceeded its iteration limit since the last call (that GEMM's output is
+ * then incomplete), AGOQ_ERR_CUDA if the synchronisation failed, else AGOQ_OK.
+ */
+agoq_status agoq_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* AGOQ_H */

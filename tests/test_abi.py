@@ -1,0 +1,108 @@
+"""The C-ABI library loads, exports every entry point include/agoq.h declares,
+and rejects bad arguments on the host before any CUDA call (so these run
+without a GPU: every call below fails validation and launches nothing)."""
+import ctypes
+import subprocess
+
+import pytest
+
+from gradient_quantization_gb300 import agoq
+
+OK, NULL, SHAPE, BITS, ALIGN, ALIAS = 0, 1, 2, 3, 4, 5
+
+
+@pytest.fixture(scope="module")
+def L():
+    return agoq.lib()
+
+
+def test_every_declared_entry_point_is_exported(L):
+    names = agoq.declared_entry_points()
+    assert len(names) >= 9
+    for name in names:
+        assert hasattr(L, name), name
+
+
+def test_exports_are_c_symbols():
+    out = subprocess.run(["nm", "-D", "--defined-only", agoq.LIB_PATH], capture_output=True,
+                         text=True, check=True).stdout
+    syms = {line.split()[-1] for line in out.splitlines() if line.strip()}
+    for name in agoq.declared_entry_points():
+        assert name in syms, name
+
+
+def test_status_strings(L):
+    for code in range(8):
+        s = L.agoq_status_string(code).decode()
+        assert s.startswith(agoq.STATUS[code])
+    assert L.agoq_status_string(99).decode() == "AGOQ_ERR_UNKNOWN"
+    assert L.agoq_version() >= 100
+
+
+P = ctypes.c_void_p
+A = 0x10000000          # fake, 16-byte-aligned addresses: never dereferenced on these paths
+B = 0x20000000
+C = 0x30000000
+
+
+def test_quant_act_validation(L):
+    assert L.agoq_quant_act(P(A), 256, 7, P(B), P(C), None) == BITS
+    assert L.agoq_quant_act(P(A), 100, 4, P(B), P(C), None) == SHAPE
+    assert L.agoq_quant_act(P(A), -128, 4, P(B), P(C), None) == SHAPE
+    assert L.agoq_quant_act(P(A), 0, 4, None, None, None) == OK          # empty: no-op
+    assert L.agoq_quant_act(None, 256, 4, P(B), P(C), None) == NULL
+    assert L.agoq_quant_act(P(A + 2), 256, 4, P(B), P(C), None) == ALIGN
+    assert L.agoq_quant_act(P(A), 256, 4, P(B + 8), P(C), None) == ALIGN
+    assert L.agoq_quant_act(P(A), 256, 4, P(B), P(C + 2), None) == ALIGN
+    # codes overlapping the input
+    assert L.agoq_quant_act(P(A), 256, 4, P(A + 256), P(C), None) == ALIAS
+    # scales overlapping the codes (2 blocks * 64 bytes)
+    assert L.agoq_quant_act(P(A), 256, 4, P(B), P(B + 64), None) == ALIAS
+
+
+def test_dequant_act_validation(L):
+    assert L.agoq_dequant_act(P(A), P(B), 256, 3, P(C), None) == BITS
+    assert L.agoq_dequant_act(P(A), P(B), 130, 4, P(C), None) == SHAPE
+    assert L.agoq_dequant_act(P(A), None, 256, 4, P(C), None) == NULL
+    assert L.agoq_dequant_act(P(A), P(B), 256, 4, P(C + 4), None) == ALIGN
+    assert L.agoq_dequant_act(P(A), P(B), 256, 4, P(A), None) == ALIAS
+    assert L.agoq_dequant_act(P(A), P(B), 0, 8, P(C), None) == OK
+
+
+def test_grad_accum_validation(L):
+    assert L.agoq_grad_accum_fp8(P(A), P(B), P(C), 127, None) == SHAPE
+    assert L.agoq_grad_accum_fp8(None, P(B), P(C), 128, None) == NULL
+    assert L.agoq_grad_accum_fp8(P(A + 1), P(B), P(C), 128, None) == ALIGN
+    assert L.agoq_grad_accum_fp8(P(A), P(B), P(A + 64), 128, None) == ALIAS
+    assert L.agoq_grad_accum_fp8(P(A), P(B), P(C), 0, None) == OK
+
+
+def test_reduce_validation(L):
+    assert L.agoq_reduce_fp8_shards(P(A), P(B), 0, 128, P(C), P(C + 4096), None, None) == SHAPE
+    assert L.agoq_reduce_fp8_shards(P(A), P(B), 2, 200, P(C), P(C + 4096), None, None) == SHAPE
+    assert L.agoq_reduce_fp8_shards(P(A), None, 2, 128, P(C), P(C + 4096), None, None) == NULL
+    assert L.agoq_reduce_fp8_shards(P(A), P(B), 2, 128, P(C + 8), P(C + 4096), None, None) == ALIGN
+    assert L.agoq_reduce_fp8_shards(P(A), P(B), 2, 128, P(C), P(C + 4096), P(C + 4100), None) == ALIGN
+    # output inside the second shard
+    assert L.agoq_reduce_fp8_shards(P(A), P(B), 2, 128, P(A + 128), P(C), None, None) == ALIAS
+    # count overlapping the output scales
+    assert L.agoq_reduce_fp8_shards(P(A), P(B), 2, 128, P(C), P(C + 4096), P(C + 4096), None) == ALIAS
+    assert L.agoq_reduce_fp8_shards(P(A), P(B), 2, 0, P(C), P(C), None, None) == OK
+
+
+def test_gemm_validation(L):
+    for fn in (L.agoq_wgrad_gemm_int4, L.agoq_wgrad_gemm_int4_f32out):
+        assert fn(P(A), P(B), P(C), 100, 256, 64, P(C + (1 << 24)), None) == SHAPE
+        assert fn(P(A), P(B), P(C), 256, 128, 64, P(C + (1 << 24)), None) == SHAPE
+        assert fn(P(A), P(B), P(C), 256, 256, 32, P(C + (1 << 24)), None) == SHAPE
+        assert fn(P(A), P(B), P(C), 0, 256, 64, P(C + (1 << 24)), None) == SHAPE
+        assert fn(None, P(B), P(C), 256, 256, 64, P(C + (1 << 24)), None) == NULL
+        assert fn(P(A), P(B), P(C + 4), 256, 256, 64, P(C + (1 << 24)), None) == ALIGN
+        assert fn(P(A), P(B), P(C), 256, 256, 64, P(A), None) == ALIAS
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(agoq, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(agoq, "_L", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        agoq.lib()
