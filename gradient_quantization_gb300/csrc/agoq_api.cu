@@ -142,7 +142,7 @@ agoq_status agoq_reduce_fp8_shards(const void *shards_e4m3, const float *shard_s
 static agoq_status wgrad_common(const void *dY, const void *xc, const float *xs, int M, int N,
                                 int K, void *dW, bool f32_out, void *stream) {
     using namespace agoq;
-    if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 256 || K % 64) return AGOQ_ERR_SHAPE;
+    if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 512 || K % 64) return AGOQ_ERR_SHAPE;
     if (!dY || !xc || !xs || !dW) return AGOQ_ERR_NULL;
     if (!aligned(dY, 16) || !aligned(xc, 16) || !aligned(xs, 16) || !aligned(dW, 16))
         return AGOQ_ERR_ALIGN;

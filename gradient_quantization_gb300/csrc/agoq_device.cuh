@@ -45,6 +45,80 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint32_t v, float &lo, float &hi) 
         : "r"(h2));
 }
 
+// Code i (bits 8i..8i+7) of a word of four E4M3 codes, as a binary32 whose
+// value is exactly e4m3(code) * 2^-120: the code's sign goes to bit 31 and its
+// 7 exponent/fraction bits to bits 26..20, which reads as a binary32 with the
+// E4M3 exponent field (bias 7 instead of 127) and fraction; E4M3 subnormals
+// land on binary32 subnormals with the same scaling.  Multiplying by 2^120, or
+// by a scale s pre-multiplied by 2^120, is therefore exact up to the single
+// rounding of the final product.
+__device__ __forceinline__ float e4m3_times_2m120(uint32_t w, int i) {
+    const uint32_t x = i == 3 ? w : (w << (24 - 8 * i));   // code i in bits 24..31
+    return __uint_as_float((x & 0x80000000u) | ((x >> 4) & 0x07F00000u));
+}
+
+constexpr float kTwo120 = 0x1p120f;
+
+// fl(e4m3(code) * s) for the codes of a word, with S = s * 2^120 precomputed
+// when s < 2^8 (so that S is exact) -- `folded` says which form `S` holds.
+__device__ __forceinline__ float e4m3_mul(uint32_t w, int i, float S, bool folded, float s) {
+    const float f = e4m3_times_2m120(w, i);
+    return folded ? __fmul_rn(f, S) : __fmul_rn(__fmul_rn(f, kTwo120), s);
+}
+
+// E4M3 codes of 8 values t[] requantized with block scale s = fl(absmax/448):
+// code_i = e4m3_rne_satfinite(fl(t_i / s)).  Returns two words of 4 codes.
+//
+// For a normal s the quotient is formed as q = fl(t * r), r = fl(1/s); q lies
+// within 3 * 2^-24 |t/s| of the binary32 quotient (plus a negligible absolute
+// term if subnormal).  The codes of fl(q * (1 - 2^-20)) and fl(q * (1 + 2^-20))
+// bracket that quotient on both sides; E4M3 rounding is monotonic, so when the
+// two codes agree they equal the quotient's code.  If any pair disagrees the
+// eight quotients are recomputed with IEEE division.  Values whose products
+// underflow are far below the smallest E4M3 midpoint (2^-10) and give a signed
+// zero either way.  s subnormal takes the division; s == 0 (all-zero block)
+// gives zero codes.
+__device__ __forceinline__ uint2 e4m3_codes8(const float t[8], float s) {
+    uint32_t c[4];
+    if (s >= 0x1p-126f) {
+        const float r = __frcp_rn(s);
+        constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
+        bool differ = false;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const float qa = __fmul_rn(t[2 * p], r), qb = __fmul_rn(t[2 * p + 1], r);
+            const uint32_t lo = e4m3x2_from_f32(__fmul_rn(qa, kDown), __fmul_rn(qb, kDown));
+            const uint32_t hi = e4m3x2_from_f32(__fmul_rn(qa, kUp), __fmul_rn(qb, kUp));
+            differ |= lo != hi;
+            c[p] = lo;
+        }
+        if (differ) {
+#pragma unroll
+            for (int p = 0; p < 4; ++p)
+                c[p] = e4m3x2_from_f32(__fdiv_rn(t[2 * p], s), __fdiv_rn(t[2 * p + 1], s));
+        }
+    } else if (s > 0.0f) {
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+            c[p] = e4m3x2_from_f32(__fdiv_rn(t[2 * p], s), __fdiv_rn(t[2 * p + 1], s));
+    } else {
+        return make_uint2(0u, 0u);
+    }
+    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+}
+
+// Round an exactly representable binary32 sum of two E4M3 values (|t| <= 448)
+// to the nearest E4M3 value, ties to even, staying in binary32: with
+// c = 1.5 * 2^(e+20), where 2^e <= |t| < 2^(e+1) (e clamped below at -6, the
+// E4M3 subnormal spacing being 2^-9), fl(t + c) keeps exactly the bits of t at
+// and above 2^(e-3) -- the E4M3 spacing -- rounding the rest to nearest even
+// (c's own bits there are even); subtracting c is exact.
+__device__ __forceinline__ float e4m3_round_f32(float t) {
+    const uint32_t e = max(__float_as_uint(t) & 0x7F800000u, (uint32_t)(127 - 6) << 23);
+    const float c = __uint_as_float(e + (20u << 23) + 0x00400000u);
+    return __fsub_rn(__fadd_rn(t, c), c);
+}
+
 // ---- block reductions --------------------------------------------------------
 // Maximum over the 16 lanes of a half warp (lanes 0-15 or 16-31).
 __device__ __forceinline__ float halfwarp_max(float v) {
@@ -61,24 +135,98 @@ __device__ __forceinline__ float octet_max(float v) {
 }
 
 // ---- integer codes ----------------------------------------------------------
-// Nearest integer, ties to even, of the binary32 quotient fl(x / s), computed
-// as rint(fl(x * r)) with r = fl(1/s) unless the product lies within 2^-14 of a
-// half-integer, in which case the quotient is formed with an IEEE division.
+// Adding 1.5 * 2^23 to a binary32 of magnitude below 2^22 rounds it to an
+// integer (round to nearest even, the addition's own rounding) and leaves that
+// integer in the low mantissa bits in two's complement: the bit pattern is
+// 0x4B400000 + k.  Subtracting the constant again recovers k exactly.
+constexpr float kRoundMagic = 12582912.0f;
+
+// Integer codes of 8 values of one block: code_i = rne_int(fl(x_i / s)), clamped
+// to [-qmax, qmax].  Returns each code as the bit pattern of fl(code + 1.5*2^23),
+// whose low bits are the code in two's complement.
 //
-// Why the shortcut is exact: with r = (1/s)(1+e1) and fl(x*r) = x*r*(1+e2),
-// |e1|,|e2| <= 2^-24, the product differs from x/s by at most 2^-23 |x/s|
-// (+ an absolute 2^-150 if it is subnormal), and fl(x/s) differs from x/s by at
-// most 2^-24 |x/s|.  Quotients here satisfy |x/s| <= qmax(1+2^-23) <= 128, so
-// product and quotient differ by less than 3 * 2^-17 < 2^-14.  Away from the
-// half-integers (the only points where the integer rounding changes) both
-// therefore round to the same integer.  Requires s normal (r finite and
-// accurate); callers use the division for subnormal s.
-__device__ __forceinline__ float rint_quotient(float x, float s, float r) {
-    const float q = __fmul_rn(x, r);
-    const float k = rintf(q);
-    const float d = fabsf(__fsub_rn(q, k));     // distance to the nearest integer, <= 1/2
-    if (__fsub_rn(0.5f, d) < 0x1p-14f) return rintf(__fdiv_rn(x, s));
-    return k;
+// For a normal scale s the quotient is formed as fl(x * r), r = fl(1/s), and
+// rounded with the magic addition; only if some product lies within 2^-14 of
+// a half-integer are the eight quotients recomputed with IEEE division.  Why
+// the shortcut is exact: with r = (1/s)(1+e1) and fl(x*r) = x*r*(1+e2),
+// |e1|,|e2| <= 2^-24, the product differs from x/s by at most 2^-23 |x/s| (plus
+// 2^-150 absolute if it is subnormal), and fl(x/s) differs from x/s by at most
+// 2^-24 |x/s|.  Here |x/s| <= qmax(1+2^-23) <= 128, so product and quotient
+// differ by less than 3 * 2^-17 < 2^-14; away from the half-integers (the only
+// points where integer rounding changes) both round to the same integer.  The
+// same bound keeps every code within [-qmax, qmax] without a clamp.  A
+// subnormal scale (absolute rounding error up to 2^-150) takes the division
+// and an explicit clamp; an all-zero block (s = 0) gives zero codes.
+template <int QMAX>
+__device__ __forceinline__ void integer_codes8(const float x[8], float s, uint32_t code_bits[8]) {
+    if (s >= 0x1p-126f) {
+        const float r = __frcp_rn(s);
+        bool near = false;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float q = __fmul_rn(x[i], r);
+            const float t = __fadd_rn(q, kRoundMagic);
+            const float k = __fsub_rn(t, kRoundMagic);
+            near |= fabsf(__fsub_rn(q, k)) > 0.5f - 0x1p-14f;
+            code_bits[i] = __float_as_uint(t);
+        }
+        if (near) {
+#pragma unroll
+            for (int i = 0; i < 8; ++i)
+                code_bits[i] = __float_as_uint(__fadd_rn(__fdiv_rn(x[i], s), kRoundMagic));
+        }
+    } else if (s > 0.0f) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const float k = fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -(float)QMAX), (float)QMAX);
+            code_bits[i] = __float_as_uint(__fadd_rn(k, kRoundMagic));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) code_bits[i] = 0u;
+    }
+}
+
+// Pack the low BITS bits of 8 words into a 64-bit little-endian chunk held as
+// two 32-bit words (field i at bit i*BITS); positions are compile-time.
+template <int BITS>
+__device__ __forceinline__ void pack_fields8(const uint32_t w[8], uint32_t &lo, uint32_t &hi) {
+    constexpr uint32_t kMask = (1u << BITS) - 1u;
+    lo = 0u;
+    hi = 0u;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint32_t f = w[i] & kMask;
+        const int pos = i * BITS;
+        if (pos + BITS <= 32) {
+            lo |= f << pos;
+        } else if (pos >= 32) {
+            hi |= f << (pos - 32);
+        } else {
+            lo |= f << pos;
+            hi |= f >> (32 - pos);
+        }
+    }
+}
+
+// binary32 value of the signed BITS-bit field at bit `pos` of (hi:lo), exact:
+// flipping the field's sign bit gives c + 2^(BITS-1) as an unsigned number,
+// which becomes the mantissa of 2^23 + c + 2^(BITS-1); subtracting that bias
+// leaves c.
+template <int BITS>
+__device__ __forceinline__ float field_value(uint32_t lo, uint32_t hi, int pos) {
+    constexpr uint32_t kMask = (1u << BITS) - 1u;
+    constexpr uint32_t kSign = 1u << (BITS - 1);
+    uint32_t u;
+    if (pos + BITS <= 32) {
+        u = lo >> pos;
+    } else if (pos >= 32) {
+        u = hi >> (pos - 32);
+    } else {
+        u = __funnelshift_r(lo, hi, pos);
+    }
+    const uint32_t biased = (u & kMask) ^ (0x4B000000u | kSign);
+    return __fsub_rn(__uint_as_float(biased), (float)(8388608 + kSign));
 }
 
 }  // namespace agoq

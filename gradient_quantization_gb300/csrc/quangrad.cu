@@ -15,6 +15,20 @@
 #include "agoq_device.cuh"
 #include "agoq_launch.h"
 
+// Implementation choices, all bit-identical (selected by measurement):
+//   AGOQ_E4M3_DECODE_CVT   1: decode codes with cvt.f16x2.e4m3x2; 0: with integer bit moves
+//   AGOQ_E4M3_REQUANT_FAST 1: reciprocal + bracketing check; 0: IEEE division per value
+//   AGOQ_NAIVE_ROUND_CVT   1: round the naive sum through an E4M3 cvt; 0: in binary32
+#ifndef AGOQ_E4M3_DECODE_CVT
+#define AGOQ_E4M3_DECODE_CVT 1
+#endif
+#ifndef AGOQ_E4M3_REQUANT_FAST
+#define AGOQ_E4M3_REQUANT_FAST 0
+#endif
+#ifndef AGOQ_NAIVE_ROUND_CVT
+#define AGOQ_NAIVE_ROUND_CVT 1
+#endif
+
 namespace agoq {
 namespace {
 
@@ -29,18 +43,45 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     return v;
 }
 
-// Requantize 8 binary32 values held by one lane, given the block's absmax `am`
-// (already reduced over the block): codes = e4m3_rne_satfinite(fl(t / s')),
-// s' = fl(am / 448); an all-zero block gives s' = +0 and zero codes.
-__device__ __forceinline__ uint2 requant8(const float t[8], float am, float &s_out) {
-    const float s = __fdiv_rn(am, kE4M3Max);
-    s_out = s;
-    if (am == 0.0f) return make_uint2(0u, 0u);
+// Requantize 8 binary32 values with the block scale s (see e4m3_codes8).
+__device__ __forceinline__ uint2 requant8(const float t[8], float s) {
+#if AGOQ_E4M3_REQUANT_FAST
+    return e4m3_codes8(t, s);
+#else
+    if (s == 0.0f) return make_uint2(0u, 0u);
     uint32_t c[4];
 #pragma unroll
     for (int p = 0; p < 4; ++p)
         c[p] = e4m3x2_from_f32(__fdiv_rn(t[2 * p], s), __fdiv_rn(t[2 * p + 1], s));
     return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+#endif
+}
+
+// fl(e4m3(code_i) * s) for the 4 codes of word w.
+__device__ __forceinline__ void decode_mul4(uint32_t w, float s, float v[4]) {
+#if AGOQ_E4M3_DECODE_CVT
+    float e[4];
+    e4m3x2_to_f32(w & 0xFFFFu, e[0], e[1]);
+    e4m3x2_to_f32(w >> 16, e[2], e[3]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(e[i], s);
+#else
+    const bool folded = s < 256.0f;
+    const float S = folded ? __fmul_rn(s, kTwo120) : s;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) v[i] = e4m3_mul(w, i, S, folded, s);
+#endif
+}
+
+// The E4M3 values of the 4 codes of word w (exact).
+__device__ __forceinline__ void decode4(uint32_t w, float e[4]) {
+#if AGOQ_E4M3_DECODE_CVT
+    e4m3x2_to_f32(w & 0xFFFFu, e[0], e[1]);
+    e4m3x2_to_f32(w >> 16, e[2], e[3]);
+#else
+#pragma unroll
+    for (int i = 0; i < 4; ++i) e[i] = __fmul_rn(e4m3_times_2m120(w, i), kTwo120);
+#endif
 }
 
 template <int UNROLL>
@@ -72,33 +113,26 @@ __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict_
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t blk = base + 2 * u + half;
-            float e[8], t[8];
-            e4m3x2_to_f32(mc[u].x & 0xFFFFu, e[0], e[1]);
-            e4m3x2_to_f32(mc[u].x >> 16, e[2], e[3]);
-            e4m3x2_to_f32(mc[u].y & 0xFFFFu, e[4], e[5]);
-            e4m3x2_to_f32(mc[u].y >> 16, e[6], e[7]);
             const float gv[8] = {bf16_lo(g[u].x), bf16_hi(g[u].x), bf16_lo(g[u].y), bf16_hi(g[u].y),
                                  bf16_lo(g[u].z), bf16_hi(g[u].z), bf16_lo(g[u].w), bf16_hi(g[u].w)};
+            float t[8];
+            decode_mul4(mc[u].x, s[u], t);
+            decode_mul4(mc[u].y, s[u], t + 4);
             float am = 0.0f;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                t[i] = __fadd_rn(__fmul_rn(e[i], s[u]), gv[i]);
+                t[i] = __fadd_rn(t[i], gv[i]);
                 am = fmaxf(am, fabsf(t[i]));
             }
             am = halfwarp_max(am);
-            float snew;
-            const uint2 out = requant8(t, am, snew);
+            const float snew = __fdiv_rn(am, kE4M3Max);
+            const uint2 out = requant8(t, snew);
             if (blk < nblocks) {
                 master[blk * 16 + j] = out;
                 if (j == 0) scales[blk] = snew;
             }
         }
     }
-}
-
-// One E4M3 value rounded again from an exact binary32 sum (|t| <= 448).
-__device__ __forceinline__ void e4m3_round_pair(float &a, float &b) {
-    e4m3x2_to_f32(e4m3x2_from_f32(a, b), a, b);
 }
 
 template <bool NAIVE, int RUNROLL>
@@ -137,29 +171,28 @@ __global__ void __launch_bounds__(kThreads) reduce_shards_kernel(
                 const uint32_t w4[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
                 float e[16];
 #pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    e4m3x2_to_f32(w4[q] & 0xFFFFu, e[4 * q], e[4 * q + 1]);
-                    e4m3x2_to_f32(w4[q] >> 16, e[4 * q + 2], e[4 * q + 3]);
-                }
+                for (int q = 0; q < 4; ++q) decode4(w4[q], e + 4 * q);
 #pragma unroll
                 for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(e[i], s[u]));
                 if constexpr (NAIVE) {
                     if (r == 0) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) nv[i] = e[i];
-                    } else if (alive) {
+                    } else {
                         float tt[16];
 #pragma unroll
                         for (int i = 0; i < 16; ++i) {
                             tt[i] = __fadd_rn(nv[i], e[i]);   // exact: both are E4M3 values
                             if (fabsf(tt[i]) > kE4M3Max) alive &= ~(1u << i);
                         }
+#if AGOQ_NAIVE_ROUND_CVT
 #pragma unroll
-                        for (int i = 0; i < 16; i += 2) {
-                            e4m3_round_pair(tt[i], tt[i + 1]);
-                            nv[i] = tt[i];
-                            nv[i + 1] = tt[i + 1];
-                        }
+                        for (int i = 0; i < 16; i += 2)
+                            e4m3x2_to_f32(e4m3x2_from_f32(tt[i], tt[i + 1]), nv[i], nv[i + 1]);
+#else
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) nv[i] = e4m3_round_f32(tt[i]);
+#endif
                     }
                 }
             }
@@ -168,12 +201,12 @@ __global__ void __launch_bounds__(kThreads) reduce_shards_kernel(
 #pragma unroll
         for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(acc[i]));
         am = octet_max(am);
-        float s0, s1;
-        const uint2 lo = requant8(acc, am, s0);
-        const uint2 hi = requant8(acc + 8, am, s1);
+        const float snew = __fdiv_rn(am, kE4M3Max);
+        const uint2 lo = requant8(acc, snew);
+        const uint2 hi = requant8(acc + 8, snew);
         if (valid) {
             out[blk * 8 + t8] = make_uint4(lo.x, lo.y, hi.x, hi.y);
-            if (t8 == 0) out_scales[blk] = s0;
+            if (t8 == 0) out_scales[blk] = snew;
             if constexpr (NAIVE) overflowed += (unsigned long long)__popc(~alive & 0xFFFFu);
         }
     }

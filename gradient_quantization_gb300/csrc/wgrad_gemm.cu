@@ -1,16 +1,491 @@
-// wgrad_gemm.cu -- INT4-dequant-fused weight-gradient GEMM (placeholder launcher).
+// wgrad_gemm.cu -- weight-gradient GEMM with the LAAQ 4-bit activation
+// dequantized in the operand path ("AGoQ: Activation and Gradient Quantization
+// for Memory-Efficient Distributed Training of LLMs", section 2.C "Kernel
+// Fusion": the tensor cores do the GEMM while the quantization logic runs on
+// the CUDA cores of the same kernel).
+//
+//   dW[M][N] = sum_k dY[k][m] * Xhat[k][n],  Xhat = bf16(fl32(code * scale))
+//
+// Blackwell design (sm_103a, one CTA per SM, persistent over 256x256 tiles):
+//   warp 0      TMA producer: per 64-deep k-block, the dY tile (256 M x 64 K,
+//               four 64x64 boxes, 128-byte swizzle), the packed 4-bit X codes
+//               (64 K rows x 128 bytes) and their scales (64 x 4 floats).
+//   warp 1      TMEM owner and MMA issuer: one elected thread issues, per
+//               k-block, 4 x 2 tcgen05.mma kind::f16 (M=128, N=256, K=16; both
+//               operands MN-major, BF16 in, FP32 accumulate) into two 256-column
+//               accumulators (rows 0-127 and 128-255 of the tile) that fill the
+//               512 TMEM columns; tcgen05.commit frees the stage.
+//   warps 2-9   dequantizers: codes -> Xhat (BF16) written straight into the
+//               MN-major, 128-byte-swizzled B tile the MMA reads, then
+//               fence.proxy.async and an mbarrier arrive.
+//   warps 10-13 epilogue: tcgen05.ld of the accumulators (each warp its 32-lane
+//               quarter), BF16 round-to-nearest-even (or FP32), global stores.
+// Every mbarrier wait has a time limit: on expiry the kernel records a code in
+// g_device_status, raises a CTA-wide abort flag, lets in-flight copies and
+// MMAs drain (with a limit), frees its TMEM and returns.
+#include <cuda.h>
+
 #include "agoq_device.cuh"
 #include "agoq_launch.h"
 
 namespace agoq {
 
-// Device-side status word: a GEMM pipeline wait that exceeds its iteration
-// limit records a non-zero code here instead of spinning forever.
+// Device-side status word: a pipeline wait that exceeds its time limit records
+// a non-zero code here instead of spinning forever.
 __device__ unsigned g_device_status;
 
-cudaError_t launch_wgrad_gemm(const void *, const void *, const float *, int, int, int, void *, bool,
-                              cudaStream_t) {
-    return cudaErrorNotSupported;
+namespace {
+
+constexpr int BM = 256, BN = 256, BK = 64, STAGES = 3;
+constexpr int kTmaWarp = 0, kMmaWarp = 1, kDeqWarp0 = 2, kDeqWarps = 8, kEpiWarp0 = 10,
+              kEpiWarps = 4;
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;   // 448
+constexpr int kAStage = BM * BK * 2;                      // 32 KiB of dY (BF16)
+constexpr int kBStage = BN * BK * 2;                      // 32 KiB of Xhat (BF16)
+constexpr int kCStage = BK * BN / 2;                      // 8 KiB of packed codes
+constexpr int kSStage = BK * 4 * 4;                       // 64 rows x 4 scales
+constexpr int kOffB = STAGES * kAStage;
+constexpr int kOffC = kOffB + STAGES * kBStage;
+constexpr int kOffS = kOffC + STAGES * kCStage;
+constexpr int kOffBar = kOffS + STAGES * kSStage;
+constexpr int kNumBars = 4 * STAGES + 3;
+constexpr int kOffMisc = kOffBar + 8 * kNumBars;
+constexpr int kSmemBytes = kOffMisc + 16 + 1024;          // + slack for 1024-byte alignment
+constexpr uint32_t kTmemCols = 512;
+constexpr unsigned kStatusTimeout = 1u;
+constexpr long long kWaitLimitCycles = 4000000000ll;      // about two seconds
+
+static_assert(kSmemBytes <= 232448, "shared memory budget");
+
+// ---------------------------------------------------------------- PTX wrappers
+__device__ __forceinline__ uint32_t smem_u32(const void *p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x,
+                                            int y) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
+          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
+          "=r"(v[31])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor (tcgen05 format) of an MN-major operand
+// stored in 128-byte-swizzled atoms of 8 K-rows x 64 BF16: `lbo` is the byte
+// distance between atoms along M/N, `sbo` between 8-row groups along K.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    uint64_t d = 0;
+    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= static_cast<uint64_t>(1) << 46;   // descriptor version for tcgen05
+    d |= static_cast<uint64_t>(2) << 61;   // 128-byte swizzle
+    return d;
+}
+
+// Instruction descriptor: kind::f16, BF16 A and B, FP32 D, A and B MN-major,
+// M = 128, N = 256.
+constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
+                            ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+
+struct Shared {
+    uint8_t *a, *b, *c;
+    float *s;
+    uint64_t *full_a, *full_x, *full_b, *empty, *tmem_full, *tmem_empty, *drain;
+    uint32_t *tmem_addr;
+    volatile int *abort;
+};
+
+// Wait for the phase of `bar` with parity `parity` to complete.  Returns false
+// if the CTA was told to abort or the wait ran past its time limit (which then
+// records the timeout and raises the abort flag).  `ignore_abort` is for the
+// final drains, which must run even after an abort.
+__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                         bool ignore_abort = false) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const long long t0 = clock64();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait(bar, parity)) return true;
+        if ((i & 255u) == 0u) {
+            if (!ignore_abort && *abort) return false;
+            if (clock64() - t0 > kWaitLimitCycles) {
+                *abort = 1;
+                atomicExch(&g_device_status, kStatusTimeout);
+                return false;
+            }
+        }
+    }
+}
+
+// The same wait for a whole warp: lane 0 polls, the outcome is broadcast, and
+// the warp leaves converged (the tcgen05 .sync.aligned instructions need that).
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+    const int lane = threadIdx.x & 31;
+    bool ok = true;
+    if (lane == 0) ok = wait_bar(bar, parity, abort);
+    ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    return ok;
+}
+
+// Dequantize one word of eight 4-bit codes (two's complement, element 2i in
+// the low nibble of byte i) with scale s into eight BF16:
+// bf16_rne(fl32(c * s)).  The code plus 8 is placed in the mantissa of 2^23
+// with a byte permute; subtracting 2^23 + 8 leaves c exactly.
+__device__ __forceinline__ uint4 dequant_word(uint32_t w, float s) {
+    const uint32_t v = w ^ 0x88888888u;                 // c + 8 in each nibble
+    const uint32_t ev = v & 0x0F0F0F0Fu;                // elements 0, 2, 4, 6
+    const uint32_t od = (v >> 4) & 0x0F0F0F0Fu;         // elements 1, 3, 5, 7
+    float y[8];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        const float fe = __uint_as_float(__byte_perm(ev, 0x4B000000u, 0x7540u + b));
+        const float fo = __uint_as_float(__byte_perm(od, 0x4B000000u, 0x7540u + b));
+        y[2 * b] = __fmul_rn(__fsub_rn(fe, 8388616.0f), s);
+        y[2 * b + 1] = __fmul_rn(__fsub_rn(fo, 8388616.0f), s);
+    }
+    return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                      pack_bf16x2(y[6], y[7]));
+}
+
+template <bool F32_OUT>
+__global__ void __launch_bounds__(kThreads, 1)
+    wgrad_gemm_int4_kernel(const __grid_constant__ CUtensorMap map_dy,
+                           const __grid_constant__ CUtensorMap map_xc,
+                           const __grid_constant__ CUtensorMap map_xs, void *__restrict__ dW, int M,
+                           int N, int K) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    Shared sh;
+    sh.a = smem;
+    sh.b = smem + kOffB;
+    sh.c = smem + kOffC;
+    sh.s = reinterpret_cast<float *>(smem + kOffS);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    sh.full_a = bars;
+    sh.full_x = bars + STAGES;
+    sh.full_b = bars + 2 * STAGES;
+    sh.empty = bars + 3 * STAGES;
+    sh.tmem_full = bars + 4 * STAGES;
+    sh.tmem_empty = bars + 4 * STAGES + 1;
+    sh.drain = bars + 4 * STAGES + 2;
+    sh.tmem_addr = reinterpret_cast<uint32_t *>(smem + kOffMisc);
+    sh.abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int n_tiles = N / BN, num_tiles = (M / BM) * n_tiles, kblocks = K / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&sh.full_a[s], 1);
+            mbar_init(&sh.full_x[s], 1);
+            mbar_init(&sh.full_b[s], kDeqWarps);
+            mbar_init(&sh.empty[s], 1);
+        }
+        mbar_init(sh.tmem_full, 1);
+        mbar_init(sh.tmem_empty, kEpiWarps);
+        mbar_init(sh.drain, 1);
+        *sh.abort = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    if (warp == kMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(sh.tmem_addr)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *sh.tmem_addr;
+
+    if (warp == kTmaWarp) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            uint32_t last_it[STAGES];       // last iteration that loaded each stage
+            for (int s = 0; s < STAGES; ++s) last_it[s] = 0xFFFFFFFFu;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+                const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+                const int sx = (n0 / 128) & ~3;
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_bar(&sh.empty[s], ph ^ 1u, sh.abort)) { ok = false; break; }
+                    const int k0 = kb * BK;
+                    mbar_expect_tx(&sh.full_a[s], kAStage);
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        tma_load_2d(sh.a + s * kAStage + c * 8192, &map_dy, &sh.full_a[s],
+                                    m0 + 64 * c, k0);
+                    mbar_expect_tx(&sh.full_x[s], kCStage + kSStage);
+                    tma_load_2d(sh.c + s * kCStage, &map_xc, &sh.full_x[s], n0 / 2, k0);
+                    tma_load_2d(sh.s + s * (kSStage / 4), &map_xs, &sh.full_x[s], sx, k0);
+                    last_it[s] = it;
+                }
+            }
+            // Drain: every issued load lands before the CTA may exit (a no-op
+            // unless the pipeline was aborted).
+            for (int s = 0; s < STAGES; ++s) {
+                if (last_it[s] == 0xFFFFFFFFu) continue;
+                const uint32_t ph = (last_it[s] / STAGES) & 1u;
+                wait_bar(&sh.full_a[s], ph, sh.abort, true);
+                wait_bar(&sh.full_x[s], ph, sh.abort, true);
+            }
+        }
+    } else if (warp == kMmaWarp) {
+        if (lane == 0) {
+            uint32_t it = 0, t = 0;
+            bool ok = true, issued = false;
+            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++t) {
+                if (!wait_bar(sh.tmem_empty, (t & 1u) ^ 1u, sh.abort)) { ok = false; break; }
+                tc_fence_after();
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int s = it % STAGES;
+                    const uint32_t ph = (it / STAGES) & 1u;
+                    if (!wait_bar(&sh.full_a[s], ph, sh.abort) || !wait_bar(&sh.full_b[s], ph, sh.abort)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t a0 = smem_u32(sh.a + s * kAStage);
+                    const uint32_t b0 = smem_u32(sh.b + s * kBStage);
+#pragma unroll
+                    for (int kk = 0; kk < BK / 16; ++kk) {
+                        const uint64_t bdesc = sw128_desc(b0 + kk * 2048, 8192, 1024);
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint64_t adesc = sw128_desc(a0 + h * 16384 + kk * 2048, 8192, 1024);
+                            umma_bf16(tmem_base + h * 256, adesc, bdesc, kIdesc,
+                                      (kb > 0 || kk > 0) ? 1u : 0u);
+                        }
+                    }
+                    issued = true;
+                    umma_commit(&sh.empty[s]);
+                }
+                if (!ok) break;
+                umma_commit(sh.tmem_full);
+            }
+            // Drain: all MMAs issued so far complete before TMEM is freed.
+            if (issued) {
+                umma_commit(sh.drain);
+                wait_bar(sh.drain, 0u, sh.abort, true);
+            }
+        }
+    } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
+        const int dt = threadIdx.x - kDeqWarp0 * 32;   // 0..255
+        const int wc = dt & 31;                         // code word column: N = 8wc .. 8wc+7
+        const int rg = dt >> 5;                         // rows rg, rg+8, ..., rg+56
+        const int chunk = wc >> 3, piece = wc & 7;
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+            const int n0 = (tile % n_tiles) * BN;
+            const int soff = ((n0 / 128) & 3) + (wc >> 4);   // scale column inside the 4-wide box
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % STAGES;
+                const uint32_t ph = (it / STAGES) & 1u;
+                if (!warp_wait(&sh.full_x[s], ph, sh.abort)) { ok = false; break; }
+                const uint32_t *codes = reinterpret_cast<const uint32_t *>(sh.c + s * kCStage);
+                const float *scales = sh.s + s * (kSStage / 4);
+                uint8_t *btile = sh.b + s * kBStage + chunk * 8192;
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    const int k = rg + 8 * i;
+                    const uint4 y = dequant_word(codes[k * 32 + wc], scales[k * 4 + soff]);
+                    *reinterpret_cast<uint4 *>(btile + k * 128 + ((piece ^ (k & 7)) << 4)) = y;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&sh.full_b[s]);
+            }
+        }
+    } else {
+        // epilogue warps: TMEM lane quarter q = warp % 4
+        const int q = warp & 3;
+        uint32_t t = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t) {
+            if (!warp_wait(sh.tmem_full, t & 1u, sh.abort)) break;
+            tc_fence_after();
+            const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+#pragma unroll 1
+            for (int h = 0; h < 2; ++h) {
+                const int row = m0 + h * 128 + 32 * q + lane;
+#pragma unroll 1
+                for (int cc = 0; cc < BN / 32; ++cc) {
+                    uint32_t v[32];
+                    tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + h * 256 + cc * 32, v);
+                    if constexpr (F32_OUT) {
+                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<float *>(dW) +
+                                                               (size_t)row * N + n0 + cc * 32);
+#pragma unroll
+                        for (int j = 0; j < 8; ++j)
+                            dst[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+                    } else {
+                        uint4 *dst = reinterpret_cast<uint4 *>(
+                            static_cast<uint16_t *>(dW) + (size_t)row * N + n0 + cc * 32);
+#pragma unroll
+                        for (int j = 0; j < 4; ++j) {
+                            const uint32_t w0 = pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1]));
+                            const uint32_t w1 = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
+                            const uint32_t w2 = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
+                            const uint32_t w3 = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
+                            dst[j] = make_uint4(w0, w1, w2, w3);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sh.tmem_empty);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    if (warp == kMmaWarp) {
+        __syncwarp();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(kTmemCols)
+                     : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
+                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
+                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static EncodeTiledFn fn = nullptr;
+    if (!fn) {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t dim0,
+               uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1,
+               CUtensorMapSwizzle swz) {
+    EncodeTiledFn fn = encode_fn();
+    if (!fn) return false;
+    const cuuint64_t dims[2] = {dim0, dim1};
+    const cuuint64_t strides[1] = {row_bytes};
+    const cuuint32_t box[2] = {box0, box1};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <bool F32_OUT>
+cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, int N, int K,
+                        void *dW, cudaStream_t st) {
+    CUtensorMap m_dy, m_xc, m_xs;
+    if (!encode_2d(&m_dy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, (uint64_t)M, (uint64_t)K,
+                   (uint64_t)M * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !encode_2d(&m_xc, CU_TENSOR_MAP_DATA_TYPE_UINT8, xc, (uint64_t)N / 2, (uint64_t)K,
+                   (uint64_t)N / 2, BN / 2, BK, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&m_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xs, (uint64_t)N / 128, (uint64_t)K,
+                   (uint64_t)(N / 128) * 4, 4, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    auto kernel = wgrad_gemm_int4_kernel<F32_OUT>;
+    static bool attr_set[kMaxDevices];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < kMaxDevices && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kSmemBytes);
+        if (e != cudaSuccess) return e;
+        attr_set[dev] = true;
+    }
+    const int num_tiles = (M / BM) * (N / BN);
+    const int grid = num_tiles < sm_count() ? num_tiles : sm_count();
+    kernel<<<grid, kThreads, kSmemBytes, st>>>(m_dy, m_xc, m_xs, dW, M, N, K);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_wgrad_gemm(const void *dY, const void *xc, const float *xs, int M, int N, int K,
+                              void *dW, bool f32_out, cudaStream_t st) {
+    return f32_out ? launch_impl<true>(dY, xc, xs, M, N, K, dW, st)
+                   : launch_impl<false>(dY, xc, xs, M, N, K, dW, st);
 }
 
 cudaError_t read_and_clear_device_status(cudaStream_t st, unsigned *status) {

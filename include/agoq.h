@@ -130,8 +130,9 @@ agoq_status agoq_reduce_fp8_shards(const void *shards_e4m3, const float *shard_s
  *   x_codes  : in, [K][N/2] bytes: row k is agoq_quant_act(bits=4) of X row k.
  *   x_scales : in, FP32 [K][N/128].
  *   dW_bf16  : out, BF16 [M][N] row-major.
- *   M and N must be multiples of 256, K a multiple of 64, all > 0
- *   (AGOQ_ERR_SHAPE otherwise).
+ *   M must be a multiple of 256, N of 512 (so that a row of scales spans a
+ *   multiple of 16 bytes) and K of 64, all > 0 (AGOQ_ERR_SHAPE otherwise).
+ *   The dY tile loads need dY 16-byte aligned; all pointers must be.
  */
 agoq_status agoq_wgrad_gemm_int4(const void *dY_bf16, const void *x_codes, const float *x_scales,
                                  int M, int N, int K, void *dW_bf16, void *stream);

@@ -92,13 +92,13 @@ def test_reduce_validation(L):
 
 def test_gemm_validation(L):
     for fn in (L.agoq_wgrad_gemm_int4, L.agoq_wgrad_gemm_int4_f32out):
-        assert fn(P(A), P(B), P(C), 100, 256, 64, P(C + (1 << 24)), None) == SHAPE
-        assert fn(P(A), P(B), P(C), 256, 128, 64, P(C + (1 << 24)), None) == SHAPE
-        assert fn(P(A), P(B), P(C), 256, 256, 32, P(C + (1 << 24)), None) == SHAPE
-        assert fn(P(A), P(B), P(C), 0, 256, 64, P(C + (1 << 24)), None) == SHAPE
-        assert fn(None, P(B), P(C), 256, 256, 64, P(C + (1 << 24)), None) == NULL
-        assert fn(P(A), P(B), P(C + 4), 256, 256, 64, P(C + (1 << 24)), None) == ALIGN
-        assert fn(P(A), P(B), P(C), 256, 256, 64, P(A), None) == ALIAS
+        assert fn(P(A), P(B), P(C), 100, 512, 64, P(C + (1 << 24)), None) == SHAPE
+        assert fn(P(A), P(B), P(C), 256, 256, 64, P(C + (1 << 24)), None) == SHAPE
+        assert fn(P(A), P(B), P(C), 256, 512, 32, P(C + (1 << 24)), None) == SHAPE
+        assert fn(P(A), P(B), P(C), 0, 512, 64, P(C + (1 << 24)), None) == SHAPE
+        assert fn(None, P(B), P(C), 256, 512, 64, P(C + (1 << 24)), None) == NULL
+        assert fn(P(A), P(B), P(C + 4), 256, 512, 64, P(C + (1 << 24)), None) == ALIGN
+        assert fn(P(A), P(B), P(C), 256, 512, 64, P(A), None) == ALIAS
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

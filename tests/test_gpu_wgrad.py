@@ -1,0 +1,103 @@
+"""GPU checks of the INT4-dequant-fused weight-gradient GEMM against the CPU
+oracle's binary64 product of the dequantized operands.
+
+Gates (the BF16 output cannot be compared with the unrounded product at 1e-3:
+rounding any value to BF16 alone costs about 1.6e-3 relative Frobenius):
+  * BF16 output vs bf16_rne(binary64 product): relative Frobenius <= 1e-3;
+  * FP32-output variant vs the binary64 product: relative Frobenius <= 1e-3,
+    and every entry within the binary32 summation bound K * 2^-23 * sum|terms|;
+  * a one-hot dY makes dW rows exactly the dequantized X rows (bit-exact).
+"""
+import numpy as np
+import pytest
+import torch
+
+from gradient_quantization_gb300 import agoq, synthetic
+from tests import gpu_util as G
+
+pytestmark = pytest.mark.gpu
+
+
+def _inputs(oracle, M, N, K, seed=4):
+    dy, x = synthetic.wgrad_inputs_np(seed=seed, M=M, N=N, K=K)
+    xc, xs = oracle.quant_act(x.reshape(-1), 4)
+    return dy, xc, xs
+
+
+def _bf16_round(a):
+    return torch.from_numpy(np.ascontiguousarray(a)).to(torch.bfloat16).double().numpy()
+
+
+def _rel_frob(got, ref):
+    return float(np.linalg.norm(got - ref) / np.linalg.norm(ref))
+
+
+def _abs_terms(oracle, dy, xc, xs, M, N, K):
+    """sum_k |dY[k][m] * Xhat[k][n]| in binary64 (for the per-entry bound)."""
+    dyv = np.abs((dy.astype(np.uint32) << 16).view(np.float32).astype(np.float64)).reshape(K, M)
+    xh = oracle.dequant_act(xc, xs, K * N, 4)
+    xhv = np.abs((xh.astype(np.uint32) << 16).view(np.float32).astype(np.float64)).reshape(K, N)
+    return dyv.T @ xhv
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 64), (256, 512, 128), (512, 1024, 192),
+                                   (768, 512, 320), (2560, 4096, 64)])
+def test_gemm_matches_fp64_product(oracle, M, N, K):
+    dy, xc, xs = _inputs(oracle, M, N, K)
+    dyd, xcd, xsd = G.dev_bf16(dy), G.dev(xc), G.dev(xs)
+    dwg = G.Guarded(M * N * 2, torch.bfloat16)
+    agoq.agoq_wgrad_gemm_int4(dyd, xcd, xsd, M, N, K, dwg.view)
+    agoq.agoq_device_status()
+    assert dwg.intact()
+    ref = oracle.wgrad_gemm_int4_f64(dy, xc, xs, M, N, K)
+    got = dwg.view.double().cpu().numpy().reshape(M, N)
+    assert _rel_frob(got, _bf16_round(ref)) <= 1e-3
+    f32 = agoq.agoq_wgrad_gemm_int4_f32out(dyd, xcd, xsd, M, N, K)
+    agoq.agoq_device_status()
+    got32 = f32.double().cpu().numpy()
+    assert _rel_frob(got32, ref) <= 1e-3
+    bound = K * 2.0 ** -23 * _abs_terms(oracle, dy, xc, xs, M, N, K) + 1e-30
+    assert (np.abs(got32 - ref) <= bound).all()
+
+
+def test_one_hot_rows_are_dequantized_rows(oracle):
+    M, N, K = 512, 1024, 256
+    _, xc, xs = _inputs(oracle, M, N, K, seed=9)
+    rng = np.random.default_rng(10)
+    pick = rng.integers(0, K, M)
+    dy = np.zeros((K, M), np.uint16)
+    dy[pick, np.arange(M)] = 0x3F80                     # 1.0
+    dw = agoq.agoq_wgrad_gemm_int4(G.dev_bf16(dy), G.dev(xc), G.dev(xs), M, N, K)
+    agoq.agoq_device_status()
+    xhat = oracle.dequant_act(xc, xs, K * N, 4).reshape(K, N)
+    assert np.array_equal(G.host_bits_bf16(dw).reshape(M, N), xhat[pick])
+
+
+def test_full_size_sampled_entries(oracle):
+    """11008 x 4096 x 8192 in the bench's launch configuration; 4096 sampled
+    entries against the oracle's binary64 dot products."""
+    M, N, K = synthetic.WGRAD_M, synthetic.WGRAD_N, synthetic.WGRAD_K
+    dy, x = synthetic.wgrad_inputs_torch(seed=4)
+    x_np = G.host_bits_bf16(x)
+    xc, xs = oracle.quant_act(x_np, 4)
+    dw = agoq.agoq_wgrad_gemm_int4(dy, G.dev(xc), G.dev(xs), M, N, K)
+    agoq.agoq_device_status()
+    rng = np.random.default_rng(11)
+    rows = rng.integers(0, M, 4096)
+    cols = rng.integers(0, N, 4096)
+    rows[:2], cols[:2] = [0, M - 1], [0, N - 1]
+    dy_np = G.host_bits_bf16(dy)
+    ref = oracle.wgrad_gemm_int4_f64_entries(dy_np, xc, xs, M, N, K, rows, cols)
+    got = dw.double().cpu().numpy()[rows, cols]
+    assert _rel_frob(got, _bf16_round(ref)) <= 1e-3
+    assert torch.isfinite(dw.float()).all()
+
+
+def test_repeatable_across_calls(oracle):
+    M, N, K = 512, 1024, 128
+    dy, xc, xs = _inputs(oracle, M, N, K, seed=12)
+    args = (G.dev_bf16(dy), G.dev(xc), G.dev(xs), M, N, K)
+    a = agoq.agoq_wgrad_gemm_int4(*args)
+    b = agoq.agoq_wgrad_gemm_int4(*args)
+    agoq.agoq_device_status()
+    assert torch.equal(a, b)
