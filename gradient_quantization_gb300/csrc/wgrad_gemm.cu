@@ -6,20 +6,31 @@
 //
 //   dW[M][N] = sum_k dY[k][m] * Xhat[k][n],  Xhat = bf16(fl32(code * scale))
 //
-// Blackwell design (sm_103a, one CTA per SM, persistent over 256x256 tiles):
-//   warp 0      TMA producer: per 64-deep k-block, the dY tile (256 M x 64 K,
-//               four 64x64 boxes, 128-byte swizzle), the packed 4-bit X codes
-//               (64 K rows x 128 bytes) and their scales (64 x 4 floats).
+// Blackwell design (sm_103a, one CTA per SM, persistent over 256x256 tiles),
+// per BK-deep k-block, with three independent shared-memory rings:
+//   A ring (NA stages)  the dY tile, 256 M x BK K as four 64-wide boxes with
+//                       128-byte swizzle, loaded by TMA;
+//   X ring (NX stages)  the packed 4-bit codes (BK rows x 128 bytes) and their
+//                       scales (BK x 4 floats), loaded by TMA;
+//   B ring (NB stages)  Xhat (BF16), written by the dequantizers in the
+//                       MN-major 128-byte-swizzled layout the MMA reads.
+// Only the A and X rings hold loads in flight, so they get most of the shared
+// memory; the B ring only bridges dequantization and the MMA.
+//   warp 0      TMA producer of the A ring.
 //   warp 1      TMEM owner and MMA issuer: one elected thread issues, per
-//               k-block, 4 x 2 tcgen05.mma kind::f16 (M=128, N=256, K=16; both
-//               operands MN-major, BF16 in, FP32 accumulate) into two 256-column
-//               accumulators (rows 0-127 and 128-255 of the tile) that fill the
-//               512 TMEM columns; tcgen05.commit frees the stage.
-//   warps 2-9   dequantizers: codes -> Xhat (BF16) written straight into the
-//               MN-major, 128-byte-swizzled B tile the MMA reads, then
-//               fence.proxy.async and an mbarrier arrive.
-//   warps 10-13 epilogue: tcgen05.ld of the accumulators (each warp its 32-lane
+//               k-block, (BK/16) x 2 tcgen05.mma kind::f16 (M=128, N=256, K=16;
+//               both operands MN-major, BF16 in, FP32 accumulate) into two
+//               256-column accumulators (rows 0-127 and 128-255 of the tile)
+//               that fill the 512 TMEM columns; tcgen05.commit frees the A and
+//               B stages.
+//   warp 2      TMA producer of the X ring.
+//   warps 3-18  dequantizers: codes -> Xhat into the B ring, fence.proxy.async,
+//               mbarrier arrives that publish the B stage and release the X
+//               stage (after its codes have been consumed).
+//   warps 19-22 epilogue: tcgen05.ld of the accumulators (each warp its 32-lane
 //               quarter), BF16 round-to-nearest-even (or FP32), global stores.
+// Waiting threads sleep in mbarrier.try_wait (suspend-time hint) rather than
+// spin, so the dequantizers keep the issue slots.
 // Every mbarrier wait has a time limit: on expiry the kernel records a code in
 // g_device_status, raises a CTA-wide abort flag, lets in-flight copies and
 // MMAs drain (with a limit), frees its TMEM and returns.
@@ -36,19 +47,55 @@ __device__ unsigned g_device_status;
 
 namespace {
 
-constexpr int BM = 256, BN = 256, BK = 64, STAGES = 3;
-constexpr int kTmaWarp = 0, kMmaWarp = 1, kDeqWarp0 = 2, kDeqWarps = 8, kEpiWarp0 = 10,
-              kEpiWarps = 4;
-constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;   // 448
+#ifndef AGOQ_GEMM_BK
+#define AGOQ_GEMM_BK 64
+#endif
+#ifndef AGOQ_GEMM_NX
+#define AGOQ_GEMM_NX 3
+#endif
+#ifndef AGOQ_GEMM_NB
+#define AGOQ_GEMM_NB 3
+#endif
+#ifndef AGOQ_GEMM_NA
+#define AGOQ_GEMM_NA 3
+#endif
+#ifndef AGOQ_GEMM_DEQ_GROUPS
+#define AGOQ_GEMM_DEQ_GROUPS 1
+#endif
+#ifndef AGOQ_GEMM_WAIT_HINT_NS
+#define AGOQ_GEMM_WAIT_HINT_NS 20000
+#endif
+
+constexpr int BM = 256, BN = 256, BK = AGOQ_GEMM_BK;
+constexpr int NA = AGOQ_GEMM_NA, NX = AGOQ_GEMM_NX, NB = AGOQ_GEMM_NB;
+constexpr int kChunk = BK * 128;                          // bytes of one 64-wide M/N chunk of a stage
+constexpr int kTmaWarp = 0, kMmaWarp = 1, kTmaXWarp = 2, kDeqWarp0 = 3, kDeqWarps = 16,
+              kEpiWarp0 = kDeqWarp0 + kDeqWarps, kEpiWarps = 4;
+constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;   // 736
+// The dequantizers form kDeqGroups groups that take k-blocks in turn, so each
+// warp has kDeqGroups MMA periods to turn its stage around.
+constexpr int kDeqGroups = AGOQ_GEMM_DEQ_GROUPS;
+constexpr int kGroupWarps = kDeqWarps / kDeqGroups;
+constexpr int kDeqRows = BK / kGroupWarps;                // k-rows per dequant thread per stage
+static_assert(kDeqRows * kGroupWarps == BK, "every k-row of a stage is dequantized exactly once");
+static_assert(NB >= kDeqGroups + 1, "B ring must cover the stages being dequantized plus one");
+// A waiter may only be one phase behind the barrier it polls (a parity test
+// cannot tell "two phases ahead" from "complete").  Each X stage must therefore
+// always be consumed by the same dequant group, whose waits then see every
+// phase of it in order.  (The B ring is safe for NB >= 2: when a group reaches
+// k-block i, the MMA has retired block i - 2*NB, so empty_b is never two
+// phases behind.)
+static_assert(NX % kDeqGroups == 0, "X ring depth must be a multiple of the dequant group count");
 constexpr int kAStage = BM * BK * 2;                      // 32 KiB of dY (BF16)
 constexpr int kBStage = BN * BK * 2;                      // 32 KiB of Xhat (BF16)
 constexpr int kCStage = BK * BN / 2;                      // 8 KiB of packed codes
-constexpr int kSStage = BK * 4 * 4;                       // 64 rows x 4 scales
-constexpr int kOffB = STAGES * kAStage;
-constexpr int kOffC = kOffB + STAGES * kBStage;
-constexpr int kOffS = kOffC + STAGES * kCStage;
-constexpr int kOffBar = kOffS + STAGES * kSStage;
-constexpr int kNumBars = 4 * STAGES + 3;
+constexpr int kSStage = BK * 4 * 4;                       // BK rows x 4 scales
+static_assert(BK % 16 == 0 && BK >= 16 && BK <= 256, "k-block depth");
+constexpr int kOffB = NA * kAStage;
+constexpr int kOffC = kOffB + NB * kBStage;
+constexpr int kOffS = kOffC + NX * kCStage;
+constexpr int kOffBar = kOffS + NX * kSStage;
+constexpr int kNumBars = 2 * NA + 2 * NX + 2 * NB + 3;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;          // + slack for 1024-byte alignment
 constexpr uint32_t kTmemCols = 512;
@@ -76,14 +123,16 @@ __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
+// Test the phase; if it is not complete the thread may sleep up to `hint_ns`
+// (it wakes as soon as the phase completes).
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
     uint32_t ok;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
         : "memory");
     return ok != 0;
 }
@@ -157,7 +206,8 @@ constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1
 struct Shared {
     uint8_t *a, *b, *c;
     float *s;
-    uint64_t *full_a, *full_x, *full_b, *empty, *tmem_full, *tmem_empty, *drain;
+    uint64_t *full_a, *empty_a, *full_x, *empty_x, *full_b, *empty_b;
+    uint64_t *tmem_full, *tmem_empty, *drain;
     uint32_t *tmem_addr;
     volatile int *abort;
 };
@@ -167,51 +217,70 @@ struct Shared {
 // records the timeout and raises the abort flag).  `ignore_abort` is for the
 // final drains, which must run even after an abort.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                         bool ignore_abort = false) {
-    if (mbar_try_wait(bar, parity)) return true;
+                                         bool ignore_abort = false,
+                                         uint32_t hint_ns = AGOQ_GEMM_WAIT_HINT_NS) {
+    if (AGOQ_GEMM_WAIT_HINT_NS == 0) hint_ns = 0;
+    if (mbar_try_wait(bar, parity, hint_ns)) return true;
     const long long t0 = clock64();
-    for (uint32_t i = 1;; ++i) {
-        if (mbar_try_wait(bar, parity)) return true;
-        if ((i & 255u) == 0u) {
-            if (!ignore_abort && *abort) return false;
-            if (clock64() - t0 > kWaitLimitCycles) {
-                *abort = 1;
-                atomicExch(&g_device_status, kStatusTimeout);
-                return false;
-            }
+    for (;;) {
+        if (mbar_try_wait(bar, parity, hint_ns)) return true;
+        if (!ignore_abort && *abort) return false;
+        if (clock64() - t0 > kWaitLimitCycles) {
+            *abort = 1;
+            atomicExch(&g_device_status, kStatusTimeout);
+            return false;
         }
     }
 }
 
 // The same wait for a whole warp: lane 0 polls, the outcome is broadcast, and
 // the warp leaves converged (the tcgen05 .sync.aligned instructions need that).
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort) {
+__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
+                                          uint32_t hint_ns = AGOQ_GEMM_WAIT_HINT_NS) {
     const int lane = threadIdx.x & 31;
     bool ok = true;
-    if (lane == 0) ok = wait_bar(bar, parity, abort);
+    if (lane == 0) ok = wait_bar(bar, parity, abort, false, hint_ns);
     ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
     __syncwarp();
     return ok;
 }
 
+// Two IEEE round-to-nearest binary32 operations per instruction (sm_100+).
+__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t pair(uint32_t lo, uint32_t hi) {
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+
 // Dequantize one word of eight 4-bit codes (two's complement, element 2i in
 // the low nibble of byte i) with scale s into eight BF16:
 // bf16_rne(fl32(c * s)).  The code plus 8 is placed in the mantissa of 2^23
-// with a byte permute; subtracting 2^23 + 8 leaves c exactly.
+// with a byte permute; subtracting 2^23 + 8 leaves c exactly; the multiply by
+// s is the one rounding before the BF16 conversion.
 __device__ __forceinline__ uint4 dequant_word(uint32_t w, float s) {
     const uint32_t v = w ^ 0x88888888u;                 // c + 8 in each nibble
     const uint32_t ev = v & 0x0F0F0F0Fu;                // elements 0, 2, 4, 6
     const uint32_t od = (v >> 4) & 0x0F0F0F0Fu;         // elements 1, 3, 5, 7
-    float y[8];
+    const uint64_t bias = pair(__float_as_uint(8388616.0f), __float_as_uint(8388616.0f));
+    const uint64_t ss = pair(__float_as_uint(s), __float_as_uint(s));
+    uint32_t out[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-        const float fe = __uint_as_float(__byte_perm(ev, 0x4B000000u, 0x7540u + b));
-        const float fo = __uint_as_float(__byte_perm(od, 0x4B000000u, 0x7540u + b));
-        y[2 * b] = __fmul_rn(__fsub_rn(fe, 8388616.0f), s);
-        y[2 * b + 1] = __fmul_rn(__fsub_rn(fo, 8388616.0f), s);
+        const uint32_t fe = __byte_perm(ev, 0x4B000000u, 0x7540u + b);   // element 2b
+        const uint32_t fo = __byte_perm(od, 0x4B000000u, 0x7540u + b);   // element 2b+1
+        const uint64_t y = f32x2_mul(f32x2_sub(pair(fe, fo), bias), ss);
+        out[b] = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(y)),
+                             __uint_as_float(static_cast<uint32_t>(y >> 32)));
     }
-    return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                      pack_bf16x2(y[6], y[7]));
+    return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 template <bool F32_OUT>
@@ -230,12 +299,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh.s = reinterpret_cast<float *>(smem + kOffS);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     sh.full_a = bars;
-    sh.full_x = bars + STAGES;
-    sh.full_b = bars + 2 * STAGES;
-    sh.empty = bars + 3 * STAGES;
-    sh.tmem_full = bars + 4 * STAGES;
-    sh.tmem_empty = bars + 4 * STAGES + 1;
-    sh.drain = bars + 4 * STAGES + 2;
+    sh.empty_a = sh.full_a + NA;
+    sh.full_x = sh.empty_a + NA;
+    sh.empty_x = sh.full_x + NX;
+    sh.full_b = sh.empty_x + NX;
+    sh.empty_b = sh.full_b + NB;
+    sh.tmem_full = sh.empty_b + NB;
+    sh.tmem_empty = sh.tmem_full + 1;
+    sh.drain = sh.tmem_empty + 1;
     sh.tmem_addr = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     sh.abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
@@ -243,11 +314,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int n_tiles = N / BN, num_tiles = (M / BM) * n_tiles, kblocks = K / BK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < STAGES; ++s) {
+        for (int s = 0; s < NA; ++s) {
             mbar_init(&sh.full_a[s], 1);
+            mbar_init(&sh.empty_a[s], 1);
+        }
+        for (int s = 0; s < NX; ++s) {
             mbar_init(&sh.full_x[s], 1);
-            mbar_init(&sh.full_b[s], kDeqWarps);
-            mbar_init(&sh.empty[s], 1);
+            mbar_init(&sh.empty_x[s], kGroupWarps);
+        }
+        for (int s = 0; s < NB; ++s) {
+            mbar_init(&sh.full_b[s], kGroupWarps);
+            mbar_init(&sh.empty_b[s], 1);
         }
         mbar_init(sh.tmem_full, 1);
         mbar_init(sh.tmem_empty, kEpiWarps);
@@ -267,38 +344,42 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *sh.tmem_addr;
 
-    if (warp == kTmaWarp) {
+    if (warp == kTmaWarp || warp == kTmaXWarp) {
+        // Producers: warp 0 fills the A ring, warp 2 the X ring.
         if (lane == 0) {
+            const bool is_a = warp == kTmaWarp;
+            const int depth = is_a ? NA : NX;
+            uint64_t *full = is_a ? sh.full_a : sh.full_x;
+            uint64_t *empty = is_a ? sh.empty_a : sh.empty_x;
             uint32_t it = 0;
-            uint32_t last_it[STAGES];       // last iteration that loaded each stage
-            for (int s = 0; s < STAGES; ++s) last_it[s] = 0xFFFFFFFFu;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
                 const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
                 const int sx = (n0 / 128) & ~3;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_bar(&sh.empty[s], ph ^ 1u, sh.abort)) { ok = false; break; }
+                    const int s = it % depth;
+                    const uint32_t ph = (it / depth) & 1u;
+                    if (!wait_bar(&empty[s], ph ^ 1u, sh.abort)) { ok = false; break; }
                     const int k0 = kb * BK;
-                    mbar_expect_tx(&sh.full_a[s], kAStage);
+                    if (is_a) {
+                        mbar_expect_tx(&full[s], kAStage);
 #pragma unroll
-                    for (int c = 0; c < 4; ++c)
-                        tma_load_2d(sh.a + s * kAStage + c * 8192, &map_dy, &sh.full_a[s],
-                                    m0 + 64 * c, k0);
-                    mbar_expect_tx(&sh.full_x[s], kCStage + kSStage);
-                    tma_load_2d(sh.c + s * kCStage, &map_xc, &sh.full_x[s], n0 / 2, k0);
-                    tma_load_2d(sh.s + s * (kSStage / 4), &map_xs, &sh.full_x[s], sx, k0);
-                    last_it[s] = it;
+                        for (int c = 0; c < 4; ++c)
+                            tma_load_2d(sh.a + s * kAStage + c * kChunk, &map_dy, &full[s],
+                                        m0 + 64 * c, k0);
+                    } else {
+                        mbar_expect_tx(&full[s], kCStage + kSStage);
+                        tma_load_2d(sh.c + s * kCStage, &map_xc, &full[s], n0 / 2, k0);
+                        tma_load_2d(sh.s + s * (kSStage / 4), &map_xs, &full[s], sx, k0);
+                    }
                 }
             }
             // Drain: every issued load lands before the CTA may exit (a no-op
-            // unless the pipeline was aborted).
-            for (int s = 0; s < STAGES; ++s) {
-                if (last_it[s] == 0xFFFFFFFFu) continue;
-                const uint32_t ph = (last_it[s] / STAGES) & 1u;
-                wait_bar(&sh.full_a[s], ph, sh.abort, true);
-                wait_bar(&sh.full_x[s], ph, sh.abort, true);
+            // unless the pipeline was aborted).  Iteration it-1-d was the last
+            // load into stage (it-1-d) % depth.
+            for (int d = 0; d < depth && d < (int)it; ++d) {
+                const uint32_t last = it - 1 - d;
+                wait_bar(&full[last % depth], (last / depth) & 1u, sh.abort, true);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -309,27 +390,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!wait_bar(sh.tmem_empty, (t & 1u) ^ 1u, sh.abort)) { ok = false; break; }
                 tc_fence_after();
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const int s = it % STAGES;
-                    const uint32_t ph = (it / STAGES) & 1u;
-                    if (!wait_bar(&sh.full_a[s], ph, sh.abort) || !wait_bar(&sh.full_b[s], ph, sh.abort)) {
+                    const int sa = it % NA, sb = it % NB;
+                    if (!wait_bar(&sh.full_a[sa], (it / NA) & 1u, sh.abort) ||
+                        !wait_bar(&sh.full_b[sb], (it / NB) & 1u, sh.abort)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t a0 = smem_u32(sh.a + s * kAStage);
-                    const uint32_t b0 = smem_u32(sh.b + s * kBStage);
+                    const uint32_t a0 = smem_u32(sh.a + sa * kAStage);
+                    const uint32_t b0 = smem_u32(sh.b + sb * kBStage);
 #pragma unroll
                     for (int kk = 0; kk < BK / 16; ++kk) {
-                        const uint64_t bdesc = sw128_desc(b0 + kk * 2048, 8192, 1024);
+                        const uint64_t bdesc = sw128_desc(b0 + kk * 2048, kChunk, 1024);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
-                            const uint64_t adesc = sw128_desc(a0 + h * 16384 + kk * 2048, 8192, 1024);
+                            const uint64_t adesc =
+                                sw128_desc(a0 + h * 2 * kChunk + kk * 2048, kChunk, 1024);
                             umma_bf16(tmem_base + h * 256, adesc, bdesc, kIdesc,
                                       (kb > 0 || kk > 0) ? 1u : 0u);
                         }
                     }
                     issued = true;
-                    umma_commit(&sh.empty[s]);
+                    umma_commit(&sh.empty_a[sa]);
+                    umma_commit(&sh.empty_b[sb]);
                 }
                 if (!ok) break;
                 umma_commit(sh.tmem_full);
@@ -341,9 +424,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
-        const int dt = threadIdx.x - kDeqWarp0 * 32;   // 0..255
-        const int wc = dt & 31;                         // code word column: N = 8wc .. 8wc+7
-        const int rg = dt >> 5;                         // rows rg, rg+8, ..., rg+56
+        const int group = (warp - kDeqWarp0) / kGroupWarps;
+        const int wc = lane;                            // code word column: N = 8wc .. 8wc+7
+        const int rg = (warp - kDeqWarp0) % kGroupWarps; // rows rg, rg+kGroupWarps, ...
         const int chunk = wc >> 3, piece = wc & 7;
         uint32_t it = 0;
         bool ok = true;
@@ -351,21 +434,36 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int n0 = (tile % n_tiles) * BN;
             const int soff = ((n0 / 128) & 3) + (wc >> 4);   // scale column inside the 4-wide box
             for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                const int s = it % STAGES;
-                const uint32_t ph = (it / STAGES) & 1u;
-                if (!warp_wait(&sh.full_x[s], ph, sh.abort)) { ok = false; break; }
-                const uint32_t *codes = reinterpret_cast<const uint32_t *>(sh.c + s * kCStage);
-                const float *scales = sh.s + s * (kSStage / 4);
-                uint8_t *btile = sh.b + s * kBStage + chunk * 8192;
+                if ((int)(it % kDeqGroups) != group) continue;   // the other group's k-block
+                const int sx = it % NX, sb = it % NB;
+                if (!warp_wait(&sh.full_x[sx], (it / NX) & 1u, sh.abort)) { ok = false; break; }
+                const uint32_t *codes = reinterpret_cast<const uint32_t *>(sh.c + sx * kCStage);
+                const float *scales = sh.s + sx * (kSStage / 4);
+                uint32_t w[kDeqRows];
+                float sc[kDeqRows];
 #pragma unroll
-                for (int i = 0; i < 8; ++i) {
-                    const int k = rg + 8 * i;
-                    const uint4 y = dequant_word(codes[k * 32 + wc], scales[k * 4 + soff]);
+                for (int i = 0; i < kDeqRows; ++i) {
+                    const int k = rg + kGroupWarps * i;
+                    w[i] = codes[k * 32 + wc];
+                    sc[i] = scales[k * 4 + soff];
+                }
+                if (!warp_wait(&sh.empty_b[sb], ((it / NB) & 1u) ^ 1u, sh.abort)) { ok = false; break; }
+                uint8_t *btile = sh.b + sb * kBStage + chunk * kChunk;
+#pragma unroll
+                for (int i = 0; i < kDeqRows; ++i) {
+                    const int k = rg + kGroupWarps * i;
+                    const uint4 y = dequant_word(w[i], sc[i]);
                     *reinterpret_cast<uint4 *>(btile + k * 128 + ((piece ^ (k & 7)) << 4)) = y;
                 }
                 asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
-                if (lane == 0) mbar_arrive(&sh.full_b[s]);
+                // The X stage is released only now: its codes have been consumed
+                // (the B stores depend on them), so no shared-memory load of it
+                // can still be in flight when the next TMA load overwrites it.
+                if (lane == 0) {
+                    mbar_arrive(&sh.full_b[sb]);
+                    mbar_arrive(&sh.empty_x[sx]);
+                }
             }
         }
     } else {
@@ -373,7 +471,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int q = warp & 3;
         uint32_t t = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t) {
-            if (!warp_wait(sh.tmem_full, t & 1u, sh.abort)) break;
+            if (!warp_wait(sh.tmem_full, t & 1u, sh.abort, 1000000)) break;
             tc_fence_after();
             const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
 #pragma unroll 1
