@@ -513,6 +513,43 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+PROFILE_CASES = ("accum", "reduce8", "reduce8_nocount", "reduce64", "gemm")
+
+
+def profile_case(name, launches=3):
+    """Launch one kernel of the path a few times on a mid-size workload (for
+    ncu captures: a few hundred MB on the device, no timing output)."""
+    import torch
+    from gradient_quantization_gb300 import agoq, synthetic
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    if name == "accum":
+        n = 1 << 28
+        m = torch.zeros(n, dtype=torch.uint8, device=dev)
+        ms = torch.zeros(n // 128, dtype=torch.float32, device=dev)
+        g = synthetic.quangrad_grad_torch(seed=2, step=0, device=dev, n=n)
+        for _ in range(launches):
+            agoq.agoq_grad_accum_fp8(m, ms, g)
+    elif name.startswith("reduce"):
+        W, n = (64, 1 << 22) if name == "reduce64" else (8, 1 << 25)
+        sh = torch.randint(0, 126, (W, n), dtype=torch.uint8, device=dev)
+        sh |= (torch.randint(0, 2, (W, n), dtype=torch.uint8, device=dev) << 7)
+        ss = torch.rand((W, n // 128), device=dev) * 1e-4
+        cnt = None if name.endswith("nocount") else torch.zeros(1, dtype=torch.int64, device=dev)
+        for _ in range(launches):
+            agoq.agoq_reduce_fp8_shards(sh, ss, W, n, naive_overflow_count=cnt)
+    elif name == "gemm":
+        M, N, K = synthetic.WGRAD_M, synthetic.WGRAD_N, synthetic.WGRAD_K
+        dy, xg = synthetic.wgrad_inputs_torch(seed=4, device=dev)
+        xc, xs = agoq.agoq_quant_act(xg, 4)
+        for _ in range(launches):
+            agoq.agoq_wgrad_gemm_int4(dy, xc, xs, M, N, K)
+        agoq.agoq_device_status()
+    else:
+        raise SystemExit("unknown profile case %r (choose from %s)" % (name, ", ".join(PROFILE_CASES)))
+    torch.cuda.synchronize()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
@@ -525,10 +562,14 @@ def main(argv=None):
                     help="target CPU seconds of the oracle baseline sample")
     ap.add_argument("--ref-step-seconds", type=float, default=4.0,
                     help="target seconds of one reference-arm step")
+    ap.add_argument("--profile-case", choices=PROFILE_CASES,
+                    help="only launch one kernel a few times on a mid-size workload (for ncu)")
     args = ap.parse_args(argv)
     args.warmup = max(3, args.warmup)     # at least 3 untimed warm-up steps
     args.steps = max(1, args.steps)
-    if args.impl == "reference":
+    if args.profile_case:
+        profile_case(args.profile_case)
+    elif args.impl == "reference":
         reference_arm(args)
     else:
         gpu_arm(args)

@@ -36,13 +36,26 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
 }
 
 // Two E4M3 codes (bits 0-7 and 8-15 of v) to binary32, exactly (every E4M3
-// value is an FP16 value, and every FP16 value a binary32 value).
+// value is an FP16 value, and every FP16 value a binary32 value).  The FP16 to
+// binary32 step is either a conversion or, with AGOQ_F16_WIDEN_BY_ADD, the
+// mixed-precision addition f32(h) + (-0), which is exact and returns h's value
+// (including its signed zero) unchanged.
+#ifndef AGOQ_F16_WIDEN_BY_ADD
+#define AGOQ_F16_WIDEN_BY_ADD 0
+#endif
 __device__ __forceinline__ void e4m3x2_to_f32(uint32_t v, float &lo, float &hi) {
     uint32_t h2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)v));
+#if AGOQ_F16_WIDEN_BY_ADD
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "add.rn.f32.f16 %0, a, 0f80000000;\n\tadd.rn.f32.f16 %1, b, 0f80000000;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(h2));
+#else
     asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
         : "=f"(lo), "=f"(hi)
         : "r"(h2));
+#endif
 }
 
 // Code i (bits 8i..8i+7) of a word of four E4M3 codes, as a binary32 whose
@@ -119,6 +132,46 @@ __device__ __forceinline__ float e4m3_round_f32(float t) {
     return __fsub_rn(__fadd_rn(t, c), c);
 }
 
+// ---- packed binary32 pairs (sm_100+): two IEEE round-to-nearest operations
+// per instruction, bit-identical to the scalar __fadd_rn/__fsub_rn/__fmul_rn.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ uint64_t u32x2(uint32_t lo, uint32_t hi) {
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+
+// Largest |value| of the BF16 pairs in w[0..N-1], as a binary32 (exact: the
+// maximum of BF16 magnitudes is a BF16 value).
+template <int N>
+__device__ __forceinline__ float bf16_absmax(const uint32_t *w) {
+    uint32_t m = w[0] & 0x7FFF7FFFu;
+#pragma unroll
+    for (int i = 1; i < N; ++i) {
+        uint32_t r;
+        asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(w[i] & 0x7FFF7FFFu));
+        m = r;
+    }
+    return fmaxf(bf16_lo(m), bf16_hi(m));
+}
+
 // ---- block reductions --------------------------------------------------------
 // Maximum over the 16 lanes of a half warp (lanes 0-15 or 16-31).
 __device__ __forceinline__ float halfwarp_max(float v) {
@@ -184,6 +237,40 @@ __device__ __forceinline__ void integer_codes8(const float x[8], float s, uint32
     } else {
 #pragma unroll
         for (int i = 0; i < 8; ++i) code_bits[i] = 0u;
+    }
+}
+
+// integer_codes8 for N values (N even) sharing one scale, with the reciprocal
+// shortcut evaluated on packed pairs.  Same contract and proof as above.
+template <int QMAX, int N>
+__device__ __forceinline__ void integer_codes_n(const float *x, float s, uint32_t *code_bits) {
+    if (s >= 0x1p-126f) {
+        const float r = __frcp_rn(s);
+        const uint64_t r2 = f32x2(r, r), m2 = f32x2(kRoundMagic, kRoundMagic);
+        float dmax = 0.0f;
+#pragma unroll
+        for (int i = 0; i < N; i += 2) {
+            const uint64_t q = mul_f32x2(f32x2(x[i], x[i + 1]), r2);
+            const uint64_t t = add_f32x2(q, m2);
+            const uint64_t d = sub_f32x2(q, sub_f32x2(t, m2));
+            dmax = fmaxf(dmax, fmaxf(fabsf(lo_f32(d)), fabsf(hi_f32(d))));
+            code_bits[i] = static_cast<uint32_t>(t);
+            code_bits[i + 1] = static_cast<uint32_t>(t >> 32);
+        }
+        if (dmax > 0.5f - 0x1p-14f) {
+#pragma unroll
+            for (int i = 0; i < N; ++i)
+                code_bits[i] = __float_as_uint(__fadd_rn(__fdiv_rn(x[i], s), kRoundMagic));
+        }
+    } else if (s > 0.0f) {
+#pragma unroll
+        for (int i = 0; i < N; ++i) {
+            const float k = fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -(float)QMAX), (float)QMAX);
+            code_bits[i] = __float_as_uint(__fadd_rn(k, kRoundMagic));
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < N; ++i) code_bits[i] = 0u;
     }
 }
 

@@ -4,17 +4,17 @@
 // "Dynamic Bit-width Compensation (DBCA-PP)" for 5, 6 and 8 bits;
 // "Herberekening versus Caching" for reading the stored input back).
 //
-// Work decomposition: a half warp owns one 128-element block; lane j of the
-// half holds elements 8j..8j+7 (one 16-byte BF16 load or store), so a warp
-// moves two adjacent blocks (512 contiguous bytes of BF16) per memory
-// instruction, and UNROLL block pairs are in flight per warp.  The block
-// absmax is a 4-step shuffle reduction inside the half warp.  Lane j's eight
-// codes form a chunk of 8*bits bits at bit 8*bits*j of the block record:
-//   bits 4, 8 : the chunk is one aligned 4- or 8-byte word;
-//   bits 5    : 4 lanes (160 bits) fill 5 aligned words; lane q of the group
-//               writes word q from its own chunk and lane q-1's, and lane 3
-//               also writes word 4;
-//   bits 6    : 2 lanes (96 bits) fill 3 words the same way.
+// Work decomposition: an octet of lanes owns one 128-element block; lane j
+// holds chunks j and j+8 (elements 8j..8j+7 and 64+8j..64+8j+7, two 16-byte
+// BF16 loads or stores), so a warp covers four adjacent blocks and UNROLL
+// such groups are in flight per warp.  The block absmax is a bf16x2 max over
+// the lane's words and a 3-step shuffle reduction inside the octet.  A chunk
+// of eight codes is 8*bits bits at bit 8*bits*c of the block record:
+//   bits 4, 8 : one aligned 4- or 8-byte word;
+//   bits 5    : 4 chunks (160 bits) fill 5 aligned words; the lane holding
+//               chunk q of the group writes word q from its chunk and the
+//               previous lane's, and the lane of chunk 3 also writes word 4;
+//   bits 6    : 2 chunks (96 bits) fill 3 words the same way.
 // The grid is one resident wave striding over the blocks.
 #include "agoq_device.cuh"
 #include "agoq_launch.h"
@@ -46,55 +46,33 @@ __device__ __forceinline__ void st_stream(uint4 *p, uint4 v) {
                  : "memory");
 }
 
-// Quantize the lane's 8 BF16 values (block scale reduced over the half warp).
+// Write one 8-code chunk set into the block record `rec` (4*BITS words):
+// lane j of the octet holds chunk (j + 8*set) as (lo, hi).  Every lane of the
+// warp must call this (5 and 6 bits shuffle); `valid` gates the stores.
 template <int BITS>
-__device__ __forceinline__ void quantize_lane(const uint4 v, float &scale, uint32_t &lo,
-                                              uint32_t &hi) {
-    constexpr int kQmax = (1 << (BITS - 1)) - 1;
-    float f[8];
-    f[0] = bf16_lo(v.x); f[1] = bf16_hi(v.x);
-    f[2] = bf16_lo(v.y); f[3] = bf16_hi(v.y);
-    f[4] = bf16_lo(v.z); f[5] = bf16_hi(v.z);
-    f[6] = bf16_lo(v.w); f[7] = bf16_hi(v.w);
-    float am = fabsf(f[0]);
-#pragma unroll
-    for (int i = 1; i < 8; ++i) am = fmaxf(am, fabsf(f[i]));
-    am = halfwarp_max(am);
-    const float s = __fdiv_rn(am, (float)kQmax);   // +0 for an all-zero block
-    scale = s;
-    uint32_t cb[8];
-    integer_codes8<kQmax>(f, s, cb);
-    pack_fields8<BITS>(cb, lo, hi);
-}
-
-// Write the lane's chunk (lo, hi) into the block record `rec` (4*BITS words).
-// Every lane of the warp must call this (5 and 6 bits shuffle); `valid` gates
-// the stores.
-template <int BITS>
-__device__ __forceinline__ void store_chunk(uint32_t *rec, int lane, uint32_t lo, uint32_t hi,
-                                            bool valid) {
-    const int j = lane & 15;
+__device__ __forceinline__ void store_chunk_set(uint32_t *rec, int j, int set, uint32_t lo,
+                                                uint32_t hi, bool valid) {
+    const int c = j + 8 * set;                              // chunk index in the block
     if constexpr (BITS == 4) {
-        if (valid) rec[j] = lo;
+        if (valid) rec[c] = lo;
     } else if constexpr (BITS == 8) {
-        if (valid) reinterpret_cast<uint2 *>(rec)[j] = make_uint2(lo, hi);
+        if (valid) reinterpret_cast<uint2 *>(rec)[c] = make_uint2(lo, hi);
     } else if constexpr (BITS == 5) {
-        // group of 4 lanes g = j/4, q = j%4; chunk q starts at bit 40q of the group's 160 bits
+        // 4 chunks (160 bits) fill 5 words; chunk q of the group starts at bit 40q
         const uint32_t plo = __shfl_up_sync(kFull, lo, 1);
         const uint32_t phi = __shfl_up_sync(kFull, hi, 1);
-        const int q = j & 3;
-        uint32_t *w = rec + 5 * (j >> 2);
+        const int q = c & 3;
+        uint32_t *w = rec + 5 * (c >> 2);
         const uint32_t word = q == 0 ? lo : (__funnelshift_rc(plo, phi, 40 - 8 * q) | (lo << (8 * q)));
         if (valid) {
             w[q] = word;
             if (q == 3) w[4] = __funnelshift_r(lo, hi, 8);
         }
-    } else {  // BITS == 6: group of 2 lanes, chunk q starts at bit 48q of 96 bits
+    } else {  // BITS == 6: 2 chunks (96 bits) fill 3 words; chunk 1 starts at bit 48
         const uint32_t phi = __shfl_up_sync(kFull, hi, 1);
-        const int q = j & 1;
-        uint32_t *w = rec + 3 * (j >> 1);
+        uint32_t *w = rec + 3 * (c >> 1);
         if (valid) {
-            if (q == 0) {
+            if ((c & 1) == 0) {
                 w[0] = lo;
             } else {
                 w[1] = phi | (lo << 16);
@@ -104,48 +82,72 @@ __device__ __forceinline__ void store_chunk(uint32_t *rec, int lane, uint32_t lo
     }
 }
 
+// A block is owned by an octet of lanes; lane j holds elements 8j..8j+7
+// (chunk j) and 64+8j..64+8j+7 (chunk j+8), so each 16-byte load instruction
+// of a warp reads 4 x 128 contiguous bytes and the per-block work (absmax
+// shuffles, scale division, reciprocal) is shared by 16 elements per lane.
 template <int BITS, int UNROLL>
 __global__ void __launch_bounds__(kThreads) laaq_quant_kernel(const uint4 *__restrict__ x,
                                                               uint32_t *__restrict__ codes,
                                                               float *__restrict__ scales,
                                                               int64_t nblocks) {
     constexpr int kWords = 4 * BITS;
+    constexpr int kQmax = (1 << (BITS - 1)) - 1;
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4, j = lane & 15;
+    const int oct = lane >> 3, j = lane & 7;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t base = warp * (2 * UNROLL); base < nblocks; base += nwarps * (2 * UNROLL)) {
-        uint4 v[UNROLL];
+    for (int64_t base = warp * (4 * UNROLL); base < nblocks; base += nwarps * (4 * UNROLL)) {
+        uint4 va[UNROLL], vb[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = base + 2 * u + half;
-            v[u] = blk < nblocks ? ld_stream(x + blk * 16 + j) : make_uint4(0, 0, 0, 0);
+            const int64_t blk = base + 4 * u + oct;
+            if (blk < nblocks) {
+                va[u] = ld_stream(x + blk * 16 + j);
+                vb[u] = ld_stream(x + blk * 16 + 8 + j);
+            } else {
+                va[u] = vb[u] = make_uint4(0, 0, 0, 0);
+            }
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = base + 2 * u + half;
+            const int64_t blk = base + 4 * u + oct;
             const bool valid = blk < nblocks;
-            float s;
+            const uint32_t w[8] = {va[u].x, va[u].y, va[u].z, va[u].w,
+                                   vb[u].x, vb[u].y, vb[u].z, vb[u].w};
+            const float am = octet_max(bf16_absmax<8>(w));
+            const float s = __fdiv_rn(am, (float)kQmax);   // +0 for an all-zero block
+            float f[16];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                f[2 * i] = bf16_lo(w[i]);
+                f[2 * i + 1] = bf16_hi(w[i]);
+            }
+            uint32_t cb[16];
+            integer_codes_n<kQmax, 16>(f, s, cb);
             uint32_t lo, hi;
-            quantize_lane<BITS>(v[u], s, lo, hi);
-            store_chunk<BITS>(codes + blk * kWords, lane, lo, hi, valid);
+            uint32_t *rec = codes + blk * kWords;
+            pack_fields8<BITS>(cb, lo, hi);
+            store_chunk_set<BITS>(rec, j, 0, lo, hi, valid);
+            pack_fields8<BITS>(cb + 8, lo, hi);
+            store_chunk_set<BITS>(rec, j, 1, lo, hi, valid);
             if (valid && j == 0) scales[blk] = s;
         }
     }
 }
 
-// The lane's 8*BITS-bit chunk of a block record, as (lo, hi).
+// Chunk c (8 codes, 8*BITS bits at bit 8*BITS*c) of a block record, as (lo, hi).
 template <int BITS>
-__device__ __forceinline__ void load_chunk(const uint32_t *rec, int j, uint32_t &lo, uint32_t &hi) {
+__device__ __forceinline__ void load_chunk(const uint32_t *rec, int c, uint32_t &lo, uint32_t &hi) {
     if constexpr (BITS == 4) {
-        lo = __ldg(rec + j);
+        lo = __ldg(rec + c);
         hi = 0u;
     } else if constexpr (BITS == 8) {
-        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(rec) + j);
+        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(rec) + c);
         lo = w.x;
         hi = w.y;
     } else {
-        const int byte = BITS * j;                          // chunk starts at this byte
+        const int byte = BITS * c;                          // chunk starts at this byte
         const uint32_t a = __ldg(rec + (byte >> 2));
         const uint32_t b = __ldg(rec + (byte >> 2) + 1);    // still inside the record
         const int sh = 8 * (byte & 3);
@@ -154,13 +156,19 @@ __device__ __forceinline__ void load_chunk(const uint32_t *rec, int j, uint32_t 
     }
 }
 
+// bf16(fl32(c_i * s)) for the 8 codes of a chunk; the code values are made
+// exact by field_value's bias trick and multiplied in packed pairs.
 template <int BITS>
-__device__ __forceinline__ uint4 dequantize_lane(uint32_t lo, uint32_t hi, float s) {
-    float y[8];
+__device__ __forceinline__ uint4 dequantize_chunk(uint32_t lo, uint32_t hi, float s) {
+    const uint64_t s2 = f32x2(s, s);
+    uint32_t out[4];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) y[i] = __fmul_rn(field_value<BITS>(lo, hi, i * BITS), s);
-    return make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
-                      pack_bf16x2(y[6], y[7]));
+    for (int p = 0; p < 4; ++p) {
+        const uint64_t y = mul_f32x2(f32x2(field_value<BITS>(lo, hi, 2 * p * BITS),
+                                           field_value<BITS>(lo, hi, (2 * p + 1) * BITS)), s2);
+        out[p] = pack_bf16x2(lo_f32(y), hi_f32(y));
+    }
+    return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
 template <int BITS, int UNROLL>
@@ -170,27 +178,31 @@ __global__ void __launch_bounds__(kThreads) laaq_dequant_kernel(const uint32_t *
                                                                 int64_t nblocks) {
     constexpr int kWords = 4 * BITS;
     const int lane = threadIdx.x & 31;
-    const int half = lane >> 4, j = lane & 15;
+    const int oct = lane >> 3, j = lane & 7;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t base = warp * (2 * UNROLL); base < nblocks; base += nwarps * (2 * UNROLL)) {
-        uint32_t lo[UNROLL], hi[UNROLL];
+    for (int64_t base = warp * (4 * UNROLL); base < nblocks; base += nwarps * (4 * UNROLL)) {
+        uint32_t alo[UNROLL], ahi[UNROLL], blo[UNROLL], bhi[UNROLL];
         float s[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = base + 2 * u + half;
+            const int64_t blk = base + 4 * u + oct;
             if (blk < nblocks) {
-                load_chunk<BITS>(codes + blk * kWords, j, lo[u], hi[u]);
+                load_chunk<BITS>(codes + blk * kWords, j, alo[u], ahi[u]);
+                load_chunk<BITS>(codes + blk * kWords, j + 8, blo[u], bhi[u]);
                 s[u] = __ldg(scales + blk);
             } else {
-                lo[u] = hi[u] = 0u;
+                alo[u] = ahi[u] = blo[u] = bhi[u] = 0u;
                 s[u] = 0.0f;
             }
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = base + 2 * u + half;
-            if (blk < nblocks) st_stream(y + blk * 16 + j, dequantize_lane<BITS>(lo[u], hi[u], s[u]));
+            const int64_t blk = base + 4 * u + oct;
+            if (blk < nblocks) {
+                st_stream(y + blk * 16 + j, dequantize_chunk<BITS>(alo[u], ahi[u], s[u]));
+                st_stream(y + blk * 16 + 8 + j, dequantize_chunk<BITS>(blo[u], bhi[u], s[u]));
+            }
         }
     }
 }
@@ -207,7 +219,7 @@ cudaError_t quant_bits(const void *x, int64_t nblocks, void *codes, float *scale
     constexpr int kU = AGOQ_QUANT_UNROLL;
     static int cache[kMaxDevices];
     auto k = laaq_quant_kernel<BITS, kU>;
-    const int64_t per_cta = 2 * kU * (kThreads / 32);
+    const int64_t per_cta = 4 * kU * (kThreads / 32);
     k<<<resident_grid(k, cache, (nblocks + per_cta - 1) / per_cta), kThreads, 0, st>>>(
         static_cast<const uint4 *>(x), static_cast<uint32_t *>(codes), scales, nblocks);
     return cudaGetLastError();
@@ -219,7 +231,7 @@ cudaError_t dequant_bits(const void *codes, const float *scales, int64_t nblocks
     constexpr int kU = AGOQ_DEQUANT_UNROLL;
     static int cache[kMaxDevices];
     auto k = laaq_dequant_kernel<BITS, kU>;
-    const int64_t per_cta = 2 * kU * (kThreads / 32);
+    const int64_t per_cta = 4 * kU * (kThreads / 32);
     k<<<resident_grid(k, cache, (nblocks + per_cta - 1) / per_cta), kThreads, 0, st>>>(
         static_cast<const uint32_t *>(codes), scales, static_cast<uint4 *>(y), nblocks);
     return cudaGetLastError();

@@ -23,7 +23,7 @@
 #define AGOQ_E4M3_DECODE_CVT 1
 #endif
 #ifndef AGOQ_E4M3_REQUANT_FAST
-#define AGOQ_E4M3_REQUANT_FAST 0
+#define AGOQ_E4M3_REQUANT_FAST 1
 #endif
 #ifndef AGOQ_NAIVE_ROUND_CVT
 #define AGOQ_NAIVE_ROUND_CVT 1

@@ -245,21 +245,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     return ok;
 }
 
-// Two IEEE round-to-nearest binary32 operations per instruction (sm_100+).
-__device__ __forceinline__ uint64_t f32x2_sub(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t f32x2_mul(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t pair(uint32_t lo, uint32_t hi) {
-    return (static_cast<uint64_t>(hi) << 32) | lo;
-}
-
 // Dequantize one word of eight 4-bit codes (two's complement, element 2i in
 // the low nibble of byte i) with scale s into eight BF16:
 // bf16_rne(fl32(c * s)).  The code plus 8 is placed in the mantissa of 2^23
@@ -269,16 +254,15 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, float s) {
     const uint32_t v = w ^ 0x88888888u;                 // c + 8 in each nibble
     const uint32_t ev = v & 0x0F0F0F0Fu;                // elements 0, 2, 4, 6
     const uint32_t od = (v >> 4) & 0x0F0F0F0Fu;         // elements 1, 3, 5, 7
-    const uint64_t bias = pair(__float_as_uint(8388616.0f), __float_as_uint(8388616.0f));
-    const uint64_t ss = pair(__float_as_uint(s), __float_as_uint(s));
+    const uint64_t bias = f32x2(8388616.0f, 8388616.0f);
+    const uint64_t ss = f32x2(s, s);
     uint32_t out[4];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
         const uint32_t fe = __byte_perm(ev, 0x4B000000u, 0x7540u + b);   // element 2b
         const uint32_t fo = __byte_perm(od, 0x4B000000u, 0x7540u + b);   // element 2b+1
-        const uint64_t y = f32x2_mul(f32x2_sub(pair(fe, fo), bias), ss);
-        out[b] = pack_bf16x2(__uint_as_float(static_cast<uint32_t>(y)),
-                             __uint_as_float(static_cast<uint32_t>(y >> 32)));
+        const uint64_t y = mul_f32x2(sub_f32x2(u32x2(fe, fo), bias), ss);
+        out[b] = pack_bf16x2(lo_f32(y), hi_f32(y));
     }
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
