@@ -47,10 +47,13 @@ METRIC = "HBM GB/s and Gelem/s per quant kernel; fraction of GB300 HBM/tensor pe
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-# dram__bytes_read.sum + dram__bytes_write.sum per launch of the dominant kernel,
-# from the ncu capture summarised in profiles/; None until one is taken for the
-# current kernel build.
-DOMINANT_TRAFFIC_BYTES = {}
+# dram__bytes_read.sum + dram__bytes_write.sum per launch, from the ncu captures
+# summarised in profiles/ (laaq_quant_b5_dbca_8192x4096_8192x11008.md); valid only
+# while those kernels are unchanged -- remove an entry when its kernel changes.
+DOMINANT_TRAFFIC_BYTES = {
+    "quant_b5_silu_in": 180433152 + 10434048,
+    "quant_b5_rmsnorm_in": 67141888 + 2043392,
+}
 
 
 def act_bytes(n, bits):
