@@ -157,6 +157,12 @@ __device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
     asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
     return d;
 }
+// a*b + c per lane with a single rounding (fused multiply-add).
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
 
 // Largest |value| of the BF16 pairs in w[0..N-1], as a binary32 (exact: the
 // maximum of BF16 magnitudes is a BF16 value).
@@ -240,24 +246,37 @@ __device__ __forceinline__ void integer_codes8(const float x[8], float s, uint32
     }
 }
 
-// integer_codes8 for N values (N even) sharing one scale, with the reciprocal
-// shortcut evaluated on packed pairs.  Same contract and proof as above.
+// Integer codes of N values (N even) sharing the scale s: the same result as
+// integer_codes8, code = clamp(rne_int(fl(x/s)), -qmax, qmax), with a cheaper
+// shortcut.  With r = fl(1/s) and r+- = fl(r * (1 +- 2^-20)), each value gives
+// t+- = fl(x * r+- + 1.5*2^23) by one fused multiply-add: the exact product
+// plus the magic constant, rounded once, i.e. x*r+- rounded to an integer held
+// in the low mantissa bits.  r+- exceed and undercut 1/s by at least 14*2^-24
+// relative (two roundings of 2^-24 each), while fl(x/s) is within 2^-24 of x/s;
+// so for |x/s| >= 1/4 the binary32 quotient lies strictly between x*r- and x*r+,
+// and rounding (monotonic) maps it between t- and t+.  When t- == t+ for all N
+// values that common integer is the code; otherwise the N quotients are formed
+// with IEEE division.  Values with |x/s| < 1/4 give 0 on every route.  The code
+// never exceeds qmax: |x * r+| <= qmax (1 + 2^-19) < qmax + 1/2.  Subnormal s
+// takes the division and an explicit clamp; s = 0 gives zero codes.
 template <int QMAX, int N>
 __device__ __forceinline__ void integer_codes_n(const float *x, float s, uint32_t *code_bits) {
     if (s >= 0x1p-126f) {
         const float r = __frcp_rn(s);
-        const uint64_t r2 = f32x2(r, r), m2 = f32x2(kRoundMagic, kRoundMagic);
-        float dmax = 0.0f;
+        const float rhi = __fmaf_rn(r, 0x1p-20f, r), rlo = __fmaf_rn(r, -0x1p-20f, r);
+        const uint64_t rhi2 = f32x2(rhi, rhi), rlo2 = f32x2(rlo, rlo);
+        const uint64_t m2 = f32x2(kRoundMagic, kRoundMagic);
+        uint64_t differ = 0;
 #pragma unroll
         for (int i = 0; i < N; i += 2) {
-            const uint64_t q = mul_f32x2(f32x2(x[i], x[i + 1]), r2);
-            const uint64_t t = add_f32x2(q, m2);
-            const uint64_t d = sub_f32x2(q, sub_f32x2(t, m2));
-            dmax = fmaxf(dmax, fmaxf(fabsf(lo_f32(d)), fabsf(hi_f32(d))));
-            code_bits[i] = static_cast<uint32_t>(t);
-            code_bits[i + 1] = static_cast<uint32_t>(t >> 32);
+            const uint64_t xx = f32x2(x[i], x[i + 1]);
+            const uint64_t th = fma_f32x2(xx, rhi2, m2);
+            const uint64_t tl = fma_f32x2(xx, rlo2, m2);
+            differ |= th ^ tl;
+            code_bits[i] = static_cast<uint32_t>(th);
+            code_bits[i + 1] = static_cast<uint32_t>(th >> 32);
         }
-        if (dmax > 0.5f - 0x1p-14f) {
+        if (differ) {
 #pragma unroll
             for (int i = 0; i < N; ++i)
                 code_bits[i] = __float_as_uint(__fadd_rn(__fdiv_rn(x[i], s), kRoundMagic));
@@ -275,23 +294,38 @@ __device__ __forceinline__ void integer_codes_n(const float *x, float s, uint32_
 }
 
 // Pack the low BITS bits of 8 words into a 64-bit little-endian chunk held as
-// two 32-bit words (field i at bit i*BITS); positions are compile-time.
+// two 32-bit words (field i at bit i*BITS).  8 bits: byte permutes gather the
+// low bytes.  4 bits: byte permutes gather the even and the odd elements' low
+// bytes, and one shift and one three-input logic op interleave their nibbles
+// (element 2j in the low nibble of byte j).  5 and 6 bits: compile-time shifts.
 template <int BITS>
 __device__ __forceinline__ void pack_fields8(const uint32_t w[8], uint32_t &lo, uint32_t &hi) {
-    constexpr uint32_t kMask = (1u << BITS) - 1u;
-    lo = 0u;
-    hi = 0u;
+    if constexpr (BITS == 8) {
+        lo = __byte_perm(__byte_perm(w[0], w[1], 0x0040), __byte_perm(w[2], w[3], 0x0040), 0x5410);
+        hi = __byte_perm(__byte_perm(w[4], w[5], 0x0040), __byte_perm(w[6], w[7], 0x0040), 0x5410);
+    } else if constexpr (BITS == 4) {
+        const uint32_t ev =
+            __byte_perm(__byte_perm(w[0], w[2], 0x0040), __byte_perm(w[4], w[6], 0x0040), 0x5410);
+        const uint32_t od =
+            __byte_perm(__byte_perm(w[1], w[3], 0x0040), __byte_perm(w[5], w[7], 0x0040), 0x5410);
+        lo = (ev & 0x0F0F0F0Fu) | ((od << 4) & 0xF0F0F0F0u);
+        hi = 0u;
+    } else {
+        constexpr uint32_t kMask = (1u << BITS) - 1u;
+        lo = 0u;
+        hi = 0u;
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const uint32_t f = w[i] & kMask;
-        const int pos = i * BITS;
-        if (pos + BITS <= 32) {
-            lo |= f << pos;
-        } else if (pos >= 32) {
-            hi |= f << (pos - 32);
-        } else {
-            lo |= f << pos;
-            hi |= f >> (32 - pos);
+        for (int i = 0; i < 8; ++i) {
+            const uint32_t f = w[i] & kMask;
+            const int pos = i * BITS;
+            if (pos + BITS <= 32) {
+                lo |= f << pos;
+            } else if (pos >= 32) {
+                hi |= f << (pos - 32);
+            } else {
+                lo |= f << pos;
+                hi |= f >> (32 - pos);
+            }
         }
     }
 }

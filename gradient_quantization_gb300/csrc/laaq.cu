@@ -25,6 +25,13 @@
 #ifndef AGOQ_DEQUANT_UNROLL
 #define AGOQ_DEQUANT_UNROLL 4
 #endif
+#ifndef AGOQ_QUANT_MIN_CTAS
+#define AGOQ_QUANT_MIN_CTAS 4
+#endif
+#ifndef AGOQ_DEQUANT_MIN_CTAS
+#define AGOQ_DEQUANT_MIN_CTAS 1
+#endif
+
 
 namespace agoq {
 namespace {
@@ -82,12 +89,39 @@ __device__ __forceinline__ void store_chunk_set(uint32_t *rec, int j, int set, u
     }
 }
 
+// Integer codes of 16 BF16 values (8 words) for a block scale s >= 2^-96:
+// code = rne_int(fl(x / s)).  The binary32 quotient is formed with Markstein's
+// correction of the reciprocal product (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): r = fl(1/s), q = fl(x*r), rho = fma(-q, s, x) (exact),
+// q' = fma(rho, r, q); then q' + 1.5*2^23 rounds it to an integer.  For BF16
+// x with |x| <= absmax and s = fl(absmax/qmax) >= 2^-96, rne_int(q') equals
+// rne_int(fl(x/s)) for every x, absmax and qmax in {7, 15, 31, 127}: checked
+// exhaustively against IEEE division (tests/test_gpu_laaq_exhaustive.py runs
+// the same check through the library).  Below 2^-96 the residual can fall
+// into the subnormal range and the correction can miss a tie, so those blocks
+// take integer_codes_n.  Codes stay within +-qmax because q' = fl(x/s).
+__device__ __forceinline__ void corrected_codes16(const uint32_t w[8], float s, uint32_t cb[16]) {
+    const float r = __frcp_rn(s);
+    const uint64_t r2 = f32x2(r, r), ns2 = f32x2(-s, -s);
+    const uint64_t m2 = f32x2(kRoundMagic, kRoundMagic);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint64_t xx = f32x2(bf16_lo(w[i]), bf16_hi(w[i]));
+        const uint64_t q = mul_f32x2(xx, r2);
+        const uint64_t rho = fma_f32x2(q, ns2, xx);
+        const uint64_t t = add_f32x2(fma_f32x2(rho, r2, q), m2);
+        cb[2 * i] = static_cast<uint32_t>(t);
+        cb[2 * i + 1] = static_cast<uint32_t>(t >> 32);
+    }
+}
+
 // A block is owned by an octet of lanes; lane j holds elements 8j..8j+7
 // (chunk j) and 64+8j..64+8j+7 (chunk j+8), so each 16-byte load instruction
 // of a warp reads 4 x 128 contiguous bytes and the per-block work (absmax
 // shuffles, scale division, reciprocal) is shared by 16 elements per lane.
 template <int BITS, int UNROLL>
-__global__ void __launch_bounds__(kThreads) laaq_quant_kernel(const uint4 *__restrict__ x,
+__global__ void __launch_bounds__(kThreads, AGOQ_QUANT_MIN_CTAS) laaq_quant_kernel(const uint4 *__restrict__ x,
                                                               uint32_t *__restrict__ codes,
                                                               float *__restrict__ scales,
                                                               int64_t nblocks) {
@@ -109,29 +143,47 @@ __global__ void __launch_bounds__(kThreads) laaq_quant_kernel(const uint4 *__res
                 va[u] = vb[u] = make_uint4(0, 0, 0, 0);
             }
         }
+        uint32_t w[UNROLL][8];
+        float s[UNROLL];
+        bool fast = true;
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            w[u][0] = va[u].x; w[u][1] = va[u].y; w[u][2] = va[u].z; w[u][3] = va[u].w;
+            w[u][4] = vb[u].x; w[u][5] = vb[u].y; w[u][6] = vb[u].z; w[u][7] = vb[u].w;
+            const float am = octet_max(bf16_absmax<8>(w[u]));
+            s[u] = __fdiv_rn(am, (float)kQmax);           // +0 for an all-zero block
+            fast &= s[u] >= 0x1p-96f;
+        }
+        uint32_t cb[UNROLL][16];
+        if (fast) {
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) corrected_codes16(w[u], s[u], cb[u]);
+        } else {
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                float f[16];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) {
+                    f[2 * i] = bf16_lo(w[u][i]);
+                    f[2 * i + 1] = bf16_hi(w[u][i]);
+                }
+                if (s[u] >= 0x1p-96f)
+                    corrected_codes16(w[u], s[u], cb[u]);
+                else
+                    integer_codes_n<kQmax, 16>(f, s[u], cb[u]);
+            }
+        }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t blk = base + 4 * u + oct;
             const bool valid = blk < nblocks;
-            const uint32_t w[8] = {va[u].x, va[u].y, va[u].z, va[u].w,
-                                   vb[u].x, vb[u].y, vb[u].z, vb[u].w};
-            const float am = octet_max(bf16_absmax<8>(w));
-            const float s = __fdiv_rn(am, (float)kQmax);   // +0 for an all-zero block
-            float f[16];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                f[2 * i] = bf16_lo(w[i]);
-                f[2 * i + 1] = bf16_hi(w[i]);
-            }
-            uint32_t cb[16];
-            integer_codes_n<kQmax, 16>(f, s, cb);
             uint32_t lo, hi;
             uint32_t *rec = codes + blk * kWords;
-            pack_fields8<BITS>(cb, lo, hi);
+            pack_fields8<BITS>(cb[u], lo, hi);
             store_chunk_set<BITS>(rec, j, 0, lo, hi, valid);
-            pack_fields8<BITS>(cb + 8, lo, hi);
+            pack_fields8<BITS>(cb[u] + 8, lo, hi);
             store_chunk_set<BITS>(rec, j, 1, lo, hi, valid);
-            if (valid && j == 0) scales[blk] = s;
+            if (valid && j == 0) scales[blk] = s[u];
         }
     }
 }
@@ -172,7 +224,7 @@ __device__ __forceinline__ uint4 dequantize_chunk(uint32_t lo, uint32_t hi, floa
 }
 
 template <int BITS, int UNROLL>
-__global__ void __launch_bounds__(kThreads) laaq_dequant_kernel(const uint32_t *__restrict__ codes,
+__global__ void __launch_bounds__(kThreads, AGOQ_DEQUANT_MIN_CTAS) laaq_dequant_kernel(const uint32_t *__restrict__ codes,
                                                                 const float *__restrict__ scales,
                                                                 uint4 *__restrict__ y,
                                                                 int64_t nblocks) {
