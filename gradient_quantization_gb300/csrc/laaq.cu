@@ -23,7 +23,7 @@
 #define AGOQ_QUANT_UNROLL 2
 #endif
 #ifndef AGOQ_DEQUANT_UNROLL
-#define AGOQ_DEQUANT_UNROLL 4
+#define AGOQ_DEQUANT_UNROLL 2
 #endif
 #ifndef AGOQ_QUANT_MIN_CTAS
 #define AGOQ_QUANT_MIN_CTAS 4
@@ -223,19 +223,16 @@ __device__ __forceinline__ uint4 dequantize_chunk(uint32_t lo, uint32_t hi, floa
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// Loads of one dequantization batch: UNROLL groups of 4 blocks per warp.
 template <int BITS, int UNROLL>
-__global__ void __launch_bounds__(kThreads, AGOQ_DEQUANT_MIN_CTAS) laaq_dequant_kernel(const uint32_t *__restrict__ codes,
-                                                                const float *__restrict__ scales,
-                                                                uint4 *__restrict__ y,
-                                                                int64_t nblocks) {
-    constexpr int kWords = 4 * BITS;
-    const int lane = threadIdx.x & 31;
-    const int oct = lane >> 3, j = lane & 7;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t base = warp * (4 * UNROLL); base < nblocks; base += nwarps * (4 * UNROLL)) {
-        uint32_t alo[UNROLL], ahi[UNROLL], blo[UNROLL], bhi[UNROLL];
-        float s[UNROLL];
+struct DequantBatch {
+    uint32_t alo[UNROLL], ahi[UNROLL], blo[UNROLL], bhi[UNROLL];
+    float s[UNROLL];
+
+    __device__ __forceinline__ void load(const uint32_t *__restrict__ codes,
+                                         const float *__restrict__ scales, int64_t base, int oct,
+                                         int j, int64_t nblocks) {
+        constexpr int kWords = 4 * BITS;
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t blk = base + 4 * u + oct;
@@ -248,14 +245,37 @@ __global__ void __launch_bounds__(kThreads, AGOQ_DEQUANT_MIN_CTAS) laaq_dequant_
                 s[u] = 0.0f;
             }
         }
+    }
+};
+
+// Software-pipelined: the next batch's code and scale loads are issued before
+// the current batch is converted and stored, so loads stay in flight.
+template <int BITS, int UNROLL>
+__global__ void __launch_bounds__(kThreads, AGOQ_DEQUANT_MIN_CTAS) laaq_dequant_kernel(const uint32_t *__restrict__ codes,
+                                                                const float *__restrict__ scales,
+                                                                uint4 *__restrict__ y,
+                                                                int64_t nblocks) {
+    const int lane = threadIdx.x & 31;
+    const int oct = lane >> 3, j = lane & 7;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t stride = nwarps * (4 * UNROLL);
+    int64_t base = warp * (4 * UNROLL);
+    if (base >= nblocks) return;
+    DequantBatch<BITS, UNROLL> cur, nxt;
+    cur.load(codes, scales, base, oct, j, nblocks);
+    for (; base < nblocks; base += stride) {
+        const bool more = base + stride < nblocks;
+        if (more) nxt.load(codes, scales, base + stride, oct, j, nblocks);
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t blk = base + 4 * u + oct;
             if (blk < nblocks) {
-                st_stream(y + blk * 16 + j, dequantize_chunk<BITS>(alo[u], ahi[u], s[u]));
-                st_stream(y + blk * 16 + 8 + j, dequantize_chunk<BITS>(blo[u], bhi[u], s[u]));
+                st_stream(y + blk * 16 + j, dequantize_chunk<BITS>(cur.alo[u], cur.ahi[u], cur.s[u]));
+                st_stream(y + blk * 16 + 8 + j, dequantize_chunk<BITS>(cur.blo[u], cur.bhi[u], cur.s[u]));
             }
         }
+        if (more) cur = nxt;
     }
 }
 
