@@ -15,6 +15,15 @@ namespace agoq {
 constexpr int kBlock = 128;          // elements per quantization block
 constexpr float kE4M3Max = 448.0f;   // largest finite E4M3 magnitude
 
+// ---- programmatic dependent launch -------------------------------------------
+// Wait until the grids this one depends on have completed and their memory is
+// visible, then let the next grid in the stream be scheduled (its own wait
+// keeps it from touching memory before this grid completes).
+__device__ __forceinline__ void pdl_wait_and_release() {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ---- BF16 ------------------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
@@ -289,15 +298,18 @@ __device__ __forceinline__ void integer_codes_n(const float *x, float s, uint32_
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < N; ++i) code_bits[i] = 0u;
+        for (int i = 0; i < N; ++i) code_bits[i] = __float_as_uint(kRoundMagic);   // code 0
     }
 }
 
 // Pack the low BITS bits of 8 words into a 64-bit little-endian chunk held as
-// two 32-bit words (field i at bit i*BITS).  8 bits: byte permutes gather the
-// low bytes.  4 bits: byte permutes gather the even and the odd elements' low
-// bytes, and one shift and one three-input logic op interleave their nibbles
-// (element 2j in the low nibble of byte j).  5 and 6 bits: compile-time shifts.
+// two 32-bit words (field i at bit i*BITS, two's complement).
+//   8 bits: byte permutes gather the low bytes.
+//   4 bits: byte permutes gather the even and the odd elements' low bytes, and
+//           one shift and one logic op interleave their nibbles (element 2j in
+//           the low nibble of byte j).
+//   5, 6 bits: compile-time shifts (measured faster than integer multiply-add
+//           packing on this GPU).
 template <int BITS>
 __device__ __forceinline__ void pack_fields8(const uint32_t w[8], uint32_t &lo, uint32_t &hi) {
     if constexpr (BITS == 8) {

@@ -27,6 +27,26 @@ int resident_per_sm(K kernel, int threads, size_t smem, int *cache) {
     return cache[dev];
 }
 
+// Launch `kernel` with programmatic stream serialization: it may be scheduled
+// while the previous kernel on the stream is finishing.  Every kernel launched
+// this way begins with pdl_wait() (griddepcontrol.wait) before touching global
+// memory, so it still observes all effects of the work before it in the stream.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem,
+                       cudaStream_t st, Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 cudaError_t launch_laaq_quant(const void *x, int64_t n, int bits, void *codes, float *scales,
                               cudaStream_t st);
 cudaError_t launch_laaq_dequant(const void *codes, const float *scales, int64_t n, int bits,

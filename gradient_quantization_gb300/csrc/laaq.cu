@@ -125,6 +125,7 @@ __global__ void __launch_bounds__(kThreads, AGOQ_QUANT_MIN_CTAS) laaq_quant_kern
                                                               uint32_t *__restrict__ codes,
                                                               float *__restrict__ scales,
                                                               int64_t nblocks) {
+    pdl_wait_and_release();
     constexpr int kWords = 4 * BITS;
     constexpr int kQmax = (1 << (BITS - 1)) - 1;
     const int lane = threadIdx.x & 31;
@@ -255,6 +256,7 @@ __global__ void __launch_bounds__(kThreads, AGOQ_DEQUANT_MIN_CTAS) laaq_dequant_
                                                                 const float *__restrict__ scales,
                                                                 uint4 *__restrict__ y,
                                                                 int64_t nblocks) {
+    pdl_wait_and_release();
     const int lane = threadIdx.x & 31;
     const int oct = lane >> 3, j = lane & 7;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -292,9 +294,9 @@ cudaError_t quant_bits(const void *x, int64_t nblocks, void *codes, float *scale
     static int cache[kMaxDevices];
     auto k = laaq_quant_kernel<BITS, kU>;
     const int64_t per_cta = 4 * kU * (kThreads / 32);
-    k<<<resident_grid(k, cache, (nblocks + per_cta - 1) / per_cta), kThreads, 0, st>>>(
-        static_cast<const uint4 *>(x), static_cast<uint32_t *>(codes), scales, nblocks);
-    return cudaGetLastError();
+    return launch_pdl(k, resident_grid(k, cache, (nblocks + per_cta - 1) / per_cta), kThreads, 0,
+                      st, static_cast<const uint4 *>(x), static_cast<uint32_t *>(codes), scales,
+                      nblocks);
 }
 
 template <int BITS>
@@ -304,9 +306,9 @@ cudaError_t dequant_bits(const void *codes, const float *scales, int64_t nblocks
     static int cache[kMaxDevices];
     auto k = laaq_dequant_kernel<BITS, kU>;
     const int64_t per_cta = 4 * kU * (kThreads / 32);
-    k<<<resident_grid(k, cache, (nblocks + per_cta - 1) / per_cta), kThreads, 0, st>>>(
-        static_cast<const uint32_t *>(codes), scales, static_cast<uint4 *>(y), nblocks);
-    return cudaGetLastError();
+    return launch_pdl(k, resident_grid(k, cache, (nblocks + per_cta - 1) / per_cta), kThreads, 0,
+                      st, static_cast<const uint32_t *>(codes), scales, static_cast<uint4 *>(y),
+                      nblocks);
 }
 
 }  // namespace

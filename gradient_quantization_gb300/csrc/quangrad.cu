@@ -89,6 +89,7 @@ __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict_
                                                               float *__restrict__ scales,
                                                               const uint4 *__restrict__ grad,
                                                               int64_t nblocks) {
+    pdl_wait_and_release();
     const int lane = threadIdx.x & 31;
     const int half = lane >> 4, j = lane & 15;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -140,6 +141,7 @@ __global__ void __launch_bounds__(kThreads) reduce_shards_kernel(
     const uint4 *__restrict__ shards, const float *__restrict__ shard_scales, int W, int64_t n,
     int64_t nblocks, uint4 *__restrict__ out, float *__restrict__ out_scales,
     unsigned long long *__restrict__ naive_count) {
+    pdl_wait_and_release();
     const int lane = threadIdx.x & 31;
     const int oct = lane >> 3, t8 = lane & 7;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -233,9 +235,9 @@ cudaError_t launch_grad_accum(void *master, float *master_scales, const void *gr
     const int64_t nb = n / kBlock;
     auto k = grad_accum_kernel<kUnroll>;
     const int64_t per_cta = 2 * kUnroll * (kThreads / 32);
-    k<<<resident_grid(k, cache, (nb + per_cta - 1) / per_cta), kThreads, 0, st>>>(
-        static_cast<uint2 *>(master), master_scales, static_cast<const uint4 *>(grad), nb);
-    return cudaGetLastError();
+    return launch_pdl(k, resident_grid(k, cache, (nb + per_cta - 1) / per_cta), kThreads, 0, st,
+                      static_cast<uint2 *>(master), master_scales,
+                      static_cast<const uint4 *>(grad), nb);
 }
 
 cudaError_t launch_reduce_shards(const void *shards, const float *shard_scales, int W, int64_t n,
@@ -250,17 +252,16 @@ cudaError_t launch_reduce_shards(const void *shards, const float *shard_scales, 
         if (e != cudaSuccess) return e;
         static int cache[kMaxDevices];
         auto k = reduce_shards_kernel<true, kRUnroll>;
-        k<<<resident_grid(k, cache, ctas), kThreads, 0, st>>>(
-            static_cast<const uint4 *>(shards), shard_scales, W, n, nb, static_cast<uint4 *>(out),
-            out_scales, naive_count);
-    } else {
-        static int cache[kMaxDevices];
-        auto k = reduce_shards_kernel<false, kRUnroll>;
-        k<<<resident_grid(k, cache, ctas), kThreads, 0, st>>>(
-            static_cast<const uint4 *>(shards), shard_scales, W, n, nb, static_cast<uint4 *>(out),
-            out_scales, nullptr);
+        return launch_pdl(k, resident_grid(k, cache, ctas), kThreads, 0, st,
+                          static_cast<const uint4 *>(shards), shard_scales, W, n, nb,
+                          static_cast<uint4 *>(out), out_scales, naive_count);
     }
-    return cudaGetLastError();
+    static int cache[kMaxDevices];
+    auto k = reduce_shards_kernel<false, kRUnroll>;
+    return launch_pdl(k, resident_grid(k, cache, ctas), kThreads, 0, st,
+                      static_cast<const uint4 *>(shards), shard_scales, W, n, nb,
+                      static_cast<uint4 *>(out), out_scales,
+                      static_cast<unsigned long long *>(nullptr));
 }
 
 }  // namespace agoq
