@@ -369,6 +369,65 @@ int or_wgrad_gemm_int4_f64_entries(const uint16_t *dY, const uint8_t *xc, const 
     return OR_OK;
 }
 
+/* QuanGrad local accumulation with a binary32 gradient, the form it takes when
+ * it is fused into the epilogue of the weight-gradient product ([AGoQ] §2.B
+ * "Lokale accumulatie" together with §2.C "Kernel Fusion": the new gradient is
+ * the product's FP32 accumulator, never rounded to BF16).  Per block:
+ *   m_i = fl(e4m3(c_i) * s)       t_i = fl(m_i + g_i)
+ *   then requantize t with a fresh block scale (or_requant_block).             */
+int or_grad_accum_fp8_f32(uint8_t *master, float *master_scales, const float *grad, int64_t n)
+{
+    if (n < 0 || n % OR_BLOCK)
+        return OR_BAD_ARG;
+    float t[OR_BLOCK];
+    for (int64_t b = 0; b < n / OR_BLOCK; ++b) {
+        uint8_t *cb = master + b * OR_BLOCK;
+        float s = master_scales[b];
+        for (int i = 0; i < OR_BLOCK; ++i) {
+            float m = or_e4m3_to_f32(cb[i]) * s;
+            t[i] = m + grad[b * OR_BLOCK + i];
+        }
+        or_requant_block(t, cb, &master_scales[b]);
+    }
+    return OR_OK;
+}
+
+/* The weight-gradient product with the QuanGrad accumulation as its epilogue
+ * ([AGoQ] §2.B "Lokale accumulatie", §2.C "Kernel Fusion"), in place on an FP8
+ * master gradient [M][N] (E4M3 codes, scales [M][N/128]):
+ *   g[i][j] = fl32(sum_k dY[k][i] * Xhat[k][j])   (binary64 sum in k order,
+ *             rounded once to binary32: the FP32 accumulator the product hands
+ *             to the epilogue, without the GEMM's own summation error)
+ *   then or_grad_accum_fp8_f32 on every 128-element block of row i.
+ * `blocks` (may be NULL) restricts the work to `count` blocks of the flat
+ * master, block b covering row b / (N/128), columns (b % (N/128))*128 ..+127;
+ * master and master_scales then hold only those blocks, [count][128] and
+ * [count].  With blocks == NULL every block is done (count is ignored).      */
+int or_wgrad_accum_fp8(const uint16_t *dY, const uint8_t *xc, const float *xs, int M, int N,
+                       int K, const int64_t *blocks, int64_t count, uint8_t *master,
+                       float *master_scales)
+{
+    if (M <= 0 || N <= 0 || K <= 0 || N % OR_BLOCK || count < 0)
+        return OR_BAD_ARG;
+    const int64_t per_row = N / OR_BLOCK;
+    const int64_t nblk = blocks ? count : (int64_t)M * per_row;
+    float g[OR_BLOCK];
+    for (int64_t e = 0; e < nblk; ++e) {
+        const int64_t b = blocks ? blocks[e] : e;
+        if (b < 0 || b >= (int64_t)M * per_row)
+            return OR_BAD_ARG;
+        const int64_t i = b / per_row, j0 = (b % per_row) * OR_BLOCK;
+        for (int jj = 0; jj < OR_BLOCK; ++jj) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)or_bf16_to_f32(dY[k * M + i]) * or_xhat(xc, xs, N, k, j0 + jj);
+            g[jj] = (float)acc;
+        }
+        or_grad_accum_fp8_f32(master + e * OR_BLOCK, master_scales + e, g, OR_BLOCK);
+    }
+    return OR_OK;
+}
+
 /* ------------------------------------------------------------------------- */
 /* Array forms of the codecs, for the codec sweeps in the tests.               */
 void or_f32_to_bf16_array(const float *src, uint16_t *dst, int64_t n)

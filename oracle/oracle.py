@@ -35,12 +35,15 @@ def lib():
         L.or_reduce_fp8_shards.argtypes = [vp, vp, i32, i64, vp, vp, vp]
         L.or_wgrad_gemm_int4_f64.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.or_wgrad_gemm_int4_f64_entries.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp]
+        L.or_grad_accum_fp8_f32.argtypes = [vp, vp, vp, i64]
+        L.or_wgrad_accum_fp8.argtypes = [vp, vp, vp, i32, i32, i32, vp, i64, vp, vp]
         L.or_f32_to_bf16_array.argtypes = [vp, vp, i64]
         L.or_f32_to_e4m3_array.argtypes = [vp, vp, i64]
         L.or_e4m3_to_f32_array.argtypes = [vp, vp, i64]
         for name in ("or_quant_act", "or_dequant_act", "or_grad_accum_fp8",
                      "or_reduce_fp8_shards", "or_wgrad_gemm_int4_f64",
-                     "or_wgrad_gemm_int4_f64_entries"):
+                     "or_wgrad_gemm_int4_f64_entries", "or_grad_accum_fp8_f32",
+                     "or_wgrad_accum_fp8"):
             getattr(L, name).restype = ctypes.c_int
         for name in ("or_f32_to_bf16_array", "or_f32_to_e4m3_array", "or_e4m3_to_f32_array"):
             getattr(L, name).restype = None
@@ -169,3 +172,39 @@ def wgrad_gemm_int4_f64_entries(dY_bf16, x_codes, x_scales, M, N, K, rows, cols)
                                                 _ptr(r), _ptr(c), r.size, _ptr(out)),
            "wgrad_gemm_int4_f64_entries")
     return out
+
+
+def grad_accum_fp8_f32(master, master_scales, grad_f32):
+    """QuanGrad accumulation of a binary32 gradient; returns new (master, scales)."""
+    m = _contig(master, np.uint8).reshape(-1).copy()
+    s = _contig(master_scales, np.float32).reshape(-1).copy()
+    g = _contig(grad_f32, np.float32).reshape(-1)
+    if g.size != m.size or s.size != m.size // BLOCK:
+        raise ValueError("shape mismatch")
+    _check(lib().or_grad_accum_fp8_f32(_ptr(m), _ptr(s), _ptr(g), m.size), "grad_accum_fp8_f32")
+    return m, s
+
+
+def wgrad_accum_fp8(dY_bf16, x_codes, x_scales, M, N, K, master, master_scales, blocks=None):
+    """The product dY^T Xhat accumulated into an FP8 master [M][N]; returns new
+    (master, scales).  With `blocks` (indices of 128-element blocks of the flat
+    master) only those blocks are computed: master/master_scales then hold just
+    them ([len(blocks)][128] and [len(blocks)])."""
+    dY = _contig(dY_bf16, np.uint16).reshape(-1)
+    xc = _contig(x_codes, np.uint8).reshape(-1)
+    xs = _contig(x_scales, np.float32).reshape(-1)
+    if dY.size != K * M or xc.size != K * N // 2 or xs.size != K * N // BLOCK:
+        raise ValueError("shape mismatch")
+    m = _contig(master, np.uint8).reshape(-1).copy()
+    s = _contig(master_scales, np.float32).reshape(-1).copy()
+    if blocks is None:
+        b, count, nblk = None, 0, M * N // BLOCK
+    else:
+        b = _contig(np.asarray(blocks, np.int64), np.int64)
+        count = nblk = b.size
+    if m.size != nblk * BLOCK or s.size != nblk:
+        raise ValueError("shape mismatch")
+    _check(lib().or_wgrad_accum_fp8(_ptr(dY), _ptr(xc), _ptr(xs), M, N, K,
+                                    _ptr(b) if b is not None else None, count, _ptr(m), _ptr(s)),
+           "wgrad_accum_fp8")
+    return m, s
