@@ -496,6 +496,29 @@ def rows_arm(device, hbm_peak, bf16_peak):
         rows["wgrad_gemm_int4_11008x4096x8192"]["torch_matmul_bf16_predequantized_us"] = round(ref_ms * 1e3, 1)
     except agoq.AgoqError as e:
         rows["wgrad_gemm_int4_11008x4096x8192"] = {"unavailable": str(e)}
+
+    # The same GEMM with the QuanGrad accumulation into an FP8 master as its epilogue
+    master = torch.zeros(M * N, dtype=torch.uint8, device=device)
+    mscales = torch.zeros(M * N // 128, dtype=torch.float32, device=device)
+    agoq.agoq_grad_accum_fp8(master, mscales, dw.view(-1))
+    name = "wgrad_gemm_int4_accum_fp8_11008x4096x8192"
+    try:
+        ms = _time_launch(lambda: agoq.agoq_wgrad_gemm_int4_accum_fp8(dy, xc, xs, M, N, K, master,
+                                                                      mscales), flush)
+        agoq.agoq_device_status()
+        tflops = 2.0 * M * N * K / (ms * 1e-3) / 1e12
+        rows[name] = {
+            "us": round(ms * 1e3, 1), "TFLOP/s": round(tflops, 1),
+            "frac_of_measured_bf16": round(tflops / bf16_peak, 4),
+            "bytes": 2 * K * M + K * N // 2 + K * (N // 128) * 4 + 2 * (M * N + M * (N // 128) * 4),
+            "vs_gemm_then_accum_us": None}
+        # the unfused sequence it replaces: BF16 dW, then the element-wise accumulation
+        def unfused():
+            agoq.agoq_wgrad_gemm_int4(dy, xc, xs, M, N, K, dw)
+            agoq.agoq_grad_accum_fp8(master, mscales, dw.view(-1))
+        rows[name]["vs_gemm_then_accum_us"] = round(_time_launch(unfused, flush) * 1e3, 1)
+    except agoq.AgoqError as e:
+        rows[name] = {"unavailable": str(e)}
     return rows
 
 
@@ -568,7 +591,7 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
-PROFILE_CASES = ("accum", "reduce8", "reduce8_nocount", "reduce64", "gemm")
+PROFILE_CASES = ("accum", "reduce8", "reduce8_nocount", "reduce64", "gemm", "gemm_accum")
 
 
 def profile_case(name, launches=3):
@@ -593,12 +616,17 @@ def profile_case(name, launches=3):
         cnt = None if name.endswith("nocount") else torch.zeros(1, dtype=torch.int64, device=dev)
         for _ in range(launches):
             agoq.agoq_reduce_fp8_shards(sh, ss, W, n, naive_overflow_count=cnt)
-    elif name == "gemm":
+    elif name in ("gemm", "gemm_accum"):
         M, N, K = synthetic.WGRAD_M, synthetic.WGRAD_N, synthetic.WGRAD_K
         dy, xg = synthetic.wgrad_inputs_torch(seed=4, device=dev)
         xc, xs = agoq.agoq_quant_act(xg, 4)
+        master = torch.zeros(M * N, dtype=torch.uint8, device=dev)
+        mscales = torch.zeros(M * N // 128, dtype=torch.float32, device=dev)
         for _ in range(launches):
-            agoq.agoq_wgrad_gemm_int4(dy, xc, xs, M, N, K)
+            if name == "gemm":
+                agoq.agoq_wgrad_gemm_int4(dy, xc, xs, M, N, K)
+            else:
+                agoq.agoq_wgrad_gemm_int4_accum_fp8(dy, xc, xs, M, N, K, master, mscales)
         agoq.agoq_device_status()
     else:
         raise SystemExit("unknown profile case %r (choose from %s)" % (name, ", ".join(PROFILE_CASES)))

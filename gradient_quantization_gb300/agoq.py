@@ -52,6 +52,7 @@ def _lib_handle():
         L.agoq_reduce_fp8_shards.argtypes = [vp, vp, i32, i64, vp, vp, vp, vp]
         L.agoq_wgrad_gemm_int4.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
         L.agoq_wgrad_gemm_int4_f32out.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
+        L.agoq_wgrad_gemm_int4_accum_fp8.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.agoq_device_status.argtypes = [vp]
         for name in ("agoq_quant_act", "agoq_dequant_act", "agoq_grad_accum_fp8",
                      "agoq_reduce_fp8_shards", "agoq_wgrad_gemm_int4",
@@ -201,6 +202,23 @@ def agoq_wgrad_gemm_int4_f32out(dY, x_codes, x_scales, M, N, K, dW=None, stream=
                                              _ptr(dW), _stream(stream)),
            "agoq_wgrad_gemm_int4_f32out")
     return dW
+
+
+def agoq_wgrad_gemm_int4_accum_fp8(dY, x_codes, x_scales, M, N, K, master, master_scales,
+                                   stream=None):
+    """The GEMM with the QuanGrad accumulation as its epilogue: the product is
+    added to the FP8 master [M][N] (uint8 E4M3 codes, float32 scales [M][N/128])
+    in place.  Returns (master, master_scales)."""
+    _need(dY, torch.bfloat16, "dY")
+    _need(x_codes, torch.uint8, "x_codes")
+    _need(x_scales, torch.float32, "x_scales")
+    _need(master, torch.uint8, "master")
+    _need(master_scales, torch.float32, "master_scales")
+    _check(lib().agoq_wgrad_gemm_int4_accum_fp8(_ptr(dY), _ptr(x_codes), _ptr(x_scales), M, N, K,
+                                                _ptr(master), _ptr(master_scales),
+                                                _stream(stream)),
+           "agoq_wgrad_gemm_int4_accum_fp8")
+    return master, master_scales
 
 
 def agoq_device_status(stream=None):

@@ -2,7 +2,7 @@
 
 Each translation unit under csrc/ is compiled in parallel, then linked into
 gradient_quantization_gb300/libagoq.so with the CUDA runtime linked
-statically.  The element-wise units are compiled with -fmad=false so that no
+statically.  Every unit is compiled with -fmad=false so that no
 multiply and add are contracted into one rounding (the kernels also use the
 explicitly rounded intrinsics).  Run ``python -m gradient_quantization_gb300.build``.
 """
@@ -24,7 +24,7 @@ UNITS = {
     "agoq_api.cu": ["-fmad=false"],
     "laaq.cu": ["-fmad=false"],
     "quangrad.cu": ["-fmad=false"],
-    "wgrad_gemm.cu": [],
+    "wgrad_gemm.cu": ["-fmad=false"],
 }
 HEADERS = ["agoq_device.cuh", "agoq_launch.h"]
 

@@ -164,6 +164,27 @@ agoq_status agoq_wgrad_gemm_int4_f32out(const void *dY_bf16, const void *x_codes
     return wgrad_common(dY_bf16, x_codes, x_scales, M, N, K, dW_f32, true, stream);
 }
 
+agoq_status agoq_wgrad_gemm_int4_accum_fp8(const void *dY_bf16, const void *x_codes,
+                                           const float *x_scales, int M, int N, int K,
+                                           void *master_e4m3, float *master_scales,
+                                           void *stream) {
+    using namespace agoq;
+    if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 512 || K % 64) return AGOQ_ERR_SHAPE;
+    if (!dY_bf16 || !x_codes || !x_scales || !master_e4m3 || !master_scales) return AGOQ_ERR_NULL;
+    if (!aligned(dY_bf16, 16) || !aligned(x_codes, 16) || !aligned(x_scales, 16) ||
+        !aligned(master_e4m3, 16) || !aligned(master_scales, 4))
+        return AGOQ_ERR_ALIGN;
+    const uint64_t dyb = 2ull * K * M, xcb = (uint64_t)K * N / 2, xsb = (uint64_t)K * (N / 128) * 4;
+    const uint64_t mb = (uint64_t)M * N, msb = (uint64_t)M * (N / 128) * 4;
+    if (overlap(master_e4m3, mb, dY_bf16, dyb) || overlap(master_e4m3, mb, x_codes, xcb) ||
+        overlap(master_e4m3, mb, x_scales, xsb) || overlap(master_scales, msb, dY_bf16, dyb) ||
+        overlap(master_scales, msb, x_codes, xcb) || overlap(master_scales, msb, x_scales, xsb) ||
+        overlap(master_e4m3, mb, master_scales, msb))
+        return AGOQ_ERR_ALIAS;
+    return from_cuda(launch_wgrad_accum_fp8(dY_bf16, x_codes, x_scales, M, N, K, master_e4m3,
+                                            master_scales, as_stream(stream)));
+}
+
 agoq_status agoq_device_status(void *stream) {
     unsigned status = 0;
     if (agoq::read_and_clear_device_status(agoq::as_stream(stream), &status) != cudaSuccess)

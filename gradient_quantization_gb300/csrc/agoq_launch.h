@@ -29,8 +29,9 @@ int resident_per_sm(K kernel, int threads, size_t smem, int *cache) {
 
 // Launch `kernel` with programmatic stream serialization: it may be scheduled
 // while the previous kernel on the stream is finishing.  Every kernel launched
-// this way begins with pdl_wait() (griddepcontrol.wait) before touching global
-// memory, so it still observes all effects of the work before it in the stream.
+// this way begins with pdl_wait_and_release() (griddepcontrol.wait) before
+// touching global memory, so it still observes all effects of the work before
+// it in the stream.
 template <typename... KArgs, typename... Args>
 cudaError_t launch_pdl(void (*kernel)(KArgs...), int grid, int block, size_t smem,
                        cudaStream_t st, Args... args) {
@@ -58,6 +59,8 @@ cudaError_t launch_reduce_shards(const void *shards, const float *shard_scales, 
                                  cudaStream_t st);
 cudaError_t launch_wgrad_gemm(const void *dY, const void *xc, const float *xs, int M, int N, int K,
                               void *dW, bool f32_out, cudaStream_t st);
+cudaError_t launch_wgrad_accum_fp8(const void *dY, const void *xc, const float *xs, int M, int N,
+                                   int K, void *master, float *master_scales, cudaStream_t st);
 // Synchronise `st`, read and clear the device status word (0 = no timeout).
 cudaError_t read_and_clear_device_status(cudaStream_t st, unsigned *status);
 

@@ -26,9 +26,20 @@
 //   warp 2      TMA producer of the X ring.
 //   warps 3-18  dequantizers: codes -> Xhat into the B ring, fence.proxy.async,
 //               mbarrier arrives that publish the B stage and release the X
-//               stage (after its codes have been consumed).
-//   warps 19-22 epilogue: tcgen05.ld of the accumulators (each warp its 32-lane
-//               quarter), BF16 round-to-nearest-even (or FP32), global stores.
+//               stage (after its codes have been consumed).  They also run the
+//               epilogue of the previous tile, once they have filled the B
+//               ring with the first stages of the next one (the MMA waits for
+//               the accumulator anyway): each warp takes one 32-row x
+//               128-column item (its TMEM lane quarter, warp % 4, and one of
+//               the four 128-column blocks of the two accumulators), reads it
+//               with tcgen05.ld, one output row per thread, and does one of
+//               - BF16 round-to-nearest-even and global stores;
+//               - the FP32 accumulator stored unrounded;
+//               - the QuanGrad accumulation into an FP8 master gradient
+//                 ("Lokale accumulatie", section 2.B): dequantize the 128
+//                 E4M3 master codes of the row block, add the FP32
+//                 accumulator, take the block absmax, requantize in place with
+//                 the new scale.  The BF16 dW never exists.
 // Waiting threads sleep in mbarrier.try_wait (suspend-time hint) rather than
 // spin, so the dequantizers keep the issue slots.
 // Every mbarrier wait has a time limit: on expiry the kernel records a code in
@@ -59,33 +70,27 @@ namespace {
 #ifndef AGOQ_GEMM_NA
 #define AGOQ_GEMM_NA 3
 #endif
-#ifndef AGOQ_GEMM_DEQ_GROUPS
-#define AGOQ_GEMM_DEQ_GROUPS 1
-#endif
 #ifndef AGOQ_GEMM_WAIT_HINT_NS
 #define AGOQ_GEMM_WAIT_HINT_NS 20000
 #endif
 
+// Epilogue kinds.
+constexpr int kEpiBf16 = 0, kEpiF32 = 1, kEpiAccumFp8 = 2;
+
 constexpr int BM = 256, BN = 256, BK = AGOQ_GEMM_BK;
 constexpr int NA = AGOQ_GEMM_NA, NX = AGOQ_GEMM_NX, NB = AGOQ_GEMM_NB;
 constexpr int kChunk = BK * 128;                          // bytes of one 64-wide M/N chunk of a stage
-constexpr int kTmaWarp = 0, kMmaWarp = 1, kTmaXWarp = 2, kDeqWarp0 = 3, kDeqWarps = 16,
-              kEpiWarp0 = kDeqWarp0 + kDeqWarps, kEpiWarps = 4;
-constexpr int kThreads = (kEpiWarp0 + kEpiWarps) * 32;   // 736
-// The dequantizers form kDeqGroups groups that take k-blocks in turn, so each
-// warp has kDeqGroups MMA periods to turn its stage around.
-constexpr int kDeqGroups = AGOQ_GEMM_DEQ_GROUPS;
-constexpr int kGroupWarps = kDeqWarps / kDeqGroups;
-constexpr int kDeqRows = BK / kGroupWarps;                // k-rows per dequant thread per stage
-static_assert(kDeqRows * kGroupWarps == BK, "every k-row of a stage is dequantized exactly once");
-static_assert(NB >= kDeqGroups + 1, "B ring must cover the stages being dequantized plus one");
+constexpr int kTmaWarp = 0, kMmaWarp = 1, kTmaXWarp = 2, kDeqWarp0 = 3, kDeqWarps = 16;
+constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;   // 608
+constexpr int kDeqRows = BK / kDeqWarps;                  // k-rows per dequant thread per stage
+static_assert(kDeqRows * kDeqWarps == BK, "every k-row of a stage is dequantized exactly once");
+static_assert(NB >= 2, "the B ring must let dequantization run ahead of the MMA");
+static_assert(kDeqWarps == 16, "epilogue items: 4 TMEM lane quarters x 4 blocks of 128 columns");
 // A waiter may only be one phase behind the barrier it polls (a parity test
-// cannot tell "two phases ahead" from "complete").  Each X stage must therefore
-// always be consumed by the same dequant group, whose waits then see every
-// phase of it in order.  (The B ring is safe for NB >= 2: when a group reaches
-// k-block i, the MMA has retired block i - 2*NB, so empty_b is never two
-// phases behind.)
-static_assert(NX % kDeqGroups == 0, "X ring depth must be a multiple of the dequant group count");
+// cannot tell "two phases ahead" from "complete").  Every ring here is waited
+// on by all of its consumers for every phase in order, and tmem_full(t + 1)
+// cannot complete before every dequant warp has waited for tmem_full(t) and
+// released the accumulator.
 constexpr int kAStage = BM * BK * 2;                      // 32 KiB of dY (BF16)
 constexpr int kBStage = BN * BK * 2;                      // 32 KiB of Xhat (BF16)
 constexpr int kCStage = BK * BN / 2;                      // 8 KiB of packed codes
@@ -99,6 +104,10 @@ constexpr int kNumBars = 2 * NA + 2 * NX + 2 * NB + 3;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;          // + slack for 1024-byte alignment
 constexpr uint32_t kTmemCols = 512;
+#ifndef AGOQ_GEMM_PREFETCH_LEAD
+#define AGOQ_GEMM_PREFETCH_LEAD 8
+#endif
+constexpr int kPrefetchLead = AGOQ_GEMM_PREFETCH_LEAD;   // k-blocks between master prefetch and use
 constexpr unsigned kStatusTimeout = 1u;
 constexpr long long kWaitLimitCycles = 4000000000ll;      // about two seconds
 
@@ -185,6 +194,27 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
+        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
+          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
+          "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+        : "r"(taddr));
+    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
+        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
+        "f"(v[15])
+        : "memory");
+}
+
 // Shared-memory matrix descriptor (tcgen05 format) of an MN-major operand
 // stored in 128-byte-swizzled atoms of 8 K-rows x 64 BF16: `lbo` is the byte
 // distance between atoms along M/N, `sbo` between 8-row groups along K.
@@ -267,12 +297,120 @@ __device__ __forceinline__ uint4 dequant_word(uint32_t w, float s) {
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
-template <bool F32_OUT>
+__device__ __forceinline__ void prefetch_l2(const void *p) {
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p));
+}
+
+// t_i = fl(fl(e4m3(c_i) * s) + acc_i) for the four E4M3 codes of word w and
+// four binary32 accumulator values (bit patterns).  Scalar __fmul_rn/__fadd_rn:
+// the two roundings must stay separate (a fused multiply-add gives a different
+// t, e.g. a signed zero where m and acc cancel).
+__device__ __forceinline__ void master_plus_acc4(uint32_t w, float s, const uint32_t *acc,
+                                                 float t[4]) {
+    float e[4];
+    e4m3x2_to_f32(w & 0xFFFFu, e[0], e[1]);
+    e4m3x2_to_f32(w >> 16, e[2], e[3]);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) t[i] = __fadd_rn(__fmul_rn(e[i], s), __uint_as_float(acc[i]));
+}
+
+__device__ __forceinline__ uint32_t word_of(const uint4 (&c)[8], int i) {
+    const uint4 v = c[i >> 2];
+    return (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
+}
+
+// QuanGrad accumulation of one 128-column block of an accumulator row into the
+// FP8 master (in place): `taddr` is the TMEM address of the block's first
+// column in this warp's lane quarter, `codes` the 128 master codes of the
+// block, `scale` its FP32 scale.  The first pass forms t = fl(fl(e4m3(c) * s)
+// + acc), takes the block absmax and writes t back over the accumulator in
+// TMEM; the second pass reads t and requantizes with the new scale.
+__device__ __forceinline__ void accum_fp8_block(uint32_t taddr, uint8_t *codes, float *scale) {
+    uint4 *mc = reinterpret_cast<uint4 *>(codes);
+    uint4 c[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) c[i] = mc[i];
+    const float s = *scale;
+    float am = 0.0f;
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+        uint32_t v[16];
+        tmem_ld16(taddr + cc * 16, v);
+        float t[16];
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+            master_plus_acc4(word_of(c, cc * 4 + w), s, v + 4 * w, t + 4 * w);
+            am = fmaxf(am, fmaxf(fmaxf(fabsf(t[4 * w]), fabsf(t[4 * w + 1])),
+                                 fmaxf(fabsf(t[4 * w + 2]), fabsf(t[4 * w + 3]))));
+        }
+        tmem_st16(taddr + cc * 16, t);
+    }
+    asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+    const float snew = __fdiv_rn(am, kE4M3Max);
+#pragma unroll
+    for (int cc = 0; cc < 8; ++cc) {
+        uint32_t v[16];
+        __syncwarp();   // lanes may have left the fast requantization path; tcgen05.ld is .aligned
+        tmem_ld16(taddr + cc * 16, v);
+        uint32_t o[4];
+#pragma unroll
+        for (int p = 0; p < 2; ++p) {
+            float t[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(v[8 * p + i]);
+            const uint2 q = e4m3_codes8(t, snew);
+            o[2 * p] = q.x;
+            o[2 * p + 1] = q.y;
+        }
+        mc[cc] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+    *scale = snew;
+}
+
+// One epilogue item: row `row`, columns col0 .. col0+127 of the output, whose
+// accumulators start at TMEM address `taddr` (this warp's lane quarter).
+template <int EPI>
+__device__ __forceinline__ void epilogue_item(uint32_t taddr, void *dW, float *mscales, int row,
+                                              int col0, int N) {
+    if constexpr (EPI == kEpiAccumFp8) {
+        accum_fp8_block(taddr, static_cast<uint8_t *>(dW) + (size_t)row * N + col0,
+                        mscales + (size_t)row * (N / 128) + col0 / 128);
+    } else {
+#pragma unroll 1
+        for (int cc = 0; cc < 4; ++cc) {
+            uint32_t v[32];
+            tmem_ld32(taddr + cc * 32, v);
+            if constexpr (EPI == kEpiF32) {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<float *>(dW) + (size_t)row * N +
+                                                       col0 + cc * 32);
+#pragma unroll
+                for (int j = 0; j < 8; ++j)
+                    dst[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+            } else {
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(dW) +
+                                                       (size_t)row * N + col0 + cc * 32);
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    uint32_t w[4];
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        w[i] = pack_bf16x2(__uint_as_float(v[8 * j + 2 * i]),
+                                           __uint_as_float(v[8 * j + 2 * i + 1]));
+                    dst[j] = make_uint4(w[0], w[1], w[2], w[3]);
+                }
+            }
+        }
+    }
+}
+
+// dW (EPI kEpiBf16 / kEpiF32) or the FP8 master codes (kEpiAccumFp8, with
+// their scales in `mscales`) are [M][N] row-major.
+template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     wgrad_gemm_int4_kernel(const __grid_constant__ CUtensorMap map_dy,
                            const __grid_constant__ CUtensorMap map_xc,
-                           const __grid_constant__ CUtensorMap map_xs, void *__restrict__ dW, int M,
-                           int N, int K) {
+                           const __grid_constant__ CUtensorMap map_xs, void *__restrict__ dW,
+                           float *__restrict__ mscales, int M, int N, int K) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -304,14 +442,14 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int s = 0; s < NX; ++s) {
             mbar_init(&sh.full_x[s], 1);
-            mbar_init(&sh.empty_x[s], kGroupWarps);
+            mbar_init(&sh.empty_x[s], kDeqWarps);
         }
         for (int s = 0; s < NB; ++s) {
-            mbar_init(&sh.full_b[s], kGroupWarps);
+            mbar_init(&sh.full_b[s], kDeqWarps);
             mbar_init(&sh.empty_b[s], 1);
         }
         mbar_init(sh.tmem_full, 1);
-        mbar_init(sh.tmem_empty, kEpiWarps);
+        mbar_init(sh.tmem_empty, kDeqWarps);
         mbar_init(sh.drain, 1);
         *sh.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -407,18 +545,47 @@ __global__ void __launch_bounds__(kThreads, 1)
                 wait_bar(sh.drain, 0u, sh.abort, true);
             }
         }
-    } else if (warp >= kDeqWarp0 && warp < kDeqWarp0 + kDeqWarps) {
-        const int group = (warp - kDeqWarp0) / kGroupWarps;
+    } else {
+        // Dequantizers, which also run the epilogue of the previous tile.
+        const int d = warp - kDeqWarp0;
         const int wc = lane;                            // code word column: N = 8wc .. 8wc+7
-        const int rg = (warp - kDeqWarp0) % kGroupWarps; // rows rg, rg+kGroupWarps, ...
         const int chunk = wc >> 3, piece = wc & 7;
-        uint32_t it = 0;
+        // Epilogue item: TMEM lane quarter q (tcgen05.ld reaches lanes
+        // 32*(warp%4) .. +31) and 128-column block `item` of the tile: rows
+        // m0 + 128*eh + 32q + lane, columns n0 + 128*ejb .. +127.
+        const int q = warp & 3, item = d >> 2, eh = item >> 1, ejb = item & 1;
+        const uint32_t etaddr = tmem_base + ((uint32_t)(32 * q) << 16) + eh * 256 + ejb * 128;
+        // The previous tile's epilogue runs once the B ring holds the first
+        // stages of this tile (or all of them, for short K).
+        const int lead = (kblocks < NB ? kblocks : NB) - 1;
+        auto epilogue = [&](int tile, uint32_t t) -> bool {
+            if (!warp_wait(sh.tmem_full, t & 1u, sh.abort)) return false;
+            tc_fence_after();
+            const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+            epilogue_item<EPI>(etaddr, dW, mscales, m0 + eh * 128 + 32 * q + lane, n0 + ejb * 128,
+                               N);
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(sh.tmem_empty);
+            return true;
+        };
+        uint32_t it = 0, t = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
+        int prev = -1;
+        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++t) {
             const int n0 = (tile % n_tiles) * BN;
             const int soff = ((n0 / 128) & 3) + (wc >> 4);   // scale column inside the 4-wide box
             for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                if ((int)(it % kDeqGroups) != group) continue;   // the other group's k-block
+                if constexpr (EPI == kEpiAccumFp8) {
+                    // Pull this thread's master block of the tile into L2 a few
+                    // k-blocks before its epilogue needs it.
+                    if (kb == (kblocks > kPrefetchLead ? kblocks - kPrefetchLead : 0)) {
+                        const size_t row =
+                            (size_t)((tile / n_tiles) * BM + eh * 128 + 32 * q + lane);
+                        prefetch_l2(static_cast<const uint8_t *>(dW) + row * N + n0 + ejb * 128);
+                        prefetch_l2(mscales + row * (N / 128) + n0 / 128 + ejb);
+                    }
+                }
                 const int sx = it % NX, sb = it % NB;
                 if (!warp_wait(&sh.full_x[sx], (it / NX) & 1u, sh.abort)) { ok = false; break; }
                 const uint32_t *codes = reinterpret_cast<const uint32_t *>(sh.c + sx * kCStage);
@@ -427,7 +594,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float sc[kDeqRows];
 #pragma unroll
                 for (int i = 0; i < kDeqRows; ++i) {
-                    const int k = rg + kGroupWarps * i;
+                    const int k = d + kDeqWarps * i;
                     w[i] = codes[k * 32 + wc];
                     sc[i] = scales[k * 4 + soff];
                 }
@@ -435,7 +602,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *btile = sh.b + sb * kBStage + chunk * kChunk;
 #pragma unroll
                 for (int i = 0; i < kDeqRows; ++i) {
-                    const int k = rg + kGroupWarps * i;
+                    const int k = d + kDeqWarps * i;
                     const uint4 y = dequant_word(w[i], sc[i]);
                     *reinterpret_cast<uint4 *>(btile + k * 128 + ((piece ^ (k & 7)) << 4)) = y;
                 }
@@ -448,47 +615,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mbar_arrive(&sh.full_b[sb]);
                     mbar_arrive(&sh.empty_x[sx]);
                 }
+                if (kb == lead && prev >= 0 && !epilogue(prev, t - 1)) { ok = false; break; }
             }
+            prev = tile;
         }
-    } else {
-        // epilogue warps: TMEM lane quarter q = warp % 4
-        const int q = warp & 3;
-        uint32_t t = 0;
-        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++t) {
-            if (!warp_wait(sh.tmem_full, t & 1u, sh.abort, 1000000)) break;
-            tc_fence_after();
-            const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
-#pragma unroll 1
-            for (int h = 0; h < 2; ++h) {
-                const int row = m0 + h * 128 + 32 * q + lane;
-#pragma unroll 1
-                for (int cc = 0; cc < BN / 32; ++cc) {
-                    uint32_t v[32];
-                    tmem_ld32(tmem_base + ((uint32_t)(32 * q) << 16) + h * 256 + cc * 32, v);
-                    if constexpr (F32_OUT) {
-                        uint4 *dst = reinterpret_cast<uint4 *>(static_cast<float *>(dW) +
-                                                               (size_t)row * N + n0 + cc * 32);
-#pragma unroll
-                        for (int j = 0; j < 8; ++j)
-                            dst[j] = make_uint4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
-                    } else {
-                        uint4 *dst = reinterpret_cast<uint4 *>(
-                            static_cast<uint16_t *>(dW) + (size_t)row * N + n0 + cc * 32);
-#pragma unroll
-                        for (int j = 0; j < 4; ++j) {
-                            const uint32_t w0 = pack_bf16x2(__uint_as_float(v[8 * j]), __uint_as_float(v[8 * j + 1]));
-                            const uint32_t w1 = pack_bf16x2(__uint_as_float(v[8 * j + 2]), __uint_as_float(v[8 * j + 3]));
-                            const uint32_t w2 = pack_bf16x2(__uint_as_float(v[8 * j + 4]), __uint_as_float(v[8 * j + 5]));
-                            const uint32_t w3 = pack_bf16x2(__uint_as_float(v[8 * j + 6]), __uint_as_float(v[8 * j + 7]));
-                            dst[j] = make_uint4(w0, w1, w2, w3);
-                        }
-                    }
-                }
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(sh.tmem_empty);
-        }
+        if (ok && prev >= 0) epilogue(prev, t - 1);
     }
 
     tc_fence_before();
@@ -535,9 +666,9 @@ bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint6
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <bool F32_OUT>
+template <int EPI>
 cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, int N, int K,
-                        void *dW, cudaStream_t st) {
+                        void *dW, float *mscales, cudaStream_t st) {
     CUtensorMap m_dy, m_xc, m_xs;
     if (!encode_2d(&m_dy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, (uint64_t)M, (uint64_t)K,
                    (uint64_t)M * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -546,7 +677,7 @@ cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, 
         !encode_2d(&m_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xs, (uint64_t)N / 128, (uint64_t)K,
                    (uint64_t)(N / 128) * 4, 4, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    auto kernel = wgrad_gemm_int4_kernel<F32_OUT>;
+    auto kernel = wgrad_gemm_int4_kernel<EPI>;
     static bool attr_set[kMaxDevices];
     int dev = 0;
     cudaGetDevice(&dev);
@@ -558,7 +689,7 @@ cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, 
     }
     const int num_tiles = (M / BM) * (N / BN);
     const int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-    kernel<<<grid, kThreads, kSmemBytes, st>>>(m_dy, m_xc, m_xs, dW, M, N, K);
+    kernel<<<grid, kThreads, kSmemBytes, st>>>(m_dy, m_xc, m_xs, dW, mscales, M, N, K);
     return cudaGetLastError();
 }
 
@@ -566,8 +697,13 @@ cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, 
 
 cudaError_t launch_wgrad_gemm(const void *dY, const void *xc, const float *xs, int M, int N, int K,
                               void *dW, bool f32_out, cudaStream_t st) {
-    return f32_out ? launch_impl<true>(dY, xc, xs, M, N, K, dW, st)
-                   : launch_impl<false>(dY, xc, xs, M, N, K, dW, st);
+    return f32_out ? launch_impl<kEpiF32>(dY, xc, xs, M, N, K, dW, nullptr, st)
+                   : launch_impl<kEpiBf16>(dY, xc, xs, M, N, K, dW, nullptr, st);
+}
+
+cudaError_t launch_wgrad_accum_fp8(const void *dY, const void *xc, const float *xs, int M, int N,
+                                   int K, void *master, float *master_scales, cudaStream_t st) {
+    return launch_impl<kEpiAccumFp8>(dY, xc, xs, M, N, K, master, master_scales, st);
 }
 
 cudaError_t read_and_clear_device_status(cudaStream_t st, unsigned *status) {

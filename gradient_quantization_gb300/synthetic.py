@@ -101,6 +101,23 @@ def wgrad_inputs_np(seed=4, M=WGRAD_M, N=WGRAD_N, K=WGRAD_K):
     return bf16_bits_from_f32(dy).reshape(K, M), bf16_bits_from_f32(x).reshape(K, N)
 
 
+def wgrad_exact_sum_inputs_np(seed=5, M=WGRAD_M, N=WGRAD_N, K=WGRAD_K):
+    """(dY BF16 [K x M], X BF16 [K x N]) on a power-of-two grid, for checks whose
+    FP32 accumulation must be exact in any summation order.  dY = i * 2^-6 with
+    i uniform in -3..3; each 128-element block of an X row is c * 2^e with c
+    uniform in -7..7, e uniform in -4..0 per block, and element 0 of the block
+    set to +-7 * 2^e (random sign) so that the block absmax is 7 * 2^e.  Draw
+    order: dY integers, X integers, block exponents, block signs."""
+    rng = np.random.default_rng(seed)
+    dy = rng.integers(-3, 4, K * M).astype(np.float32) * np.float32(2.0 ** -6)
+    c = rng.integers(-7, 8, (K, N // 128, 128)).astype(np.float32)
+    e = rng.integers(-4, 1, (K, N // 128, 1))
+    sign = np.where(rng.random((K, N // 128)) < 0.5, -1.0, 1.0).astype(np.float32)
+    c[:, :, 0] = 7.0 * sign
+    x = (c * np.ldexp(np.float32(1.0), e).astype(np.float32)).astype(np.float32)
+    return bf16_bits_from_f32(dy).reshape(K, M), bf16_bits_from_f32(x.reshape(-1)).reshape(K, N)
+
+
 # ---------------------------------------------------------------- torch recipes
 def _gen(device, seed):
     g = torch.Generator(device=device)

@@ -147,6 +147,26 @@ agoq_status agoq_wgrad_gemm_int4_f32out(const void *dY_bf16, const void *x_codes
                                         void *stream);
 
 /*
+ * The same product with the QuanGrad local accumulation as its epilogue (AGoQ
+ * section 2.B "Lokale accumulatie" fused per section 2.C "Kernel Fusion"), IN
+ * PLACE on an FP8 master gradient laid out like dW: for each 128-column block
+ * of each row m (block b = m * N/128 + n/128 of the flat [M][N] master),
+ *   g_i   = the FP32 accumulator of dW[m][n] (never rounded to BF16);
+ *   m_i   = fl32(e4m3(c_i) * scale);  t_i = fl32(m_i + g_i);
+ *   scale' = fl32(absmax(t) / 448);   c_i' = e4m3_rne_satfinite(fl32(t_i / scale')),
+ * i.e. agoq_grad_accum_fp8 with the accumulator as the gradient.
+ *   master_e4m3   : in/out, [M][N] E4M3 codes, 16-byte aligned.
+ *   master_scales : in/out, [M][N/128] FP32 scales.
+ * Shape rules and the other arguments as agoq_wgrad_gemm_int4; the master must
+ * not overlap the operands.  The FP32 accumulation order is the tensor cores'
+ * (not specified), so codes match a reference that rounds the exact product
+ * once to FP32 only where that accumulation is exact.
+ */
+agoq_status agoq_wgrad_gemm_int4_accum_fp8(const void *dY_bf16, const void *x_codes,
+                                           const float *x_scales, int M, int N, int K,
+                                           void *master_e4m3, float *master_scales, void *stream);
+
+/*
  * Synchronise `stream`, then read and clear the library's device-side status
  * word for the current device.  Returns AGOQ_ERR_TIMEOUT if a GEMM pipeline
  * wait exceeded its iteration limit since the last call (that GEMM's output is

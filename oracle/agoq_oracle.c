@@ -410,10 +410,24 @@ int or_wgrad_accum_fp8(const uint16_t *dY, const uint8_t *xc, const float *xs, i
     if (M <= 0 || N <= 0 || K <= 0 || N % OR_BLOCK || count < 0)
         return OR_BAD_ARG;
     const int64_t per_row = N / OR_BLOCK;
-    const int64_t nblk = blocks ? count : (int64_t)M * per_row;
+    if (!blocks) {
+        /* every block: the full binary64 product (same k-order sums), then
+         * round each entry once and accumulate */
+        double *dw = (double *)malloc(sizeof(double) * (size_t)M * (size_t)N);
+        float *g32 = (float *)malloc(sizeof(float) * (size_t)M * (size_t)N);
+        int rc = (dw && g32) ? or_wgrad_gemm_int4_f64(dY, xc, xs, M, N, K, dw) : OR_BAD_ARG;
+        if (rc == OR_OK) {
+            for (int64_t e = 0; e < (int64_t)M * N; ++e)
+                g32[e] = (float)dw[e];
+            rc = or_grad_accum_fp8_f32(master, master_scales, g32, (int64_t)M * N);
+        }
+        free(dw);
+        free(g32);
+        return rc;
+    }
     float g[OR_BLOCK];
-    for (int64_t e = 0; e < nblk; ++e) {
-        const int64_t b = blocks ? blocks[e] : e;
+    for (int64_t e = 0; e < count; ++e) {
+        const int64_t b = blocks[e];
         if (b < 0 || b >= (int64_t)M * per_row)
             return OR_BAD_ARG;
         const int64_t i = b / per_row, j0 = (b % per_row) * OR_BLOCK;

@@ -101,6 +101,21 @@ def test_gemm_validation(L):
         assert fn(P(A), P(B), P(C), 256, 512, 64, P(A), None) == ALIAS
 
 
+def test_gemm_accum_validation(L):
+    fn = L.agoq_wgrad_gemm_int4_accum_fp8
+    D = C + (1 << 24)
+    E = C + (1 << 26)
+    assert fn(P(A), P(B), P(C), 100, 512, 64, P(D), P(E), None) == SHAPE
+    assert fn(P(A), P(B), P(C), 256, 512, 0, P(D), P(E), None) == SHAPE
+    assert fn(P(A), P(B), P(C), 256, 512, 64, None, P(E), None) == NULL
+    assert fn(P(A), P(B), P(C), 256, 512, 64, P(D), None, None) == NULL
+    assert fn(P(A), P(B), P(C), 256, 512, 64, P(D + 8), P(E), None) == ALIGN
+    assert fn(P(A), P(B), P(C), 256, 512, 64, P(D), P(E + 2), None) == ALIGN
+    assert fn(P(A), P(B), P(C), 256, 512, 64, P(A), P(E), None) == ALIAS       # master on dY
+    assert fn(P(A), P(B), P(C), 256, 512, 64, P(D), P(B), None) == ALIAS       # scales on codes
+    assert fn(P(A), P(B), P(C), 256, 512, 64, P(D), P(D + 4096), None) == ALIAS
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(agoq, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(agoq, "_L", None)
