@@ -26,7 +26,12 @@
 #define AGOQ_DEQUANT_UNROLL 2
 #endif
 #ifndef AGOQ_QUANT_MIN_CTAS
-#define AGOQ_QUANT_MIN_CTAS 4
+#define AGOQ_QUANT_MIN_CTAS 3
+#endif
+// 1: each warp issues the loads of its next group of blocks before the
+// arithmetic of the current one (register double buffering).
+#ifndef AGOQ_QUANT_PIPELINE
+#define AGOQ_QUANT_PIPELINE 1
 #endif
 #ifndef AGOQ_DEQUANT_MIN_CTAS
 #define AGOQ_DEQUANT_MIN_CTAS 1
@@ -132,18 +137,32 @@ __global__ void __launch_bounds__(kThreads, AGOQ_QUANT_MIN_CTAS) laaq_quant_kern
     const int oct = lane >> 3, j = lane & 7;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t base = warp * (4 * UNROLL); base < nblocks; base += nwarps * (4 * UNROLL)) {
-        uint4 va[UNROLL], vb[UNROLL];
+    const int64_t stride = nwarps * (4 * UNROLL);
+    auto load_group = [&](int64_t b0, uint4 (&a)[UNROLL], uint4 (&b)[UNROLL]) {
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = base + 4 * u + oct;
+            const int64_t blk = b0 + 4 * u + oct;
             if (blk < nblocks) {
-                va[u] = ld_stream(x + blk * 16 + j);
-                vb[u] = ld_stream(x + blk * 16 + 8 + j);
+                a[u] = ld_stream(x + blk * 16 + j);
+                b[u] = ld_stream(x + blk * 16 + 8 + j);
             } else {
-                va[u] = vb[u] = make_uint4(0, 0, 0, 0);
+                a[u] = b[u] = make_uint4(0, 0, 0, 0);
             }
         }
+    };
+#if AGOQ_QUANT_PIPELINE
+    // The next group's loads are issued before this group's arithmetic.
+    uint4 va[UNROLL], vb[UNROLL];
+    load_group(warp * (4 * UNROLL), va, vb);
+#endif
+    for (int64_t base = warp * (4 * UNROLL); base < nblocks; base += stride) {
+#if AGOQ_QUANT_PIPELINE
+        uint4 na[UNROLL], nb[UNROLL];
+        load_group(base + stride, na, nb);
+#else
+        uint4 va[UNROLL], vb[UNROLL];
+        load_group(base, va, vb);
+#endif
         uint32_t w[UNROLL][8];
         float s[UNROLL];
         bool fast = true;
@@ -186,6 +205,13 @@ __global__ void __launch_bounds__(kThreads, AGOQ_QUANT_MIN_CTAS) laaq_quant_kern
             store_chunk_set<BITS>(rec, j, 1, lo, hi, valid);
             if (valid && j == 0) scales[blk] = s[u];
         }
+#if AGOQ_QUANT_PIPELINE
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            va[u] = na[u];
+            vb[u] = nb[u];
+        }
+#endif
     }
 }
 
