@@ -28,6 +28,20 @@
 #ifndef AGOQ_NAIVE_ROUND_CVT
 #define AGOQ_NAIVE_ROUND_CVT 1
 #endif
+#ifndef AGOQ_REDUCE_RUNROLL
+#define AGOQ_REDUCE_RUNROLL 8
+#endif
+#ifndef AGOQ_REDUCE_COUNT_RUNROLL
+#define AGOQ_REDUCE_COUNT_RUNROLL 4
+#endif
+// 1: the naive FP8 running sum is kept as FP16 pairs (every E4M3 value is an
+//    FP16 value) and added with the mixed add.rn.f32.f16; 0: kept in binary32.
+#ifndef AGOQ_NAIVE_MIXED_ADD
+#define AGOQ_NAIVE_MIXED_ADD 1
+#endif
+#ifndef AGOQ_REDUCE_MIN_CTAS
+#define AGOQ_REDUCE_MIN_CTAS 1
+#endif
 
 namespace agoq {
 namespace {
@@ -136,8 +150,24 @@ __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict_
     }
 }
 
+// Two E4M3 codes (bits 0-15 of v) to an FP16 pair, exactly.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)v));
+    return h2;
+}
+
+// d_k = fl(f32(half k of h2) + c_k): binary32 additions of an FP16 operand.
+__device__ __forceinline__ void add_f16x2_f32(uint32_t h2, float c0, float c1, float &d0,
+                                              float &d1) {
+    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
+        "add.rn.f32.f16 %0, a, %3;\n\tadd.rn.f32.f16 %1, b, %4;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(h2), "f"(c0), "f"(c1));
+}
+
 template <bool NAIVE, int RUNROLL>
-__global__ void __launch_bounds__(kThreads) reduce_shards_kernel(
+__global__ void __launch_bounds__(kThreads, AGOQ_REDUCE_MIN_CTAS) reduce_shards_kernel(
     const uint4 *__restrict__ shards, const float *__restrict__ shard_scales, int W, int64_t n,
     int64_t nblocks, uint4 *__restrict__ out, float *__restrict__ out_scales,
     unsigned long long *__restrict__ naive_count) {
@@ -147,36 +177,82 @@ __global__ void __launch_bounds__(kThreads) reduce_shards_kernel(
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int64_t shard_vec = n / 16;   // uint4 per shard
+    const int64_t stride = nwarps * 4;
+    const int nchunk = (W + RUNROLL - 1) / RUNROLL;
+    // Codes and scales of shards ch*RUNROLL .. +RUNROLL-1 for the octet's block
+    // of the group at b0 (clamped in range; the results of idle lanes are dropped).
+    auto load = [&](int64_t b0, int ch, uint4 (&c)[RUNROLL], float (&sc)[RUNROLL]) {
+        const int64_t blk = b0 + oct;
+        const int64_t blk_c = blk < nblocks ? blk : nblocks - 1;
+#pragma unroll
+        for (int u = 0; u < RUNROLL; ++u) {
+            const int r = ch * RUNROLL + u < W ? ch * RUNROLL + u : W - 1;
+            c[u] = ld_stream(shards + (int64_t)r * shard_vec + blk_c * 8 + t8);
+            sc[u] = __ldg(shard_scales + (int64_t)r * nblocks + blk_c);
+        }
+    };
     unsigned long long overflowed = 0;
-    for (int64_t base = warp * 4; base < nblocks; base += nwarps * 4) {
-        const int64_t blk = base + oct;
-        const bool valid = blk < nblocks;
-        const int64_t blk_c = valid ? blk : nblocks - 1;   // in-range address for idle lanes
+    int64_t base = warp * 4;
+    if (base < nblocks) {
+        // The loads of the next (block group, shard chunk) are always in flight
+        // while the current chunk is accumulated.
+        uint4 cn[RUNROLL];
+        float sn[RUNROLL];
+        load(base, 0, cn, sn);
+        int ch = 0;
         float acc[16];
+#if AGOQ_NAIVE_MIXED_ADD
+        uint32_t nvh[8];   // naive running sum, FP16 pairs
+#else
         float nv[16];
+#endif
         uint32_t alive = 0xFFFFu;
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-        for (int r0 = 0; r0 < W; r0 += RUNROLL) {
+        for (;;) {
             uint4 c[RUNROLL];
-            float s[RUNROLL];
+            float sc[RUNROLL];
 #pragma unroll
             for (int u = 0; u < RUNROLL; ++u) {
-                const int r = r0 + u < W ? r0 + u : W - 1;
-                c[u] = ld_stream(shards + (int64_t)r * shard_vec + blk_c * 8 + t8);
-                s[u] = __ldg(shard_scales + (int64_t)r * nblocks + blk_c);
+                c[u] = cn[u];
+                sc[u] = sn[u];
             }
+            int64_t nbase = base;
+            int nch = ch + 1;
+            if (nch == nchunk) {
+                nch = 0;
+                nbase = base + stride;
+            }
+            if (nbase < nblocks) load(nbase, nch, cn, sn);
 #pragma unroll
             for (int u = 0; u < RUNROLL; ++u) {
-                const int r = r0 + u;
+                const int r = ch * RUNROLL + u;
                 if (r >= W) break;
                 const uint32_t w4[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
                 float e[16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) decode4(w4[q], e + 4 * q);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(e[i], s[u]));
+                for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(e[i], sc[u]));
                 if constexpr (NAIVE) {
+#if AGOQ_NAIVE_MIXED_ADD
+                    if (r == 0) {
+#pragma unroll
+                        for (int q = 0; q < 4; ++q) {
+                            nvh[2 * q] = e4m3x2_to_f16x2(w4[q] & 0xFFFFu);
+                            nvh[2 * q + 1] = e4m3x2_to_f16x2(w4[q] >> 16);
+                        }
+                    } else {
+#pragma unroll
+                        for (int p = 0; p < 8; ++p) {
+                            float t0, t1;   // exact: both operands are E4M3 values
+                            add_f16x2_f32(nvh[p], e[2 * p], e[2 * p + 1], t0, t1);
+                            if (fabsf(t0) > kE4M3Max) alive &= ~(1u << (2 * p));
+                            if (fabsf(t1) > kE4M3Max) alive &= ~(2u << (2 * p));
+                            nvh[p] = e4m3x2_to_f16x2(e4m3x2_from_f32(t0, t1));
+                        }
+                    }
+#else
                     if (r == 0) {
 #pragma unroll
                         for (int i = 0; i < 16; ++i) nv[i] = e[i];
@@ -196,20 +272,32 @@ __global__ void __launch_bounds__(kThreads) reduce_shards_kernel(
                         for (int i = 0; i < 16; ++i) nv[i] = e4m3_round_f32(tt[i]);
 #endif
                     }
+#endif
                 }
             }
-        }
-        float am = 0.0f;
+            if (nch == 0) {
+                // all W shards of the block group are in: requantize and store
+                const int64_t blk = base + oct;
+                const bool valid = blk < nblocks;
+                float am = 0.0f;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(acc[i]));
-        am = octet_max(am);
-        const float snew = __fdiv_rn(am, kE4M3Max);
-        const uint2 lo = requant8(acc, snew);
-        const uint2 hi = requant8(acc + 8, snew);
-        if (valid) {
-            out[blk * 8 + t8] = make_uint4(lo.x, lo.y, hi.x, hi.y);
-            if (t8 == 0) out_scales[blk] = snew;
-            if constexpr (NAIVE) overflowed += (unsigned long long)__popc(~alive & 0xFFFFu);
+                for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(acc[i]));
+                am = octet_max(am);
+                const float snew = __fdiv_rn(am, kE4M3Max);
+                const uint2 lo = requant8(acc, snew);
+                const uint2 hi = requant8(acc + 8, snew);
+                if (valid) {
+                    out[blk * 8 + t8] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                    if (t8 == 0) out_scales[blk] = snew;
+                    if constexpr (NAIVE) overflowed += (unsigned long long)__popc(~alive & 0xFFFFu);
+                }
+#pragma unroll
+                for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+                alive = 0xFFFFu;
+            }
+            if (nbase >= nblocks) break;
+            base = nbase;
+            ch = nch;
         }
     }
     if constexpr (NAIVE) {
@@ -243,7 +331,7 @@ cudaError_t launch_grad_accum(void *master, float *master_scales, const void *gr
 cudaError_t launch_reduce_shards(const void *shards, const float *shard_scales, int W, int64_t n,
                                  void *out, float *out_scales, unsigned long long *naive_count,
                                  cudaStream_t st) {
-    constexpr int kRUnroll = 4;
+    constexpr int kRUnroll = AGOQ_REDUCE_RUNROLL;
     const int64_t nb = n / kBlock;
     const int64_t per_cta = 4 * (kThreads / 32);
     const int64_t ctas = (nb + per_cta - 1) / per_cta;
@@ -251,7 +339,7 @@ cudaError_t launch_reduce_shards(const void *shards, const float *shard_scales, 
         cudaError_t e = cudaMemsetAsync(naive_count, 0, sizeof(unsigned long long), st);
         if (e != cudaSuccess) return e;
         static int cache[kMaxDevices];
-        auto k = reduce_shards_kernel<true, kRUnroll>;
+        auto k = reduce_shards_kernel<true, AGOQ_REDUCE_COUNT_RUNROLL>;
         return launch_pdl(k, resident_grid(k, cache, ctas), kThreads, 0, st,
                           static_cast<const uint4 *>(shards), shard_scales, W, n, nb,
                           static_cast<uint4 *>(out), out_scales, naive_count);
