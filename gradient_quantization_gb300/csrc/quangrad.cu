@@ -28,6 +28,12 @@
 #ifndef AGOQ_NAIVE_ROUND_CVT
 #define AGOQ_NAIVE_ROUND_CVT 1
 #endif
+#ifndef AGOQ_ACCUM_PIPELINE
+#define AGOQ_ACCUM_PIPELINE 0
+#endif
+#ifndef AGOQ_ACCUM_UNROLL
+#define AGOQ_ACCUM_UNROLL 4
+#endif
 #ifndef AGOQ_REDUCE_RUNROLL
 #define AGOQ_REDUCE_RUNROLL 8
 #endif
@@ -108,13 +114,11 @@ __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict_
     const int half = lane >> 4, j = lane & 15;
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    for (int64_t base = warp * (2 * UNROLL); base < nblocks; base += nwarps * (2 * UNROLL)) {
-        uint2 mc[UNROLL];
-        uint4 g[UNROLL];
-        float s[UNROLL];
+    const int64_t stride = nwarps * (2 * UNROLL);
+    auto load = [&](int64_t b0, uint2 (&mc)[UNROLL], float (&s)[UNROLL], uint4 (&g)[UNROLL]) {
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = base + 2 * u + half;
+            const int64_t blk = b0 + 2 * u + half;
             if (blk < nblocks) {
                 mc[u] = master[blk * 16 + j];
                 s[u] = scales[blk];
@@ -125,6 +129,30 @@ __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict_
                 g[u] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
+    };
+#if AGOQ_ACCUM_PIPELINE
+    // The next group's loads are issued before this group's arithmetic (each
+    // lane reads and rewrites only its own master words, so reading ahead is safe).
+    uint2 mcn[UNROLL];
+    float sn[UNROLL];
+    uint4 gn[UNROLL];
+    load(warp * (2 * UNROLL), mcn, sn, gn);
+#endif
+    for (int64_t base = warp * (2 * UNROLL); base < nblocks; base += stride) {
+        uint2 mc[UNROLL];
+        uint4 g[UNROLL];
+        float s[UNROLL];
+#if AGOQ_ACCUM_PIPELINE
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            mc[u] = mcn[u];
+            s[u] = sn[u];
+            g[u] = gn[u];
+        }
+        load(base + stride, mcn, sn, gn);
+#else
+        load(base, mc, s, g);
+#endif
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t blk = base + 2 * u + half;
@@ -318,7 +346,7 @@ int resident_grid(K kernel, int *cache, int64_t work_ctas) {
 
 cudaError_t launch_grad_accum(void *master, float *master_scales, const void *grad, int64_t n,
                               cudaStream_t st) {
-    constexpr int kUnroll = 2;
+    constexpr int kUnroll = AGOQ_ACCUM_UNROLL;
     static int cache[kMaxDevices];
     const int64_t nb = n / kBlock;
     auto k = grad_accum_kernel<kUnroll>;
