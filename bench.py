@@ -50,7 +50,10 @@ FALLBACK_BF16_TFLOPS = 1900.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch, from the ncu captures
 # summarised in profiles/ (laaq_quant_b5_dbca_8192x4096_8192x11008.md); valid only
 # while those kernels are unchanged -- remove an entry when its kernel changes.
-DOMINANT_TRAFFIC_BYTES = {}
+DOMINANT_TRAFFIC_BYTES = {
+    "quant_b5_silu_in": 180406528 + 11280384,
+    "quant_b5_rmsnorm_in": 67150080 + 2028544,
+}
 
 
 def act_bytes(n, bits):
