@@ -71,6 +71,33 @@ uint16_t or_f32_to_bf16(float f)
 }
 
 /* ------------------------------------------------------------------------- */
+/* Rounding a binary64 value to a binary floating-point format with p significand
+ * bits (the leading one included), smallest normal exponent emin and largest
+ * exponent emax: to nearest, ties to even, with gradual underflow below 2^emin;
+ * a result beyond the largest finite value 2^emax * (2 - 2^(1-p)) becomes
+ * infinity (so the midpoint above it, a tie, goes to infinity as IEEE 754
+ * rounds it).  The value is scaled by its quantum (a power of two, exact),
+ * rounded to an integer with nearbyint in the default rounding mode (ties to
+ * even) and scaled back (exact).  BF16: p = 8, emin = -126, emax = 127;
+ * FP16 (IEEE binary16): p = 11, emin = -14, emax = 15.                         */
+double or_round_format(double v, int p, int emin, int emax)
+{
+    if (v == 0.0 || isnan(v) || isinf(v))
+        return v;
+    int e;
+    frexp(fabs(v), &e); /* |v| in [2^(e-1), 2^e) */
+    int lead = e - 1;
+    if (lead < emin)
+        lead = emin;
+    double quantum = ldexp(1.0, lead - (p - 1));
+    double out = nearbyint(v / quantum) * quantum;
+    double maxf = ldexp(2.0 - ldexp(1.0, 1 - p), emax);
+    if (fabs(out) > maxf)
+        return copysign(INFINITY, v);
+    return out;
+}
+
+/* ------------------------------------------------------------------------- */
 /* FP8 E4M3 in its "FN" form (OCP 8-bit floating point): 1 sign bit, 4 exponent
  * bits with bias 7, 3 fraction bits; exponent field 0 is subnormal with value
  * m * 2^-9; S.1111.111 is NaN; there is no infinity; the largest finite
@@ -254,6 +281,40 @@ int or_grad_accum_fp8(uint8_t *master, float *master_scales, const uint16_t *gra
         for (int i = 0; i < OR_BLOCK; ++i) {
             float m = or_e4m3_to_f32(cb[i]) * s;
             t[i] = m + or_bf16_to_f32(grad[b * OR_BLOCK + i]);
+        }
+        or_requant_block(t, cb, &master_scales[b]);
+    }
+    return OR_OK;
+}
+
+/* QuanGrad local accumulation with the intermediate held in BF16 or FP16, as
+ * the summary states it ([AGoQ] §2.B "Lokale accumulatie": the FP8 master is
+ * dequantized to FP16/BF16, the new local gradient is added, the sum is
+ * quantized back to FP8).  With R the rounding to the intermediate format
+ * (mid = 1: BF16, mid = 2: FP16; or_round_format), per element:
+ *   m = R(fl(e4m3(c_i) * s))      the dequantized master (binary32 product, then R)
+ *   g = R(bf16(g_i))              the BF16 gradient in the intermediate format
+ *   t = R(m + g)                  the sum, rounded once
+ * then or_requant_block on t.  m and g have at most 11 significant bits, so
+ * their binary64 sum is exact unless the smaller is below 2^-42 of the larger,
+ * where it cannot move the rounding to the format; R of the binary64 sum is
+ * therefore R of the exact sum.  In FP16 the intermediate overflows to
+ * infinity beyond 65504 (a precondition of that format, not checked).          */
+int or_grad_accum_fp8_mid(uint8_t *master, float *master_scales, const uint16_t *grad, int64_t n,
+                          int mid)
+{
+    if (n < 0 || n % OR_BLOCK || (mid != 1 && mid != 2))
+        return OR_BAD_ARG;
+    const int p = mid == 1 ? 8 : 11, emin = mid == 1 ? -126 : -14, emax = mid == 1 ? 127 : 15;
+    float t[OR_BLOCK];
+    for (int64_t b = 0; b < n / OR_BLOCK; ++b) {
+        uint8_t *cb = master + b * OR_BLOCK;
+        float s = master_scales[b];
+        for (int i = 0; i < OR_BLOCK; ++i) {
+            float m32 = or_e4m3_to_f32(cb[i]) * s;
+            double m = or_round_format((double)m32, p, emin, emax);
+            double g = or_round_format((double)or_bf16_to_f32(grad[b * OR_BLOCK + i]), p, emin, emax);
+            t[i] = (float)or_round_format(m + g, p, emin, emax); /* exact in binary32 */
         }
         or_requant_block(t, cb, &master_scales[b]);
     }
@@ -454,6 +515,12 @@ void or_f32_to_e4m3_array(const float *src, uint8_t *dst, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)
         dst[i] = or_f32_to_e4m3(src[i]);
+}
+
+void or_round_format_array(const double *src, double *dst, int64_t n, int p, int emin, int emax)
+{
+    for (int64_t i = 0; i < n; ++i)
+        dst[i] = or_round_format(src[i], p, emin, emax);
 }
 
 void or_e4m3_to_f32_array(const uint8_t *src, float *dst, int64_t n)

@@ -36,6 +36,8 @@ def lib():
         L.or_wgrad_gemm_int4_f64.argtypes = [vp, vp, vp, i32, i32, i32, vp]
         L.or_wgrad_gemm_int4_f64_entries.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp]
         L.or_grad_accum_fp8_f32.argtypes = [vp, vp, vp, i64]
+        L.or_grad_accum_fp8_mid.argtypes = [vp, vp, vp, i64, i32]
+        L.or_round_format_array.argtypes = [vp, vp, i64, i32, i32, i32]
         L.or_wgrad_accum_fp8.argtypes = [vp, vp, vp, i32, i32, i32, vp, i64, vp, vp]
         L.or_f32_to_bf16_array.argtypes = [vp, vp, i64]
         L.or_f32_to_e4m3_array.argtypes = [vp, vp, i64]
@@ -43,9 +45,10 @@ def lib():
         for name in ("or_quant_act", "or_dequant_act", "or_grad_accum_fp8",
                      "or_reduce_fp8_shards", "or_wgrad_gemm_int4_f64",
                      "or_wgrad_gemm_int4_f64_entries", "or_grad_accum_fp8_f32",
-                     "or_wgrad_accum_fp8"):
+                     "or_wgrad_accum_fp8", "or_grad_accum_fp8_mid"):
             getattr(L, name).restype = ctypes.c_int
-        for name in ("or_f32_to_bf16_array", "or_f32_to_e4m3_array", "or_e4m3_to_f32_array"):
+        for name in ("or_f32_to_bf16_array", "or_f32_to_e4m3_array", "or_e4m3_to_f32_array",
+                     "or_round_format_array"):
             getattr(L, name).restype = None
         _lib = L
     return _lib
@@ -207,4 +210,28 @@ def wgrad_accum_fp8(dY_bf16, x_codes, x_scales, M, N, K, master, master_scales, 
     _check(lib().or_wgrad_accum_fp8(_ptr(dY), _ptr(xc), _ptr(xs), M, N, K,
                                     _ptr(b) if b is not None else None, count, _ptr(m), _ptr(s)),
            "wgrad_accum_fp8")
+    return m, s
+
+
+MID_BF16, MID_FP16 = 1, 2
+_FORMATS = {MID_BF16: (8, -126, 127), MID_FP16: (11, -14, 15)}
+
+
+def round_format(x, mid):
+    """Round binary64 values to BF16 (mid=1) or FP16 (mid=2), to nearest even; returns float64."""
+    src = _contig(np.asarray(x, np.float64), np.float64).reshape(-1)
+    dst = np.empty_like(src)
+    p, emin, emax = _FORMATS[mid]
+    lib().or_round_format_array(_ptr(src), _ptr(dst), src.size, p, emin, emax)
+    return dst
+
+
+def grad_accum_fp8_mid(master, master_scales, grad_bf16, mid):
+    """QuanGrad accumulation with a BF16 (mid=1) or FP16 (mid=2) intermediate."""
+    m = _contig(master, np.uint8).reshape(-1).copy()
+    s = _contig(master_scales, np.float32).reshape(-1).copy()
+    g = _contig(grad_bf16, np.uint16).reshape(-1)
+    if g.size != m.size or s.size != m.size // BLOCK:
+        raise ValueError("shape mismatch")
+    _check(lib().or_grad_accum_fp8_mid(_ptr(m), _ptr(s), _ptr(g), m.size, mid), "grad_accum_fp8_mid")
     return m, s

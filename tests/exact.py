@@ -78,3 +78,28 @@ def to_e4m3_code(q: Fraction, negative_zero: bool = False) -> int:
 def e4m3_value(code: int) -> Fraction:
     mag = _MAGS[code & 0x7F]
     return -mag if code & 0x80 else mag
+
+
+def round_format(q: Fraction, p: int, emin: int, emax: int):
+    """Nearest value of a binary format with p significand bits, smallest normal
+    exponent emin and largest exponent emax, ties to even, gradual underflow;
+    beyond the largest finite value the result is +-inf (a float).  Returns a
+    Fraction for finite results.  The sign of a zero result is not tracked."""
+    if q == 0:
+        return Fraction(0)
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    e = math.floor(math.log2(a.numerator) - math.log2(a.denominator))
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    quantum = Fraction(2) ** (max(e, emin) - (p - 1))
+    r = round_half_even(a / quantum) * quantum
+    if r > (2 - Fraction(2) ** (1 - p)) * Fraction(2) ** emax:
+        return sign * math.inf
+    return sign * r
+
+
+BF16_FORMAT = (8, -126, 127)
+FP16_FORMAT = (11, -14, 15)
