@@ -474,6 +474,10 @@ def rows_arm(device, hbm_peak, bf16_peak):
     nbytes = n * 4 + (n // 128) * 8
     row("quangrad_accum_2^30", nbytes, n,
         _time_launch(lambda: agoq.agoq_grad_accum_fp8(m, ms_, g), flush, reps=5, warm=1))
+    for mid, label in ((agoq.MID_BF16, "bf16"), (agoq.MID_FP16, "fp16")):
+        row("quangrad_accum_%smid_2^30" % label, nbytes, n,
+            _time_launch(lambda mid=mid: agoq.agoq_grad_accum_fp8_mid(m, ms_, g, mid), flush,
+                         reps=5, warm=1))
     del m, ms_, g
 
     # FP8 shard local reduce, 2^25 elements per shard

@@ -22,7 +22,8 @@ HEADER = os.path.join(os.path.dirname(HERE), "include", "agoq.h")
 BLOCK = 128
 
 STATUS = {0: "AGOQ_OK", 1: "AGOQ_ERR_NULL", 2: "AGOQ_ERR_SHAPE", 3: "AGOQ_ERR_BITS",
-          4: "AGOQ_ERR_ALIGN", 5: "AGOQ_ERR_ALIAS", 6: "AGOQ_ERR_CUDA", 7: "AGOQ_ERR_TIMEOUT"}
+          4: "AGOQ_ERR_ALIGN", 5: "AGOQ_ERR_ALIAS", 6: "AGOQ_ERR_CUDA", 7: "AGOQ_ERR_TIMEOUT",
+          8: "AGOQ_ERR_FORMAT"}
 
 
 class AgoqError(RuntimeError):
@@ -49,6 +50,7 @@ def _lib_handle():
         L.agoq_quant_act.argtypes = [vp, i64, i32, vp, vp, vp]
         L.agoq_dequant_act.argtypes = [vp, vp, i64, i32, vp, vp]
         L.agoq_grad_accum_fp8.argtypes = [vp, vp, vp, i64, vp]
+        L.agoq_grad_accum_fp8_mid.argtypes = [vp, vp, vp, i64, i32, vp]
         L.agoq_reduce_fp8_shards.argtypes = [vp, vp, i32, i64, vp, vp, vp, vp]
         L.agoq_wgrad_gemm_int4.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
         L.agoq_wgrad_gemm_int4_f32out.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
@@ -152,6 +154,24 @@ def agoq_grad_accum_fp8(master, master_scales, grad, stream=None):
         raise ValueError("master/scales do not match the gradient size")
     _check(lib().agoq_grad_accum_fp8(_ptr(master), _ptr(master_scales), _ptr(grad), n,
                                      _stream(stream)), "agoq_grad_accum_fp8")
+    return master, master_scales
+
+
+MID_FP32, MID_BF16, MID_FP16 = 0, 1, 2
+
+
+def agoq_grad_accum_fp8_mid(master, master_scales, grad, mid_format, stream=None):
+    """In-place QuanGrad accumulation with the intermediate held in binary32
+    (MID_FP32), BF16 (MID_BF16) or FP16 (MID_FP16)."""
+    _need(master, torch.uint8, "master")
+    _need(master_scales, torch.float32, "master_scales")
+    _need(grad, torch.bfloat16, "grad")
+    n = grad.numel()
+    if master.numel() != n or master_scales.numel() != n // BLOCK:
+        raise ValueError("master/scales do not match the gradient size")
+    _check(lib().agoq_grad_accum_fp8_mid(_ptr(master), _ptr(master_scales), _ptr(grad), n,
+                                         int(mid_format), _stream(stream)),
+           "agoq_grad_accum_fp8_mid")
     return master, master_scales
 
 

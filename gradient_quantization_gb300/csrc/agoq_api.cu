@@ -57,6 +57,7 @@ const char *agoq_status_string(agoq_status s) {
         case AGOQ_ERR_ALIAS: return "AGOQ_ERR_ALIAS: an output overlaps an input";
         case AGOQ_ERR_CUDA: return "AGOQ_ERR_CUDA: CUDA runtime error";
         case AGOQ_ERR_TIMEOUT: return "AGOQ_ERR_TIMEOUT: a GEMM pipeline wait gave up";
+        case AGOQ_ERR_FORMAT: return "AGOQ_ERR_FORMAT: unsupported intermediate format";
     }
     return "AGOQ_ERR_UNKNOWN";
 }
@@ -95,7 +96,15 @@ agoq_status agoq_dequant_act(const void *codes, const float *scales, int64_t n, 
 
 agoq_status agoq_grad_accum_fp8(void *master_e4m3, float *master_scales, const void *grad_bf16,
                                 int64_t n, void *stream) {
+    return agoq_grad_accum_fp8_mid(master_e4m3, master_scales, grad_bf16, n, AGOQ_MID_FP32, stream);
+}
+
+agoq_status agoq_grad_accum_fp8_mid(void *master_e4m3, float *master_scales,
+                                    const void *grad_bf16, int64_t n, int mid_format,
+                                    void *stream) {
     using namespace agoq;
+    if (mid_format != AGOQ_MID_FP32 && mid_format != AGOQ_MID_BF16 && mid_format != AGOQ_MID_FP16)
+        return AGOQ_ERR_FORMAT;
     if (n < 0 || n % kBlockElems) return AGOQ_ERR_SHAPE;
     if (n == 0) return AGOQ_OK;
     if (!master_e4m3 || !master_scales || !grad_bf16) return AGOQ_ERR_NULL;
@@ -106,7 +115,8 @@ agoq_status agoq_grad_accum_fp8(void *master_e4m3, float *master_scales, const v
     if (overlap(master_e4m3, mb, grad_bf16, gb) || overlap(master_scales, sb, grad_bf16, gb) ||
         overlap(master_e4m3, mb, master_scales, sb))
         return AGOQ_ERR_ALIAS;
-    return from_cuda(launch_grad_accum(master_e4m3, master_scales, grad_bf16, n, as_stream(stream)));
+    return from_cuda(
+        launch_grad_accum(master_e4m3, master_scales, grad_bf16, n, mid_format, as_stream(stream)));
 }
 
 agoq_status agoq_reduce_fp8_shards(const void *shards_e4m3, const float *shard_scales, int W,

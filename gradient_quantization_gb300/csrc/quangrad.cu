@@ -104,7 +104,39 @@ __device__ __forceinline__ void decode4(uint32_t w, float e[4]) {
 #endif
 }
 
-template <int UNROLL>
+// Intermediate formats of the accumulation: MID 0 binary32 (t = fl(m + g));
+// MID 1 BF16 and MID 2 FP16 (m and g rounded to the format, their sum rounded
+// once to it: the page's "dequantize to FP16/BF16, add").
+constexpr int kMidF32 = 0, kMidBf16 = 1, kMidF16 = 2;
+
+// In place on t[8] (binary32 products fl(e4m3(c) * s)) and the 8 BF16 gradient
+// values of g: t = R(R(t) + R(g)) with R the rounding to the MID format.  The
+// format's own add rounds the exact sum once.
+template <int MID>
+__device__ __forceinline__ void add_in_format(float t[8], const uint4 &g) {
+    const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        uint32_t r;
+        if constexpr (MID == kMidBf16) {
+            const uint32_t m = pack_bf16x2(t[2 * p], t[2 * p + 1]);
+            asm("add.rn.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(gw[p]));
+            t[2 * p] = bf16_lo(r);
+            t[2 * p + 1] = bf16_hi(r);
+        } else {
+            uint32_t m, gh;
+            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(m) : "f"(t[2 * p + 1]), "f"(t[2 * p]));
+            asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(gh) : "f"(bf16_hi(gw[p])), "f"(bf16_lo(gw[p])));
+            asm("add.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(gh));
+            asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\t"
+                "cvt.f32.f16 %1, b;\n\t}"
+                : "=f"(t[2 * p]), "=f"(t[2 * p + 1])
+                : "r"(r));
+        }
+    }
+}
+
+template <int UNROLL, int MID>
 __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict__ master,
                                                               float *__restrict__ scales,
                                                               const uint4 *__restrict__ grad,
@@ -162,11 +194,14 @@ __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict_
             decode_mul4(mc[u].x, s[u], t);
             decode_mul4(mc[u].y, s[u], t + 4);
             float am = 0.0f;
+            if constexpr (MID == kMidF32) {
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-                t[i] = __fadd_rn(t[i], gv[i]);
-                am = fmaxf(am, fabsf(t[i]));
+                for (int i = 0; i < 8; ++i) t[i] = __fadd_rn(t[i], gv[i]);
+            } else {
+                add_in_format<MID>(t, g[u]);
             }
+#pragma unroll
+            for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(t[i]));
             am = halfwarp_max(am);
             const float snew = __fdiv_rn(am, kE4M3Max);
             const uint2 out = requant8(t, snew);
@@ -344,16 +379,28 @@ int resident_grid(K kernel, int *cache, int64_t work_ctas) {
 
 }  // namespace
 
-cudaError_t launch_grad_accum(void *master, float *master_scales, const void *grad, int64_t n,
-                              cudaStream_t st) {
+namespace {
+template <int MID>
+cudaError_t launch_grad_accum_mid(void *master, float *master_scales, const void *grad, int64_t n,
+                                  cudaStream_t st) {
     constexpr int kUnroll = AGOQ_ACCUM_UNROLL;
     static int cache[kMaxDevices];
     const int64_t nb = n / kBlock;
-    auto k = grad_accum_kernel<kUnroll>;
+    auto k = grad_accum_kernel<kUnroll, MID>;
     const int64_t per_cta = 2 * kUnroll * (kThreads / 32);
     return launch_pdl(k, resident_grid(k, cache, (nb + per_cta - 1) / per_cta), kThreads, 0, st,
                       static_cast<uint2 *>(master), master_scales,
                       static_cast<const uint4 *>(grad), nb);
+}
+}  // namespace
+
+cudaError_t launch_grad_accum(void *master, float *master_scales, const void *grad, int64_t n,
+                              int mid, cudaStream_t st) {
+    switch (mid) {
+        case kMidBf16: return launch_grad_accum_mid<kMidBf16>(master, master_scales, grad, n, st);
+        case kMidF16: return launch_grad_accum_mid<kMidF16>(master, master_scales, grad, n, st);
+        default: return launch_grad_accum_mid<kMidF32>(master, master_scales, grad, n, st);
+    }
 }
 
 cudaError_t launch_reduce_shards(const void *shards, const float *shard_scales, int W, int64_t n,

@@ -55,8 +55,16 @@ typedef enum {
     AGOQ_ERR_ALIGN = 4,   /* pointer not aligned as required */
     AGOQ_ERR_ALIAS = 5,   /* an output overlaps an input */
     AGOQ_ERR_CUDA = 6,    /* the CUDA runtime reported an error at launch */
-    AGOQ_ERR_TIMEOUT = 7  /* a GEMM pipeline wait gave up (see agoq_device_status) */
+    AGOQ_ERR_TIMEOUT = 7, /* a GEMM pipeline wait gave up (see agoq_device_status) */
+    AGOQ_ERR_FORMAT = 8   /* unsupported intermediate format (agoq_grad_accum_fp8_mid) */
 } agoq_status;
+
+/* Intermediate formats of the QuanGrad accumulation (agoq_grad_accum_fp8_mid). */
+typedef enum {
+    AGOQ_MID_FP32 = 0,  /* binary32 (agoq_grad_accum_fp8) */
+    AGOQ_MID_BF16 = 1,
+    AGOQ_MID_FP16 = 2
+} agoq_mid_format;
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *agoq_status_string(agoq_status status);
@@ -98,6 +106,23 @@ agoq_status agoq_dequant_act(const void *codes, const float *scales, int64_t n, 
  */
 agoq_status agoq_grad_accum_fp8(void *master_e4m3, float *master_scales, const void *grad_bf16,
                                 int64_t n, void *stream);
+
+/*
+ * The same accumulation with the intermediate held in the format the page
+ * names (AGoQ section 2.B, "Lokale accumulatie": the FP8 master gradient is
+ * dequantized to FP16/BF16, the new gradient added, the sum requantized).
+ * With R the rounding to nearest even to the intermediate format, per element
+ *   m_i = R(fl32(e4m3(c_i) * scale));  g_i' = R(g_i);  t_i = R(m_i + g_i')
+ * (the exact sum rounded once), then the requantization of
+ * agoq_grad_accum_fp8.  mid_format: AGOQ_MID_FP32 (identical to
+ * agoq_grad_accum_fp8), AGOQ_MID_BF16 or AGOQ_MID_FP16; anything else returns
+ * AGOQ_ERR_FORMAT.  FP16 has gradual underflow below 2^-14 and overflows to
+ * infinity beyond 65504: magnitudes must stay below that (not checked).
+ * Other arguments and errors as agoq_grad_accum_fp8.
+ */
+agoq_status agoq_grad_accum_fp8_mid(void *master_e4m3, float *master_scales,
+                                    const void *grad_bf16, int64_t n, int mid_format,
+                                    void *stream);
 
 /*
  * Local reduce of the precision-preserved all-reduce (AGoQ section 2.B,

@@ -32,7 +32,7 @@ def test_exports_are_c_symbols():
 
 
 def test_status_strings(L):
-    for code in range(8):
+    for code in range(9):
         s = L.agoq_status_string(code).decode()
         assert s.startswith(agoq.STATUS[code])
     assert L.agoq_status_string(99).decode() == "AGOQ_ERR_UNKNOWN"
@@ -75,6 +75,19 @@ def test_grad_accum_validation(L):
     assert L.agoq_grad_accum_fp8(P(A + 1), P(B), P(C), 128, None) == ALIGN
     assert L.agoq_grad_accum_fp8(P(A), P(B), P(A + 64), 128, None) == ALIAS
     assert L.agoq_grad_accum_fp8(P(A), P(B), P(C), 0, None) == OK
+
+
+def test_grad_accum_mid_validation(L):
+    FORMAT = 8
+    fn = L.agoq_grad_accum_fp8_mid
+    assert fn(P(A), P(B), P(C), 128, 3, None) == FORMAT
+    assert fn(P(A), P(B), P(C), 128, -1, None) == FORMAT
+    assert fn(P(A), P(B), P(C), 127, 1, None) == SHAPE
+    assert fn(None, P(B), P(C), 128, 2, None) == NULL
+    assert fn(P(A + 1), P(B), P(C), 128, 1, None) == ALIGN
+    assert fn(P(A), P(B), P(A + 64), 128, 2, None) == ALIAS
+    for mid in (0, 1, 2):
+        assert fn(P(A), P(B), P(C), 0, mid, None) == OK
 
 
 def test_reduce_validation(L):
