@@ -247,6 +247,36 @@ int or_dequant_act(const uint8_t *codes, const float *scales, int64_t n, int bit
     return OR_OK;
 }
 
+/* Backward of SiLU recomputed from the stored low-bit input, [AGoQ] §2.A
+ * "Herberekening versus Caching": only the quantized input x is kept; the
+ * backward pass dequantizes it and recomputes what it needs.  With
+ * xh = bf16(fl(c * s)) (exactly or_dequant_act), sigma = 1 / (1 + exp(-xh)):
+ *   silu(xh)  = xh * sigma                          -> y[i]  (binary64)
+ *   silu'(xh) = sigma * (1 + xh * (1 - sigma))      (the derivative of x * sigma(x))
+ *   dx[i]     = dy[i] * silu'(xh)                   -> dx[i] (binary64)
+ * in binary64 throughout: the reference values the GPU's rounded BF16
+ * outputs are measured against.  y may be NULL.                              */
+int or_silu_backward(const uint8_t *codes, const float *scales, const uint16_t *dy, int64_t n,
+                     int bits, double *dx, double *y)
+{
+    if (!or_bits_ok(bits) || n < 0 || n % OR_BLOCK)
+        return OR_BAD_ARG;
+    const int64_t rec_bytes = 16 * (int64_t)bits;
+    for (int64_t b = 0; b < n / OR_BLOCK; ++b) {
+        const uint8_t *rec = codes + b * rec_bytes;
+        float s = scales[b];
+        for (int i = 0; i < OR_BLOCK; ++i) {
+            const int64_t k = b * OR_BLOCK + i;
+            double xh = (double)or_bf16_to_f32(or_f32_to_bf16((float)or_get_field(rec, i, bits) * s));
+            double sigma = 1.0 / (1.0 + exp(-xh));
+            dx[k] = (double)or_bf16_to_f32(dy[k]) * (sigma * (1.0 + xh * (1.0 - sigma)));
+            if (y)
+                y[k] = xh * sigma;
+        }
+    }
+    return OR_OK;
+}
+
 /* Requantize 128 binary32 values to E4M3 with a fresh block scale:
  * s' = fl(absmax / 448); c_i = e4m3_rne_satfinite(fl(t_i / s')).
  * An all-zero block (absmax 0, whatever the signs) stores s' = +0, codes 0x00. */

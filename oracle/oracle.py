@@ -37,6 +37,7 @@ def lib():
         L.or_wgrad_gemm_int4_f64_entries.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, i64, vp]
         L.or_grad_accum_fp8_f32.argtypes = [vp, vp, vp, i64]
         L.or_grad_accum_fp8_mid.argtypes = [vp, vp, vp, i64, i32]
+        L.or_silu_backward.argtypes = [vp, vp, vp, i64, i32, vp, vp]
         L.or_round_format_array.argtypes = [vp, vp, i64, i32, i32, i32]
         L.or_wgrad_accum_fp8.argtypes = [vp, vp, vp, i32, i32, i32, vp, i64, vp, vp]
         L.or_f32_to_bf16_array.argtypes = [vp, vp, i64]
@@ -45,7 +46,7 @@ def lib():
         for name in ("or_quant_act", "or_dequant_act", "or_grad_accum_fp8",
                      "or_reduce_fp8_shards", "or_wgrad_gemm_int4_f64",
                      "or_wgrad_gemm_int4_f64_entries", "or_grad_accum_fp8_f32",
-                     "or_wgrad_accum_fp8", "or_grad_accum_fp8_mid"):
+                     "or_wgrad_accum_fp8", "or_grad_accum_fp8_mid", "or_silu_backward"):
             getattr(L, name).restype = ctypes.c_int
         for name in ("or_f32_to_bf16_array", "or_f32_to_e4m3_array", "or_e4m3_to_f32_array",
                      "or_round_format_array"):
@@ -235,3 +236,17 @@ def grad_accum_fp8_mid(master, master_scales, grad_bf16, mid):
         raise ValueError("shape mismatch")
     _check(lib().or_grad_accum_fp8_mid(_ptr(m), _ptr(s), _ptr(g), m.size, mid), "grad_accum_fp8_mid")
     return m, s
+
+
+def silu_backward(codes, scales, dy_bf16, n, bits, want_y=True):
+    """SiLU backward recomputed from LAAQ codes: (dx, y) in binary64 (y None if not wanted)."""
+    codes = _contig(codes, np.uint8).reshape(-1)
+    scales = _contig(scales, np.float32).reshape(-1)
+    dy = _contig(dy_bf16, np.uint16).reshape(-1)
+    if codes.size < n // BLOCK * record_bytes(bits) or scales.size < n // BLOCK or dy.size != n:
+        raise ValueError("shape mismatch")
+    dx = np.empty(n, np.float64)
+    y = np.empty(n, np.float64) if want_y else None
+    _check(lib().or_silu_backward(_ptr(codes), _ptr(scales), _ptr(dy), n, bits, _ptr(dx),
+                                  _ptr(y) if want_y else None), "silu_backward")
+    return dx, y
