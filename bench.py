@@ -465,6 +465,21 @@ def rows_arm(device, hbm_peak, bf16_peak):
         _time_launch(lambda: agoq.agoq_dequant_act(c, s, n, 4, y), flush))
     del x, c, s, y
 
+    # SiLU backward recomputed from the 4-bit SiLU input (8192 x 11008)
+    xs_ = synthetic.dbca_activations_torch(seed=1, device=device)[1]
+    n = xs_.numel()
+    c, s = agoq.agoq_quant_act(xs_, 4)
+    del xs_
+    dy = torch.randn(n, device=device).to(torch.bfloat16)
+    dx = torch.empty_like(dy)
+    y = torch.empty_like(dy)
+    base = n * 4 // 8 + (n // 128) * 4 + 2 * n + 2 * n
+    row("silu_backward_b4_8192x11008", base, n,
+        _time_launch(lambda: agoq.agoq_silu_backward(c, s, dy, n, 4, dx), flush))
+    row("silu_backward_b4_with_forward_8192x11008", base + 2 * n, n,
+        _time_launch(lambda: agoq.agoq_silu_backward(c, s, dy, n, 4, dx, y), flush))
+    del c, s, dy, dx, y
+
     # QuanGrad accumulation, 2^30 elements
     n = synthetic.QUANGRAD_N
     m = torch.zeros(n, dtype=torch.uint8, device=device)

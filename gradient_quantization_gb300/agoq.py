@@ -50,6 +50,7 @@ def _lib_handle():
         L.agoq_quant_act.argtypes = [vp, i64, i32, vp, vp, vp]
         L.agoq_dequant_act.argtypes = [vp, vp, i64, i32, vp, vp]
         L.agoq_grad_accum_fp8.argtypes = [vp, vp, vp, i64, vp]
+        L.agoq_silu_backward.argtypes = [vp, vp, vp, i64, i32, vp, vp, vp]
         L.agoq_grad_accum_fp8_mid.argtypes = [vp, vp, vp, i64, i32, vp]
         L.agoq_reduce_fp8_shards.argtypes = [vp, vp, i32, i64, vp, vp, vp, vp]
         L.agoq_wgrad_gemm_int4.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
@@ -155,6 +156,24 @@ def agoq_grad_accum_fp8(master, master_scales, grad, stream=None):
     _check(lib().agoq_grad_accum_fp8(_ptr(master), _ptr(master_scales), _ptr(grad), n,
                                      _stream(stream)), "agoq_grad_accum_fp8")
     return master, master_scales
+
+
+def agoq_silu_backward(codes, scales, dy, n, bits, dx=None, y=None, want_y=False, stream=None):
+    """SiLU backward recomputed from LAAQ codes: returns (dx, y) as BF16 tensors
+    (y is None unless `y` is given or want_y is set)."""
+    _need(codes, torch.uint8, "codes")
+    _need(scales, torch.float32, "scales")
+    _need(dy, torch.bfloat16, "dy")
+    if dx is None:
+        dx = torch.empty(n, dtype=torch.bfloat16, device=dy.device)
+    if y is None and want_y:
+        y = torch.empty(n, dtype=torch.bfloat16, device=dy.device)
+    _need(dx, torch.bfloat16, "dx")
+    if y is not None:
+        _need(y, torch.bfloat16, "y")
+    _check(lib().agoq_silu_backward(_ptr(codes), _ptr(scales), _ptr(dy), n, bits, _ptr(dx),
+                                    _ptr(y), _stream(stream)), "agoq_silu_backward")
+    return dx, y
 
 
 MID_FP32, MID_BF16, MID_FP16 = 0, 1, 2

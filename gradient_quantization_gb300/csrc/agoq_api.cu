@@ -94,6 +94,27 @@ agoq_status agoq_dequant_act(const void *codes, const float *scales, int64_t n, 
     return from_cuda(launch_laaq_dequant(codes, scales, n, bits, y_bf16, as_stream(stream)));
 }
 
+agoq_status agoq_silu_backward(const void *codes, const float *scales, const void *dy_bf16,
+                               int64_t n, int bits, void *dx_bf16, void *y_bf16, void *stream) {
+    using namespace agoq;
+    if (!bits_ok(bits)) return AGOQ_ERR_BITS;
+    if (n < 0 || n % kBlockElems) return AGOQ_ERR_SHAPE;
+    if (n == 0) return AGOQ_OK;
+    if (!codes || !scales || !dy_bf16 || !dx_bf16) return AGOQ_ERR_NULL;
+    if (!aligned(codes, 16) || !aligned(scales, 4) || !aligned(dy_bf16, 16) ||
+        !aligned(dx_bf16, 16) || (y_bf16 && !aligned(y_bf16, 16)))
+        return AGOQ_ERR_ALIGN;
+    const uint64_t nb = (uint64_t)n / kBlockElems;
+    const uint64_t cb = nb * 16 * bits, sb = nb * 4, vb = 2ull * n, yb = y_bf16 ? vb : 0;
+    if (overlap(dx_bf16, vb, codes, cb) || overlap(dx_bf16, vb, scales, sb) ||
+        overlap(dx_bf16, vb, dy_bf16, vb) || overlap(y_bf16, yb, codes, cb) ||
+        overlap(y_bf16, yb, scales, sb) || overlap(y_bf16, yb, dy_bf16, vb) ||
+        overlap(y_bf16, yb, dx_bf16, vb))
+        return AGOQ_ERR_ALIAS;
+    return from_cuda(
+        launch_silu_backward(codes, scales, dy_bf16, n, bits, dx_bf16, y_bf16, as_stream(stream)));
+}
+
 agoq_status agoq_grad_accum_fp8(void *master_e4m3, float *master_scales, const void *grad_bf16,
                                 int64_t n, void *stream) {
     return agoq_grad_accum_fp8_mid(master_e4m3, master_scales, grad_bf16, n, AGOQ_MID_FP32, stream);

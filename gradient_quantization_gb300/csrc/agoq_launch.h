@@ -52,6 +52,8 @@ cudaError_t launch_laaq_quant(const void *x, int64_t n, int bits, void *codes, f
                               cudaStream_t st);
 cudaError_t launch_laaq_dequant(const void *codes, const float *scales, int64_t n, int bits,
                                 void *y, cudaStream_t st);
+cudaError_t launch_silu_backward(const void *codes, const float *scales, const void *dy, int64_t n,
+                                 int bits, void *dx, void *y, cudaStream_t st);
 // mid: intermediate format of the sum (0 binary32, 1 BF16, 2 FP16).
 cudaError_t launch_grad_accum(void *master, float *master_scales, const void *grad, int64_t n,
                               int mid, cudaStream_t st);

@@ -30,6 +30,9 @@
 #endif
 // 1: each warp issues the loads of its next group of blocks before the
 // arithmetic of the current one (register double buffering).
+#ifndef AGOQ_SILU_UNROLL
+#define AGOQ_SILU_UNROLL 1
+#endif
 #ifndef AGOQ_QUANT_PIPELINE
 #define AGOQ_QUANT_PIPELINE 1
 #endif
@@ -307,6 +310,103 @@ __global__ void __launch_bounds__(kThreads, AGOQ_DEQUANT_MIN_CTAS) laaq_dequant_
     }
 }
 
+// ---- SiLU backward recomputed from the stored input ("Herberekening versus
+// Caching", section 2.A: only the low-bit input is kept; the backward pass
+// dequantizes it and recomputes the intermediates).  For the 8 dequantized
+// values xh of a chunk and the matching upstream gradients dy, in binary32:
+//   sigma = 1 / (1 + exp(-xh));  silu'(xh) = sigma * (1 + xh * (1 - sigma));
+//   dx = bf16(dy * silu'(xh));   y = bf16(xh * sigma)  (the recomputed forward output).
+template <bool WITH_Y>
+__device__ __forceinline__ void silu_backward_chunk(uint4 xh, uint4 dy, uint4 &dx, uint4 &y) {
+    const uint32_t xw[4] = {xh.x, xh.y, xh.z, xh.w};
+    const uint32_t dw[4] = {dy.x, dy.y, dy.z, dy.w};
+    uint32_t o[4], yo[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        float r[2], yy[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const float x = h ? bf16_hi(xw[p]) : bf16_lo(xw[p]);
+            const float d = h ? bf16_hi(dw[p]) : bf16_lo(dw[p]);
+            const float sg = __frcp_rn(__fadd_rn(1.0f, expf(-x)));
+            const float g = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(x, __fsub_rn(1.0f, sg))));
+            r[h] = __fmul_rn(d, g);
+            yy[h] = __fmul_rn(x, sg);
+        }
+        o[p] = pack_bf16x2(r[0], r[1]);
+        if constexpr (WITH_Y) yo[p] = pack_bf16x2(yy[0], yy[1]);
+    }
+    dx = make_uint4(o[0], o[1], o[2], o[3]);
+    if constexpr (WITH_Y) y = make_uint4(yo[0], yo[1], yo[2], yo[3]);
+}
+
+// Same decomposition as the dequantizer (an octet per block, lane j holding
+// chunks j and j+8), plus the 16-byte upstream-gradient loads of those chunks;
+// the next batch's code, scale and gradient loads are issued before the
+// current batch's arithmetic.
+template <int BITS, int UNROLL, bool WITH_Y>
+__global__ void __launch_bounds__(kThreads, 1) laaq_silu_backward_kernel(
+    const uint32_t *__restrict__ codes, const float *__restrict__ scales,
+    const uint4 *__restrict__ dy, uint4 *__restrict__ dx, uint4 *__restrict__ y,
+    int64_t nblocks) {
+    pdl_wait_and_release();
+    const int lane = threadIdx.x & 31;
+    const int oct = lane >> 3, j = lane & 7;
+    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    const int64_t stride = nwarps * (4 * UNROLL);
+    int64_t base = warp * (4 * UNROLL);
+    if (base >= nblocks) return;
+    auto load_dy = [&](int64_t b0, uint4 (&a)[UNROLL], uint4 (&b)[UNROLL]) {
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t blk = b0 + 4 * u + oct;
+            if (blk < nblocks) {
+                a[u] = ld_stream(dy + blk * 16 + j);
+                b[u] = ld_stream(dy + blk * 16 + 8 + j);
+            } else {
+                a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    };
+    DequantBatch<BITS, UNROLL> cur, nxt;
+    uint4 da[UNROLL], db[UNROLL], na[UNROLL], nb[UNROLL];
+    cur.load(codes, scales, base, oct, j, nblocks);
+    load_dy(base, da, db);
+    for (; base < nblocks; base += stride) {
+        const bool more = base + stride < nblocks;
+        if (more) {
+            nxt.load(codes, scales, base + stride, oct, j, nblocks);
+            load_dy(base + stride, na, nb);
+        }
+#pragma unroll
+        for (int u = 0; u < UNROLL; ++u) {
+            const int64_t blk = base + 4 * u + oct;
+            if (blk < nblocks) {
+                uint4 ga, gb, ya, yb;
+                silu_backward_chunk<WITH_Y>(dequantize_chunk<BITS>(cur.alo[u], cur.ahi[u], cur.s[u]),
+                                            da[u], ga, ya);
+                silu_backward_chunk<WITH_Y>(dequantize_chunk<BITS>(cur.blo[u], cur.bhi[u], cur.s[u]),
+                                            db[u], gb, yb);
+                st_stream(dx + blk * 16 + j, ga);
+                st_stream(dx + blk * 16 + 8 + j, gb);
+                if constexpr (WITH_Y) {
+                    st_stream(y + blk * 16 + j, ya);
+                    st_stream(y + blk * 16 + 8 + j, yb);
+                }
+            }
+        }
+        if (more) {
+            cur = nxt;
+#pragma unroll
+            for (int u = 0; u < UNROLL; ++u) {
+                da[u] = na[u];
+                db[u] = nb[u];
+            }
+        }
+    }
+}
+
 template <typename K>
 int resident_grid(K kernel, int *cache, int64_t work_ctas) {
     int64_t g = (int64_t)sm_count() * resident_per_sm(kernel, kThreads, 0, cache);
@@ -337,6 +437,26 @@ cudaError_t dequant_bits(const void *codes, const float *scales, int64_t nblocks
                       nblocks);
 }
 
+template <int BITS, bool WITH_Y>
+cudaError_t silu_backward_bits(const void *codes, const float *scales, const void *dy,
+                               int64_t nblocks, void *dx, void *y, cudaStream_t st) {
+    constexpr int kU = AGOQ_SILU_UNROLL;
+    static int cache[kMaxDevices];
+    auto k = laaq_silu_backward_kernel<BITS, kU, WITH_Y>;
+    const int64_t per_cta = 4 * kU * (kThreads / 32);
+    return launch_pdl(k, resident_grid(k, cache, (nblocks + per_cta - 1) / per_cta), kThreads, 0,
+                      st, static_cast<const uint32_t *>(codes), scales,
+                      static_cast<const uint4 *>(dy), static_cast<uint4 *>(dx),
+                      static_cast<uint4 *>(y), nblocks);
+}
+
+template <int BITS>
+cudaError_t silu_backward_dispatch(const void *codes, const float *scales, const void *dy,
+                                   int64_t nblocks, void *dx, void *y, cudaStream_t st) {
+    return y ? silu_backward_bits<BITS, true>(codes, scales, dy, nblocks, dx, y, st)
+             : silu_backward_bits<BITS, false>(codes, scales, dy, nblocks, dx, y, st);
+}
+
 }  // namespace
 
 cudaError_t launch_laaq_quant(const void *x, int64_t n, int bits, void *codes, float *scales,
@@ -359,6 +479,22 @@ cudaError_t launch_laaq_dequant(const void *codes, const float *scales, int64_t 
         case 5: return dequant_bits<5>(codes, scales, nb, y, st);
         case 6: return dequant_bits<6>(codes, scales, nb, y, st);
         case 8: return dequant_bits<8>(codes, scales, nb, y, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace agoq
+
+namespace agoq {
+
+cudaError_t launch_silu_backward(const void *codes, const float *scales, const void *dy, int64_t n,
+                                 int bits, void *dx, void *y, cudaStream_t st) {
+    const int64_t nb = n / kBlock;
+    switch (bits) {
+        case 4: return silu_backward_dispatch<4>(codes, scales, dy, nb, dx, y, st);
+        case 5: return silu_backward_dispatch<5>(codes, scales, dy, nb, dx, y, st);
+        case 6: return silu_backward_dispatch<6>(codes, scales, dy, nb, dx, y, st);
+        case 8: return silu_backward_dispatch<8>(codes, scales, dy, nb, dx, y, st);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -95,6 +95,26 @@ agoq_status agoq_dequant_act(const void *codes, const float *scales, int64_t n, 
                              void *y_bf16, void *stream);
 
 /*
+ * SiLU backward recomputed from the stored low-bit input (AGoQ section 2.A,
+ * "Herberekening versus Caching": only the quantized input is kept; the
+ * backward pass dequantizes it and recomputes the intermediates).  With
+ * xh_i = bf16(fl32(c_i * scale)) (exactly agoq_dequant_act), in binary32:
+ *   sigma_i = 1 / (1 + exp(-xh_i));
+ *   dx_i = bf16_rne(dy_i * sigma_i * (1 + xh_i * (1 - sigma_i)));   (dy * silu'(xh))
+ *   y_i  = bf16_rne(xh_i * sigma_i);                                 (silu(xh), optional)
+ *   codes, scales : in, as written by agoq_quant_act with the same n and bits.
+ *   dy_bf16       : in, n BF16 upstream gradients (of the SiLU output).
+ *   dx_bf16       : out, n BF16 gradients of the SiLU input.
+ *   y_bf16        : out, n BF16 recomputed SiLU outputs, or NULL to skip them.
+ * exp is CUDA's expf (at most 2 ulp from the exact value) and the other steps
+ * are single binary32 roundings, so each output is within half a BF16 ulp
+ * plus 2^-20 * |dy| * (1 + |xh|) (dx) or 2^-20 * |xh| (y) of the exact value.
+ * Outputs must not overlap the inputs or each other.
+ */
+agoq_status agoq_silu_backward(const void *codes, const float *scales, const void *dy_bf16,
+                               int64_t n, int bits, void *dx_bf16, void *y_bf16, void *stream);
+
+/*
  * QuanGrad local accumulation (AGoQ section 2.B, "Lokale accumulatie"), IN
  * PLACE on an FP8 master gradient.  Per block of 128:
  *   m_i = fl32(e4m3(c_i) * scale);  t_i = fl32(m_i + g_i);

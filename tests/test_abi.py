@@ -77,6 +77,21 @@ def test_grad_accum_validation(L):
     assert L.agoq_grad_accum_fp8(P(A), P(B), P(C), 0, None) == OK
 
 
+def test_silu_backward_validation(L):
+    fn = L.agoq_silu_backward
+    D = C + (1 << 20)
+    assert fn(P(A), P(B), P(C), 256, 3, P(D), None, None) == BITS
+    assert fn(P(A), P(B), P(C), 200, 4, P(D), None, None) == SHAPE
+    assert fn(P(A), P(B), P(C), 0, 4, None, None, None) == OK
+    assert fn(P(A), None, P(C), 256, 4, P(D), None, None) == NULL
+    assert fn(P(A), P(B), P(C), 256, 4, None, None, None) == NULL
+    assert fn(P(A), P(B), P(C + 2), 256, 4, P(D), None, None) == ALIGN
+    assert fn(P(A), P(B), P(C), 256, 4, P(D), P(D + 8 + 4096), None) == ALIGN
+    assert fn(P(A), P(B), P(C), 256, 4, P(C + 256), None, None) == ALIAS     # dx on dy
+    assert fn(P(A), P(B), P(C), 256, 4, P(D), P(D + 256), None) == ALIAS     # y on dx
+    assert fn(P(A), P(B), P(C), 256, 4, P(D), P(A), None) == ALIAS           # y on codes
+
+
 def test_grad_accum_mid_validation(L):
     FORMAT = 8
     fn = L.agoq_grad_accum_fp8_mid
