@@ -277,6 +277,52 @@ int or_silu_backward(const uint8_t *codes, const float *scales, const uint16_t *
     return OR_OK;
 }
 
+/* Backward of RMSNorm recomputed from the stored low-bit input, [AGoQ] §2.A
+ * "Herberekening versus Caching".  The forward pass normalises each row t of
+ * the [T][H] input as  y[t][i] = x[t][i] * r_t * w[i],  r_t = 1 / sqrt(mean_i
+ * x[t][i]^2 + eps)  and keeps only the quantized x; the backward pass uses
+ * xh = or_dequant_act of the codes (row t = blocks t*H/128 ..) and, with
+ * g[i] = dy[t][i] * w[i]:
+ *   rstd[t]  = r_t
+ *   dx[t][i] = r_t * g[i] - xh[t][i] * r_t^3 * (sum_j g[j] * xh[t][j]) / H
+ *   dw[i]    = sum_t dy[t][i] * xh[t][i] * r_t
+ * all in binary64 (the exact derivatives of y with respect to x and w).
+ * dy and w are BF16.  H must be a multiple of 128.                            */
+int or_rmsnorm_backward(const uint8_t *codes, const float *scales, const uint16_t *dy,
+                        const uint16_t *w, int64_t T, int64_t H, int bits, double eps, double *dx,
+                        double *rstd, double *dw)
+{
+    if (!or_bits_ok(bits) || T < 0 || H <= 0 || H % OR_BLOCK)
+        return OR_BAD_ARG;
+    uint16_t *xrow = (uint16_t *)malloc(sizeof(uint16_t) * (size_t)H);
+    if (!xrow)
+        return OR_BAD_ARG;
+    const int64_t rec_bytes = 16 * (int64_t)bits, per_row = H / OR_BLOCK;
+    for (int64_t i = 0; i < H; ++i)
+        dw[i] = 0.0;
+    for (int64_t t = 0; t < T; ++t) {
+        or_dequant_act(codes + t * per_row * rec_bytes, scales + t * per_row, H, bits, xrow);
+        double sxx = 0.0, sgx = 0.0;
+        for (int64_t i = 0; i < H; ++i) {
+            double x = or_bf16_to_f32(xrow[i]);
+            double g = (double)or_bf16_to_f32(dy[t * H + i]) * or_bf16_to_f32(w[i]);
+            sxx += x * x;
+            sgx += g * x;
+        }
+        double r = 1.0 / sqrt(sxx / (double)H + eps);
+        rstd[t] = r;
+        for (int64_t i = 0; i < H; ++i) {
+            double x = or_bf16_to_f32(xrow[i]);
+            double d = or_bf16_to_f32(dy[t * H + i]);
+            double g = d * or_bf16_to_f32(w[i]);
+            dx[t * H + i] = r * g - x * r * r * r * sgx / (double)H;
+            dw[i] += d * x * r;
+        }
+    }
+    free(xrow);
+    return OR_OK;
+}
+
 /* Requantize 128 binary32 values to E4M3 with a fresh block scale:
  * s' = fl(absmax / 448); c_i = e4m3_rne_satfinite(fl(t_i / s')).
  * An all-zero block (absmax 0, whatever the signs) stores s' = +0, codes 0x00. */

@@ -38,6 +38,8 @@ def lib():
         L.or_grad_accum_fp8_f32.argtypes = [vp, vp, vp, i64]
         L.or_grad_accum_fp8_mid.argtypes = [vp, vp, vp, i64, i32]
         L.or_silu_backward.argtypes = [vp, vp, vp, i64, i32, vp, vp]
+        L.or_rmsnorm_backward.argtypes = [vp, vp, vp, vp, i64, i64, i32, ctypes.c_double, vp, vp,
+                                          vp]
         L.or_round_format_array.argtypes = [vp, vp, i64, i32, i32, i32]
         L.or_wgrad_accum_fp8.argtypes = [vp, vp, vp, i32, i32, i32, vp, i64, vp, vp]
         L.or_f32_to_bf16_array.argtypes = [vp, vp, i64]
@@ -46,7 +48,8 @@ def lib():
         for name in ("or_quant_act", "or_dequant_act", "or_grad_accum_fp8",
                      "or_reduce_fp8_shards", "or_wgrad_gemm_int4_f64",
                      "or_wgrad_gemm_int4_f64_entries", "or_grad_accum_fp8_f32",
-                     "or_wgrad_accum_fp8", "or_grad_accum_fp8_mid", "or_silu_backward"):
+                     "or_wgrad_accum_fp8", "or_grad_accum_fp8_mid", "or_silu_backward",
+                     "or_rmsnorm_backward"):
             getattr(L, name).restype = ctypes.c_int
         for name in ("or_f32_to_bf16_array", "or_f32_to_e4m3_array", "or_e4m3_to_f32_array",
                      "or_round_format_array"):
@@ -250,3 +253,23 @@ def silu_backward(codes, scales, dy_bf16, n, bits, want_y=True):
     _check(lib().or_silu_backward(_ptr(codes), _ptr(scales), _ptr(dy), n, bits, _ptr(dx),
                                   _ptr(y) if want_y else None), "silu_backward")
     return dx, y
+
+
+def rmsnorm_backward(codes, scales, dy_bf16, w_bf16, T, H, bits, eps):
+    """RMSNorm backward recomputed from LAAQ codes of x [T][H]: (dx [T][H], rstd [T],
+    dw [H]) in binary64."""
+    codes = _contig(codes, np.uint8).reshape(-1)
+    scales = _contig(scales, np.float32).reshape(-1)
+    dy = _contig(dy_bf16, np.uint16).reshape(-1)
+    w = _contig(w_bf16, np.uint16).reshape(-1)
+    n = T * H
+    if (codes.size < n // BLOCK * record_bytes(bits) or scales.size < n // BLOCK or dy.size != n
+            or w.size != H):
+        raise ValueError("shape mismatch")
+    dx = np.empty((T, H), np.float64)
+    rstd = np.empty(T, np.float64)
+    dw = np.empty(H, np.float64)
+    _check(lib().or_rmsnorm_backward(_ptr(codes), _ptr(scales), _ptr(dy), _ptr(w), T, H, bits,
+                                     float(eps), _ptr(dx), _ptr(rstd), _ptr(dw)),
+           "rmsnorm_backward")
+    return dx, rstd, dw
