@@ -480,6 +480,27 @@ def rows_arm(device, hbm_peak, bf16_peak):
         _time_launch(lambda: agoq.agoq_silu_backward(c, s, dy, n, 4, dx, y), flush))
     del c, s, dy, dx, y
 
+    # RMSNorm backward recomputed from the 4-bit RMSNorm input (8192 x 4096)
+    T, H = synthetic.DBCA_RMSNORM_SHAPE
+    xr = synthetic.dbca_activations_torch(seed=1, device=device)[0]
+    c, s = agoq.agoq_quant_act(xr, 4)
+    del xr
+    dy = torch.randn(T * H, device=device).to(torch.bfloat16)
+    wt = (1 + 0.1 * torch.randn(H, device=device)).to(torch.bfloat16)
+    dx = torch.empty((T, H), dtype=torch.bfloat16, device=device)
+    rstd = torch.empty(T, dtype=torch.float32, device=device)
+    dwt = torch.empty(H, dtype=torch.float32, device=device)
+    n = T * H
+    base = n * 4 // 8 + (n // 128) * 4 + 2 * n + 2 * n + 2 * H + 4 * T
+    row("rmsnorm_backward_dx_b4_8192x4096", base, n,
+        _time_launch(lambda: agoq.agoq_rmsnorm_backward(c, s, dy, wt, T, H, 4, 1e-6, dx, rstd,
+                                                        want_dw=False), flush))
+    row("rmsnorm_backward_dx_dw_b4_8192x4096", base + 4 * H, n,
+        _time_launch(lambda: agoq.agoq_rmsnorm_backward(c, s, dy, wt, T, H, 4, 1e-6, dx, rstd,
+                                                        dwt), flush),
+        {"note": "algorithmic bytes read the input once; dw reads codes and dy a second time"})
+    del c, s, dy, dx
+
     # QuanGrad accumulation, 2^30 elements
     n = synthetic.QUANGRAD_N
     m = torch.zeros(n, dtype=torch.uint8, device=device)

@@ -51,6 +51,8 @@ def _lib_handle():
         L.agoq_dequant_act.argtypes = [vp, vp, i64, i32, vp, vp]
         L.agoq_grad_accum_fp8.argtypes = [vp, vp, vp, i64, vp]
         L.agoq_silu_backward.argtypes = [vp, vp, vp, i64, i32, vp, vp, vp]
+        L.agoq_rmsnorm_backward.argtypes = [vp, vp, vp, vp, i64, i64, i32, ctypes.c_float, vp,
+                                            vp, vp, vp]
         L.agoq_grad_accum_fp8_mid.argtypes = [vp, vp, vp, i64, i32, vp]
         L.agoq_reduce_fp8_shards.argtypes = [vp, vp, i32, i64, vp, vp, vp, vp]
         L.agoq_wgrad_gemm_int4.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
@@ -174,6 +176,27 @@ def agoq_silu_backward(codes, scales, dy, n, bits, dx=None, y=None, want_y=False
     _check(lib().agoq_silu_backward(_ptr(codes), _ptr(scales), _ptr(dy), n, bits, _ptr(dx),
                                     _ptr(y), _stream(stream)), "agoq_silu_backward")
     return dx, y
+
+
+def agoq_rmsnorm_backward(codes, scales, dy, w, T, H, bits, eps, dx=None, rstd=None, dw=None,
+                          want_dw=True, stream=None):
+    """RMSNorm backward recomputed from LAAQ codes of x [T][H]: returns (dx BF16 [T][H],
+    rstd FP32 [T], dw FP32 [H] or None)."""
+    _need(codes, torch.uint8, "codes")
+    _need(scales, torch.float32, "scales")
+    _need(dy, torch.bfloat16, "dy")
+    _need(w, torch.bfloat16, "w")
+    dev = dy.device
+    if dx is None:
+        dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if rstd is None:
+        rstd = torch.empty(T, dtype=torch.float32, device=dev)
+    if dw is None and want_dw:
+        dw = torch.empty(H, dtype=torch.float32, device=dev)
+    _check(lib().agoq_rmsnorm_backward(_ptr(codes), _ptr(scales), _ptr(dy), _ptr(w), T, H, bits,
+                                       float(eps), _ptr(dx), _ptr(rstd), _ptr(dw),
+                                       _stream(stream)), "agoq_rmsnorm_backward")
+    return dx, rstd, dw
 
 
 MID_FP32, MID_BF16, MID_FP16 = 0, 1, 2

@@ -25,6 +25,7 @@ UNITS = {
     "laaq.cu": ["-fmad=false"],
     "quangrad.cu": ["-fmad=false"],
     "wgrad_gemm.cu": ["-fmad=false"],
+    "rmsnorm.cu": ["-fmad=false"],
 }
 HEADERS = ["agoq_device.cuh", "agoq_launch.h"]
 

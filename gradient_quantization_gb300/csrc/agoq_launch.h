@@ -54,6 +54,10 @@ cudaError_t launch_laaq_dequant(const void *codes, const float *scales, int64_t 
                                 void *y, cudaStream_t st);
 cudaError_t launch_silu_backward(const void *codes, const float *scales, const void *dy, int64_t n,
                                  int bits, void *dx, void *y, cudaStream_t st);
+// RMSNorm backward from LAAQ codes of x [T][H]; dw may be NULL (then not computed).
+cudaError_t launch_rmsnorm_backward(const void *codes, const float *scales, const void *dy,
+                                    const void *w, int64_t T, int64_t H, int bits, float eps,
+                                    void *dx, float *rstd, float *dw, cudaStream_t st);
 // mid: intermediate format of the sum (0 binary32, 1 BF16, 2 FP16).
 cudaError_t launch_grad_accum(void *master, float *master_scales, const void *grad, int64_t n,
                               int mid, cudaStream_t st);

@@ -218,41 +218,6 @@ __global__ void __launch_bounds__(kThreads, AGOQ_QUANT_MIN_CTAS) laaq_quant_kern
     }
 }
 
-// Chunk c (8 codes, 8*BITS bits at bit 8*BITS*c) of a block record, as (lo, hi).
-template <int BITS>
-__device__ __forceinline__ void load_chunk(const uint32_t *rec, int c, uint32_t &lo, uint32_t &hi) {
-    if constexpr (BITS == 4) {
-        lo = __ldg(rec + c);
-        hi = 0u;
-    } else if constexpr (BITS == 8) {
-        const uint2 w = __ldg(reinterpret_cast<const uint2 *>(rec) + c);
-        lo = w.x;
-        hi = w.y;
-    } else {
-        const int byte = BITS * c;                          // chunk starts at this byte
-        const uint32_t a = __ldg(rec + (byte >> 2));
-        const uint32_t b = __ldg(rec + (byte >> 2) + 1);    // still inside the record
-        const int sh = 8 * (byte & 3);
-        lo = __funnelshift_r(a, b, sh);
-        hi = b >> sh;
-    }
-}
-
-// bf16(fl32(c_i * s)) for the 8 codes of a chunk; the code values are made
-// exact by field_value's bias trick and multiplied in packed pairs.
-template <int BITS>
-__device__ __forceinline__ uint4 dequantize_chunk(uint32_t lo, uint32_t hi, float s) {
-    const uint64_t s2 = f32x2(s, s);
-    uint32_t out[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        const uint64_t y = mul_f32x2(f32x2(field_value<BITS>(lo, hi, 2 * p * BITS),
-                                           field_value<BITS>(lo, hi, (2 * p + 1) * BITS)), s2);
-        out[p] = pack_bf16x2(lo_f32(y), hi_f32(y));
-    }
-    return make_uint4(out[0], out[1], out[2], out[3]);
-}
-
 // Loads of one dequantization batch: UNROLL groups of 4 blocks per warp.
 template <int BITS, int UNROLL>
 struct DequantBatch {

@@ -115,6 +115,32 @@ agoq_status agoq_silu_backward(const void *codes, const float *scales, const voi
                                int64_t n, int bits, void *dx_bf16, void *y_bf16, void *stream);
 
 /*
+ * RMSNorm backward recomputed from the stored low-bit input (AGoQ section 2.A,
+ * "Herberekening versus Caching").  The forward pass computed, per row t of
+ * the [T][H] input x, y[t][i] = x[t][i] * r_t * w[i] with r_t = 1/sqrt(mean_i
+ * x[t][i]^2 + eps), and kept only agoq_quant_act(x, bits) (row t = blocks
+ * t*H/128 ..).  With xh its dequantization (exactly agoq_dequant_act) and
+ * g[i] = dy[t][i] * w[i], in binary32:
+ *   rstd[t]  = 1 / sqrt(sum_i xh[t][i]^2 / H + eps)
+ *   dx[t][i] = bf16_rne(rstd[t] * g[i] - xh[t][i] * rstd[t]^3 * (sum_j g[j] xh[t][j]) / H)
+ *   dw[i]    = sum_t dy[t][i] * xh[t][i] * rstd[t]
+ *   codes, scales : in, the stored input (n = T*H elements, `bits` wide).
+ *   dy_bf16       : in, BF16 [T][H] upstream gradients.   w_bf16 : in, BF16 [H] weight.
+ *   dx_bf16       : out, BF16 [T][H].  rstd : out, FP32 [T].
+ *   dw            : out, FP32 [H] (set, not accumulated), or NULL to skip it.
+ * Sums are formed in a fixed order, so results are deterministic; they differ
+ * from exact values by binary32 summation error (bounded by (H + 16) * 2^-24
+ * relative to the sums of absolute terms for the row sums, (T/64 + H + 32) *
+ * 2^-24 for dw) plus the output rounding.  H must be a multiple of 256 and at
+ * most 8192, eps finite and >= 0 (AGOQ_ERR_SHAPE otherwise).  The input is read
+ * once for dx and rstd; dw reads the codes and dy a second time.  Outputs must
+ * not overlap the inputs or each other.
+ */
+agoq_status agoq_rmsnorm_backward(const void *codes, const float *scales, const void *dy_bf16,
+                                  const void *w_bf16, int64_t T, int64_t H, int bits, float eps,
+                                  void *dx_bf16, float *rstd, float *dw, void *stream);
+
+/*
  * QuanGrad local accumulation (AGoQ section 2.B, "Lokale accumulatie"), IN
  * PLACE on an FP8 master gradient.  Per block of 128:
  *   m_i = fl32(e4m3(c_i) * scale);  t_i = fl32(m_i + g_i);

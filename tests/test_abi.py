@@ -92,6 +92,25 @@ def test_silu_backward_validation(L):
     assert fn(P(A), P(B), P(C), 256, 4, P(D), P(A), None) == ALIAS           # y on codes
 
 
+def test_rmsnorm_backward_validation(L):
+    fn = L.agoq_rmsnorm_backward
+    f = ctypes.c_float
+    D, E, F = C + (1 << 20), C + (1 << 22), C + (1 << 23)
+    args = lambda T, H, bits, eps=1e-6: (P(A), P(B), P(C), P(C + (1 << 19)), T, H, bits, f(eps))
+    assert fn(*args(4, 256, 7), P(D), P(E), P(F), None) == BITS
+    assert fn(*args(4, 384, 4), P(D), P(E), P(F), None) == SHAPE       # H % 256
+    assert fn(*args(4, 8448, 4), P(D), P(E), P(F), None) == SHAPE      # H > 8192
+    assert fn(*args(4, 256, 4, -1.0), P(D), P(E), P(F), None) == SHAPE
+    assert fn(*args(4, 256, 4, float("nan")), P(D), P(E), P(F), None) == SHAPE
+    assert fn(*args(0, 256, 4), P(D), P(E), None, None) == OK
+    assert fn(*args(4, 256, 4), None, P(E), P(F), None) == NULL
+    assert fn(*args(4, 256, 4), P(D), None, P(F), None) == NULL
+    assert fn(*args(4, 256, 4), P(D + 8), P(E), P(F), None) == ALIGN
+    assert fn(*args(4, 256, 4), P(C), P(E), P(F), None) == ALIAS         # dx on dy
+    assert fn(*args(4, 256, 4), P(D), P(D + 64), P(F), None) == ALIAS    # rstd inside dx
+    assert fn(*args(4, 256, 4), P(D), P(E), P(A), None) == ALIAS         # dw on codes
+
+
 def test_grad_accum_mid_validation(L):
     FORMAT = 8
     fn = L.agoq_grad_accum_fp8_mid
