@@ -463,7 +463,29 @@ def rows_arm(device, hbm_peak, bf16_peak):
         _time_launch(lambda: agoq.agoq_quant_act(x, 4, c, s), flush))
     row("laaq_int4_dequant_2048x4096", act_bytes(n, 4), n,
         _time_launch(lambda: agoq.agoq_dequant_act(c, s, n, 4, y), flush))
-    del x, c, s, y
+    # 100 back-to-back calls captured in one CUDA graph, rotating over 16 copies
+    # of the activation and its outputs (16 x 21 MB of traffic > L2): the
+    # per-call rate without launch gaps
+    k = 16
+    xs_c = [x.clone() for _ in range(k)]
+    cs_c = [torch.empty_like(c) for _ in range(k)]
+    ss_c = [torch.empty_like(s) for _ in range(k)]
+    ys_c = [torch.empty_like(x) for _ in range(k)]
+    for name, fn in (("laaq_int4_quant_2048x4096_graph100",
+                      lambda i: agoq.agoq_quant_act(xs_c[i % k], 4, cs_c[i % k], ss_c[i % k])),
+                     ("laaq_int4_dequant_2048x4096_graph100",
+                      lambda i: agoq.agoq_dequant_act(cs_c[i % k], ss_c[i % k], n, 4, ys_c[i % k]))):
+        for i in range(k):
+            fn(i)
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(100):
+                fn(i)
+        ms = _time_launch(graph.replay, flush) / 100
+        row(name, act_bytes(n, 4), n, ms, {"calls_per_graph": 100, "rotating_copies": k})
+        del graph
+    del x, c, s, y, xs_c, cs_c, ss_c, ys_c
 
     # SiLU backward recomputed from the 4-bit SiLU input (8192 x 11008)
     xs_ = synthetic.dbca_activations_torch(seed=1, device=device)[1]
@@ -645,7 +667,8 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
-PROFILE_CASES = ("accum", "reduce8", "reduce8_nocount", "reduce64", "gemm", "gemm_accum")
+PROFILE_CASES = ("accum", "reduce8", "reduce8_nocount", "reduce64", "gemm", "gemm_accum", "silu",
+                 "rmsnorm")
 
 
 def profile_case(name, launches=3):
@@ -682,6 +705,21 @@ def profile_case(name, launches=3):
             else:
                 agoq.agoq_wgrad_gemm_int4_accum_fp8(dy, xc, xs, M, N, K, master, mscales)
         agoq.agoq_device_status()
+    elif name == "silu":
+        x = synthetic.dbca_activations_torch(seed=1, device=dev)[1]
+        n = x.numel()
+        c, s = agoq.agoq_quant_act(x, 4)
+        dy = torch.randn(n, device=dev).to(torch.bfloat16)
+        for _ in range(launches):
+            agoq.agoq_silu_backward(c, s, dy, n, 4)
+    elif name == "rmsnorm":
+        x = synthetic.dbca_activations_torch(seed=1, device=dev)[0]
+        T, H = x.shape
+        c, s = agoq.agoq_quant_act(x, 4)
+        dy = torch.randn(T * H, device=dev).to(torch.bfloat16)
+        w = torch.ones(H, device=dev).to(torch.bfloat16)
+        for _ in range(launches):
+            agoq.agoq_rmsnorm_backward(c, s, dy, w, T, H, 4, 1e-6)
     else:
         raise SystemExit("unknown profile case %r (choose from %s)" % (name, ", ".join(PROFILE_CASES)))
     torch.cuda.synchronize()

@@ -33,6 +33,12 @@
 #ifndef AGOQ_SILU_UNROLL
 #define AGOQ_SILU_UNROLL 1
 #endif
+#ifndef AGOQ_SILU_MIN_CTAS
+#define AGOQ_SILU_MIN_CTAS 3
+#endif
+#ifndef AGOQ_SILU_FAST_EXP
+#define AGOQ_SILU_FAST_EXP 1
+#endif
 #ifndef AGOQ_QUANT_PIPELINE
 #define AGOQ_QUANT_PIPELINE 1
 #endif
@@ -293,8 +299,18 @@ __device__ __forceinline__ void silu_backward_chunk(uint4 xh, uint4 dy, uint4 &d
         for (int h = 0; h < 2; ++h) {
             const float x = h ? bf16_hi(xw[p]) : bf16_lo(xw[p]);
             const float d = h ? bf16_hi(dw[p]) : bf16_lo(dw[p]);
+#if AGOQ_SILU_FAST_EXP
+            // exp through the hardware base-2 exponential, 1 / (1 + e) by the
+            // approximate division: both within a few binary32 ulps
+            const float sg = __fdividef(1.0f, __fadd_rn(1.0f, __expf(-x)));
+#else
             const float sg = __frcp_rn(__fadd_rn(1.0f, expf(-x)));
+#endif
+#if AGOQ_SILU_FAST_EXP
+            const float g = sg * fmaf(x, 1.0f - sg, 1.0f);
+#else
             const float g = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(x, __fsub_rn(1.0f, sg))));
+#endif
             r[h] = __fmul_rn(d, g);
             yy[h] = __fmul_rn(x, sg);
         }
@@ -310,7 +326,7 @@ __device__ __forceinline__ void silu_backward_chunk(uint4 xh, uint4 dy, uint4 &d
 // the next batch's code, scale and gradient loads are issued before the
 // current batch's arithmetic.
 template <int BITS, int UNROLL, bool WITH_Y>
-__global__ void __launch_bounds__(kThreads, 1) laaq_silu_backward_kernel(
+__global__ void __launch_bounds__(kThreads, AGOQ_SILU_MIN_CTAS) laaq_silu_backward_kernel(
     const uint32_t *__restrict__ codes, const float *__restrict__ scales,
     const uint4 *__restrict__ dy, uint4 *__restrict__ dx, uint4 *__restrict__ y,
     int64_t nblocks) {

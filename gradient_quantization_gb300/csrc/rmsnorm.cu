@@ -11,16 +11,17 @@
 //   dx[t][i] = r_t * g[i] - xh[t][i] * (r_t^3 * sum_j g[j] xh[t][j] / H)
 //   dw[i]    = sum_t dy[t][i] * xh[t][i] * r_t
 //
-// Row kernel: one CTA of 256 threads per row (an octet of lanes per 128-element
-// block, lane j holding chunks j and j+8, at most kRowBlocks blocks per octet
-// held in registers): the codes, scales, dy and w of the row are read once,
-// the two row sums are reduced over the CTA in a fixed order, and dx and rstd
-// are written.
-// Weight-gradient kernel: a cluster of 8 CTAs per 256-column slice; each of the
-// 64 warps of the cluster sums every 64th row for its 256 columns (one chunk
-// of 8 columns per lane), the warps' sums are added in a fixed order in shared
-// memory, and rank 0 adds the 8 CTAs' sums in rank order through distributed
-// shared memory.  No global scratch, no atomics: dw is deterministic.
+// Row kernels: the codes, scales, dy and w of each row are read once, the two
+// row sums are reduced in a fixed order, and dx and rstd are written.  For
+// H = 4096 one warp owns a row (shuffle reductions only, w staged in shared
+// memory); other H (multiples of 256 up to 8192) use one CTA of 256 threads per
+// row with an octet of lanes per 128-element block.
+// Weight-gradient kernel: a cluster of 8 CTAs per 128-column slice; each of the
+// 128 half warps of the cluster sums every 128th row for its 128 columns (one
+// chunk of 8 columns per lane, 8 rows in flight), the half warps' sums are
+// added in a fixed order in shared memory, and rank 0 adds the 8 CTAs' sums in
+// rank order through distributed shared memory.  No global scratch, no
+// atomics: dw is deterministic.
 #include <cooperative_groups.h>
 
 #include "agoq_device.cuh"
@@ -37,8 +38,8 @@ constexpr int kRowOctets = kRowThreads / 8;
 constexpr int kRowBlocks = 2;                    // 128-element blocks per octet (H <= 8192)
 constexpr int kDwThreads = 256;                  // 8 warps
 constexpr int kDwCluster = 8;                    // CTAs per cluster (ranks along y)
-constexpr int kDwCols = 256;                     // columns per slice (32 lanes x 8)
-constexpr int kDwUnroll = 4;                     // rows in flight per warp
+constexpr int kDwCols = 128;                     // columns per slice (16 lanes x 8)
+constexpr int kDwUnroll = 8;                     // rows in flight per half warp
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     uint4 v;
@@ -54,6 +55,9 @@ __device__ __forceinline__ float elem(const uint4 &v, int k) {
     return (k & 1) ? bf16_hi(w) : bf16_lo(w);
 }
 
+// General row kernel (any H that is a multiple of 256, up to 8192): a CTA of
+// 256 threads per row, an octet of lanes per 128-element block (lane j holding
+// chunks j and j+8, at most kRowBlocks blocks per octet in registers).
 template <int BITS>
 __global__ void __launch_bounds__(kRowThreads) rmsnorm_backward_rows_kernel(
     const uint32_t *__restrict__ codes, const float *__restrict__ scales,
@@ -85,7 +89,6 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_backward_rows_kernel(
                 }
             }
         }
-        // row sums
 #pragma unroll
         for (int q = 0; q < kRowBlocks; ++q) {
             const int b = oct + kRowOctets * q;
@@ -101,6 +104,7 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_backward_rows_kernel(
                     }
             }
         }
+        // fixed-order reduction: lanes (xor tree), then the 8 warps in order
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) {
             sxx = __fadd_rn(sxx, __shfl_xor_sync(kFull, sxx, o));
@@ -147,22 +151,190 @@ __global__ void __launch_bounds__(kRowThreads) rmsnorm_backward_rows_kernel(
     }
 }
 
+__device__ __forceinline__ void cp_async16(void *dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async4(void *dst, const void *src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(dst))),
+                 "l"(src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Chunk c (8 codes) of a row's concatenated block records in shared memory:
+// the row's records are contiguous, so chunk c starts at byte BITS * c.
 template <int BITS>
-__global__ void __launch_bounds__(kDwThreads) rmsnorm_dw_kernel(
+__device__ __forceinline__ void chunk_from_smem(const uint32_t *rowcodes, int c, uint32_t &lo,
+                                                uint32_t &hi) {
+    if constexpr (BITS == 4) {
+        lo = rowcodes[c];
+        hi = 0u;
+    } else if constexpr (BITS == 8) {
+        const uint2 v = reinterpret_cast<const uint2 *>(rowcodes)[c];
+        lo = v.x;
+        hi = v.y;
+    } else {
+        const int byte = BITS * c;
+        const uint32_t a = rowcodes[byte >> 2], b = rowcodes[(byte >> 2) + 1];
+        const int sh = 8 * (byte & 3);
+        lo = __funnelshift_r(a, b, sh);
+        hi = b >> sh;
+    }
+}
+
+constexpr int kWarpRowThreads = 128;             // 4 warps per CTA, one row per warp at a time
+
+// Shared-memory words of one warp's row stage: dy (H/8 x 16 B), the row's
+// codes (H*BITS/8 B, padded by 16 B so a 5/6-bit chunk read may touch the
+// next word) and its H/128 scales.
+template <int BITS, int H>
+struct RowStage {
+    static constexpr int kDy = H / 8;                        // uint4
+    static constexpr int kCodes = H * BITS / 128 + 1;        // uint4
+    static constexpr int kScales = (H / kBlock + 3) / 4;     // uint4
+    static constexpr int kU4 = kDy + kCodes + kScales;
+};
+
+// Row kernel for H = 256 * C (C chunks of 8 elements per lane): one warp per
+// row, lane l handling chunks l, l + 32, ...  The warp stages its row's dy,
+// codes and scales in shared memory with cp.async (the next row's copies in
+// flight while the current row is computed), forms the row sums from shared
+// memory, reduces them with shuffles alone, then forms dx.  w is staged once
+// per CTA.  The cp.async waits are hardware group completions.
+template <int BITS, int C>
+__global__ void __launch_bounds__(kWarpRowThreads) rmsnorm_backward_warp_rows_kernel(
+    const uint32_t *__restrict__ codes, const float *__restrict__ scales,
+    const uint4 *__restrict__ dy, const uint4 *__restrict__ w, int64_t T, float eps,
+    uint4 *__restrict__ dx, float *__restrict__ rstd) {
+    pdl_wait_and_release();
+    constexpr int H = 256 * C, nb = H / kBlock;
+    using St = RowStage<BITS, H>;
+    extern __shared__ uint4 smem4[];
+    uint4 *ws = smem4;                                       // H/8
+    const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+    uint4 *stage0 = smem4 + H / 8 + (size_t)wid * 2 * St::kU4;
+    for (int i = threadIdx.x; i < H / 8; i += blockDim.x) ws[i] = __ldg(w + i);
+    __syncthreads();
+    const int64_t gw = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    auto issue = [&](int64_t t, int buf) {
+        uint4 *st = stage0 + buf * St::kU4;
+        const uint4 *dyr = dy + t * (H / 8);
+#pragma unroll
+        for (int k = 0; k < C; ++k) cp_async16(st + lane + 32 * k, dyr + lane + 32 * k);
+        const uint4 *cr = reinterpret_cast<const uint4 *>(codes + (size_t)t * nb * 4 * BITS);
+        for (int i = lane; i < St::kCodes - 1; i += 32) cp_async16(st + St::kDy + i, cr + i);
+        float *sc = reinterpret_cast<float *>(st + St::kDy + St::kCodes);
+        for (int i = lane; i < nb; i += 32) cp_async4(sc + i, scales + t * nb + i);
+        cp_async_commit();
+    };
+    int64_t t = gw;
+    int buf = 0;
+    if (t < T) issue(t, 0);
+    for (; t < T; t += nw, buf ^= 1) {
+        if (t + nw < T) {
+            issue(t + nw, buf ^ 1);
+            cp_async_wait<1>();
+        } else {
+            cp_async_wait<0>();
+        }
+        __syncwarp();
+        const uint4 *dyS = stage0 + buf * St::kU4;
+        const uint32_t *cS = reinterpret_cast<const uint32_t *>(dyS + St::kDy);
+        const float *sS = reinterpret_cast<const float *>(dyS + St::kDy + St::kCodes);
+        auto xh_of = [&](int k) {
+            const int c = lane + 32 * k;
+            uint32_t lo, hi;
+            chunk_from_smem<BITS>(cS, c, lo, hi);
+            return dequantize_chunk<BITS>(lo, hi, sS[c / 16]);
+        };
+        // Row sums in packed pairs with fused multiply-adds (a tolerance-
+        // bounded result: fusing only removes roundings).
+        uint64_t sxx2 = 0ull, sgx2 = 0ull;
+#pragma unroll 4
+        for (int k = 0; k < C; ++k) {
+            const uint4 xh = xh_of(k);
+            const uint4 dv = dyS[lane + 32 * k];
+            const uint4 wv = ws[lane + 32 * k];
+            const uint32_t xw[4] = {xh.x, xh.y, xh.z, xh.w}, dw4[4] = {dv.x, dv.y, dv.z, dv.w},
+                           ww[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const uint64_t x2 = u32x2(xw[p] << 16, xw[p] & 0xFFFF0000u);
+                const uint64_t g2 = mul_f32x2(u32x2(dw4[p] << 16, dw4[p] & 0xFFFF0000u),
+                                              u32x2(ww[p] << 16, ww[p] & 0xFFFF0000u));
+                sxx2 = fma_f32x2(x2, x2, sxx2);
+                sgx2 = fma_f32x2(g2, x2, sgx2);
+            }
+        }
+        float sxx = __fadd_rn(lo_f32(sxx2), hi_f32(sxx2));
+        float sgx = __fadd_rn(lo_f32(sgx2), hi_f32(sgx2));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sxx = __fadd_rn(sxx, __shfl_xor_sync(kFull, sxx, o));
+            sgx = __fadd_rn(sgx, __shfl_xor_sync(kFull, sgx, o));
+        }
+        const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(__fdiv_rn(sxx, (float)H), eps)));
+        const float kk = __fmul_rn(__fmul_rn(__fmul_rn(r, r), r), __fdiv_rn(sgx, (float)H));
+        if (lane == 0) rstd[t] = r;
+        const uint64_t r2 = f32x2(r, r), nkk2 = f32x2(-kk, -kk);
+#pragma unroll 4
+        for (int k = 0; k < C; ++k) {
+            const uint4 xh = xh_of(k);
+            const uint4 dv = dyS[lane + 32 * k];
+            const uint4 wv = ws[lane + 32 * k];
+            const uint32_t xw[4] = {xh.x, xh.y, xh.z, xh.w}, dw4[4] = {dv.x, dv.y, dv.z, dv.w},
+                           ww[4] = {wv.x, wv.y, wv.z, wv.w};
+            uint32_t o[4];
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                const uint64_t x2 = u32x2(xw[p] << 16, xw[p] & 0xFFFF0000u);
+                const uint64_t g2 = mul_f32x2(u32x2(dw4[p] << 16, dw4[p] & 0xFFFF0000u),
+                                              u32x2(ww[p] << 16, ww[p] & 0xFFFF0000u));
+                // dx = r * g - xh * kk
+                const uint64_t d2 = fma_f32x2(r2, g2, mul_f32x2(x2, nkk2));
+                o[p] = pack_bf16x2(lo_f32(d2), hi_f32(d2));
+            }
+            dx[t * (H / 8) + lane + 32 * k] = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+        __syncwarp();   // every lane is done with this stage before it is refilled
+    }
+}
+
+template <int BITS, int C>
+constexpr size_t warp_rows_smem() {
+    return sizeof(uint4) * (256 * C / 8 + (kWarpRowThreads / 32) * 2 * RowStage<BITS, 256 * C>::kU4);
+}
+
+template <int BITS>
+__global__ void __launch_bounds__(kDwThreads, 2) rmsnorm_dw_kernel(
     const uint32_t *__restrict__ codes, const float *__restrict__ scales,
     const uint4 *__restrict__ dy, const float *__restrict__ rstd, int64_t T, int H,
     float *__restrict__ dw) {
     pdl_wait_and_release();
     constexpr int kWords = 4 * BITS;
-    __shared__ float part[kDwThreads / 32][kDwCols];
+    constexpr int kHalves = 2 * (kDwThreads / 32);                 // row groups per CTA
+    __shared__ float part[kHalves][kDwCols];
     __shared__ float csum[kDwCols];
     cg::cluster_group cluster = cg::this_cluster();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int rank = (int)cluster.block_rank();                  // 0 .. kDwCluster-1
-    const int group = rank * (kDwThreads / 32) + warp;            // 0 .. 63
-    constexpr int kGroups = kDwCluster * (kDwThreads / 32);
+    const int half = lane >> 4, l16 = lane & 15;
+    const int rank = (int)cluster.block_rank();                    // 0 .. kDwCluster-1
+    const int hw = 2 * warp + half;                                // 0 .. kHalves-1
+    const int group = rank * kHalves + hw;                          // 0 .. 127
+    constexpr int kGroups = kDwCluster * kHalves;
     const int nb = H / kBlock;
-    const int col0 = blockIdx.x * kDwCols + 8 * lane;             // this lane's 8 columns
+    const int col0 = blockIdx.x * kDwCols + 8 * l16;                // this lane's 8 columns
     const int b = col0 / kBlock, chunk = (col0 % kBlock) / 8;
     float acc[8];
 #pragma unroll
@@ -195,16 +367,16 @@ __global__ void __launch_bounds__(kDwThreads) rmsnorm_dw_kernel(
         }
     }
 #pragma unroll
-    for (int k = 0; k < 8; ++k) part[warp][8 * lane + k] = acc[k];
+    for (int k = 0; k < 8; ++k) part[hw][8 * l16 + k] = acc[k];
     __syncthreads();
-    {
+    if (threadIdx.x < kDwCols) {
         float v = 0.0f;
 #pragma unroll
-        for (int i = 0; i < kDwThreads / 32; ++i) v = __fadd_rn(v, part[i][threadIdx.x]);
+        for (int i = 0; i < kHalves; ++i) v = __fadd_rn(v, part[i][threadIdx.x]);
         csum[threadIdx.x] = v;
     }
     cluster.sync();
-    if (rank == 0) {
+    if (rank == 0 && threadIdx.x < kDwCols) {
         float v = 0.0f;
         for (int q = 0; q < kDwCluster; ++q)
             v = __fadd_rn(v, cluster.map_shared_rank(csum, q)[threadIdx.x]);
@@ -225,11 +397,33 @@ template <int BITS>
 cudaError_t rmsnorm_bits(const void *codes, const float *scales, const void *dy, const void *w,
                          int64_t T, int H, float eps, void *dx, float *rstd, float *dw,
                          cudaStream_t st) {
-    auto kr = rmsnorm_backward_rows_kernel<BITS>;
-    cudaError_t e = launch_pdl(kr, rows_grid(kr, T), kRowThreads, 0, st,
-                               static_cast<const uint32_t *>(codes), scales,
-                               static_cast<const uint4 *>(dy), static_cast<const uint4 *>(w), T, H,
-                               eps, static_cast<uint4 *>(dx), rstd);
+    cudaError_t e;
+    if (H == 4096) {
+        auto kr = rmsnorm_backward_warp_rows_kernel<BITS, 16>;
+        constexpr size_t smem = warp_rows_smem<BITS, 16>();
+        static int per_sm[kMaxDevices];
+        static bool attr_set[kMaxDevices];
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev >= 0 && dev < kMaxDevices && !attr_set[dev]) {
+            e = cudaFuncSetAttribute(kr, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            if (e != cudaSuccess) return e;
+            attr_set[dev] = true;
+        }
+        int64_t g = (int64_t)sm_count() * resident_per_sm(kr, kWarpRowThreads, smem, per_sm);
+        const int64_t need = (T + kWarpRowThreads / 32 - 1) / (kWarpRowThreads / 32);
+        if (need < g) g = need;
+        e = launch_pdl(kr, (int)(g > 0 ? g : 1), kWarpRowThreads, smem, st,
+                       static_cast<const uint32_t *>(codes), scales,
+                       static_cast<const uint4 *>(dy), static_cast<const uint4 *>(w), T, eps,
+                       static_cast<uint4 *>(dx), rstd);
+    } else {
+        auto kr = rmsnorm_backward_rows_kernel<BITS>;
+        e = launch_pdl(kr, rows_grid(kr, T), kRowThreads, 0, st,
+                       static_cast<const uint32_t *>(codes), scales,
+                       static_cast<const uint4 *>(dy), static_cast<const uint4 *>(w), T, H, eps,
+                       static_cast<uint4 *>(dx), rstd);
+    }
     if (e != cudaSuccess || !dw) return e;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(H / kDwCols, kDwCluster, 1);

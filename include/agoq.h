@@ -106,9 +106,10 @@ agoq_status agoq_dequant_act(const void *codes, const float *scales, int64_t n, 
  *   dy_bf16       : in, n BF16 upstream gradients (of the SiLU output).
  *   dx_bf16       : out, n BF16 gradients of the SiLU input.
  *   y_bf16        : out, n BF16 recomputed SiLU outputs, or NULL to skip them.
- * exp is CUDA's expf (at most 2 ulp from the exact value) and the other steps
- * are single binary32 roundings, so each output is within half a BF16 ulp
- * plus 2^-20 * |dy| * (1 + |xh|) (dx) or 2^-20 * |xh| (y) of the exact value.
+ * exp is the hardware base-2 exponential of xh * log2(e) (__expf), 1/(1+e) the
+ * approximate division, and 1 + xh * (1 - sigma) a fused multiply-add; each
+ * output is within half a BF16 ulp plus 2^-20 * |dy| * (1 + |xh|) (dx) or
+ * 2^-20 * |xh| (y) of the exact value.
  * Outputs must not overlap the inputs or each other.
  */
 agoq_status agoq_silu_backward(const void *codes, const float *scales, const void *dy_bf16,
@@ -128,10 +129,11 @@ agoq_status agoq_silu_backward(const void *codes, const float *scales, const voi
  *   dy_bf16       : in, BF16 [T][H] upstream gradients.   w_bf16 : in, BF16 [H] weight.
  *   dx_bf16       : out, BF16 [T][H].  rstd : out, FP32 [T].
  *   dw            : out, FP32 [H] (set, not accumulated), or NULL to skip it.
- * Sums are formed in a fixed order, so results are deterministic; they differ
- * from exact values by binary32 summation error (bounded by (H + 16) * 2^-24
- * relative to the sums of absolute terms for the row sums, (T/64 + H + 32) *
- * 2^-24 for dw) plus the output rounding.  H must be a multiple of 256 and at
+ * Sums are formed in a fixed order (fused multiply-adds where that only
+ * removes roundings), so results are deterministic; they differ from exact
+ * values by binary32 summation error (bounded by (H + 16) * 2^-24 relative to
+ * the sums of absolute terms for the row sums, (T/64 + H + 32) * 2^-24 for dw)
+ * plus the output rounding.  H must be a multiple of 256 and at
  * most 8192, eps finite and >= 0 (AGOQ_ERR_SHAPE otherwise).  The input is read
  * once for dx and rstd; dw reads the codes and dy a second time.  Outputs must
  * not overlap the inputs or each other.
