@@ -59,9 +59,12 @@ def _lib_handle():
         L.agoq_wgrad_gemm_int4_f32out.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
         L.agoq_wgrad_gemm_int4_accum_fp8.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.agoq_device_status.argtypes = [vp]
+        L.agoq_dbca_pp_bits.argtypes = [i32, i32, i32, vp]
         for name in ("agoq_quant_act", "agoq_dequant_act", "agoq_grad_accum_fp8",
                      "agoq_reduce_fp8_shards", "agoq_wgrad_gemm_int4",
-                     "agoq_wgrad_gemm_int4_f32out", "agoq_device_status"):
+                     "agoq_wgrad_gemm_int4_f32out", "agoq_device_status",
+                     "agoq_wgrad_gemm_int4_accum_fp8", "agoq_grad_accum_fp8_mid",
+                     "agoq_silu_backward", "agoq_rmsnorm_backward", "agoq_dbca_pp_bits"):
             getattr(L, name).restype = i32
         _L = L
     return _L
@@ -197,6 +200,14 @@ def agoq_rmsnorm_backward(codes, scales, dy, w, T, H, bits, eps, dx=None, rstd=N
                                        float(eps), _ptr(dx), _ptr(rstd), _ptr(dw),
                                        _stream(stream)), "agoq_rmsnorm_backward")
     return dx, rstd, dw
+
+
+def agoq_dbca_pp_bits(stages, microbatches, base_bits=4):
+    """DBCA-PP widths per pipeline stage (host-side): a list of `stages` ints."""
+    out = (ctypes.c_int * max(int(stages), 1))()
+    _check(lib().agoq_dbca_pp_bits(int(stages), int(microbatches), int(base_bits), out),
+           "agoq_dbca_pp_bits")
+    return list(out)[:stages]
 
 
 MID_FP32, MID_BF16, MID_FP16 = 0, 1, 2

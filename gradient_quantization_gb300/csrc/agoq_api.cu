@@ -245,6 +245,23 @@ agoq_status agoq_wgrad_gemm_int4_accum_fp8(const void *dY_bf16, const void *x_co
                                             master_scales, as_stream(stream)));
 }
 
+agoq_status agoq_dbca_pp_bits(int stages, int microbatches, int base_bits, int *bits) {
+    if (stages < 1 || microbatches < 1) return AGOQ_ERR_SHAPE;
+    if (base_bits != 4 && base_bits != 5 && base_bits != 6 && base_bits != 8) return AGOQ_ERR_BITS;
+    if (!bits) return AGOQ_ERR_NULL;
+    static const int kWidths[4] = {4, 5, 6, 8};
+    const long long first = stages < microbatches ? stages : microbatches;   // stage 0's batches
+    const long long cap = first * base_bits;
+    for (int s = 0; s < stages; ++s) {
+        const long long live = (stages - s) < microbatches ? (stages - s) : microbatches;
+        int b = base_bits;
+        for (int i = 0; i < 4; ++i)
+            if (kWidths[i] >= base_bits && live * kWidths[i] <= cap) b = kWidths[i];
+        bits[s] = b;
+    }
+    return AGOQ_OK;
+}
+
 agoq_status agoq_device_status(void *stream) {
     unsigned status = 0;
     if (agoq::read_and_clear_device_status(agoq::as_stream(stream), &status) != cudaSuccess)

@@ -240,6 +240,21 @@ agoq_status agoq_wgrad_gemm_int4_accum_fp8(const void *dY_bf16, const void *x_co
                                            void *master_e4m3, float *master_scales, void *stream);
 
 /*
+ * DBCA-PP bit-width assignment (AGoQ section 2.A, "Dynamic Bit-width
+ * Compensation (DBCA-PP)": pipeline stages that hold fewer activation batches
+ * get wider codes, the stages with the most batches the base width, so that
+ * no stage stores more activation bytes than the fullest one).  Host-side, no
+ * GPU work.  Under the one-forward-one-backward schedule, stage s (0 = first)
+ * holds live_s = min(stages - s, microbatches) micro-batches of activations at
+ * its peak; stage 0 holds the most.  Each stage gets the largest width b in
+ * {4, 5, 6, 8}, b >= base_bits, with live_s * b <= live_0 * base_bits.
+ *   bits : out, `stages` ints (the width for agoq_quant_act on that stage).
+ * AGOQ_ERR_SHAPE if stages or microbatches < 1, AGOQ_ERR_BITS for a base
+ * width outside {4, 5, 6, 8}.
+ */
+agoq_status agoq_dbca_pp_bits(int stages, int microbatches, int base_bits, int *bits);
+
+/*
  * Synchronise `stream`, then read and clear the library's device-side status
  * word for the current device.  Returns AGOQ_ERR_TIMEOUT if a GEMM pipeline
  * wait exceeded its iteration limit since the last call (that GEMM's output is
