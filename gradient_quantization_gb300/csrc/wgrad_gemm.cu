@@ -71,7 +71,7 @@ namespace {
 #define AGOQ_GEMM_NA 3
 #endif
 #ifndef AGOQ_GEMM_WAIT_HINT_NS
-#define AGOQ_GEMM_WAIT_HINT_NS 20000
+#define AGOQ_GEMM_WAIT_HINT_NS 0
 #endif
 
 // Epilogue kinds.

@@ -579,6 +579,29 @@ int or_wgrad_accum_fp8(const uint16_t *dY, const uint8_t *xc, const float *xs, i
     return OR_OK;
 }
 
+/* A linear layer's forward product with the LAAQ quantization of its output
+ * fused into the GEMM ([AGoQ] §2.C "Kernel Fusion" with §2.A "Strategie" /
+ * "DBCA-PP": the activation kept for the backward pass is quantized where it
+ * is produced).  X is BF16 [T][K], W is BF16 [N][K] (K contiguous in both):
+ *   Y[t][n] = bf16(fl32(sum_k X[t][k] * W[n][k]))   (binary64 sum in k order,
+ *             rounded once to binary32, then to BF16)
+ *   codes, scales = or_quant_act(Y, T*N, bits)      (row t = blocks t*N/128 ..)
+ * y receives Y's BF16 bit patterns [T][N].                                    */
+int or_fwd_gemm_quant(const uint16_t *x, const uint16_t *w, int T, int N, int K, int bits,
+                      uint16_t *y, uint8_t *codes, float *scales)
+{
+    if (T <= 0 || N <= 0 || K <= 0 || N % OR_BLOCK || !or_bits_ok(bits))
+        return OR_BAD_ARG;
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t n = 0; n < N; ++n) {
+            double acc = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                acc += (double)or_bf16_to_f32(x[t * K + k]) * or_bf16_to_f32(w[n * K + k]);
+            y[t * N + n] = or_f32_to_bf16((float)acc);
+        }
+    return or_quant_act(y, (int64_t)T * N, bits, codes, scales);
+}
+
 /* ------------------------------------------------------------------------- */
 /* Array forms of the codecs, for the codec sweeps in the tests.               */
 void or_f32_to_bf16_array(const float *src, uint16_t *dst, int64_t n)

@@ -38,6 +38,7 @@ def lib():
         L.or_grad_accum_fp8_f32.argtypes = [vp, vp, vp, i64]
         L.or_grad_accum_fp8_mid.argtypes = [vp, vp, vp, i64, i32]
         L.or_silu_backward.argtypes = [vp, vp, vp, i64, i32, vp, vp]
+        L.or_fwd_gemm_quant.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp]
         L.or_rmsnorm_backward.argtypes = [vp, vp, vp, vp, i64, i64, i32, ctypes.c_double, vp, vp,
                                           vp]
         L.or_round_format_array.argtypes = [vp, vp, i64, i32, i32, i32]
@@ -49,7 +50,7 @@ def lib():
                      "or_reduce_fp8_shards", "or_wgrad_gemm_int4_f64",
                      "or_wgrad_gemm_int4_f64_entries", "or_grad_accum_fp8_f32",
                      "or_wgrad_accum_fp8", "or_grad_accum_fp8_mid", "or_silu_backward",
-                     "or_rmsnorm_backward"):
+                     "or_rmsnorm_backward", "or_fwd_gemm_quant"):
             getattr(L, name).restype = ctypes.c_int
         for name in ("or_f32_to_bf16_array", "or_f32_to_e4m3_array", "or_e4m3_to_f32_array",
                      "or_round_format_array"):
@@ -273,3 +274,18 @@ def rmsnorm_backward(codes, scales, dy_bf16, w_bf16, T, H, bits, eps):
                                      float(eps), _ptr(dx), _ptr(rstd), _ptr(dw)),
            "rmsnorm_backward")
     return dx, rstd, dw
+
+
+def fwd_gemm_quant(x_bf16, w_bf16, T, N, K, bits):
+    """Forward product Y = bf16(fl32(X W^T)) (X [T][K], W [N][K], BF16 bits) and its
+    LAAQ quantization: returns (Y bits [T][N], codes, scales)."""
+    x = _contig(x_bf16, np.uint16).reshape(-1)
+    w = _contig(w_bf16, np.uint16).reshape(-1)
+    if x.size != T * K or w.size != N * K:
+        raise ValueError("shape mismatch")
+    y = np.empty(T * N, np.uint16)
+    codes = np.empty(T * N // BLOCK * record_bytes(bits), np.uint8)
+    scales = np.empty(T * N // BLOCK, np.float32)
+    _check(lib().or_fwd_gemm_quant(_ptr(x), _ptr(w), T, N, K, bits, _ptr(y), _ptr(codes),
+                                   _ptr(scales)), "fwd_gemm_quant")
+    return y.reshape(T, N), codes, scales
