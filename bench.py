@@ -573,6 +573,31 @@ def rows_arm(device, hbm_peak, bf16_peak):
     except agoq.AgoqError as e:
         rows["wgrad_gemm_int4_11008x4096x8192"] = {"unavailable": str(e)}
 
+    # Forward GEMM (LLaMA-7B gate projection, 8192 x 4096 -> 11008) with the 4-bit
+    # LAAQ quantization of its output fused; beside it the unfused sequence
+    # (cuBLAS BF16 matmul, then the quantizer) and cuBLAS alone
+    Tf, Kf, Nf = 8192, 4096, 11008
+    xf = torch.randn(Tf, Kf, device=device).to(torch.bfloat16)
+    wf = (torch.randn(Nf, Kf, device=device) * 0.02).to(torch.bfloat16)
+    yf = torch.empty(Tf, Nf, dtype=torch.bfloat16, device=device)
+    cf = torch.empty(Tf * Nf // 128 * 64, dtype=torch.uint8, device=device)
+    sf = torch.empty(Tf * Nf // 128, dtype=torch.float32, device=device)
+    name = "fwd_gemm_quant_b4_8192x4096x11008"
+    try:
+        ms = _time_launch(lambda: agoq.agoq_fwd_gemm_quant(xf, wf, Tf, Nf, Kf, 4, yf, cf, sf), flush)
+        agoq.agoq_device_status()
+        tflops = 2.0 * Tf * Nf * Kf / (ms * 1e-3) / 1e12
+        rows[name] = {"us": round(ms * 1e3, 1), "TFLOP/s": round(tflops, 1),
+                      "frac_of_measured_bf16": round(tflops / bf16_peak, 4)}
+        rows[name]["cublas_matmul_then_quant_us"] = round(_time_launch(
+            lambda: (torch.matmul(xf, wf.t(), out=yf), agoq.agoq_quant_act(yf, 4, cf, sf)),
+            flush) * 1e3, 1)
+        rows[name]["cublas_matmul_alone_us"] = round(_time_launch(
+            lambda: torch.matmul(xf, wf.t(), out=yf), flush) * 1e3, 1)
+    except agoq.AgoqError as e:
+        rows[name] = {"unavailable": str(e)}
+    del xf, wf, yf, cf, sf
+
     # The same GEMM with the QuanGrad accumulation into an FP8 master as its epilogue
     master = torch.zeros(M * N, dtype=torch.uint8, device=device)
     mscales = torch.zeros(M * N // 128, dtype=torch.float32, device=device)
@@ -668,7 +693,7 @@ def reference_arm(args):
 
 
 PROFILE_CASES = ("accum", "reduce8", "reduce8_nocount", "reduce64", "gemm", "gemm_accum", "silu",
-                 "rmsnorm")
+                 "rmsnorm", "fwd_gemm")
 
 
 def profile_case(name, launches=3):
@@ -704,6 +729,13 @@ def profile_case(name, launches=3):
                 agoq.agoq_wgrad_gemm_int4(dy, xc, xs, M, N, K)
             else:
                 agoq.agoq_wgrad_gemm_int4_accum_fp8(dy, xc, xs, M, N, K, master, mscales)
+        agoq.agoq_device_status()
+    elif name == "fwd_gemm":
+        T, K, N = 8192, 4096, 11008
+        x = torch.randn(T, K, device=dev).to(torch.bfloat16)
+        w = (torch.randn(N, K, device=dev) * 0.02).to(torch.bfloat16)
+        for _ in range(launches):
+            agoq.agoq_fwd_gemm_quant(x, w, T, N, K, 4)
         agoq.agoq_device_status()
     elif name == "silu":
         x = synthetic.dbca_activations_torch(seed=1, device=dev)[1]

@@ -60,11 +60,13 @@ def _lib_handle():
         L.agoq_wgrad_gemm_int4_accum_fp8.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.agoq_device_status.argtypes = [vp]
         L.agoq_dbca_pp_bits.argtypes = [i32, i32, i32, vp]
+        L.agoq_fwd_gemm_quant.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
         for name in ("agoq_quant_act", "agoq_dequant_act", "agoq_grad_accum_fp8",
                      "agoq_reduce_fp8_shards", "agoq_wgrad_gemm_int4",
                      "agoq_wgrad_gemm_int4_f32out", "agoq_device_status",
                      "agoq_wgrad_gemm_int4_accum_fp8", "agoq_grad_accum_fp8_mid",
-                     "agoq_silu_backward", "agoq_rmsnorm_backward", "agoq_dbca_pp_bits"):
+                     "agoq_silu_backward", "agoq_rmsnorm_backward", "agoq_dbca_pp_bits",
+                     "agoq_fwd_gemm_quant"):
             getattr(L, name).restype = i32
         _L = L
     return _L
@@ -208,6 +210,23 @@ def agoq_dbca_pp_bits(stages, microbatches, base_bits=4):
     _check(lib().agoq_dbca_pp_bits(int(stages), int(microbatches), int(base_bits), out),
            "agoq_dbca_pp_bits")
     return list(out)[:stages]
+
+
+def agoq_fwd_gemm_quant(x, w, T, N, K, bits, y=None, codes=None, scales=None, stream=None):
+    """Forward GEMM Y = bf16(X W^T) (X [T][K], W [N][K], BF16) with the LAAQ
+    quantization of Y fused: returns (Y [T][N], codes, scales)."""
+    _need(x, torch.bfloat16, "x")
+    _need(w, torch.bfloat16, "w")
+    dev = x.device
+    if y is None:
+        y = torch.empty((T, N), dtype=torch.bfloat16, device=dev)
+    if codes is None:
+        codes = torch.empty(T * N // BLOCK * record_bytes(bits), dtype=torch.uint8, device=dev)
+    if scales is None:
+        scales = torch.empty(T * N // BLOCK, dtype=torch.float32, device=dev)
+    _check(lib().agoq_fwd_gemm_quant(_ptr(x), _ptr(w), T, N, K, bits, _ptr(y), _ptr(codes),
+                                     _ptr(scales), _stream(stream)), "agoq_fwd_gemm_quant")
+    return y, codes, scales
 
 
 MID_FP32, MID_BF16, MID_FP16 = 0, 1, 2

@@ -26,8 +26,9 @@ UNITS = {
     "quangrad.cu": ["-fmad=false"],
     "wgrad_gemm.cu": ["-fmad=false"],
     "rmsnorm.cu": ["-fmad=false"],
+    "fwd_gemm.cu": ["-fmad=false"],
 }
-HEADERS = ["agoq_device.cuh", "agoq_launch.h"]
+HEADERS = ["agoq_device.cuh", "agoq_launch.h", "gemm_common.cuh"]
 
 
 def _nvcc():

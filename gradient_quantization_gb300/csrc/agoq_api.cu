@@ -262,11 +262,37 @@ agoq_status agoq_dbca_pp_bits(int stages, int microbatches, int base_bits, int *
     return AGOQ_OK;
 }
 
+agoq_status agoq_fwd_gemm_quant(const void *x_bf16, const void *w_bf16, int T, int N, int K,
+                                int bits, void *y_bf16, void *codes, float *scales, void *stream) {
+    using namespace agoq;
+    if (!bits_ok(bits)) return AGOQ_ERR_BITS;
+    if (T <= 0 || N <= 0 || K <= 0 || T % 128 || N % 256 || K % 64) return AGOQ_ERR_SHAPE;
+    if (!x_bf16 || !w_bf16 || !y_bf16 || !codes || !scales) return AGOQ_ERR_NULL;
+    if (!aligned(x_bf16, 16) || !aligned(w_bf16, 16) || !aligned(y_bf16, 16) ||
+        !aligned(codes, 16) || !aligned(scales, 4))
+        return AGOQ_ERR_ALIGN;
+    const uint64_t n = (uint64_t)T * N, nb = n / kBlockElems;
+    const uint64_t xb = 2ull * T * K, wb = 2ull * N * K, yb = 2 * n, cb = nb * 16 * bits,
+                   sb = nb * 4;
+    const void *in[2] = {x_bf16, w_bf16};
+    const uint64_t inb[2] = {xb, wb};
+    for (int i = 0; i < 2; ++i)
+        if (overlap(y_bf16, yb, in[i], inb[i]) || overlap(codes, cb, in[i], inb[i]) ||
+            overlap(scales, sb, in[i], inb[i]))
+            return AGOQ_ERR_ALIAS;
+    if (overlap(y_bf16, yb, codes, cb) || overlap(y_bf16, yb, scales, sb) ||
+        overlap(codes, cb, scales, sb))
+        return AGOQ_ERR_ALIAS;
+    return from_cuda(launch_fwd_gemm_quant(x_bf16, w_bf16, T, N, K, bits, y_bf16, codes, scales,
+                                           as_stream(stream)));
+}
+
 agoq_status agoq_device_status(void *stream) {
-    unsigned status = 0;
-    if (agoq::read_and_clear_device_status(agoq::as_stream(stream), &status) != cudaSuccess)
+    unsigned status = 0, fwd = 0;
+    if (agoq::read_and_clear_device_status(agoq::as_stream(stream), &status) != cudaSuccess ||
+        agoq::read_and_clear_fwd_status(&fwd) != cudaSuccess)
         return AGOQ_ERR_CUDA;
-    return status ? AGOQ_ERR_TIMEOUT : AGOQ_OK;
+    return (status || fwd) ? AGOQ_ERR_TIMEOUT : AGOQ_OK;
 }
 
 }  // extern "C"

@@ -398,4 +398,31 @@ __device__ __forceinline__ uint4 dequantize_chunk(uint32_t lo, uint32_t hi, floa
     return make_uint4(out[0], out[1], out[2], out[3]);
 }
 
+// Integer codes of 16 BF16 values (8 words) for a block scale s >= 2^-96:
+// code = rne_int(fl(x / s)).  The binary32 quotient is formed with Markstein's
+// correction of the reciprocal product (P. Markstein, "Computation of
+// elementary functions on the IBM RISC System/6000 processor", IBM J. Res.
+// Dev. 34(1), 1990): r = fl(1/s), q = fl(x*r), rho = fma(-q, s, x) (exact),
+// q' = fma(rho, r, q); then q' + 1.5*2^23 rounds it to an integer.  For BF16
+// x with |x| <= absmax and s = fl(absmax/qmax) >= 2^-96, rne_int(q') equals
+// rne_int(fl(x/s)) for every x, absmax and qmax in {7, 15, 31, 127}: checked
+// exhaustively against IEEE division (tests/test_gpu_laaq_exhaustive.py runs
+// the same check through the library).  Below 2^-96 the residual can fall
+// into the subnormal range and the correction can miss a tie, so those blocks
+// take integer_codes_n.  Codes stay within +-qmax because q' = fl(x/s).
+__device__ __forceinline__ void corrected_codes16(const uint32_t w[8], float s, uint32_t cb[16]) {
+    const float r = __frcp_rn(s);
+    const uint64_t r2 = f32x2(r, r), ns2 = f32x2(-s, -s);
+    const uint64_t m2 = f32x2(kRoundMagic, kRoundMagic);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const uint64_t xx = f32x2(bf16_lo(w[i]), bf16_hi(w[i]));
+        const uint64_t q = mul_f32x2(xx, r2);
+        const uint64_t rho = fma_f32x2(q, ns2, xx);
+        const uint64_t t = add_f32x2(fma_f32x2(rho, r2, q), m2);
+        cb[2 * i] = static_cast<uint32_t>(t);
+        cb[2 * i + 1] = static_cast<uint32_t>(t >> 32);
+    }
+}
+
 }  // namespace agoq

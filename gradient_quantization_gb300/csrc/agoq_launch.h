@@ -68,6 +68,10 @@ cudaError_t launch_wgrad_gemm(const void *dY, const void *xc, const float *xs, i
                               void *dW, bool f32_out, cudaStream_t st);
 cudaError_t launch_wgrad_accum_fp8(const void *dY, const void *xc, const float *xs, int M, int N,
                                    int K, void *master, float *master_scales, cudaStream_t st);
+cudaError_t launch_fwd_gemm_quant(const void *x, const void *w, int T, int N, int K, int bits,
+                                  void *y, void *codes, float *scales, cudaStream_t st);
+// Read and clear the forward GEMM's status word (call after synchronising).
+cudaError_t read_and_clear_fwd_status(unsigned *status);
 // Synchronise `st`, read and clear the device status word (0 = no timeout).
 cudaError_t read_and_clear_device_status(cudaStream_t st, unsigned *status);
 

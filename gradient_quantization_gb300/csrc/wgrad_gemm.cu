@@ -49,6 +49,7 @@
 
 #include "agoq_device.cuh"
 #include "agoq_launch.h"
+#include "gemm_common.cuh"
 
 namespace agoq {
 
@@ -57,6 +58,8 @@ namespace agoq {
 __device__ unsigned g_device_status;
 
 namespace {
+
+using namespace gemm;
 
 #ifndef AGOQ_GEMM_BK
 #define AGOQ_GEMM_BK 64
@@ -69,9 +72,6 @@ namespace {
 #endif
 #ifndef AGOQ_GEMM_NA
 #define AGOQ_GEMM_NA 3
-#endif
-#ifndef AGOQ_GEMM_WAIT_HINT_NS
-#define AGOQ_GEMM_WAIT_HINT_NS 0
 #endif
 
 // Epilogue kinds.
@@ -108,125 +108,8 @@ constexpr uint32_t kTmemCols = 512;
 #define AGOQ_GEMM_PREFETCH_LEAD 8
 #endif
 constexpr int kPrefetchLead = AGOQ_GEMM_PREFETCH_LEAD;   // k-blocks between master prefetch and use
-constexpr unsigned kStatusTimeout = 1u;
-constexpr long long kWaitLimitCycles = 4000000000ll;      // about two seconds
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
-
-// ---------------------------------------------------------------- PTX wrappers
-__device__ __forceinline__ uint32_t smem_u32(const void *p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count));
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint64_t *bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
-                 "r"(bytes)
-                 : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
-}
-
-// Test the phase; if it is not complete the thread may sleep up to `hint_ns`
-// (it wakes as soon as the phase completes).
-__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity, uint32_t hint_ns) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, uint64_t *bar, int x,
-                                            int y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%3, %4}], [%2];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(x), "r"(y)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_fence_before() {
-    asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
-}
-__device__ __forceinline__ void tc_fence_after() {
-    asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
-__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
-        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-          "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]), "=r"(v[17]), "=r"(v[18]),
-          "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
-          "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
-          "=r"(v[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-          "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float (&v)[16]) {
-    asm volatile(
-        "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
-        "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
-        "f"(v[8]), "f"(v[9]), "f"(v[10]), "f"(v[11]), "f"(v[12]), "f"(v[13]), "f"(v[14]),
-        "f"(v[15])
-        : "memory");
-}
-
-// Shared-memory matrix descriptor (tcgen05 format) of an MN-major operand
-// stored in 128-byte-swizzled atoms of 8 K-rows x 64 BF16: `lbo` is the byte
-// distance between atoms along M/N, `sbo` between 8-row groups along K.
-__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
-    uint64_t d = 0;
-    d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
-    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
-    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
-    d |= static_cast<uint64_t>(1) << 46;   // descriptor version for tcgen05
-    d |= static_cast<uint64_t>(2) << 61;   // 128-byte swizzle
-    return d;
-}
 
 // Instruction descriptor: kind::f16, BF16 A and B, FP32 D, A and B MN-major,
 // M = 128, N = 256.
@@ -241,39 +124,6 @@ struct Shared {
     uint32_t *tmem_addr;
     volatile int *abort;
 };
-
-// Wait for the phase of `bar` with parity `parity` to complete.  Returns false
-// if the CTA was told to abort or the wait ran past its time limit (which then
-// records the timeout and raises the abort flag).  `ignore_abort` is for the
-// final drains, which must run even after an abort.
-__device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                         bool ignore_abort = false,
-                                         uint32_t hint_ns = AGOQ_GEMM_WAIT_HINT_NS) {
-    if (AGOQ_GEMM_WAIT_HINT_NS == 0) hint_ns = 0;
-    if (mbar_try_wait(bar, parity, hint_ns)) return true;
-    const long long t0 = clock64();
-    for (;;) {
-        if (mbar_try_wait(bar, parity, hint_ns)) return true;
-        if (!ignore_abort && *abort) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
-            *abort = 1;
-            atomicExch(&g_device_status, kStatusTimeout);
-            return false;
-        }
-    }
-}
-
-// The same wait for a whole warp: lane 0 polls, the outcome is broadcast, and
-// the warp leaves converged (the tcgen05 .sync.aligned instructions need that).
-__device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
-                                          uint32_t hint_ns = AGOQ_GEMM_WAIT_HINT_NS) {
-    const int lane = threadIdx.x & 31;
-    bool ok = true;
-    if (lane == 0) ok = wait_bar(bar, parity, abort, false, hint_ns);
-    ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-    __syncwarp();
-    return ok;
-}
 
 // Dequantize one word of eight 4-bit codes (two's complement, element 2i in
 // the low nibble of byte i) with scale s into eight BF16:
@@ -481,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % depth;
                     const uint32_t ph = (it / depth) & 1u;
-                    if (!wait_bar(&empty[s], ph ^ 1u, sh.abort)) { ok = false; break; }
+                    if (!wait_bar(&empty[s], ph ^ 1u, sh.abort, &g_device_status)) { ok = false; break; }
                     const int k0 = kb * BK;
                     if (is_a) {
                         mbar_expect_tx(&full[s], kAStage);
@@ -501,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // load into stage (it-1-d) % depth.
             for (int d = 0; d < depth && d < (int)it; ++d) {
                 const uint32_t last = it - 1 - d;
-                wait_bar(&full[last % depth], (last / depth) & 1u, sh.abort, true);
+                wait_bar(&full[last % depth], (last / depth) & 1u, sh.abort, &g_device_status, true);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -509,12 +359,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0, t = 0;
             bool ok = true, issued = false;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++t) {
-                if (!wait_bar(sh.tmem_empty, (t & 1u) ^ 1u, sh.abort)) { ok = false; break; }
+                if (!wait_bar(sh.tmem_empty, (t & 1u) ^ 1u, sh.abort, &g_device_status)) { ok = false; break; }
                 tc_fence_after();
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int sa = it % NA, sb = it % NB;
-                    if (!wait_bar(&sh.full_a[sa], (it / NA) & 1u, sh.abort) ||
-                        !wait_bar(&sh.full_b[sb], (it / NB) & 1u, sh.abort)) {
+                    if (!wait_bar(&sh.full_a[sa], (it / NA) & 1u, sh.abort, &g_device_status) ||
+                        !wait_bar(&sh.full_b[sb], (it / NB) & 1u, sh.abort, &g_device_status)) {
                         ok = false;
                         break;
                     }
@@ -542,7 +392,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             // Drain: all MMAs issued so far complete before TMEM is freed.
             if (issued) {
                 umma_commit(sh.drain);
-                wait_bar(sh.drain, 0u, sh.abort, true);
+                wait_bar(sh.drain, 0u, sh.abort, &g_device_status, true);
             }
         }
     } else {
@@ -559,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         // stages of this tile (or all of them, for short K).
         const int lead = (kblocks < NB ? kblocks : NB) - 1;
         auto epilogue = [&](int tile, uint32_t t) -> bool {
-            if (!warp_wait(sh.tmem_full, t & 1u, sh.abort)) return false;
+            if (!warp_wait(sh.tmem_full, t & 1u, sh.abort, &g_device_status)) return false;
             tc_fence_after();
             const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
             epilogue_item<EPI>(etaddr, dW, mscales, m0 + eh * 128 + 32 * q + lane, n0 + ejb * 128,
@@ -587,7 +437,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                 }
                 const int sx = it % NX, sb = it % NB;
-                if (!warp_wait(&sh.full_x[sx], (it / NX) & 1u, sh.abort)) { ok = false; break; }
+                if (!warp_wait(&sh.full_x[sx], (it / NX) & 1u, sh.abort, &g_device_status)) { ok = false; break; }
                 const uint32_t *codes = reinterpret_cast<const uint32_t *>(sh.c + sx * kCStage);
                 const float *scales = sh.s + sx * (kSStage / 4);
                 uint32_t w[kDeqRows];
@@ -598,7 +448,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     w[i] = codes[k * 32 + wc];
                     sc[i] = scales[k * 4 + soff];
                 }
-                if (!warp_wait(&sh.empty_b[sb], ((it / NB) & 1u) ^ 1u, sh.abort)) { ok = false; break; }
+                if (!warp_wait(&sh.empty_b[sb], ((it / NB) & 1u) ^ 1u, sh.abort, &g_device_status)) { ok = false; break; }
                 uint8_t *btile = sh.b + sb * kBStage + chunk * kChunk;
 #pragma unroll
                 for (int i = 0; i < kDeqRows; ++i) {
@@ -634,38 +484,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // ---------------------------------------------------------------- host side
-using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                   const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                   const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                   CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static EncodeTiledFn fn = nullptr;
-    if (!fn) {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeTiledFn>(p);
-    }
-    return fn;
-}
-
-bool encode_2d(CUtensorMap *map, CUtensorMapDataType dt, const void *base, uint64_t dim0,
-               uint64_t dim1, uint64_t row_bytes, uint32_t box0, uint32_t box1,
-               CUtensorMapSwizzle swz) {
-    EncodeTiledFn fn = encode_fn();
-    if (!fn) return false;
-    const cuuint64_t dims[2] = {dim0, dim1};
-    const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {box0, box1};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(map, dt, 2, const_cast<void *>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, swz, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <int EPI>
 cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, int N, int K,
                         void *dW, float *mscales, cudaStream_t st) {

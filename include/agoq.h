@@ -240,6 +240,25 @@ agoq_status agoq_wgrad_gemm_int4_accum_fp8(const void *dY_bf16, const void *x_co
                                            void *master_e4m3, float *master_scales, void *stream);
 
 /*
+ * A linear layer's forward GEMM with the LAAQ quantization of its output fused
+ * into the epilogue (AGoQ section 2.C, "Kernel Fusion", with section 2.A: the
+ * activation kept for the backward pass is stored in `bits`-wide codes):
+ *   Y[t][n] = bf16_rne(acc[t][n]),  acc = sum_k X[t][k] * W[n][k] accumulated
+ *             in FP32 on the tensor cores (order unspecified);
+ *   codes, scales = agoq_quant_act(Y, T*N, bits) (row t = blocks t*N/128 ..).
+ *   x_bf16 : in, BF16 [T][K] (K contiguous).   w_bf16 : in, BF16 [N][K] (K contiguous,
+ *            the torch Linear weight layout).
+ *   y_bf16 : out, BF16 [T][N].   codes : out, (T*N/128) records of 16*bits bytes.
+ *   scales : out, FP32 [T][N/128].
+ * T must be a multiple of 128, N of 256, K of 64, all > 0 (AGOQ_ERR_SHAPE);
+ * bits in {4, 5, 6, 8}; all pointers 16-byte aligned (scales 4-byte).  Outputs
+ * must not overlap the operands or each other.  Pipeline waits are
+ * time-limited: see agoq_device_status.
+ */
+agoq_status agoq_fwd_gemm_quant(const void *x_bf16, const void *w_bf16, int T, int N, int K,
+                                int bits, void *y_bf16, void *codes, float *scales, void *stream);
+
+/*
  * DBCA-PP bit-width assignment (AGoQ section 2.A, "Dynamic Bit-width
  * Compensation (DBCA-PP)": pipeline stages that hold fewer activation batches
  * get wider codes, the stages with the most batches the base width, so that
@@ -256,9 +275,10 @@ agoq_status agoq_dbca_pp_bits(int stages, int microbatches, int base_bits, int *
 
 /*
  * Synchronise `stream`, then read and clear the library's device-side status
- * word for the current device.  Returns AGOQ_ERR_TIMEOUT if a GEMM pipeline
- * wait exceeded its iteration limit since the last call (that GEMM's output is
- * then incomplete), AGOQ_ERR_CUDA if the synchronisation failed, else AGOQ_OK.
+ * words for the current device.  Returns AGOQ_ERR_TIMEOUT if a pipeline wait
+ * of a GEMM (agoq_wgrad_gemm_int4*, agoq_fwd_gemm_quant) exceeded its time
+ * limit since the last call (that GEMM's output is then incomplete),
+ * AGOQ_ERR_CUDA if the synchronisation failed, else AGOQ_OK.
  */
 agoq_status agoq_device_status(void *stream);
 

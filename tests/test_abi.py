@@ -163,6 +163,19 @@ def test_gemm_accum_validation(L):
     assert fn(P(A), P(B), P(C), 256, 512, 64, P(D), P(D + 4096), None) == ALIAS
 
 
+def test_fwd_gemm_quant_validation(L):
+    fn = L.agoq_fwd_gemm_quant
+    D, E, F = C + (1 << 24), C + (1 << 26), C + (1 << 27)
+    assert fn(P(A), P(B), 128, 256, 64, 3, P(D), P(E), P(F), None) == BITS
+    assert fn(P(A), P(B), 100, 256, 64, 4, P(D), P(E), P(F), None) == SHAPE
+    assert fn(P(A), P(B), 128, 128, 64, 4, P(D), P(E), P(F), None) == SHAPE
+    assert fn(P(A), P(B), 128, 256, 48, 4, P(D), P(E), P(F), None) == SHAPE
+    assert fn(P(A), None, 128, 256, 64, 4, P(D), P(E), P(F), None) == NULL
+    assert fn(P(A), P(B), 128, 256, 64, 4, P(D + 2), P(E), P(F), None) == ALIGN
+    assert fn(P(A), P(B), 128, 256, 64, 4, P(A), P(E), P(F), None) == ALIAS      # y on x
+    assert fn(P(A), P(B), 128, 256, 64, 4, P(D), P(D + 256), P(F), None) == ALIAS
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(agoq, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(agoq, "_L", None)
