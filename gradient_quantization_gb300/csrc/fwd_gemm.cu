@@ -49,6 +49,36 @@ constexpr int kSmemBytes = kOffMisc + 16 + 1024;
 constexpr uint32_t kTmemCols = 512;
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
+#ifndef AGOQ_FWD_BAND
+#define AGOQ_FWD_BAND 16
+#endif
+#ifndef AGOQ_FWD_STREAM_STORES
+#define AGOQ_FWD_STREAM_STORES 1
+#endif
+
+// Tile order: bands of kBand consecutive N-panels; within a band the tiles run
+// N-fastest, then M, so the CTAs working at the same time share a few W panels
+// and X row blocks (a working set that stays in L2).
+constexpr int kBand = AGOQ_FWD_BAND;
+
+__device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &m0, int &n0) {
+    const int band = tile / (kBand * num_m);
+    const int nb = min(kBand, num_n - band * kBand);            // panels in this band
+    const int r = tile - band * kBand * num_m;
+    m0 = (r / nb) * BM;
+    n0 = (band * kBand + r % nb) * BN;
+}
+
+__device__ __forceinline__ void st_stream16(void *p, uint4 v) {
+#if AGOQ_FWD_STREAM_STORES
+    asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
+                 "r"(v.w)
+                 : "memory");
+#else
+    *static_cast<uint4 *>(p) = v;
+#endif
+}
+
 // kind::f16, BF16 A and B, FP32 D, both K-major, M = 128, N = 256.
 constexpr uint32_t kIdescK = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                              ((uint32_t)(BM >> 4) << 24);
@@ -121,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint32_t it = 0;
             bool ok = true;
             for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int m0 = (tile % num_m) * BM, n0 = (tile / num_m) * BN;
+                int m0, n0;
+                tile_coords(tile, num_m, num_n, m0, n0);
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % NS;
                     if (!wait_bar(&empty[s], ((it / NS) & 1u) ^ 1u, abort, status)) {
@@ -180,7 +211,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int buf = t & 1;
             if (!warp_wait(&tfull[buf], (t >> 1) & 1u, abort, status)) break;
             tc_fence_after();
-            const int m0 = (tile % num_m) * BM, n0 = (tile / num_m) * BN;
+            int m0, n0;
+            tile_coords(tile, num_m, num_n, m0, n0);
             const int row = m0 + 32 * q + lane;
             const uint32_t tbase = tmem_base + ((uint32_t)(32 * q) << 16) + buf * BN;
 #pragma unroll 1
@@ -200,7 +232,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint4 *dst = reinterpret_cast<uint4 *>(y + (size_t)row * N + col0 + cc * 32);
 #pragma unroll
                     for (int i = 0; i < 4; ++i)
-                        dst[i] = make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]);
+                        st_stream16(dst + i, make_uint4(h[4 * i], h[4 * i + 1], h[4 * i + 2], h[4 * i + 3]));
                     am = fmaxf(am, bf16_absmax<16>(h));
                 }
                 const float s = __fdiv_rn(am, (float)kQmax);   // +0 for an all-zero block
@@ -238,8 +270,15 @@ __global__ void __launch_bounds__(kThreads, 1)
                             sink.put((static_cast<uint64_t>(hi) << 32) | lo, 8 * BITS);
                         }
                     }
+                    if constexpr (BITS % 4 == 0) {
 #pragma unroll
-                    for (int i = 0; i < BITS; ++i) rec[cc * BITS + i] = out[i];
+                        for (int i = 0; i < BITS; i += 4)
+                            st_stream16(rec + cc * BITS + i,
+                                        make_uint4(out[i], out[i + 1], out[i + 2], out[i + 3]));
+                    } else {
+#pragma unroll
+                        for (int i = 0; i < BITS; ++i) rec[cc * BITS + i] = out[i];
+                    }
                 }
                 scales[(size_t)row * rec_per_row + col0 / kBlock] = s;
             }
