@@ -82,8 +82,23 @@ constexpr int NA = AGOQ_GEMM_NA, NX = AGOQ_GEMM_NX, NB = AGOQ_GEMM_NB;
 constexpr int kChunk = BK * 128;                          // bytes of one 64-wide M/N chunk of a stage
 constexpr int kTmaWarp = 0, kMmaWarp = 1, kTmaXWarp = 2, kDeqWarp0 = 3, kDeqWarps = 16;
 constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;   // 608
-constexpr int kDeqRows = BK / kDeqWarps;                  // k-rows per dequant thread per stage
-static_assert(kDeqRows * kDeqWarps == BK, "every k-row of a stage is dequantized exactly once");
+#ifndef AGOQ_GEMM_CLUSTER
+#define AGOQ_GEMM_CLUSTER 1
+#endif
+// With kCluster > 1 the CTAs of a cluster share the dequantized operand: the
+// kCluster CTAs of a cluster take tiles with the same N columns and
+// consecutive M rows, each dequantizes kSliceRows of the BK k-rows of every
+// stage and writes them into the X-hat stage of every CTA of the cluster
+// (distributed shared memory), and every MMA's commit releases the stage in
+// every CTA.  This divides the dequantization work by kCluster but couples the
+// CTAs' rings; measured on GB300 the cross-SM handoff per k-block costs more
+// than the dequantization it saves, so the default is 1 (no cluster).
+constexpr int kCluster = AGOQ_GEMM_CLUSTER;
+constexpr int kSliceRows = BK / kCluster;                 // k-rows of a stage this CTA dequantizes
+constexpr int kDeqRows = kSliceRows / kDeqWarps;          // k-rows per dequant thread per stage
+static_assert(kCluster == 1 || kCluster == 2 || kCluster == 4, "cluster size");
+static_assert(kDeqRows >= 1 && kDeqRows * kDeqWarps * kCluster == BK,
+              "every k-row of a stage is dequantized exactly once in the cluster");
 static_assert(NB >= 2, "the B ring must let dequantization run ahead of the MMA");
 static_assert(kDeqWarps == 16, "epilogue items: 4 TMEM lane quarters x 4 blocks of 128 columns");
 // A waiter may only be one phase behind the barrier it polls (a parity test
@@ -93,8 +108,8 @@ static_assert(kDeqWarps == 16, "epilogue items: 4 TMEM lane quarters x 4 blocks 
 // released the accumulator.
 constexpr int kAStage = BM * BK * 2;                      // 32 KiB of dY (BF16)
 constexpr int kBStage = BN * BK * 2;                      // 32 KiB of Xhat (BF16)
-constexpr int kCStage = BK * BN / 2;                      // 8 KiB of packed codes
-constexpr int kSStage = BK * 4 * 4;                       // BK rows x 4 scales
+constexpr int kCStage = kSliceRows * BN / 2;              // this CTA's rows of packed codes
+constexpr int kSStage = kSliceRows * 4 * 4;               // ... and their 4-wide scale boxes
 static_assert(BK % 16 == 0 && BK >= 16 && BK <= 256, "k-block depth");
 constexpr int kOffB = NA * kAStage;
 constexpr int kOffC = kOffB + NB * kBStage;
@@ -169,61 +184,92 @@ __device__ __forceinline__ uint32_t word_of(const uint4 (&c)[8], int i) {
     return (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
 }
 
+#ifndef AGOQ_ACCUM_LD_GROUP
+#define AGOQ_ACCUM_LD_GROUP 1
+#endif
+#ifndef AGOQ_ACCUM_EARLY_LOAD
+#define AGOQ_ACCUM_EARLY_LOAD 0
+#endif
+constexpr int kLdGroup = AGOQ_ACCUM_LD_GROUP;   // TMEM loads issued per wait
+
+// The 128 E4M3 master codes and the scale of one row block, loaded before the
+// accumulator is ready (the loads do not depend on it).
+struct MasterBlock {
+    uint4 c[8];
+    float s;
+    __device__ __forceinline__ void load(const uint8_t *codes, const float *scale) {
+        const uint4 *mc = reinterpret_cast<const uint4 *>(codes);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = mc[i];
+        s = *scale;
+    }
+};
+
 // QuanGrad accumulation of one 128-column block of an accumulator row into the
 // FP8 master (in place): `taddr` is the TMEM address of the block's first
-// column in this warp's lane quarter, `codes` the 128 master codes of the
-// block, `scale` its FP32 scale.  The first pass forms t = fl(fl(e4m3(c) * s)
-// + acc), takes the block absmax and writes t back over the accumulator in
-// TMEM; the second pass reads t and requantizes with the new scale.
-__device__ __forceinline__ void accum_fp8_block(uint32_t taddr, uint8_t *codes, float *scale) {
+// column in this warp's lane quarter, `mb` the block's master codes and scale
+// (already loaded), `codes`/`scale` where the new ones go.  The first pass
+// forms t = fl(fl(e4m3(c) * s) + acc), takes the block absmax and writes t
+// back over the accumulator in TMEM; the second pass reads t and requantizes
+// with the new scale.  TMEM loads go in pairs behind one wait.
+__device__ __forceinline__ void accum_fp8_block(uint32_t taddr, const MasterBlock &mb,
+                                                uint8_t *codes, float *scale) {
     uint4 *mc = reinterpret_cast<uint4 *>(codes);
-    uint4 c[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = mc[i];
-    const float s = *scale;
     float am = 0.0f;
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-        uint32_t v[16];
-        tmem_ld16(taddr + cc * 16, v);
-        float t[16];
+    for (int cc = 0; cc < 8; cc += kLdGroup) {
+        uint32_t v[kLdGroup][16];
+        __syncwarp();
 #pragma unroll
-        for (int w = 0; w < 4; ++w) {
-            master_plus_acc4(word_of(c, cc * 4 + w), s, v + 4 * w, t + 4 * w);
-            am = fmaxf(am, fmaxf(fmaxf(fabsf(t[4 * w]), fabsf(t[4 * w + 1])),
-                                 fmaxf(fabsf(t[4 * w + 2]), fabsf(t[4 * w + 3]))));
+        for (int h = 0; h < kLdGroup; ++h) tmem_ld16_nowait(taddr + (cc + h) * 16, v[h]);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < kLdGroup; ++h) {
+            float t[16];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                master_plus_acc4(word_of(mb.c, (cc + h) * 4 + w), mb.s, v[h] + 4 * w, t + 4 * w);
+                am = fmaxf(am, fmaxf(fmaxf(fabsf(t[4 * w]), fabsf(t[4 * w + 1])),
+                                     fmaxf(fabsf(t[4 * w + 2]), fabsf(t[4 * w + 3]))));
+            }
+            tmem_st16(taddr + (cc + h) * 16, t);
         }
-        tmem_st16(taddr + cc * 16, t);
     }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     const float snew = __fdiv_rn(am, kE4M3Max);
 #pragma unroll
-    for (int cc = 0; cc < 8; ++cc) {
-        uint32_t v[16];
+    for (int cc = 0; cc < 8; cc += kLdGroup) {
+        uint32_t v[kLdGroup][16];
         __syncwarp();   // lanes may have left the fast requantization path; tcgen05.ld is .aligned
-        tmem_ld16(taddr + cc * 16, v);
-        uint32_t o[4];
 #pragma unroll
-        for (int p = 0; p < 2; ++p) {
-            float t[8];
+        for (int h = 0; h < kLdGroup; ++h) tmem_ld16_nowait(taddr + (cc + h) * 16, v[h]);
+        tmem_wait_ld();
 #pragma unroll
-            for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(v[8 * p + i]);
-            const uint2 q = e4m3_codes8(t, snew);
-            o[2 * p] = q.x;
-            o[2 * p + 1] = q.y;
+        for (int h = 0; h < kLdGroup; ++h) {
+            uint32_t o[4];
+#pragma unroll
+            for (int p = 0; p < 2; ++p) {
+                float t[8];
+#pragma unroll
+                for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(v[h][8 * p + i]);
+                const uint2 q = e4m3_codes8(t, snew);
+                o[2 * p] = q.x;
+                o[2 * p + 1] = q.y;
+            }
+            mc[cc + h] = make_uint4(o[0], o[1], o[2], o[3]);
         }
-        mc[cc] = make_uint4(o[0], o[1], o[2], o[3]);
     }
     *scale = snew;
 }
 
 // One epilogue item: row `row`, columns col0 .. col0+127 of the output, whose
-// accumulators start at TMEM address `taddr` (this warp's lane quarter).
+// accumulators start at TMEM address `taddr` (this warp's lane quarter); `mb`
+// holds the item's master block for the accumulation epilogue.
 template <int EPI>
 __device__ __forceinline__ void epilogue_item(uint32_t taddr, void *dW, float *mscales, int row,
-                                              int col0, int N) {
+                                              int col0, int N, const MasterBlock &mb) {
     if constexpr (EPI == kEpiAccumFp8) {
-        accum_fp8_block(taddr, static_cast<uint8_t *>(dW) + (size_t)row * N + col0,
+        accum_fp8_block(taddr, mb, static_cast<uint8_t *>(dW) + (size_t)row * N + col0,
                         mscales + (size_t)row * (N / 128) + col0 / 128);
     } else {
 #pragma unroll 1
@@ -283,7 +329,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh.abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tiles = N / BN, num_tiles = (M / BM) * n_tiles, kblocks = K / BK;
+    const int n_tiles = N / BN, kblocks = K / BK;
+    // Cluster tiling: group g covers kCluster consecutive M tiles of one N panel;
+    // this CTA (cluster rank `rank`) takes M tile (g / n_tiles) * kCluster + rank,
+    // which may lie past M for the last group (then it only helps dequantize).
+    const int rank = (int)(blockIdx.x % kCluster);
+    const int cluster_id = (int)(blockIdx.x / kCluster), num_clusters = (int)(gridDim.x / kCluster);
+    const int m_tiles = M / BM, num_groups = ((m_tiles + kCluster - 1) / kCluster) * n_tiles;
+    auto tile_of = [&](int g, int &m0, int &n0) -> bool {
+        const int mt = (g / n_tiles) * kCluster + rank;
+        m0 = mt * BM;
+        n0 = (g % n_tiles) * BN;
+        return mt < m_tiles;
+    };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NA; ++s) {
@@ -295,8 +353,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.empty_x[s], kDeqWarps);
         }
         for (int s = 0; s < NB; ++s) {
-            mbar_init(&sh.full_b[s], kDeqWarps);
-            mbar_init(&sh.empty_b[s], 1);
+            mbar_init(&sh.full_b[s], kDeqWarps * kCluster);   // every dequant warp of the cluster
+            mbar_init(&sh.empty_b[s], kCluster);              // every MMA of the cluster
         }
         mbar_init(sh.tmem_full, 1);
         mbar_init(sh.tmem_empty, kDeqWarps);
@@ -314,6 +372,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if constexpr (kCluster > 1) cluster_sync_all();   // peers' barriers are initialised
     const uint32_t tmem_base = *sh.tmem_addr;
 
     if (warp == kTmaWarp || warp == kTmaXWarp) {
@@ -325,8 +384,9 @@ __global__ void __launch_bounds__(kThreads, 1)
             uint64_t *empty = is_a ? sh.empty_a : sh.empty_x;
             uint32_t it = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x) {
-                const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
+            for (int g = cluster_id; ok && g < num_groups; g += num_clusters) {
+                int m0, n0;
+                const bool valid = tile_of(g, m0, n0);
                 const int sx = (n0 / 128) & ~3;
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % depth;
@@ -334,15 +394,21 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!wait_bar(&empty[s], ph ^ 1u, sh.abort, &g_device_status)) { ok = false; break; }
                     const int k0 = kb * BK;
                     if (is_a) {
+                        if (!valid) {      // no rows of dY: the MMA's result is discarded
+                            mbar_arrive(&full[s]);
+                            continue;
+                        }
                         mbar_expect_tx(&full[s], kAStage);
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
                             tma_load_2d(sh.a + s * kAStage + c * kChunk, &map_dy, &full[s],
                                         m0 + 64 * c, k0);
                     } else {
+                        // this CTA's slice of the k-block's codes and scales
+                        const int kr = k0 + rank * kSliceRows;
                         mbar_expect_tx(&full[s], kCStage + kSStage);
-                        tma_load_2d(sh.c + s * kCStage, &map_xc, &full[s], n0 / 2, k0);
-                        tma_load_2d(sh.s + s * (kSStage / 4), &map_xs, &full[s], sx, k0);
+                        tma_load_2d(sh.c + s * kCStage, &map_xc, &full[s], n0 / 2, kr);
+                        tma_load_2d(sh.s + s * (kSStage / 4), &map_xs, &full[s], sx, kr);
                     }
                 }
             }
@@ -358,13 +424,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane == 0) {
             uint32_t it = 0, t = 0;
             bool ok = true, issued = false;
-            for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++t) {
+            for (int g = cluster_id; ok && g < num_groups; g += num_clusters, ++t) {
                 if (!wait_bar(sh.tmem_empty, (t & 1u) ^ 1u, sh.abort, &g_device_status)) { ok = false; break; }
                 tc_fence_after();
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int sa = it % NA, sb = it % NB;
                     if (!wait_bar(&sh.full_a[sa], (it / NA) & 1u, sh.abort, &g_device_status) ||
-                        !wait_bar(&sh.full_b[sb], (it / NB) & 1u, sh.abort, &g_device_status)) {
+                        !(kCluster > 1 ? wait_bar_cluster(&sh.full_b[sb], (it / NB) & 1u,
+                                                          sh.abort, &g_device_status)
+                                       : wait_bar(&sh.full_b[sb], (it / NB) & 1u, sh.abort,
+                                                  &g_device_status))) {
                         ok = false;
                         break;
                     }
@@ -384,7 +453,11 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     issued = true;
                     umma_commit(&sh.empty_a[sa]);
-                    umma_commit(&sh.empty_b[sb]);
+                    // the X-hat stage is free once every MMA of the cluster has read it
+                    if constexpr (kCluster > 1)
+                        umma_commit_multicast(&sh.empty_b[sb], (uint16_t)((1u << kCluster) - 1u));
+                    else
+                        umma_commit(&sh.empty_b[sb]);
                 }
                 if (!ok) break;
                 umma_commit(sh.tmem_full);
@@ -408,12 +481,25 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The previous tile's epilogue runs once the B ring holds the first
         // stages of this tile (or all of them, for short K).
         const int lead = (kblocks < NB ? kblocks : NB) - 1;
-        auto epilogue = [&](int tile, uint32_t t) -> bool {
+        auto epilogue = [&](int g, uint32_t t) -> bool {
+            int m0, n0;
+            const bool valid = tile_of(g, m0, n0);
+            const int row = m0 + eh * 128 + 32 * q + lane, col0 = n0 + ejb * 128;
+            MasterBlock mb;
+            if constexpr (EPI == kEpiAccumFp8 && AGOQ_ACCUM_EARLY_LOAD) {
+                // the master block's loads overlap the wait for the accumulator
+                if (valid)
+                    mb.load(static_cast<const uint8_t *>(dW) + (size_t)row * N + col0,
+                            mscales + (size_t)row * (N / 128) + col0 / 128);
+            }
             if (!warp_wait(sh.tmem_full, t & 1u, sh.abort, &g_device_status)) return false;
             tc_fence_after();
-            const int m0 = (tile / n_tiles) * BM, n0 = (tile % n_tiles) * BN;
-            epilogue_item<EPI>(etaddr, dW, mscales, m0 + eh * 128 + 32 * q + lane, n0 + ejb * 128,
-                               N);
+            if constexpr (EPI == kEpiAccumFp8 && !AGOQ_ACCUM_EARLY_LOAD) {
+                if (valid)
+                    mb.load(static_cast<const uint8_t *>(dW) + (size_t)row * N + col0,
+                            mscales + (size_t)row * (N / 128) + col0 / 128);
+            }
+            if (valid) epilogue_item<EPI>(etaddr, dW, mscales, row, col0, N, mb);
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(sh.tmem_empty);
@@ -422,16 +508,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t it = 0, t = 0;
         bool ok = true;
         int prev = -1;
-        for (int tile = blockIdx.x; ok && tile < num_tiles; tile += gridDim.x, ++t) {
-            const int n0 = (tile % n_tiles) * BN;
+        for (int g = cluster_id; ok && g < num_groups; g += num_clusters, ++t) {
+            int m0, n0;
+            const bool valid = tile_of(g, m0, n0);
             const int soff = ((n0 / 128) & 3) + (wc >> 4);   // scale column inside the 4-wide box
             for (int kb = 0; kb < kblocks; ++kb, ++it) {
                 if constexpr (EPI == kEpiAccumFp8) {
                     // Pull this thread's master block of the tile into L2 a few
                     // k-blocks before its epilogue needs it.
-                    if (kb == (kblocks > kPrefetchLead ? kblocks - kPrefetchLead : 0)) {
-                        const size_t row =
-                            (size_t)((tile / n_tiles) * BM + eh * 128 + 32 * q + lane);
+                    if (valid && kb == (kblocks > kPrefetchLead ? kblocks - kPrefetchLead : 0)) {
+                        const size_t row = (size_t)(m0 + eh * 128 + 32 * q + lane);
                         prefetch_l2(static_cast<const uint8_t *>(dW) + row * N + n0 + ejb * 128);
                         prefetch_l2(mscales + row * (N / 128) + n0 / 128 + ejb);
                     }
@@ -444,30 +530,53 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float sc[kDeqRows];
 #pragma unroll
                 for (int i = 0; i < kDeqRows; ++i) {
-                    const int k = d + kDeqWarps * i;
-                    w[i] = codes[k * 32 + wc];
-                    sc[i] = scales[k * 4 + soff];
+                    const int lr = d + kDeqWarps * i;           // row of this CTA's slice
+                    w[i] = codes[lr * 32 + wc];
+                    sc[i] = scales[lr * 4 + soff];
                 }
-                if (!warp_wait(&sh.empty_b[sb], ((it / NB) & 1u) ^ 1u, sh.abort, &g_device_status)) { ok = false; break; }
+                // The stage may be overwritten once every MMA of the cluster has read it.
+                if (!(kCluster > 1
+                          ? warp_wait_cluster(&sh.empty_b[sb], ((it / NB) & 1u) ^ 1u, sh.abort,
+                                              &g_device_status)
+                          : warp_wait(&sh.empty_b[sb], ((it / NB) & 1u) ^ 1u, sh.abort,
+                                      &g_device_status))) {
+                    ok = false;
+                    break;
+                }
                 uint8_t *btile = sh.b + sb * kBStage + chunk * kChunk;
 #pragma unroll
                 for (int i = 0; i < kDeqRows; ++i) {
-                    const int k = d + kDeqWarps * i;
+                    const int k = rank * kSliceRows + d + kDeqWarps * i;   // row of the stage
                     const uint4 y = dequant_word(w[i], sc[i]);
-                    *reinterpret_cast<uint4 *>(btile + k * 128 + ((piece ^ (k & 7)) << 4)) = y;
+                    uint8_t *dst = btile + k * 128 + ((piece ^ (k & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(dst) = y;
+                    if constexpr (kCluster > 1) {
+#pragma unroll
+                        for (int p = 1; p < kCluster; ++p)       // the same row in every peer
+                            st_cluster_v4(mapa_shared(smem_u32(dst), (rank + p) % kCluster), y);
+                    }
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                if constexpr (kCluster > 1)
+                    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
+                else
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 // The X stage is released only now: its codes have been consumed
                 // (the B stores depend on them), so no shared-memory load of it
                 // can still be in flight when the next TMA load overwrites it.
                 if (lane == 0) {
                     mbar_arrive(&sh.full_b[sb]);
+                    if constexpr (kCluster > 1) {
+#pragma unroll
+                        for (int p = 1; p < kCluster; ++p)
+                            mbar_arrive_remote(
+                                mapa_shared(smem_u32(&sh.full_b[sb]), (rank + p) % kCluster));
+                    }
                     mbar_arrive(&sh.empty_x[sx]);
                 }
                 if (kb == lead && prev >= 0 && !epilogue(prev, t - 1)) { ok = false; break; }
             }
-            prev = tile;
+            prev = g;
         }
         if (ok && prev >= 0) epilogue(prev, t - 1);
     }
@@ -475,6 +584,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    // No CTA leaves while a peer may still write its X-hat stages or barriers.
+    if constexpr (kCluster > 1) cluster_sync_all();
     if (warp == kMmaWarp) {
         __syncwarp();
         asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
@@ -491,9 +602,9 @@ cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, 
     if (!encode_2d(&m_dy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, (uint64_t)M, (uint64_t)K,
                    (uint64_t)M * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&m_xc, CU_TENSOR_MAP_DATA_TYPE_UINT8, xc, (uint64_t)N / 2, (uint64_t)K,
-                   (uint64_t)N / 2, BN / 2, BK, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   (uint64_t)N / 2, BN / 2, kSliceRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&m_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xs, (uint64_t)N / 128, (uint64_t)K,
-                   (uint64_t)(N / 128) * 4, 4, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   (uint64_t)(N / 128) * 4, 4, kSliceRows, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     auto kernel = wgrad_gemm_int4_kernel<EPI>;
     static bool attr_set[kMaxDevices];
@@ -505,10 +616,36 @@ cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, 
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    const int num_tiles = (M / BM) * (N / BN);
-    const int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-    kernel<<<grid, kThreads, kSmemBytes, st>>>(m_dy, m_xc, m_xs, dW, mscales, M, N, K);
-    return cudaGetLastError();
+    const int groups = ((M / BM + kCluster - 1) / kCluster) * (N / BN);
+    if constexpr (kCluster == 1) {
+        const int grid = groups < sm_count() ? groups : sm_count();
+        kernel<<<grid, kThreads, kSmemBytes, st>>>(m_dy, m_xc, m_xs, dW, mscales, M, N, K);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = kSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    // Persistent grid: as many clusters as can be resident at once (a cluster
+    // must fit in one GPC, so this can be below sm_count / kCluster).
+    static int resident[kMaxDevices];
+    if (dev >= 0 && dev < kMaxDevices && resident[dev] == 0) {
+        cfg.gridDim = dim3(sm_count() / kCluster * kCluster);
+        int n = 0;
+        if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0)
+            n = sm_count() / kCluster;
+        resident[dev] = n;
+    }
+    const int clusters = (dev >= 0 && dev < kMaxDevices) ? resident[dev] : sm_count() / kCluster;
+    cfg.gridDim = dim3((groups < clusters ? groups : clusters) * kCluster);
+    return cudaLaunchKernelEx(&cfg, kernel, m_dy, m_xc, m_xs, dW, mscales, M, N, K);
 }
 
 }  // namespace
