@@ -174,9 +174,24 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
 }
 
 // Largest |value| of the BF16 pairs in w[0..N-1], as a binary32 (exact: the
-// maximum of BF16 magnitudes is a BF16 value).
+// maximum of BF16 magnitudes is a BF16 value).  With AGOQ_ABSMAX_XORSIGN,
+// max.xorsign.abs compares magnitudes directly (its sign bit, the XOR of the
+// inputs', is masked once at the end) instead of masking every word first.
+#ifndef AGOQ_ABSMAX_XORSIGN
+#define AGOQ_ABSMAX_XORSIGN 1
+#endif
 template <int N>
 __device__ __forceinline__ float bf16_absmax(const uint32_t *w) {
+#if AGOQ_ABSMAX_XORSIGN
+    uint32_t m = w[0];
+#pragma unroll
+    for (int i = 1; i < N; ++i) {
+        uint32_t r;
+        asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(w[i]));
+        m = r;
+    }
+    m &= 0x7FFF7FFFu;
+#else
     uint32_t m = w[0] & 0x7FFF7FFFu;
 #pragma unroll
     for (int i = 1; i < N; ++i) {
@@ -184,7 +199,26 @@ __device__ __forceinline__ float bf16_absmax(const uint32_t *w) {
         asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(w[i] & 0x7FFF7FFFu));
         m = r;
     }
+#endif
     return fmaxf(bf16_lo(m), bf16_hi(m));
+}
+
+// fl(am / QMAX) for a BF16 magnitude am (a binary32 holding a non-negative
+// BF16 value, +0 included) and QMAX in {7, 15, 31, 127}, by Markstein's
+// correction of the reciprocal product (P. Markstein, IBM J. Res. Dev. 34(1),
+// 1990): y = fl(1/QMAX), q = fl(am*y), rho = fma(-q, QMAX, am), result
+// fma(rho, y, q).  For these divisors rho is exact and the result equals the
+// IEEE quotient for every BF16 am, subnormals included (checked against exact
+// rational arithmetic for all 32,640 finite magnitudes per divisor; the
+// library's exhaustive quantization test checks the scales of every BF16
+// absmax against IEEE division on the device).
+template <int QMAX>
+__device__ __forceinline__ float bf16_div_qmax(float am) {
+    static_assert(QMAX == 7 || QMAX == 15 || QMAX == 31 || QMAX == 127, "checked divisors only");
+    constexpr float kY = 1.0f / (float)QMAX;
+    const float q = __fmul_rn(am, kY);
+    const float rho = __fmaf_rn(-q, (float)QMAX, am);
+    return __fmaf_rn(rho, kY, q);
 }
 
 // ---- block reductions --------------------------------------------------------
@@ -268,13 +302,17 @@ __device__ __forceinline__ void integer_codes8(const float x[8], float s, uint32
 // with IEEE division.  Values with |x/s| < 1/4 give 0 on every route.  The code
 // never exceeds qmax: |x * r+| <= qmax (1 + 2^-19) < qmax + 1/2.  Subnormal s
 // takes the division and an explicit clamp; s = 0 gives zero codes.
-template <int QMAX, int N>
+//
+// With BIAS > 0 every result is the bit pattern of fl(code + BIAS + 1.5*2^23)
+// instead (see kRoundMagic): the same rounding, as BIAS is an even integer.
+template <int QMAX, int N, int BIAS = 0>
 __device__ __forceinline__ void integer_codes_n(const float *x, float s, uint32_t *code_bits) {
+    constexpr float kMagic = kRoundMagic + (float)BIAS;
     if (s >= 0x1p-126f) {
         const float r = __frcp_rn(s);
         const float rhi = __fmaf_rn(r, 0x1p-20f, r), rlo = __fmaf_rn(r, -0x1p-20f, r);
         const uint64_t rhi2 = f32x2(rhi, rhi), rlo2 = f32x2(rlo, rlo);
-        const uint64_t m2 = f32x2(kRoundMagic, kRoundMagic);
+        const uint64_t m2 = f32x2(kMagic, kMagic);
         uint64_t differ = 0;
 #pragma unroll
         for (int i = 0; i < N; i += 2) {
@@ -288,17 +326,17 @@ __device__ __forceinline__ void integer_codes_n(const float *x, float s, uint32_
         if (differ) {
 #pragma unroll
             for (int i = 0; i < N; ++i)
-                code_bits[i] = __float_as_uint(__fadd_rn(__fdiv_rn(x[i], s), kRoundMagic));
+                code_bits[i] = __float_as_uint(__fadd_rn(__fdiv_rn(x[i], s), kMagic));
         }
     } else if (s > 0.0f) {
 #pragma unroll
         for (int i = 0; i < N; ++i) {
             const float k = fminf(fmaxf(rintf(__fdiv_rn(x[i], s)), -(float)QMAX), (float)QMAX);
-            code_bits[i] = __float_as_uint(__fadd_rn(k, kRoundMagic));
+            code_bits[i] = __float_as_uint(__fadd_rn(k, kMagic));
         }
     } else {
 #pragma unroll
-        for (int i = 0; i < N; ++i) code_bits[i] = __float_as_uint(kRoundMagic);   // code 0
+        for (int i = 0; i < N; ++i) code_bits[i] = __float_as_uint(kMagic);   // code 0
     }
 }
 
@@ -340,6 +378,65 @@ __device__ __forceinline__ void pack_fields8(const uint32_t w[8], uint32_t &lo, 
             }
         }
     }
+}
+
+// Sums over the fields of an 8-field chunk of BITS-bit fields: v shifted to
+// each field's position, the part landing in bits 0-31 (packed_lo) or in bits
+// 32-63 (packed_hi, as a 32-bit word), modulo 2^32.
+template <int BITS>
+__host__ __device__ constexpr uint32_t packed_lo(uint32_t v) {
+    uint32_t r = 0u;
+    for (int i = 0; i < 8; ++i)
+        if (i * BITS < 32) r += v << (i * BITS);
+    return r;
+}
+template <int BITS>
+__host__ __device__ constexpr uint32_t packed_hi(uint32_t v) {
+    uint32_t r = 0u;
+    for (int i = 0; i < 8; ++i) {
+        const int pos = i * BITS;
+        if (pos >= 32) r += v << (pos - 32);
+        else if (pos + BITS > 32) r += v >> (32 - pos);
+    }
+    return r;
+}
+
+// The same chunk as pack_fields8 (BITS in {4, 5, 6}), from words t[i] that hold
+// 0x4B400000 + code_i + 2^(BITS-1), as integer_codes_n and corrected_codes16
+// return them with BIAS = 2^(BITS-1).  The field code + 2^(BITS-1) lies in
+// [0, 2^BITS) and nothing above it differs from 0x4B400000, so the words are
+// added at their shifts without masking (no field carries into the next) and
+// the constant's contribution is subtracted once; flipping each field's top
+// bit then turns offset binary into two's complement.  The low 22 bits of
+// 0x4B400000 are zero, so the right shift of a field that straddles bit 32
+// splits t into the constant's and the field's parts exactly.
+// 1: the shifted additions are written as integer multiply-adds, which the
+// compiler can place on the FMA pipe (measured faster than shifts and adds).
+#ifndef AGOQ_PACK_MAD
+#define AGOQ_PACK_MAD 1
+#endif
+template <int BITS>
+__device__ __forceinline__ void pack_biased8(const uint32_t t[8], uint32_t &lo, uint32_t &hi) {
+    constexpr uint32_t kC = 0x4B400000u;
+    constexpr uint32_t kSign = 1u << (BITS - 1);
+    constexpr uint32_t kCLo = packed_lo<BITS>(kC), kCHi = packed_hi<BITS>(kC);
+    constexpr uint32_t kSLo = packed_lo<BITS>(kSign), kSHi = packed_hi<BITS>(kSign);
+    uint32_t l = 0u - kCLo, h = 0u - kCHi;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int pos = i * BITS;
+#if AGOQ_PACK_MAD
+        // integer multiply-adds (power-of-two multipliers)
+        if (pos < 32) asm("mad.lo.u32 %0, %1, %2, %0;" : "+r"(l) : "r"(t[i]), "r"(1u << pos));
+        if (pos >= 32) asm("mad.lo.u32 %0, %1, %2, %0;" : "+r"(h) : "r"(t[i]), "r"(1u << (pos - 32)));
+#else
+        if (pos < 32) l += t[i] << pos;
+        if (pos >= 32) h += t[i] << (pos - 32);
+#endif
+        else if (pos + BITS > 32) h += t[i] >> (32 - pos);
+    }
+    lo = l ^ kSLo;
+    hi = h ^ kSHi;
 }
 
 // binary32 value of the signed BITS-bit field at bit `pos` of (hi:lo), exact:
@@ -410,18 +507,21 @@ __device__ __forceinline__ uint4 dequantize_chunk(uint32_t lo, uint32_t hi, floa
 // the same check through the library).  Below 2^-96 the residual can fall
 // into the subnormal range and the correction can miss a tie, so those blocks
 // take integer_codes_n.  Codes stay within +-qmax because q' = fl(x/s).
+// BIAS as for integer_codes_n.
+template <int BIAS = 0>
 __device__ __forceinline__ void corrected_codes16(const uint32_t w[8], float s, uint32_t cb[16]) {
+    constexpr float kMagic = kRoundMagic + (float)BIAS;
     const float r = __frcp_rn(s);
     const uint64_t r2 = f32x2(r, r), ns2 = f32x2(-s, -s);
-    const uint64_t m2 = f32x2(kRoundMagic, kRoundMagic);
+    const uint64_t m2 = f32x2(kMagic, kMagic);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const uint64_t xx = f32x2(bf16_lo(w[i]), bf16_hi(w[i]));
         const uint64_t q = mul_f32x2(xx, r2);
         const uint64_t rho = fma_f32x2(q, ns2, xx);
         const uint64_t t = add_f32x2(fma_f32x2(rho, r2, q), m2);
-        cb[2 * i] = static_cast<uint32_t>(t);
-        cb[2 * i + 1] = static_cast<uint32_t>(t >> 32);
+        cb[2 * i] = __float_as_uint(lo_f32(t));
+        cb[2 * i + 1] = __float_as_uint(hi_f32(t));
     }
 }
 

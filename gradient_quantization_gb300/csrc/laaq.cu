@@ -45,6 +45,15 @@
 #ifndef AGOQ_DEQUANT_MIN_CTAS
 #define AGOQ_DEQUANT_MIN_CTAS 1
 #endif
+// 1: codes of 4, 5 and 6 bits are rounded with a biased constant and packed by
+// shifted additions (pack_biased8) instead of masks and shifts.
+#ifndef AGOQ_PACK_BIASED
+#define AGOQ_PACK_BIASED 1
+#endif
+// 1: block scales fl(absmax / qmax) by bf16_div_qmax instead of IEEE division.
+#ifndef AGOQ_SCALE_MARKSTEIN
+#define AGOQ_SCALE_MARKSTEIN 1
+#endif
 
 
 namespace agoq {
@@ -79,15 +88,19 @@ __device__ __forceinline__ void store_chunk_set(uint32_t *rec, int j, int set, u
     } else if constexpr (BITS == 8) {
         if (valid) reinterpret_cast<uint2 *>(rec)[c] = make_uint2(lo, hi);
     } else if constexpr (BITS == 5) {
-        // 4 chunks (160 bits) fill 5 words; chunk q of the group starts at bit 40q
-        const uint32_t plo = __shfl_up_sync(kFull, lo, 1);
-        const uint32_t phi = __shfl_up_sync(kFull, hi, 1);
+        // 4 chunks (160 bits) fill 5 words; chunk q of the group starts at bit
+        // 40q.  Word q >= 1 is the top 8q bits of chunk q-1 below the low
+        // 32-8q bits of chunk q, and word 4 is the top 32 bits of chunk 3.
+        // Each lane sends the next one its top 8(q+1) bits (for q = 3 that is
+        // word 4 itself); hi holds only the chunk's bits 32-39.
         const int q = c & 3;
+        const uint32_t top = __funnelshift_rc(lo, hi, 32 - 8 * q);
+        const uint32_t prev = __shfl_up_sync(kFull, top, 1);
+        const uint32_t word = (q == 0 ? 0u : prev) | (lo << (8 * q));
         uint32_t *w = rec + 5 * (c >> 2);
-        const uint32_t word = q == 0 ? lo : (__funnelshift_rc(plo, phi, 40 - 8 * q) | (lo << (8 * q)));
         if (valid) {
             w[q] = word;
-            if (q == 3) w[4] = __funnelshift_r(lo, hi, 8);
+            if (q == 3) w[4] = top;
         }
     } else {  // BITS == 6: 2 chunks (96 bits) fill 3 words; chunk 1 starts at bit 48
         const uint32_t phi = __shfl_up_sync(kFull, hi, 1);
@@ -107,26 +120,31 @@ __device__ __forceinline__ void store_chunk_set(uint32_t *rec, int j, int set, u
 // (chunk j) and 64+8j..64+8j+7 (chunk j+8), so each 16-byte load instruction
 // of a warp reads 4 x 128 contiguous bytes and the per-block work (absmax
 // shuffles, scale division, reciprocal) is shared by 16 elements per lane.
+//
+// Block indices are 32-bit: the launcher splits inputs of more than
+// kMaxLaunchBlocks blocks into several launches.
 template <int BITS, int UNROLL>
-__global__ void __launch_bounds__(kThreads, AGOQ_QUANT_MIN_CTAS) laaq_quant_kernel(const uint4 *__restrict__ x,
-                                                              uint32_t *__restrict__ codes,
-                                                              float *__restrict__ scales,
-                                                              int64_t nblocks) {
+__global__ void __launch_bounds__(kThreads, AGOQ_QUANT_MIN_CTAS)
+laaq_quant_kernel(const uint4 *__restrict__ x, uint32_t *__restrict__ codes,
+                  float *__restrict__ scales, int nblocks) {
     pdl_wait_and_release();
     constexpr int kWords = 4 * BITS;
     constexpr int kQmax = (1 << (BITS - 1)) - 1;
+    constexpr bool kBiased = AGOQ_PACK_BIASED && BITS < 8;
+    constexpr int kBias = kBiased ? (1 << (BITS - 1)) : 0;
     const int lane = threadIdx.x & 31;
     const int oct = lane >> 3, j = lane & 7;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t stride = nwarps * (4 * UNROLL);
-    auto load_group = [&](int64_t b0, uint4 (&a)[UNROLL], uint4 (&b)[UNROLL]) {
+    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+    const int stride = nwarps * (4 * UNROLL);
+    auto load_group = [&](int b0, uint4 (&a)[UNROLL], uint4 (&b)[UNROLL]) {
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = b0 + 4 * u + oct;
+            const int blk = b0 + 4 * u + oct;
             if (blk < nblocks) {
-                a[u] = ld_stream(x + blk * 16 + j);
-                b[u] = ld_stream(x + blk * 16 + 8 + j);
+                const uint4 *p = x + (size_t)(unsigned)blk * 16 + j;
+                a[u] = ld_stream(p);
+                b[u] = ld_stream(p + 8);
             } else {
                 a[u] = b[u] = make_uint4(0, 0, 0, 0);
             }
@@ -137,7 +155,7 @@ __global__ void __launch_bounds__(kThreads, AGOQ_QUANT_MIN_CTAS) laaq_quant_kern
     uint4 va[UNROLL], vb[UNROLL];
     load_group(warp * (4 * UNROLL), va, vb);
 #endif
-    for (int64_t base = warp * (4 * UNROLL); base < nblocks; base += stride) {
+    for (int base = warp * (4 * UNROLL); base < nblocks; base += stride) {
 #if AGOQ_QUANT_PIPELINE
         uint4 na[UNROLL], nb[UNROLL];
         load_group(base + stride, na, nb);
@@ -153,13 +171,17 @@ __global__ void __launch_bounds__(kThreads, AGOQ_QUANT_MIN_CTAS) laaq_quant_kern
             w[u][0] = va[u].x; w[u][1] = va[u].y; w[u][2] = va[u].z; w[u][3] = va[u].w;
             w[u][4] = vb[u].x; w[u][5] = vb[u].y; w[u][6] = vb[u].z; w[u][7] = vb[u].w;
             const float am = octet_max(bf16_absmax<8>(w[u]));
-            s[u] = __fdiv_rn(am, (float)kQmax);           // +0 for an all-zero block
+#if AGOQ_SCALE_MARKSTEIN
+            s[u] = bf16_div_qmax<kQmax>(am);               // +0 for an all-zero block
+#else
+            s[u] = __fdiv_rn(am, (float)kQmax);
+#endif
             fast &= s[u] >= 0x1p-96f;
         }
         uint32_t cb[UNROLL][16];
         if (fast) {
 #pragma unroll
-            for (int u = 0; u < UNROLL; ++u) corrected_codes16(w[u], s[u], cb[u]);
+            for (int u = 0; u < UNROLL; ++u) corrected_codes16<kBias>(w[u], s[u], cb[u]);
         } else {
 #pragma unroll
             for (int u = 0; u < UNROLL; ++u) {
@@ -170,20 +192,22 @@ __global__ void __launch_bounds__(kThreads, AGOQ_QUANT_MIN_CTAS) laaq_quant_kern
                     f[2 * i + 1] = bf16_hi(w[u][i]);
                 }
                 if (s[u] >= 0x1p-96f)
-                    corrected_codes16(w[u], s[u], cb[u]);
+                    corrected_codes16<kBias>(w[u], s[u], cb[u]);
                 else
-                    integer_codes_n<kQmax, 16>(f, s[u], cb[u]);
+                    integer_codes_n<kQmax, 16, kBias>(f, s[u], cb[u]);
             }
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = base + 4 * u + oct;
+            const int blk = base + 4 * u + oct;
             const bool valid = blk < nblocks;
             uint32_t lo, hi;
-            uint32_t *rec = codes + blk * kWords;
-            pack_fields8<BITS>(cb[u], lo, hi);
+            uint32_t *rec = codes + (size_t)(unsigned)blk * kWords;
+            if constexpr (kBiased) pack_biased8<BITS>(cb[u], lo, hi);
+            else pack_fields8<BITS>(cb[u], lo, hi);
             store_chunk_set<BITS>(rec, j, 0, lo, hi, valid);
-            pack_fields8<BITS>(cb[u] + 8, lo, hi);
+            if constexpr (kBiased) pack_biased8<BITS>(cb[u] + 8, lo, hi);
+            else pack_fields8<BITS>(cb[u] + 8, lo, hi);
             store_chunk_set<BITS>(rec, j, 1, lo, hi, valid);
             if (valid && j == 0) scales[blk] = s[u];
         }
@@ -204,15 +228,16 @@ struct DequantBatch {
     float s[UNROLL];
 
     __device__ __forceinline__ void load(const uint32_t *__restrict__ codes,
-                                         const float *__restrict__ scales, int64_t base, int oct,
-                                         int j, int64_t nblocks) {
+                                         const float *__restrict__ scales, int base, int oct,
+                                         int j, int nblocks) {
         constexpr int kWords = 4 * BITS;
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = base + 4 * u + oct;
+            const int blk = base + 4 * u + oct;
             if (blk < nblocks) {
-                load_chunk<BITS>(codes + blk * kWords, j, alo[u], ahi[u]);
-                load_chunk<BITS>(codes + blk * kWords, j + 8, blo[u], bhi[u]);
+                const uint32_t *rec = codes + (size_t)(unsigned)blk * kWords;
+                load_chunk<BITS>(rec, j, alo[u], ahi[u]);
+                load_chunk<BITS>(rec, j + 8, blo[u], bhi[u]);
                 s[u] = __ldg(scales + blk);
             } else {
                 alo[u] = ahi[u] = blo[u] = bhi[u] = 0u;
@@ -228,14 +253,14 @@ template <int BITS, int UNROLL>
 __global__ void __launch_bounds__(kThreads, AGOQ_DEQUANT_MIN_CTAS) laaq_dequant_kernel(const uint32_t *__restrict__ codes,
                                                                 const float *__restrict__ scales,
                                                                 uint4 *__restrict__ y,
-                                                                int64_t nblocks) {
+                                                                int nblocks) {
     pdl_wait_and_release();
     const int lane = threadIdx.x & 31;
     const int oct = lane >> 3, j = lane & 7;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t stride = nwarps * (4 * UNROLL);
-    int64_t base = warp * (4 * UNROLL);
+    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+    const int stride = nwarps * (4 * UNROLL);
+    int base = warp * (4 * UNROLL);
     if (base >= nblocks) return;
     DequantBatch<BITS, UNROLL> cur, nxt;
     cur.load(codes, scales, base, oct, j, nblocks);
@@ -244,10 +269,11 @@ __global__ void __launch_bounds__(kThreads, AGOQ_DEQUANT_MIN_CTAS) laaq_dequant_
         if (more) nxt.load(codes, scales, base + stride, oct, j, nblocks);
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = base + 4 * u + oct;
+            const int blk = base + 4 * u + oct;
             if (blk < nblocks) {
-                st_stream(y + blk * 16 + j, dequantize_chunk<BITS>(cur.alo[u], cur.ahi[u], cur.s[u]));
-                st_stream(y + blk * 16 + 8 + j, dequantize_chunk<BITS>(cur.blo[u], cur.bhi[u], cur.s[u]));
+                uint4 *out = y + (size_t)(unsigned)blk * 16 + j;
+                st_stream(out, dequantize_chunk<BITS>(cur.alo[u], cur.ahi[u], cur.s[u]));
+                st_stream(out + 8, dequantize_chunk<BITS>(cur.blo[u], cur.bhi[u], cur.s[u]));
             }
         }
         if (more) cur = nxt;
@@ -302,22 +328,23 @@ template <int BITS, int UNROLL, bool WITH_Y>
 __global__ void __launch_bounds__(kThreads, AGOQ_SILU_MIN_CTAS) laaq_silu_backward_kernel(
     const uint32_t *__restrict__ codes, const float *__restrict__ scales,
     const uint4 *__restrict__ dy, uint4 *__restrict__ dx, uint4 *__restrict__ y,
-    int64_t nblocks) {
+    int nblocks) {
     pdl_wait_and_release();
     const int lane = threadIdx.x & 31;
     const int oct = lane >> 3, j = lane & 7;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t stride = nwarps * (4 * UNROLL);
-    int64_t base = warp * (4 * UNROLL);
+    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+    const int stride = nwarps * (4 * UNROLL);
+    int base = warp * (4 * UNROLL);
     if (base >= nblocks) return;
-    auto load_dy = [&](int64_t b0, uint4 (&a)[UNROLL], uint4 (&b)[UNROLL]) {
+    auto load_dy = [&](int b0, uint4 (&a)[UNROLL], uint4 (&b)[UNROLL]) {
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = b0 + 4 * u + oct;
+            const int blk = b0 + 4 * u + oct;
             if (blk < nblocks) {
-                a[u] = ld_stream(dy + blk * 16 + j);
-                b[u] = ld_stream(dy + blk * 16 + 8 + j);
+                const uint4 *p = dy + (size_t)(unsigned)blk * 16 + j;
+                a[u] = ld_stream(p);
+                b[u] = ld_stream(p + 8);
             } else {
                 a[u] = b[u] = make_uint4(0u, 0u, 0u, 0u);
             }
@@ -335,18 +362,19 @@ __global__ void __launch_bounds__(kThreads, AGOQ_SILU_MIN_CTAS) laaq_silu_backwa
         }
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = base + 4 * u + oct;
+            const int blk = base + 4 * u + oct;
             if (blk < nblocks) {
+                const size_t off = (size_t)(unsigned)blk * 16 + j;
                 uint4 ga, gb, ya, yb;
                 silu_backward_chunk<WITH_Y>(dequantize_chunk<BITS>(cur.alo[u], cur.ahi[u], cur.s[u]),
                                             da[u], ga, ya);
                 silu_backward_chunk<WITH_Y>(dequantize_chunk<BITS>(cur.blo[u], cur.bhi[u], cur.s[u]),
                                             db[u], gb, yb);
-                st_stream(dx + blk * 16 + j, ga);
-                st_stream(dx + blk * 16 + 8 + j, gb);
+                st_stream(dx + off, ga);
+                st_stream(dx + off + 8, gb);
                 if constexpr (WITH_Y) {
-                    st_stream(y + blk * 16 + j, ya);
-                    st_stream(y + blk * 16 + 8 + j, yb);
+                    st_stream(y + off, ya);
+                    st_stream(y + off + 8, yb);
                 }
             }
         }
@@ -368,15 +396,25 @@ int resident_grid(K kernel, int *cache, int64_t work_ctas) {
     return (int)(g > 0 ? g : 1);
 }
 
+// Largest block count of one quantization launch (32-bit block indices, with
+// headroom for the stride arithmetic).
+constexpr int64_t kMaxLaunchBlocks = int64_t(1) << 30;
+
 template <int BITS>
 cudaError_t quant_bits(const void *x, int64_t nblocks, void *codes, float *scales, cudaStream_t st) {
     constexpr int kU = AGOQ_QUANT_UNROLL;
     static int cache[kMaxDevices];
     auto k = laaq_quant_kernel<BITS, kU>;
     const int64_t per_cta = 4 * kU * (kThreads / 32);
-    return launch_pdl(k, resident_grid(k, cache, (nblocks + per_cta - 1) / per_cta), kThreads, 0,
-                      st, static_cast<const uint4 *>(x), static_cast<uint32_t *>(codes), scales,
-                      nblocks);
+    for (int64_t b0 = 0; b0 < nblocks; b0 += kMaxLaunchBlocks) {
+        const int64_t nb = nblocks - b0 < kMaxLaunchBlocks ? nblocks - b0 : kMaxLaunchBlocks;
+        const cudaError_t e = launch_pdl(
+            k, resident_grid(k, cache, (nb + per_cta - 1) / per_cta), kThreads, 0, st,
+            static_cast<const uint4 *>(x) + b0 * 16,
+            static_cast<uint32_t *>(codes) + b0 * 4 * BITS, scales + b0, static_cast<int>(nb));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 template <int BITS>
@@ -386,9 +424,15 @@ cudaError_t dequant_bits(const void *codes, const float *scales, int64_t nblocks
     static int cache[kMaxDevices];
     auto k = laaq_dequant_kernel<BITS, kU>;
     const int64_t per_cta = 4 * kU * (kThreads / 32);
-    return launch_pdl(k, resident_grid(k, cache, (nblocks + per_cta - 1) / per_cta), kThreads, 0,
-                      st, static_cast<const uint32_t *>(codes), scales, static_cast<uint4 *>(y),
-                      nblocks);
+    for (int64_t b0 = 0; b0 < nblocks; b0 += kMaxLaunchBlocks) {
+        const int64_t nb = nblocks - b0 < kMaxLaunchBlocks ? nblocks - b0 : kMaxLaunchBlocks;
+        const cudaError_t e = launch_pdl(
+            k, resident_grid(k, cache, (nb + per_cta - 1) / per_cta), kThreads, 0, st,
+            static_cast<const uint32_t *>(codes) + b0 * 4 * BITS, scales + b0,
+            static_cast<uint4 *>(y) + b0 * 16, static_cast<int>(nb));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 template <int BITS, bool WITH_Y>
@@ -398,10 +442,16 @@ cudaError_t silu_backward_bits(const void *codes, const float *scales, const voi
     static int cache[kMaxDevices];
     auto k = laaq_silu_backward_kernel<BITS, kU, WITH_Y>;
     const int64_t per_cta = 4 * kU * (kThreads / 32);
-    return launch_pdl(k, resident_grid(k, cache, (nblocks + per_cta - 1) / per_cta), kThreads, 0,
-                      st, static_cast<const uint32_t *>(codes), scales,
-                      static_cast<const uint4 *>(dy), static_cast<uint4 *>(dx),
-                      static_cast<uint4 *>(y), nblocks);
+    for (int64_t b0 = 0; b0 < nblocks; b0 += kMaxLaunchBlocks) {
+        const int64_t nb = nblocks - b0 < kMaxLaunchBlocks ? nblocks - b0 : kMaxLaunchBlocks;
+        const cudaError_t e = launch_pdl(
+            k, resident_grid(k, cache, (nb + per_cta - 1) / per_cta), kThreads, 0, st,
+            static_cast<const uint32_t *>(codes) + b0 * 4 * BITS, scales + b0,
+            static_cast<const uint4 *>(dy) + b0 * 16, static_cast<uint4 *>(dx) + b0 * 16,
+            y ? static_cast<uint4 *>(y) + b0 * 16 : nullptr, static_cast<int>(nb));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 template <int BITS>
