@@ -21,7 +21,9 @@ Also reported:
   rows          each other kernel of the path on its own workload (QuanGrad
                 accumulation of 2^30 elements, FP8 shard reduce W=8/64 of 2^25,
                 INT4-fused weight-gradient GEMM 11008x4096x8192, the 2048x4096
-                4-bit round trip), L2 flushed before each timed launch.
+                4-bit round trip), L2 flushed before each timed launch (a 256 MB
+                buffer written, then another 256 MB read, so the launch starts
+                from a cold L2 holding no dirty lines).
 
 --impl reference times the CPU oracle (the plain restatement the kernels are
 checked against) on a bounded sample of the same workload.
@@ -48,11 +50,13 @@ NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 # dram__bytes_read.sum + dram__bytes_write.sum per launch, from the ncu captures
-# summarised in profiles/ (laaq_quant_b5_dbca_8192x4096_8192x11008.md); valid only
-# while those kernels are unchanged -- remove an entry when its kernel changes.
+# summarised in profiles/ (laaq_quant_b5_dbca_8192x4096_8192x11008.md,
+# laaq_dequant_b8_silu_8192x11008.md); valid only while those kernels are
+# unchanged -- remove an entry when its kernel changes.
 DOMINANT_TRAFFIC_BYTES = {
-    "quant_b5_silu_in": 180406528 + 11280384,
-    "quant_b5_rmsnorm_in": 67150080 + 2028544,
+    "quant_b5_silu_in": 180401152 + 9678848,
+    "quant_b5_rmsnorm_in": 67146496 + 1888256,
+    "dequant_b8_silu_in": 93018880 + 121340416,
 }
 
 
@@ -318,6 +322,8 @@ def gpu_arm(args):
         }
         if rows is not None:
             line["rows"] = rows
+            line["rows_timing"] = ("median of 5 launches, each after an L2 flush that writes 256 MB "
+                                   "and then reads another 256 MB (cold L2, no dirty lines)")
         print(json.dumps(line), flush=True)
 
 
@@ -445,8 +451,12 @@ def e2e_arm(args, tensors, codes, scales, outs, calls, device):
                        "bound by the host link (copies alone take copies_only_ms_per_step)"}
 
 
-def _flush_l2(buf):
+def _flush_l2(buf, clean):
+    """Evict the L2: write `buf` (larger than L2), then read `clean` (larger than
+    L2) so that the written lines are written back before the timed launch and
+    it starts from a cold cache holding no dirty lines."""
     buf.add_(1)
+    clean.sum()
 
 
 def _time_launch(fn, flush, reps=5, warm=2):
@@ -472,7 +482,8 @@ def rows_arm(device, hbm_peak, bf16_peak):
     from gradient_quantization_gb300 import agoq, synthetic
     rows = {}
     flushbuf = torch.zeros(256 << 20 >> 2, dtype=torch.float32, device=device)
-    flush = lambda: _flush_l2(flushbuf)   # noqa: E731
+    cleanbuf = torch.ones(256 << 20 >> 2, dtype=torch.float32, device=device)
+    flush = lambda: _flush_l2(flushbuf, cleanbuf)   # noqa: E731
 
     def row(name, nbytes, elems, ms, extra=None):
         gbs = nbytes / (ms * 1e-3) / 1e9

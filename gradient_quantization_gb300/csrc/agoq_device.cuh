@@ -480,16 +480,62 @@ __device__ __forceinline__ void load_chunk(const uint32_t *rec, int c, uint32_t 
     }
 }
 
-// bf16(fl32(c_i * s)) for the 8 codes of a chunk; the code values are made
-// exact by field_value's bias trick and multiplied in packed pairs.
+// The 8 fields of a chunk as biased binary32 words: word i holds
+// 0x4B000000 + (code_i + 2^(BITS-1)), whose value is 2^23 + code_i + 2^(BITS-1)
+// (field_value's bias trick).  With AGOQ_DEQUANT_PRMT, 4- and 8-bit fields
+// are moved into place by byte permutes: the sign bits of a whole word are
+// flipped at once, the nibbles of 4-bit fields are first spread over the
+// bytes of two words (even and odd fields), and one permute per field puts
+// its byte below the constant bytes 00 00 4B.
+#ifndef AGOQ_DEQUANT_PRMT
+#define AGOQ_DEQUANT_PRMT 1
+#endif
+template <int BITS>
+__device__ __forceinline__ void biased_words8(uint32_t lo, uint32_t hi, uint32_t wv[8]) {
+    constexpr uint32_t kHigh = 0x4B000000u;
+    if constexpr (AGOQ_DEQUANT_PRMT && BITS == 8) {
+        const uint32_t a = lo ^ 0x80808080u, b = hi ^ 0x80808080u;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            wv[i] = __byte_perm(a, kHigh, 0x7650 + i);
+            wv[4 + i] = __byte_perm(b, kHigh, 0x7650 + i);
+        }
+    } else if constexpr (AGOQ_DEQUANT_PRMT && BITS == 4) {
+        const uint32_t a = lo ^ 0x88888888u;
+        const uint32_t even = a & 0x0F0F0F0Fu, odd = (a >> 4) & 0x0F0F0F0Fu;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+            wv[2 * k] = __byte_perm(even, kHigh, 0x7650 + k);
+            wv[2 * k + 1] = __byte_perm(odd, kHigh, 0x7650 + k);
+        }
+    } else {
+        constexpr uint32_t kMask = (1u << BITS) - 1u;
+        constexpr uint32_t kSign = 1u << (BITS - 1);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int pos = i * BITS;
+            uint32_t u;
+            if (pos + BITS <= 32) u = lo >> pos;
+            else if (pos >= 32) u = hi >> (pos - 32);
+            else u = __funnelshift_r(lo, hi, pos);
+            wv[i] = (u & kMask) ^ (kHigh | kSign);
+        }
+    }
+}
+
+// bf16(fl32(c_i * s)) for the 8 codes of a chunk: the biased words minus
+// 2^23 + 2^(BITS-1) give the codes exactly, then one product rounding, in
+// packed pairs.
 template <int BITS>
 __device__ __forceinline__ uint4 dequantize_chunk(uint32_t lo, uint32_t hi, float s) {
-    const uint64_t s2 = f32x2(s, s);
+    constexpr float kK = 8388608.0f + (float)(1 << (BITS - 1));
+    uint32_t wv[8];
+    biased_words8<BITS>(lo, hi, wv);
+    const uint64_t s2 = f32x2(s, s), k2 = f32x2(kK, kK);
     uint32_t out[4];
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
-        const uint64_t y = mul_f32x2(f32x2(field_value<BITS>(lo, hi, 2 * p * BITS),
-                                           field_value<BITS>(lo, hi, (2 * p + 1) * BITS)), s2);
+        const uint64_t y = mul_f32x2(sub_f32x2(u32x2(wv[2 * p], wv[2 * p + 1]), k2), s2);
         out[p] = pack_bf16x2(lo_f32(y), hi_f32(y));
     }
     return make_uint4(out[0], out[1], out[2], out[3]);

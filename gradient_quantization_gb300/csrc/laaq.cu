@@ -34,7 +34,10 @@
 #define AGOQ_SILU_UNROLL 1
 #endif
 #ifndef AGOQ_SILU_MIN_CTAS
-#define AGOQ_SILU_MIN_CTAS 3
+#define AGOQ_SILU_MIN_CTAS 4
+#endif
+#ifndef AGOQ_SILU_Y_MIN_CTAS
+#define AGOQ_SILU_Y_MIN_CTAS 3
 #endif
 #ifndef AGOQ_SILU_FAST_EXP
 #define AGOQ_SILU_FAST_EXP 1
@@ -286,11 +289,47 @@ __global__ void __launch_bounds__(kThreads, AGOQ_DEQUANT_MIN_CTAS) laaq_dequant_
 // values xh of a chunk and the matching upstream gradients dy, in binary32:
 //   sigma = 1 / (1 + exp(-xh));  silu'(xh) = sigma * (1 + xh * (1 - sigma));
 //   dx = bf16(dy * silu'(xh));   y = bf16(xh * sigma)  (the recomputed forward output).
+#if AGOQ_SILU_FAST_EXP
+// e^-x as 2^(-x log2 e) by the hardware's approximate base-2 exponential, and
+// the approximate reciprocal (each within a few binary32 ulps; subnormal
+// results flush to zero, which leaves sigma at 1 or 0 where they occur).
+__device__ __forceinline__ float ex2_approx(float a) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+    return r;
+}
+__device__ __forceinline__ float rcp_approx(float a) {
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
+    return r;
+}
+#endif
+
 template <bool WITH_Y>
 __device__ __forceinline__ void silu_backward_chunk(uint4 xh, uint4 dy, uint4 &dx, uint4 &y) {
     const uint32_t xw[4] = {xh.x, xh.y, xh.z, xh.w};
     const uint32_t dw[4] = {dy.x, dy.y, dy.z, dy.w};
     uint32_t o[4], yo[4];
+#if AGOQ_SILU_FAST_EXP
+    constexpr float kNegLog2e = -1.4426950408889634f;
+    const uint64_t nl2e = f32x2(kNegLog2e, kNegLog2e), one = f32x2(1.0f, 1.0f);
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        // element pairs in packed binary32; every operation rounds separately
+        const uint64_t x = f32x2(bf16_lo(xw[p]), bf16_hi(xw[p]));
+        const uint64_t d = f32x2(bf16_lo(dw[p]), bf16_hi(dw[p]));
+        const uint64_t t = mul_f32x2(x, nl2e);
+        const uint64_t den = add_f32x2(f32x2(ex2_approx(lo_f32(t)), ex2_approx(hi_f32(t))), one);
+        const uint64_t sg = f32x2(rcp_approx(lo_f32(den)), rcp_approx(hi_f32(den)));
+        const uint64_t g = mul_f32x2(sg, fma_f32x2(x, sub_f32x2(one, sg), one));
+        const uint64_t r = mul_f32x2(d, g);
+        o[p] = pack_bf16x2(lo_f32(r), hi_f32(r));
+        if constexpr (WITH_Y) {
+            const uint64_t yy = mul_f32x2(x, sg);
+            yo[p] = pack_bf16x2(lo_f32(yy), hi_f32(yy));
+        }
+    }
+#else
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
         float r[2], yy[2];
@@ -298,24 +337,15 @@ __device__ __forceinline__ void silu_backward_chunk(uint4 xh, uint4 dy, uint4 &d
         for (int h = 0; h < 2; ++h) {
             const float x = h ? bf16_hi(xw[p]) : bf16_lo(xw[p]);
             const float d = h ? bf16_hi(dw[p]) : bf16_lo(dw[p]);
-#if AGOQ_SILU_FAST_EXP
-            // exp through the hardware base-2 exponential, 1 / (1 + e) by the
-            // approximate division: both within a few binary32 ulps
-            const float sg = __fdividef(1.0f, __fadd_rn(1.0f, __expf(-x)));
-#else
             const float sg = __frcp_rn(__fadd_rn(1.0f, expf(-x)));
-#endif
-#if AGOQ_SILU_FAST_EXP
-            const float g = sg * fmaf(x, 1.0f - sg, 1.0f);
-#else
             const float g = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(x, __fsub_rn(1.0f, sg))));
-#endif
             r[h] = __fmul_rn(d, g);
             yy[h] = __fmul_rn(x, sg);
         }
         o[p] = pack_bf16x2(r[0], r[1]);
         if constexpr (WITH_Y) yo[p] = pack_bf16x2(yy[0], yy[1]);
     }
+#endif
     dx = make_uint4(o[0], o[1], o[2], o[3]);
     if constexpr (WITH_Y) y = make_uint4(yo[0], yo[1], yo[2], yo[3]);
 }
@@ -325,7 +355,7 @@ __device__ __forceinline__ void silu_backward_chunk(uint4 xh, uint4 dy, uint4 &d
 // the next batch's code, scale and gradient loads are issued before the
 // current batch's arithmetic.
 template <int BITS, int UNROLL, bool WITH_Y>
-__global__ void __launch_bounds__(kThreads, AGOQ_SILU_MIN_CTAS) laaq_silu_backward_kernel(
+__global__ void __launch_bounds__(kThreads, WITH_Y ? AGOQ_SILU_Y_MIN_CTAS : AGOQ_SILU_MIN_CTAS) laaq_silu_backward_kernel(
     const uint32_t *__restrict__ codes, const float *__restrict__ scales,
     const uint4 *__restrict__ dy, uint4 *__restrict__ dx, uint4 *__restrict__ y,
     int nblocks) {

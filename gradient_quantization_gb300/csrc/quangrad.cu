@@ -48,6 +48,14 @@
 #ifndef AGOQ_REDUCE_MIN_CTAS
 #define AGOQ_REDUCE_MIN_CTAS 1
 #endif
+#ifndef AGOQ_REDUCE_COUNT_MIN_CTAS
+#define AGOQ_REDUCE_COUNT_MIN_CTAS 2
+#endif
+// 1: the overflow test keeps the largest |naive sum| of each element and
+//    compares it with 448 once per block; 0: a flag per element and step.
+#ifndef AGOQ_NAIVE_MAX
+#define AGOQ_NAIVE_MAX 1
+#endif
 
 namespace agoq {
 namespace {
@@ -229,33 +237,39 @@ __device__ __forceinline__ void add_f16x2_f32(uint32_t h2, float c0, float c1, f
         : "r"(h2), "f"(c0), "f"(c1));
 }
 
+//
+// Block indices are 32-bit (the launcher splits larger inputs); shard r of
+// block b is at shards[r * shard_vec + 8 b ...] and its scale at
+// shard_scales[r * scale_stride + b].
 template <bool NAIVE, int RUNROLL>
-__global__ void __launch_bounds__(kThreads, AGOQ_REDUCE_MIN_CTAS) reduce_shards_kernel(
-    const uint4 *__restrict__ shards, const float *__restrict__ shard_scales, int W, int64_t n,
-    int64_t nblocks, uint4 *__restrict__ out, float *__restrict__ out_scales,
-    unsigned long long *__restrict__ naive_count) {
+__global__ void __launch_bounds__(kThreads, NAIVE ? AGOQ_REDUCE_COUNT_MIN_CTAS : AGOQ_REDUCE_MIN_CTAS)
+reduce_shards_kernel(
+    const uint4 *__restrict__ shards, const float *__restrict__ shard_scales, int W,
+    int64_t shard_vec, int64_t scale_stride, int nblocks, uint4 *__restrict__ out,
+    float *__restrict__ out_scales, unsigned long long *__restrict__ naive_count) {
     pdl_wait_and_release();
     const int lane = threadIdx.x & 31;
     const int oct = lane >> 3, t8 = lane & 7;
-    const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
-    const int64_t shard_vec = n / 16;   // uint4 per shard
-    const int64_t stride = nwarps * 4;
+    const int warp = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+    const int nwarps = (int)((gridDim.x * blockDim.x) >> 5);
+    const int stride = nwarps * 4;
     const int nchunk = (W + RUNROLL - 1) / RUNROLL;
     // Codes and scales of shards ch*RUNROLL .. +RUNROLL-1 for the octet's block
     // of the group at b0 (clamped in range; the results of idle lanes are dropped).
-    auto load = [&](int64_t b0, int ch, uint4 (&c)[RUNROLL], float (&sc)[RUNROLL]) {
-        const int64_t blk = b0 + oct;
-        const int64_t blk_c = blk < nblocks ? blk : nblocks - 1;
+    auto load = [&](int b0, int ch, uint4 (&c)[RUNROLL], float (&sc)[RUNROLL]) {
+        const int blk = b0 + oct;
+        const int blk_c = blk < nblocks ? blk : nblocks - 1;
+        const uint4 *p = shards + (size_t)(unsigned)blk_c * 8 + t8;
+        const float *q = shard_scales + blk_c;
 #pragma unroll
         for (int u = 0; u < RUNROLL; ++u) {
             const int r = ch * RUNROLL + u < W ? ch * RUNROLL + u : W - 1;
-            c[u] = ld_stream(shards + (int64_t)r * shard_vec + blk_c * 8 + t8);
-            sc[u] = __ldg(shard_scales + (int64_t)r * nblocks + blk_c);
+            c[u] = ld_stream(p + (int64_t)r * shard_vec);
+            sc[u] = __ldg(q + (int64_t)r * scale_stride);
         }
     };
     unsigned long long overflowed = 0;
-    int64_t base = warp * 4;
+    int base = warp * 4;
     if (base < nblocks) {
         // The loads of the next (block group, shard chunk) are always in flight
         // while the current chunk is accumulated.
@@ -269,7 +283,13 @@ __global__ void __launch_bounds__(kThreads, AGOQ_REDUCE_MIN_CTAS) reduce_shards_
 #else
         float nv[16];
 #endif
+#if AGOQ_NAIVE_MAX
+        float nmax[16];    // largest |naive sum| seen per element
+#pragma unroll
+        for (int i = 0; i < 16; ++i) nmax[i] = 0.0f;
+#else
         uint32_t alive = 0xFFFFu;
+#endif
 #pragma unroll
         for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
         for (;;) {
@@ -280,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, AGOQ_REDUCE_MIN_CTAS) reduce_shards_
                 c[u] = cn[u];
                 sc[u] = sn[u];
             }
-            int64_t nbase = base;
+            int nbase = base;
             int nch = ch + 1;
             if (nch == nchunk) {
                 nch = 0;
@@ -310,8 +330,13 @@ __global__ void __launch_bounds__(kThreads, AGOQ_REDUCE_MIN_CTAS) reduce_shards_
                         for (int p = 0; p < 8; ++p) {
                             float t0, t1;   // exact: both operands are E4M3 values
                             add_f16x2_f32(nvh[p], e[2 * p], e[2 * p + 1], t0, t1);
+#if AGOQ_NAIVE_MAX
+                            nmax[2 * p] = fmaxf(nmax[2 * p], fabsf(t0));
+                            nmax[2 * p + 1] = fmaxf(nmax[2 * p + 1], fabsf(t1));
+#else
                             if (fabsf(t0) > kE4M3Max) alive &= ~(1u << (2 * p));
                             if (fabsf(t1) > kE4M3Max) alive &= ~(2u << (2 * p));
+#endif
                             nvh[p] = e4m3x2_to_f16x2(e4m3x2_from_f32(t0, t1));
                         }
                     }
@@ -340,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, AGOQ_REDUCE_MIN_CTAS) reduce_shards_
             }
             if (nch == 0) {
                 // all W shards of the block group are in: requantize and store
-                const int64_t blk = base + oct;
+                const int blk = base + oct;
                 const bool valid = blk < nblocks;
                 float am = 0.0f;
 #pragma unroll
@@ -350,13 +375,27 @@ __global__ void __launch_bounds__(kThreads, AGOQ_REDUCE_MIN_CTAS) reduce_shards_
                 const uint2 lo = requant8(acc, snew);
                 const uint2 hi = requant8(acc + 8, snew);
                 if (valid) {
-                    out[blk * 8 + t8] = make_uint4(lo.x, lo.y, hi.x, hi.y);
+                    out[(size_t)(unsigned)blk * 8 + t8] = make_uint4(lo.x, lo.y, hi.x, hi.y);
                     if (t8 == 0) out_scales[blk] = snew;
-                    if constexpr (NAIVE) overflowed += (unsigned long long)__popc(~alive & 0xFFFFu);
+                    if constexpr (NAIVE) {
+#if AGOQ_NAIVE_MAX
+                        int k = 0;
+#pragma unroll
+                        for (int i = 0; i < 16; ++i) k += nmax[i] > kE4M3Max;
+                        overflowed += (unsigned long long)k;
+#else
+                        overflowed += (unsigned long long)__popc(~alive & 0xFFFFu);
+#endif
+                    }
                 }
 #pragma unroll
                 for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+#if AGOQ_NAIVE_MAX
+#pragma unroll
+                for (int i = 0; i < 16; ++i) nmax[i] = 0.0f;
+#else
                 alive = 0xFFFFu;
+#endif
             }
             if (nbase >= nblocks) break;
             base = nbase;
@@ -407,24 +446,32 @@ cudaError_t launch_reduce_shards(const void *shards, const float *shard_scales, 
                                  void *out, float *out_scales, unsigned long long *naive_count,
                                  cudaStream_t st) {
     constexpr int kRUnroll = AGOQ_REDUCE_RUNROLL;
-    const int64_t nb = n / kBlock;
+    constexpr int64_t kMaxLaunchBlocks = int64_t(1) << 30;
+    const int64_t nb_all = n / kBlock;
     const int64_t per_cta = 4 * (kThreads / 32);
-    const int64_t ctas = (nb + per_cta - 1) / per_cta;
     if (naive_count) {
         cudaError_t e = cudaMemsetAsync(naive_count, 0, sizeof(unsigned long long), st);
         if (e != cudaSuccess) return e;
-        static int cache[kMaxDevices];
-        auto k = reduce_shards_kernel<true, AGOQ_REDUCE_COUNT_RUNROLL>;
-        return launch_pdl(k, resident_grid(k, cache, ctas), kThreads, 0, st,
-                          static_cast<const uint4 *>(shards), shard_scales, W, n, nb,
-                          static_cast<uint4 *>(out), out_scales, naive_count);
     }
-    static int cache[kMaxDevices];
-    auto k = reduce_shards_kernel<false, kRUnroll>;
-    return launch_pdl(k, resident_grid(k, cache, ctas), kThreads, 0, st,
-                      static_cast<const uint4 *>(shards), shard_scales, W, n, nb,
-                      static_cast<uint4 *>(out), out_scales,
-                      static_cast<unsigned long long *>(nullptr));
+    static int cache_count[kMaxDevices], cache_plain[kMaxDevices];
+    auto kc = reduce_shards_kernel<true, AGOQ_REDUCE_COUNT_RUNROLL>;
+    auto kp = reduce_shards_kernel<false, kRUnroll>;
+    for (int64_t b0 = 0; b0 < nb_all; b0 += kMaxLaunchBlocks) {
+        const int64_t nb = nb_all - b0 < kMaxLaunchBlocks ? nb_all - b0 : kMaxLaunchBlocks;
+        const int64_t ctas = (nb + per_cta - 1) / per_cta;
+        const uint4 *sh = static_cast<const uint4 *>(shards) + b0 * 8;
+        uint4 *o = static_cast<uint4 *>(out) + b0 * 8;
+        const cudaError_t e =
+            naive_count
+                ? launch_pdl(kc, resident_grid(kc, cache_count, ctas), kThreads, 0, st, sh,
+                             shard_scales + b0, W, n / 16, nb_all, (int)nb, o, out_scales + b0,
+                             naive_count)
+                : launch_pdl(kp, resident_grid(kp, cache_plain, ctas), kThreads, 0, st, sh,
+                             shard_scales + b0, W, n / 16, nb_all, (int)nb, o, out_scales + b0,
+                             static_cast<unsigned long long *>(nullptr));
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace agoq

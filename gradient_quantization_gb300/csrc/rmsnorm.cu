@@ -39,7 +39,10 @@ constexpr int kRowBlocks = 2;                    // 128-element blocks per octet
 constexpr int kDwThreads = 256;                  // 8 warps
 constexpr int kDwCluster = 8;                    // CTAs per cluster (ranks along y)
 constexpr int kDwCols = 128;                     // columns per slice (16 lanes x 8)
-constexpr int kDwUnroll = 8;                     // rows in flight per half warp
+#ifndef AGOQ_DW_UNROLL
+#define AGOQ_DW_UNROLL 4
+#endif
+constexpr int kDwUnroll = AGOQ_DW_UNROLL;        // rows in flight per half warp
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     uint4 v;
@@ -339,32 +342,45 @@ __global__ void __launch_bounds__(kDwThreads, 2) rmsnorm_dw_kernel(
     float acc[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
-    for (int64_t t0 = group; t0 < T; t0 += (int64_t)kGroups * kDwUnroll) {
+    // kDwUnroll rows per batch; the next batch's loads are issued before the
+    // current batch is accumulated (register double buffering)
+    struct Batch {
         uint32_t lo[kDwUnroll], hi[kDwUnroll];
         float s[kDwUnroll], r[kDwUnroll];
         uint4 d[kDwUnroll];
+    };
+    auto load = [&](int64_t t0, Batch &bt) {
 #pragma unroll
         for (int u = 0; u < kDwUnroll; ++u) {
             const int64_t t = t0 + (int64_t)kGroups * u;
             if (t < T) {
                 const int64_t blk = t * nb + b;
-                load_chunk<BITS>(codes + blk * kWords, chunk, lo[u], hi[u]);
-                s[u] = __ldg(scales + blk);
-                r[u] = __ldg(rstd + t);
-                d[u] = ld_stream(dy + (t * H + col0) / 8);
+                load_chunk<BITS>(codes + blk * kWords, chunk, bt.lo[u], bt.hi[u]);
+                bt.s[u] = __ldg(scales + blk);
+                bt.r[u] = __ldg(rstd + t);
+                bt.d[u] = ld_stream(dy + (t * H + col0) / 8);
             } else {
-                lo[u] = hi[u] = 0u;
-                s[u] = r[u] = 0.0f;
-                d[u] = make_uint4(0u, 0u, 0u, 0u);
+                bt.lo[u] = bt.hi[u] = 0u;
+                bt.s[u] = bt.r[u] = 0.0f;
+                bt.d[u] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
+    };
+    constexpr int64_t kStep = (int64_t)kGroups * kDwUnroll;
+    Batch cur, nxt;
+    int64_t t0 = group;
+    if (t0 < T) load(t0, cur);
+    for (; t0 < T; t0 += kStep) {
+        const bool more = t0 + kStep < T;
+        if (more) load(t0 + kStep, nxt);
 #pragma unroll
         for (int u = 0; u < kDwUnroll; ++u) {
-            const uint4 xh = dequantize_chunk<BITS>(lo[u], hi[u], s[u]);
+            const uint4 xh = dequantize_chunk<BITS>(cur.lo[u], cur.hi[u], cur.s[u]);
 #pragma unroll
             for (int k = 0; k < 8; ++k)
-                acc[k] = __fadd_rn(acc[k], __fmul_rn(__fmul_rn(elem(d[u], k), elem(xh, k)), r[u]));
+                acc[k] = __fadd_rn(acc[k], __fmul_rn(__fmul_rn(elem(cur.d[u], k), elem(xh, k)), cur.r[u]));
         }
+        if (more) cur = nxt;
     }
 #pragma unroll
     for (int k = 0; k < 8; ++k) part[hw][8 * l16 + k] = acc[k];
