@@ -150,22 +150,58 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t raddr, uint4 v) {
-    asm volatile("st.shared::cluster.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(raddr), "r"(v.x),
-                 "r"(v.y), "r"(v.z), "r"(v.w)
-                 : "memory");
-}
-// Arrive (release, cluster scope) on an mbarrier of another CTA of the cluster.
+// Arrive on an mbarrier of another CTA of the cluster: with
+// AGOQ_REMOTE_ARRIVE_CLUSTER a release at cluster scope, otherwise the
+// instruction's default release semantics (measured far cheaper on GB300; the
+// data that the arrival publishes is read by the tensor core's asynchronous
+// proxy, which the writer's proxy fence already ordered).
+#ifndef AGOQ_REMOTE_ARRIVE_CLUSTER
+#define AGOQ_REMOTE_ARRIVE_CLUSTER 0
+#endif
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t raddr) {
+#if AGOQ_REMOTE_ARRIVE_CLUSTER
     asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr)
                  : "memory");
+#else
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
+#endif
 }
-// tcgen05.commit whose mbarrier arrive goes to the same barrier in every CTA of `mask`.
-__device__ __forceinline__ void umma_commit_multicast(uint64_t *bar, uint16_t mask) {
+// This CTA's rank in its cluster.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// ---- CTA pairs (cta_group::2): the two CTAs of a cluster of two share one
+// MMA.  A pair MMA with M = 256 takes rows 0-127 of A from the issuing CTA's
+// shared memory and rows 128-255 from the peer's (same offset), and the N
+// columns of B half from each CTA; each CTA's TMEM receives its 128 rows of
+// the accumulator at the same TMEM address.  TMEM is allocated for both CTAs
+// by one warp of each.
+__device__ __forceinline__ void umma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                               uint32_t idesc, uint32_t accumulate) {
     asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+// Commit of the pair MMAs issued so far: one arrive on the barrier at the same
+// offset in every CTA of `mask`.
+__device__ __forceinline__ void umma_commit_pair_multicast(uint64_t *bar, uint16_t mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
         " [%0], %1;" ::"r"(smem_u32(bar)),
         "h"(mask)
+        : "memory");
+}
+// Commit of the pair MMAs issued so far to a barrier of this CTA.
+__device__ __forceinline__ void umma_commit_pair(uint64_t *bar) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
+            smem_u32(bar))
         : "memory");
 }
 // mbarrier phase test with cluster-scope acquire (arrivals come from other CTAs).

@@ -82,40 +82,58 @@ constexpr int NA = AGOQ_GEMM_NA, NX = AGOQ_GEMM_NX, NB = AGOQ_GEMM_NB;
 constexpr int kChunk = BK * 128;                          // bytes of one 64-wide M/N chunk of a stage
 constexpr int kTmaWarp = 0, kMmaWarp = 1, kTmaXWarp = 2, kDeqWarp0 = 3, kDeqWarps = 16;
 constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;   // 608
-#ifndef AGOQ_GEMM_CLUSTER
-#define AGOQ_GEMM_CLUSTER 1
+#ifndef AGOQ_GEMM_PAIR
+#define AGOQ_GEMM_PAIR 1
 #endif
-// With kCluster > 1 the CTAs of a cluster share the dequantized operand: the
-// kCluster CTAs of a cluster take tiles with the same N columns and
-// consecutive M rows, each dequantizes kSliceRows of the BK k-rows of every
-// stage and writes them into the X-hat stage of every CTA of the cluster
-// (distributed shared memory), and every MMA's commit releases the stage in
-// every CTA.  This divides the dequantization work by kCluster but couples the
-// CTAs' rings; measured on GB300 the cross-SM handoff per k-block costs more
-// than the dequantization it saves, so the default is 1 (no cluster).
-constexpr int kCluster = AGOQ_GEMM_CLUSTER;
-constexpr int kSliceRows = BK / kCluster;                 // k-rows of a stage this CTA dequantizes
-constexpr int kDeqRows = kSliceRows / kDeqWarps;          // k-rows per dequant thread per stage
-static_assert(kCluster == 1 || kCluster == 2 || kCluster == 4, "cluster size");
-static_assert(kDeqRows >= 1 && kDeqRows * kDeqWarps * kCluster == BK,
-              "every k-row of a stage is dequantized exactly once in the cluster");
+// 1: CTA 0 waits for the peer's arrivals with cluster-scope acquire; 0: with
+// the default (CTA-scope) acquire of mbarrier.try_wait.
+#ifndef AGOQ_PAIR_CLUSTER_WAIT
+#define AGOQ_PAIR_CLUSTER_WAIT 0
+#endif
+// 1: the peer's dequantizer warps arrive directly on CTA 0's full_b barrier
+// (which then counts both CTAs' warps) and the relay only forwards the A
+// stage; 0: the relay forwards both.
+#ifndef AGOQ_PAIR_DIRECT_B
+#define AGOQ_PAIR_DIRECT_B 1
+#endif
+constexpr bool kDirectB = AGOQ_GEMM_PAIR && AGOQ_PAIR_DIRECT_B;
+// With AGOQ_GEMM_PAIR the two CTAs of a cluster of two form a tcgen05 CTA
+// pair working on one 512 x 256 tile: each CTA holds 256 rows of dY (two
+// 128-row halves) and dequantizes only its 128 of the 256 X-hat columns; CTA
+// 0 issues pair MMAs (M = 256, N = 256) that read the A rows and the B columns
+// of both CTAs and accumulate each CTA's rows in its own TMEM.  Per output
+// element this halves the dequantization work and the shared-memory traffic
+// of the B operand.  The peer's producers publish a k-block to the issuing
+// CTA through one remote mbarrier arrive (a relay thread), and every MMA
+// commit is multicast to both CTAs' release barriers.
+constexpr int kPair = AGOQ_GEMM_PAIR ? 2 : 1;             // CTAs per tile
+constexpr int kTileRows = BM * kPair;                      // output rows per tile
+constexpr int kBCols = BN / kPair;                         // X-hat columns this CTA holds
+constexpr int kWordsPerRow = kBCols / 8;                   // 4-bit code words per k-row
+constexpr int kRowsPerWarp = 32 / kWordsPerRow;            // k-rows a dequant warp covers at once
+constexpr int kDeqRows = BK / (kRowsPerWarp * kDeqWarps);  // code words per dequant thread per stage
+static_assert(kDeqRows >= 1 && kDeqRows * kRowsPerWarp * kDeqWarps == BK,
+              "every k-row of a stage is dequantized exactly once");
 static_assert(NB >= 2, "the B ring must let dequantization run ahead of the MMA");
 static_assert(kDeqWarps == 16, "epilogue items: 4 TMEM lane quarters x 4 blocks of 128 columns");
 // A waiter may only be one phase behind the barrier it polls (a parity test
 // cannot tell "two phases ahead" from "complete").  Every ring here is waited
 // on by all of its consumers for every phase in order, and tmem_full(t + 1)
 // cannot complete before every dequant warp has waited for tmem_full(t) and
-// released the accumulator.
+// released the accumulator.  The pair-ready ring (CTA 0 only) has min(NA, NB)
+// slots: the relay can be at most that many k-blocks ahead of the MMA, since
+// its producers need the stages the MMA releases.
+constexpr int NP = NA < NB ? NA : NB;
 constexpr int kAStage = BM * BK * 2;                      // 32 KiB of dY (BF16)
-constexpr int kBStage = BN * BK * 2;                      // 32 KiB of Xhat (BF16)
-constexpr int kCStage = kSliceRows * BN / 2;              // this CTA's rows of packed codes
-constexpr int kSStage = kSliceRows * 4 * 4;               // ... and their 4-wide scale boxes
+constexpr int kBStage = kBCols * BK * 2;                  // this CTA's X-hat columns (BF16)
+constexpr int kCStage = BK * kBCols / 2;                  // their packed codes
+constexpr int kSStage = BK * 4 * 4;                       // ... and 4-wide scale boxes
 static_assert(BK % 16 == 0 && BK >= 16 && BK <= 256, "k-block depth");
 constexpr int kOffB = NA * kAStage;
 constexpr int kOffC = kOffB + NB * kBStage;
 constexpr int kOffS = kOffC + NX * kCStage;
 constexpr int kOffBar = kOffS + NX * kSStage;
-constexpr int kNumBars = 2 * NA + 2 * NX + 2 * NB + 3;
+constexpr int kNumBars = 2 * NA + 2 * NX + 2 * NB + NP + 3;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;          // + slack for 1024-byte alignment
 constexpr uint32_t kTmemCols = 512;
@@ -127,15 +145,15 @@ constexpr int kPrefetchLead = AGOQ_GEMM_PREFETCH_LEAD;   // k-blocks between mas
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // Instruction descriptor: kind::f16, BF16 A and B, FP32 D, A and B MN-major,
-// M = 128, N = 256.
+// M = 128 per CTA (256 for a pair), N = 256.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
-                            ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(128 >> 4) << 24);
+                            ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((128 * kPair) >> 4) << 24);
 
 struct Shared {
     uint8_t *a, *b, *c;
     float *s;
     uint64_t *full_a, *empty_a, *full_x, *empty_x, *full_b, *empty_b;
-    uint64_t *tmem_full, *tmem_empty, *drain;
+    uint64_t *tmem_full, *tmem_empty, *drain, *pair_ready;
     uint32_t *tmem_addr;
     volatile int *abort;
 };
@@ -322,26 +340,27 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh.empty_x = sh.full_x + NX;
     sh.full_b = sh.empty_x + NX;
     sh.empty_b = sh.full_b + NB;
-    sh.tmem_full = sh.empty_b + NB;
+    sh.pair_ready = sh.empty_b + NB;
+    sh.tmem_full = sh.pair_ready + NP;
     sh.tmem_empty = sh.tmem_full + 1;
     sh.drain = sh.tmem_empty + 1;
     sh.tmem_addr = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     sh.abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
-
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_tiles = N / BN, kblocks = K / BK;
-    // Cluster tiling: group g covers kCluster consecutive M tiles of one N panel;
-    // this CTA (cluster rank `rank`) takes M tile (g / n_tiles) * kCluster + rank,
-    // which may lie past M for the last group (then it only helps dequantize).
-    const int rank = (int)(blockIdx.x % kCluster);
-    const int cluster_id = (int)(blockIdx.x / kCluster), num_clusters = (int)(gridDim.x / kCluster);
-    const int m_tiles = M / BM, num_groups = ((m_tiles + kCluster - 1) / kCluster) * n_tiles;
-    auto tile_of = [&](int g, int &m0, int &n0) -> bool {
-        const int mt = (g / n_tiles) * kCluster + rank;
-        m0 = mt * BM;
+    // Tile g covers rows m0 .. m0 + kTileRows - 1 and columns n0 .. n0 + 255;
+    // this CTA (rank in the pair) holds rows half_row(h) .. +127 of M-half h
+    // and X-hat columns n0 + rank * kBCols .. + kBCols - 1.  Rows at or past M
+    // (the second half of the last tile) are neither multiplied nor stored.
+    const int rank = kPair > 1 ? (int)cluster_ctarank() : 0;
+    const int cluster_id = (int)(blockIdx.x / kPair), num_clusters = (int)(gridDim.x / kPair);
+    const int m_tiles = (M + kTileRows - 1) / kTileRows, num_groups = m_tiles * n_tiles;
+    auto tile_of = [&](int g, int &m0, int &n0) {
+        m0 = (g / n_tiles) * kTileRows;
         n0 = (g % n_tiles) * BN;
-        return mt < m_tiles;
     };
+    auto half_row = [&](int m0, int h) { return m0 + h * 128 * kPair + 128 * rank; };
+    auto half_valid = [&](int m0, int h) { return m0 + h * 128 * kPair < M; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NA; ++s) {
@@ -353,26 +372,35 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.empty_x[s], kDeqWarps);
         }
         for (int s = 0; s < NB; ++s) {
-            mbar_init(&sh.full_b[s], kDeqWarps * kCluster);   // every dequant warp of the cluster
-            mbar_init(&sh.empty_b[s], kCluster);              // every MMA of the cluster
+            mbar_init(&sh.full_b[s], kDirectB ? kDeqWarps * kPair : kDeqWarps);
+            mbar_init(&sh.empty_b[s], 1);
         }
+        for (int s = 0; s < NP; ++s) mbar_init(&sh.pair_ready[s], 1);
         mbar_init(sh.tmem_full, 1);
-        mbar_init(sh.tmem_empty, kDeqWarps);
+        mbar_init(sh.tmem_empty, kDeqWarps * kPair);   // every epilogue warp of the pair
         mbar_init(sh.drain, 1);
         *sh.abort = 0;
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kMmaWarp) {
-        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                         smem_u32(sh.tmem_addr)),
-                     "r"(kTmemCols)
-                     : "memory");
-        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        if constexpr (kPair > 1) {
+            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(sh.tmem_addr)),
+                         "r"(kTmemCols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+        } else {
+            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                             smem_u32(sh.tmem_addr)),
+                         "r"(kTmemCols)
+                         : "memory");
+            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+        }
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if constexpr (kCluster > 1) cluster_sync_all();   // peers' barriers are initialised
+    if constexpr (kPair > 1) cluster_sync_all();   // the peer's barriers are initialised
     const uint32_t tmem_base = *sh.tmem_addr;
 
     if (warp == kTmaWarp || warp == kTmaXWarp) {
@@ -386,29 +414,26 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int g = cluster_id; ok && g < num_groups; g += num_clusters) {
                 int m0, n0;
-                const bool valid = tile_of(g, m0, n0);
-                const int sx = (n0 / 128) & ~3;
+                tile_of(g, m0, n0);
+                const int cb = n0 + rank * kBCols;   // first X-hat column of this CTA
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % depth;
                     const uint32_t ph = (it / depth) & 1u;
                     if (!wait_bar(&empty[s], ph ^ 1u, sh.abort, &g_device_status)) { ok = false; break; }
                     const int k0 = kb * BK;
                     if (is_a) {
-                        if (!valid) {      // no rows of dY: the MMA's result is discarded
-                            mbar_arrive(&full[s]);
-                            continue;
-                        }
-                        mbar_expect_tx(&full[s], kAStage);
+                        const int halves = (kPair == 1 || half_valid(m0, 1)) ? 2 : 1;
+                        mbar_expect_tx(&full[s], halves * (kAStage / 2));
+                        for (int h = 0; h < halves; ++h) {
 #pragma unroll
-                        for (int c = 0; c < 4; ++c)
-                            tma_load_2d(sh.a + s * kAStage + c * kChunk, &map_dy, &full[s],
-                                        m0 + 64 * c, k0);
+                            for (int c = 0; c < 2; ++c)
+                                tma_load_2d(sh.a + s * kAStage + (2 * h + c) * kChunk, &map_dy,
+                                            &full[s], half_row(m0, h) + 64 * c, k0);
+                        }
                     } else {
-                        // this CTA's slice of the k-block's codes and scales
-                        const int kr = k0 + rank * kSliceRows;
                         mbar_expect_tx(&full[s], kCStage + kSStage);
-                        tma_load_2d(sh.c + s * kCStage, &map_xc, &full[s], n0 / 2, kr);
-                        tma_load_2d(sh.s + s * (kSStage / 4), &map_xs, &full[s], sx, kr);
+                        tma_load_2d(sh.c + s * kCStage, &map_xc, &full[s], cb / 2, k0);
+                        tma_load_2d(sh.s + s * (kSStage / 4), &map_xs, &full[s], (cb / 128) & ~3, k0);
                     }
                 }
             }
@@ -421,19 +446,31 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0) {
+        if (lane == 0 && rank == 0) {
+            // MMA issuer (CTA 0 of a pair issues for both CTAs).
             uint32_t it = 0, t = 0;
             bool ok = true, issued = false;
             for (int g = cluster_id; ok && g < num_groups; g += num_clusters, ++t) {
-                if (!wait_bar(sh.tmem_empty, (t & 1u) ^ 1u, sh.abort, &g_device_status)) { ok = false; break; }
+                int m0, n0;
+                tile_of(g, m0, n0);
+                const bool v1 = half_valid(m0, 1);
+                if (!(kPair > 1 && AGOQ_PAIR_CLUSTER_WAIT
+                          ? wait_bar_cluster(sh.tmem_empty, (t & 1u) ^ 1u, sh.abort, &g_device_status)
+                          : wait_bar(sh.tmem_empty, (t & 1u) ^ 1u, sh.abort, &g_device_status))) {
+                    ok = false;
+                    break;
+                }
                 tc_fence_after();
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int sa = it % NA, sb = it % NB;
                     if (!wait_bar(&sh.full_a[sa], (it / NA) & 1u, sh.abort, &g_device_status) ||
-                        !(kCluster > 1 ? wait_bar_cluster(&sh.full_b[sb], (it / NB) & 1u,
-                                                          sh.abort, &g_device_status)
-                                       : wait_bar(&sh.full_b[sb], (it / NB) & 1u, sh.abort,
-                                                  &g_device_status))) {
+                        !wait_bar(&sh.full_b[sb], (it / NB) & 1u, sh.abort, &g_device_status) ||
+                        (kPair > 1 &&
+                         !(AGOQ_PAIR_CLUSTER_WAIT
+                               ? wait_bar_cluster(&sh.pair_ready[it % NP], (it / NP) & 1u, sh.abort,
+                                                  &g_device_status)
+                               : wait_bar(&sh.pair_ready[it % NP], (it / NP) & 1u, sh.abort,
+                                          &g_device_status)))) {
                         ok = false;
                         break;
                     }
@@ -445,46 +482,82 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t bdesc = sw128_desc(b0 + kk * 2048, kChunk, 1024);
 #pragma unroll
                         for (int h = 0; h < 2; ++h) {
+                            if (kPair > 1 && h == 1 && !v1) break;
                             const uint64_t adesc =
                                 sw128_desc(a0 + h * 2 * kChunk + kk * 2048, kChunk, 1024);
-                            umma_bf16(tmem_base + h * 256, adesc, bdesc, kIdesc,
-                                      (kb > 0 || kk > 0) ? 1u : 0u);
+                            const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
+                            if constexpr (kPair > 1)
+                                umma_bf16_pair(tmem_base + h * 256, adesc, bdesc, kIdesc, acc);
+                            else
+                                umma_bf16(tmem_base + h * 256, adesc, bdesc, kIdesc, acc);
                         }
                     }
                     issued = true;
-                    umma_commit(&sh.empty_a[sa]);
-                    // the X-hat stage is free once every MMA of the cluster has read it
-                    if constexpr (kCluster > 1)
-                        umma_commit_multicast(&sh.empty_b[sb], (uint16_t)((1u << kCluster) - 1u));
-                    else
+                    if constexpr (kPair > 1) {
+                        umma_commit_pair_multicast(&sh.empty_a[sa], 3);
+                        umma_commit_pair_multicast(&sh.empty_b[sb], 3);
+                    } else {
+                        umma_commit(&sh.empty_a[sa]);
                         umma_commit(&sh.empty_b[sb]);
+                    }
                 }
                 if (!ok) break;
-                umma_commit(sh.tmem_full);
+                if constexpr (kPair > 1)
+                    umma_commit_pair_multicast(sh.tmem_full, 3);
+                else
+                    umma_commit(sh.tmem_full);
             }
             // Drain: all MMAs issued so far complete before TMEM is freed.
             if (issued) {
-                umma_commit(sh.drain);
+                if constexpr (kPair > 1)
+                    umma_commit_pair(sh.drain);
+                else
+                    umma_commit(sh.drain);
                 wait_bar(sh.drain, 0u, sh.abort, &g_device_status, true);
+            }
+        } else if (lane == 0 && kPair > 1) {
+            // Relay (CTA 1 of a pair): once this CTA's A stage of a k-block
+            // has landed (and, without kDirectB, its X-hat stage is written),
+            // tell the issuing CTA with one remote arrive.
+            const uint32_t ready0 = mapa_shared(smem_u32(sh.pair_ready), 0);
+            uint32_t it = 0;
+            bool ok = true;
+            for (int g = cluster_id; ok && g < num_groups; g += num_clusters) {
+                for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                    const int sa = it % NA, sb = it % NB;
+                    if (!wait_bar(&sh.full_a[sa], (it / NA) & 1u, sh.abort, &g_device_status) ||
+                        (!kDirectB &&
+                         !wait_bar(&sh.full_b[sb], (it / NB) & 1u, sh.abort, &g_device_status))) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_remote(ready0 + (uint32_t)(it % NP) * 8u);
+                }
             }
         }
     } else {
         // Dequantizers, which also run the epilogue of the previous tile.
         const int d = warp - kDeqWarp0;
-        const int wc = lane;                            // code word column: N = 8wc .. 8wc+7
+        const int wc = lane % kWordsPerRow;             // code word column: X-hat cols 8wc .. 8wc+7
+        const int rsub = lane / kWordsPerRow;
         const int chunk = wc >> 3, piece = wc & 7;
         // Epilogue item: TMEM lane quarter q (tcgen05.ld reaches lanes
         // 32*(warp%4) .. +31) and 128-column block `item` of the tile: rows
-        // m0 + 128*eh + 32q + lane, columns n0 + 128*ejb .. +127.
+        // half_row(eh) + 32q + lane, columns n0 + 128*ejb .. +127.
         const int q = warp & 3, item = d >> 2, eh = item >> 1, ejb = item & 1;
         const uint32_t etaddr = tmem_base + ((uint32_t)(32 * q) << 16) + eh * 256 + ejb * 128;
+        const uint32_t tmem_empty0 =
+            kPair > 1 ? mapa_shared(smem_u32(sh.tmem_empty), 0) : smem_u32(sh.tmem_empty);
+        const uint32_t full_b0 =
+            kPair > 1 ? mapa_shared(smem_u32(sh.full_b), 0) : smem_u32(sh.full_b);
         // The previous tile's epilogue runs once the B ring holds the first
         // stages of this tile (or all of them, for short K).
         const int lead = (kblocks < NB ? kblocks : NB) - 1;
         auto epilogue = [&](int g, uint32_t t) -> bool {
             int m0, n0;
-            const bool valid = tile_of(g, m0, n0);
-            const int row = m0 + eh * 128 + 32 * q + lane, col0 = n0 + ejb * 128;
+            tile_of(g, m0, n0);
+            const bool valid = half_valid(m0, eh);   // the same for the whole warp
+            const int row = half_row(m0, eh) + 32 * q + lane, col0 = n0 + ejb * 128;
             MasterBlock mb;
             if constexpr (EPI == kEpiAccumFp8 && AGOQ_ACCUM_EARLY_LOAD) {
                 // the master block's loads overlap the wait for the accumulator
@@ -502,7 +575,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (valid) epilogue_item<EPI>(etaddr, dW, mscales, row, col0, N, mb);
             tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(sh.tmem_empty);
+            if (lane == 0) {
+                if (kPair > 1 && rank != 0)
+                    mbar_arrive_remote(tmem_empty0);
+                else
+                    mbar_arrive(sh.tmem_empty);
+            }
             return true;
         };
         uint32_t it = 0, t = 0;
@@ -510,14 +588,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         int prev = -1;
         for (int g = cluster_id; ok && g < num_groups; g += num_clusters, ++t) {
             int m0, n0;
-            const bool valid = tile_of(g, m0, n0);
-            const int soff = ((n0 / 128) & 3) + (wc >> 4);   // scale column inside the 4-wide box
+            tile_of(g, m0, n0);
+            const int cb = n0 + rank * kBCols;
+            const int soff = ((cb / 128) & 3) + (wc >> 4);   // scale column inside the 4-wide box
             for (int kb = 0; kb < kblocks; ++kb, ++it) {
                 if constexpr (EPI == kEpiAccumFp8) {
                     // Pull this thread's master block of the tile into L2 a few
                     // k-blocks before its epilogue needs it.
-                    if (valid && kb == (kblocks > kPrefetchLead ? kblocks - kPrefetchLead : 0)) {
-                        const size_t row = (size_t)(m0 + eh * 128 + 32 * q + lane);
+                    if (half_valid(m0, eh) &&
+                        kb == (kblocks > kPrefetchLead ? kblocks - kPrefetchLead : 0)) {
+                        const size_t row = (size_t)(half_row(m0, eh) + 32 * q + lane);
                         prefetch_l2(static_cast<const uint8_t *>(dW) + row * N + n0 + ejb * 128);
                         prefetch_l2(mscales + row * (N / 128) + n0 / 128 + ejb);
                     }
@@ -530,48 +610,33 @@ __global__ void __launch_bounds__(kThreads, 1)
                 float sc[kDeqRows];
 #pragma unroll
                 for (int i = 0; i < kDeqRows; ++i) {
-                    const int lr = d + kDeqWarps * i;           // row of this CTA's slice
-                    w[i] = codes[lr * 32 + wc];
-                    sc[i] = scales[lr * 4 + soff];
+                    const int k = kRowsPerWarp * (d + kDeqWarps * i) + rsub;   // row of the stage
+                    w[i] = codes[k * kWordsPerRow + wc];
+                    sc[i] = scales[k * 4 + soff];
                 }
-                // The stage may be overwritten once every MMA of the cluster has read it.
-                if (!(kCluster > 1
-                          ? warp_wait_cluster(&sh.empty_b[sb], ((it / NB) & 1u) ^ 1u, sh.abort,
-                                              &g_device_status)
-                          : warp_wait(&sh.empty_b[sb], ((it / NB) & 1u) ^ 1u, sh.abort,
-                                      &g_device_status))) {
+                // The stage may be overwritten once the MMA has read it.
+                if (!warp_wait(&sh.empty_b[sb], ((it / NB) & 1u) ^ 1u, sh.abort, &g_device_status)) {
                     ok = false;
                     break;
                 }
                 uint8_t *btile = sh.b + sb * kBStage + chunk * kChunk;
 #pragma unroll
                 for (int i = 0; i < kDeqRows; ++i) {
-                    const int k = rank * kSliceRows + d + kDeqWarps * i;   // row of the stage
+                    const int k = kRowsPerWarp * (d + kDeqWarps * i) + rsub;
                     const uint4 y = dequant_word(w[i], sc[i]);
                     uint8_t *dst = btile + k * 128 + ((piece ^ (k & 7)) << 4);
                     *reinterpret_cast<uint4 *>(dst) = y;
-                    if constexpr (kCluster > 1) {
-#pragma unroll
-                        for (int p = 1; p < kCluster; ++p)       // the same row in every peer
-                            st_cluster_v4(mapa_shared(smem_u32(dst), (rank + p) % kCluster), y);
-                    }
                 }
-                if constexpr (kCluster > 1)
-                    asm volatile("fence.proxy.async.shared::cluster;" ::: "memory");
-                else
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
                 __syncwarp();
                 // The X stage is released only now: its codes have been consumed
                 // (the B stores depend on them), so no shared-memory load of it
                 // can still be in flight when the next TMA load overwrites it.
                 if (lane == 0) {
-                    mbar_arrive(&sh.full_b[sb]);
-                    if constexpr (kCluster > 1) {
-#pragma unroll
-                        for (int p = 1; p < kCluster; ++p)
-                            mbar_arrive_remote(
-                                mapa_shared(smem_u32(&sh.full_b[sb]), (rank + p) % kCluster));
-                    }
+                    if (kDirectB && rank != 0)
+                        mbar_arrive_remote(full_b0 + (uint32_t)sb * 8u);
+                    else
+                        mbar_arrive(&sh.full_b[sb]);
                     mbar_arrive(&sh.empty_x[sx]);
                 }
                 if (kb == lead && prev >= 0 && !epilogue(prev, t - 1)) { ok = false; break; }
@@ -584,13 +649,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    // No CTA leaves while a peer may still write its X-hat stages or barriers.
-    if constexpr (kCluster > 1) cluster_sync_all();
+    // Neither CTA of a pair leaves (or frees TMEM) while the other may still
+    // arrive on its barriers or have the pair's MMAs read its shared memory.
+    if constexpr (kPair > 1) cluster_sync_all();
     if (warp == kMmaWarp) {
         __syncwarp();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                     "r"(kTmemCols)
-                     : "memory");
+        if constexpr (kPair > 1)
+            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"(kTmemCols)
+                         : "memory");
+        else
+            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                         "r"(kTmemCols)
+                         : "memory");
     }
 }
 
@@ -602,9 +673,9 @@ cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, 
     if (!encode_2d(&m_dy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, (uint64_t)M, (uint64_t)K,
                    (uint64_t)M * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&m_xc, CU_TENSOR_MAP_DATA_TYPE_UINT8, xc, (uint64_t)N / 2, (uint64_t)K,
-                   (uint64_t)N / 2, BN / 2, kSliceRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+                   (uint64_t)N / 2, kBCols / 2, BK, CU_TENSOR_MAP_SWIZZLE_NONE) ||
         !encode_2d(&m_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xs, (uint64_t)N / 128, (uint64_t)K,
-                   (uint64_t)(N / 128) * 4, 4, kSliceRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   (uint64_t)(N / 128) * 4, 4, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
     auto kernel = wgrad_gemm_int4_kernel<EPI>;
     static bool attr_set[kMaxDevices];
@@ -616,8 +687,8 @@ cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, 
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    const int groups = ((M / BM + kCluster - 1) / kCluster) * (N / BN);
-    if constexpr (kCluster == 1) {
+    const int groups = ((M + kTileRows - 1) / kTileRows) * (N / BN);
+    if constexpr (kPair == 1) {
         const int grid = groups < sm_count() ? groups : sm_count();
         kernel<<<grid, kThreads, kSmemBytes, st>>>(m_dy, m_xc, m_xs, dW, mscales, M, N, K);
         return cudaGetLastError();
@@ -628,23 +699,23 @@ cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, 
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = kCluster;
+    attr[0].val.clusterDim.x = kPair;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    // Persistent grid: as many clusters as can be resident at once (a cluster
-    // must fit in one GPC, so this can be below sm_count / kCluster).
+    // Persistent grid: as many pairs as can be resident at once (a cluster
+    // must fit in one GPC, so this can be below sm_count / 2).
     static int resident[kMaxDevices];
     if (dev >= 0 && dev < kMaxDevices && resident[dev] == 0) {
-        cfg.gridDim = dim3(sm_count() / kCluster * kCluster);
+        cfg.gridDim = dim3(sm_count() / kPair * kPair);
         int n = 0;
         if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess || n <= 0)
-            n = sm_count() / kCluster;
+            n = sm_count() / kPair;
         resident[dev] = n;
     }
-    const int clusters = (dev >= 0 && dev < kMaxDevices) ? resident[dev] : sm_count() / kCluster;
-    cfg.gridDim = dim3((groups < clusters ? groups : clusters) * kCluster);
+    const int clusters = (dev >= 0 && dev < kMaxDevices) ? resident[dev] : sm_count() / kPair;
+    cfg.gridDim = dim3((groups < clusters ? groups : clusters) * kPair);
     return cudaLaunchKernelEx(&cfg, kernel, m_dy, m_xc, m_xs, dW, mscales, M, N, K);
 }
 
