@@ -25,10 +25,11 @@ UNITS = {
     "laaq.cu": ["-fmad=false"],
     "quangrad.cu": ["-fmad=false"],
     "wgrad_gemm.cu": ["-fmad=false"],
+    "wgrad_gemm_k64.cu": ["-fmad=false"],
     "rmsnorm.cu": ["-fmad=false"],
     "fwd_gemm.cu": ["-fmad=false"],
 }
-HEADERS = ["agoq_device.cuh", "agoq_launch.h", "gemm_common.cuh"]
+HEADERS = ["agoq_device.cuh", "agoq_launch.h", "gemm_common.cuh", "wgrad_gemm_impl.cuh"]
 
 
 def _nvcc():

@@ -40,8 +40,11 @@ def _abs_terms(oracle, dy, xc, xs, M, N, K):
     return dyv.T @ xhv
 
 
+# K a multiple of 128 runs the 128-deep instance, the other multiples of 64 the
+# 64-deep one; M = 256 and 768 leave the second half of a 512-row pair tile empty.
 @pytest.mark.parametrize("M,N,K", [(256, 512, 64), (256, 512, 128), (512, 1024, 192),
-                                   (768, 512, 320), (2560, 4096, 64)])
+                                   (768, 512, 320), (2560, 4096, 64), (512, 1024, 384),
+                                   (768, 512, 640), (2560, 4096, 128)])
 def test_gemm_matches_fp64_product(oracle, M, N, K):
     dy, xc, xs = _inputs(oracle, M, N, K)
     dyd, xcd, xsd = G.dev_bf16(dy), G.dev(xc), G.dev(xs)

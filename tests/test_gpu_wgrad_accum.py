@@ -60,7 +60,7 @@ def _assert_same(got, want):
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 512, 64), (256, 512, 320), (512, 1024, 128),
-                                   (768, 1536, 192)])
+                                   (768, 1536, 192), (768, 1536, 384)])
 def test_exact_sums_match_oracle_bitwise(oracle, M, N, K):
     dy, xc, xs = _exact_inputs(oracle, M, N, K, seed=50 + K)
     master, scales = _master(oracle, M * N, seed=60 + M, sd=2.0)
@@ -68,9 +68,10 @@ def test_exact_sums_match_oracle_bitwise(oracle, M, N, K):
     _assert_same(got, oracle.wgrad_accum_fp8(dy, xc, xs, M, N, K, master, scales))
 
 
-def test_exact_sums_over_many_tiles_and_waves(oracle):
+@pytest.mark.parametrize("K", [64, 128])
+def test_exact_sums_over_many_tiles_and_waves(oracle, K):
     """More tiles than SMs (several persistent waves); every block checked."""
-    M, N, K = 2560, 4096, 64
+    M, N = 2560, 4096
     dy, xc, xs = _exact_inputs(oracle, M, N, K, seed=70)
     master, scales = _master(oracle, M * N, seed=71, sd=0.5)
     got = _run(dy, xc, xs, M, N, K, master, scales)
