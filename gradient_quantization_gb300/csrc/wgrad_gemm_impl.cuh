@@ -6,33 +6,39 @@
 //
 //   dW[M][N] = sum_k dY[k][m] * Xhat[k][n],  Xhat = bf16(fl32(code * scale))
 //
-// Blackwell design (sm_103a, one CTA per SM, persistent over 256x256 tiles),
-// per BK-deep k-block, with three independent shared-memory rings:
-//   A ring (NA stages)  the dY tile, 256 M x BK K as four 64-wide boxes with
-//                       128-byte swizzle, loaded by TMA;
-//   X ring (NX stages)  the packed 4-bit codes (BK rows x 128 bytes) and their
-//                       scales (BK x 4 floats), loaded by TMA;
-//   B ring (NB stages)  Xhat (BF16), written by the dequantizers in the
-//                       MN-major 128-byte-swizzled layout the MMA reads.
-// Only the A and X rings hold loads in flight, so they get most of the shared
-// memory; the B ring only bridges dequantization and the MMA.
+// Blackwell design (sm_103a): one CTA per SM; with AGOQ_GEMM_PAIR (the
+// default) the two CTAs of a cluster of two form a tcgen05 CTA pair that is
+// persistent over 512 x 256 output tiles (256 rows per CTA, as two 128-row
+// halves).  Per BK-deep k-block each CTA has three shared-memory rings:
+//   A ring (NA stages)  its 256 dY rows x BK, four 64-wide boxes with the
+//                       128-byte swizzle, loaded by TMA (rows past M read as
+//                       zeros and are not multiplied);
+//   X ring (NX stages)  the packed 4-bit codes of its 128 X-hat columns (BK
+//                       rows x 64 bytes) and their scales, loaded by TMA;
+//   B ring (NB stages)  its 128 X-hat columns (BF16), written by the
+//                       dequantizers in the MN-major 128-byte-swizzled layout
+//                       the MMA reads.
 //   warp 0      TMA producer of the A ring.
-//   warp 1      TMEM owner and MMA issuer: one elected thread issues, per
-//               k-block, (BK/16) x 2 tcgen05.mma kind::f16 (M=128, N=256, K=16;
-//               both operands MN-major, BF16 in, FP32 accumulate) into two
-//               256-column accumulators (rows 0-127 and 128-255 of the tile)
-//               that fill the 512 TMEM columns; tcgen05.commit frees the A and
-//               B stages.
+//   warp 1      TMEM allocation for the pair; in CTA 0 one thread issues, per
+//               k-block, (BK/16) x 2 pair MMAs tcgen05.mma.cta_group::2
+//               kind::f16 (M=256: 128 rows from each CTA; N=256: 128 B
+//               columns from each CTA; K=16; both operands MN-major, BF16 in,
+//               FP32 accumulate) into two 256-column accumulators per CTA
+//               (its rows of the two M-halves, all 512 TMEM columns); the
+//               commits, multicast to both CTAs, free the A and B stages.
+//               In CTA 1 one thread relays each landed A stage to CTA 0 with
+//               a remote mbarrier arrive.
 //   warp 2      TMA producer of the X ring.
 //   warps 3-18  dequantizers: codes -> Xhat into the B ring, fence.proxy.async,
-//               mbarrier arrives that publish the B stage and release the X
-//               stage (after its codes have been consumed).  They also run the
-//               epilogue of the previous tile, once they have filled the B
-//               ring with the first stages of the next one (the MMA waits for
-//               the accumulator anyway): each warp takes one 32-row x
-//               128-column item (its TMEM lane quarter, warp % 4, and one of
-//               the four 128-column blocks of the two accumulators), reads it
-//               with tcgen05.ld, one output row per thread, and does one of
+//               an arrive on CTA 0's B barrier (remote from CTA 1) and the
+//               release of the X stage (after its codes have been consumed).
+//               They also run the epilogue of the previous tile, once they
+//               have filled the B ring with the first stages of the next one
+//               (the MMA waits for the accumulator anyway): each warp takes
+//               one 32-row x 128-column item of its CTA's accumulators (its
+//               TMEM lane quarter, warp % 4, and one of four 128-column
+//               blocks), reads it with tcgen05.ld, one output row per thread,
+//               and does one of
 //               - BF16 round-to-nearest-even and global stores;
 //               - the FP32 accumulator stored unrounded;
 //               - the QuanGrad accumulation into an FP8 master gradient
@@ -40,11 +46,13 @@
 //                 E4M3 master codes of the row block, add the FP32
 //                 accumulator, take the block absmax, requantize in place with
 //                 the new scale.  The BF16 dW never exists.
-// Waiting threads sleep in mbarrier.try_wait (suspend-time hint) rather than
-// spin, so the dequantizers keep the issue slots.
+// Without AGOQ_GEMM_PAIR each CTA works alone on 256 x 256 tiles with the
+// same roles (M=128 MMAs of cta_group::1, all 256 X-hat columns dequantized
+// locally).
 // Every mbarrier wait has a time limit: on expiry the kernel records a code in
 // g_device_status, raises a CTA-wide abort flag, lets in-flight copies and
-// MMAs drain (with a limit), frees its TMEM and returns.
+// MMAs drain (with a limit), frees its TMEM and returns; both CTAs of a pair
+// meet at a cluster barrier before either frees TMEM or exits.
 #pragma once
 #include <cuda.h>
 
