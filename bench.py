@@ -280,6 +280,9 @@ def gpu_arm(args):
     # ---- end to end through host buffers
     e2e = e2e_arm(args, tensors, codes, scales, outs, calls, device)
 
+    # ---- the precision-preserved all-reduce across the ranks (N > 1 only)
+    allreduce = allreduce_arm(device, world) if world > 1 and not args.no_rows else None
+
     # ---- other rows of the path
     rows = None
     if rank == 0 and not args.no_rows:
@@ -320,6 +323,8 @@ def gpu_arm(args):
             "clocks": clocks,
             "cpu_baseline": cpu,
         }
+        if allreduce is not None:
+            line["allreduce"] = allreduce
         if rows is not None:
             line["rows"] = rows
             line["rows_timing"] = ("median of 5 launches, each after an L2 flush that writes 256 MB "
@@ -449,6 +454,41 @@ def e2e_arm(args, tensors, codes, scales, outs, calls, device):
             "copies_only_ms_per_step": round(copy_ms, 3),
             "overlap": "copies in, kernels and copies out (4 streams) overlapped; the step is "
                        "bound by the host link (copies alone take copies_only_ms_per_step)"}
+
+
+def allreduce_arm(device, world, reps=10, warm=3):
+    """QuanGrad's precision-preserved all-reduce (all-to-all of FP8 shards, the
+    library's local reduce, all-gather) over all ranks: every rank holds an FP8
+    gradient of world * 2^25 elements, so each local reduce sees world shards of
+    2^25 (the shard reduce's configuration at world = 8).  Times with CUDA events
+    between barriers, max over ranks."""
+    import torch
+    from gradient_quantization_gb300 import synthetic
+    from gradient_quantization_gb300.allreduce import precision_preserved_allreduce
+    try:
+        n = world * synthetic.REDUCE_N
+        g = torch.Generator(device=device)
+        g.manual_seed(7 + dist_env()[1])
+        codes = torch.randint(0, 126, (n,), dtype=torch.uint8, device=device, generator=g)
+        codes |= torch.randint(0, 2, (n,), dtype=torch.uint8, device=device, generator=g) << 7
+        scales = torch.rand(n // 128, device=device, generator=g) * 1e-4
+        for _ in range(warm):
+            precision_preserved_allreduce(codes, scales)
+        torch.cuda.synchronize()
+        dist_barrier(device)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            precision_preserved_allreduce(codes, scales)
+        b.record()
+        torch.cuda.synchronize()
+        ms = max_over_ranks(a.elapsed_time(b) / reps, device)
+        nbytes = n + (n // 128) * 4
+        return {"us": round(ms * 1e3, 1), "elements_per_rank": n, "ranks": world,
+                "gradient_GB/s_per_rank": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                "steps": "all-to-all (NCCL) -> agoq_reduce_fp8_shards -> all-gather (NCCL)"}
+    except Exception as e:   # a failing collective must not lose the bench line
+        return {"unavailable": "%s: %s" % (type(e).__name__, str(e)[:200])}
 
 
 def _flush_l2(buf, clean):
