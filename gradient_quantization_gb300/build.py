@@ -28,8 +28,9 @@ UNITS = {
     "wgrad_gemm_k64.cu": ["-fmad=false"],
     "rmsnorm.cu": ["-fmad=false"],
     "fwd_gemm.cu": ["-fmad=false"],
+    "fwd_gemm_k64.cu": ["-fmad=false"],
 }
-HEADERS = ["agoq_device.cuh", "agoq_launch.h", "gemm_common.cuh", "wgrad_gemm_impl.cuh"]
+HEADERS = ["agoq_device.cuh", "agoq_launch.h", "gemm_common.cuh", "wgrad_gemm_impl.cuh", "fwd_gemm_impl.cuh"]
 
 
 def _nvcc():

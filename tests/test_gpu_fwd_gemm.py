@@ -49,7 +49,10 @@ def _unpack(codes, nblocks, bits):
 
 
 @pytest.mark.parametrize("bits", [4, 5, 6, 8])
-@pytest.mark.parametrize("T,N,K", [(128, 256, 64), (256, 512, 192), (384, 768, 320)])
+# K a multiple of 128 runs the 128-deep instance, the other multiples of 64 the
+# 64-deep one; T = 128 and 384 leave half of a 256-row pair tile empty.
+@pytest.mark.parametrize("T,N,K", [(128, 256, 64), (256, 512, 192), (384, 768, 320),
+                                   (128, 256, 128), (384, 768, 384), (512, 1024, 256)])
 def test_exact_sums_bitwise(oracle, bits, T, N, K):
     x, w = _exact_operands(T, N, K, seed=T + N + K + bits)
     y, c, s = _run(x, w, T, N, K, bits)
@@ -59,9 +62,11 @@ def test_exact_sums_bitwise(oracle, bits, T, N, K):
     assert np.array_equal(s.view(np.uint32), ws.view(np.uint32))
 
 
-def test_exact_sums_many_tiles(oracle):
-    """160 tiles of 128 x 256 on 152 SMs (a second persistent round, both TMEM buffers)."""
-    T, N, K, bits = 1280, 4096, 64, 4
+@pytest.mark.parametrize("K", [64, 128])
+def test_exact_sums_many_tiles(oracle, K):
+    """80 tiles of 256 x 256 on 76 CTA pairs (a second persistent round, both
+    TMEM buffers), for both k-block depths."""
+    T, N, bits = 1280, 4096, 4
     x, w = _exact_operands(T, N, K, seed=77)
     y, c, s = _run(x, w, T, N, K, bits)
     wy, wc, ws = oracle.fwd_gemm_quant(x, w, T, N, K, bits)
