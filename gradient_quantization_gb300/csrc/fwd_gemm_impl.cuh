@@ -7,21 +7,31 @@
 //   Y[t][n] = bf16(fl32(sum_k X[t][k] * W[n][k]))     X [T][K], W [N][K], BF16
 //   codes, scales = LAAQ b-bit quantization of Y (128-column blocks of each row)
 //
-// Blackwell design (sm_103a), persistent, one CTA per SM, 128 x 256 output
-// tiles with both operands K-major:
-//   warp 0      TMA producer: per 64-deep k-block, a 128 x 64 tile of X and a
-//               256 x 64 tile of W, 128-byte swizzled, into a 4-stage ring;
-//   warp 1      TMEM owner and MMA issuer: 4 x tcgen05.mma kind::f16 (M=128,
-//               N=256, K=16, both operands K-major) per k-block into one of two
-//               256-column accumulators, so the epilogue of a tile overlaps the
-//               mainloop of the next;
-//   warps 2-5   epilogue: one output row per thread (its TMEM lane quarter is
-//               warp % 4); per 128-column block, a first pass reads the
-//               accumulator (tcgen05.ld), rounds it to BF16, stores Y and takes
-//               the block absmax; a second pass reads it again, forms the codes
-//               (corrected-reciprocal quotient, as the LAAQ quantizer) and
-//               stores the packed record and the scale.
-// Every mbarrier wait is time-limited (status word, CTA abort flag, drains).
+// Blackwell design (sm_103a), persistent, one CTA per SM; with AGOQ_FWD_PAIR
+// (the default) the two CTAs of a cluster of two form a tcgen05 CTA pair on
+// 256 x 256 output tiles, both operands K-major:
+//   warp 0      TMA producer: per BK-deep k-block, this CTA's 128 rows of X
+//               and its 128 of the tile's 256 rows of W (64-wide boxes with
+//               the 128-byte swizzle) into an NS-stage ring;
+//   warp 1      TMEM allocation for the pair; in CTA 0 one thread issues BK/16
+//               pair MMAs tcgen05.mma.cta_group::2 kind::f16 (M=256: 128 rows
+//               from each CTA; N=256: 128 W rows from each CTA; K=16) per
+//               k-block into one of two 256-column accumulators per CTA, so the
+//               epilogue of a tile overlaps the mainloop of the next; the
+//               commits are multicast to both CTAs.  In CTA 1 one thread
+//               relays each landed stage to CTA 0 (remote mbarrier arrive).
+//   warps 2-5   epilogue, in each CTA for its own rows: one output row per
+//               thread (its TMEM lane quarter is warp % 4); per 128-column
+//               block, a first pass reads the accumulator (tcgen05.ld), rounds
+//               it to BF16, stores Y and takes the block absmax; a second pass
+//               reads it again, forms the codes (corrected-reciprocal quotient,
+//               as the LAAQ quantizer) and stores the packed record and the
+//               scale.  CTA 1's warps release an accumulator with a remote
+//               arrive on CTA 0's barrier.
+// Without AGOQ_FWD_PAIR each CTA works alone on 128 x 256 tiles (M=128 MMAs,
+// all 256 W rows loaded locally; it needs BK = 64, AGOQ_FWD_STAGES = 4 to fit).
+// Every mbarrier wait is time-limited (status word, CTA abort flag, drains); the
+// two CTAs of a pair meet at a cluster barrier before either frees TMEM.
 #pragma once
 #include "agoq_device.cuh"
 #include "agoq_launch.h"
