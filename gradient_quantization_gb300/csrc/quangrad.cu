@@ -56,6 +56,12 @@
 #ifndef AGOQ_NAIVE_MAX
 #define AGOQ_NAIVE_MAX 1
 #endif
+// 1: with the naive count, the shard products are formed with packed binary32
+//    multiplies (two per instruction) and added with scalar round-to-nearest
+//    adds (measured faster there, slower without the count); 0: all scalar.
+#ifndef AGOQ_REDUCE_PACKED_MUL
+#define AGOQ_REDUCE_PACKED_MUL 1
+#endif
 
 namespace agoq {
 namespace {
@@ -315,8 +321,19 @@ reduce_shards_kernel(
                 float e[16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) decode4(w4[q], e + 4 * q);
+                if constexpr (NAIVE && AGOQ_REDUCE_PACKED_MUL) {
+                    // products in packed pairs, each sum a scalar round-to-nearest add
+                    const uint64_t sc2 = f32x2(sc[u], sc[u]);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(e[i], sc[u]));
+                    for (int i = 0; i < 16; i += 2) {
+                        const uint64_t p2 = mul_f32x2(f32x2(e[i], e[i + 1]), sc2);
+                        acc[i] = __fadd_rn(acc[i], lo_f32(p2));
+                        acc[i + 1] = __fadd_rn(acc[i + 1], hi_f32(p2));
+                    }
+                } else {
+#pragma unroll
+                    for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(e[i], sc[u]));
+                }
                 if constexpr (NAIVE) {
 #if AGOQ_NAIVE_MIXED_ADD
                     if (r == 0) {
