@@ -330,6 +330,11 @@ def gpu_arm(args):
             line["rows_timing"] = ("median of 5 launches, each after an L2 flush that writes 256 MB "
                                    "and then reads another 256 MB (cold L2, no dirty lines)")
         print(json.dumps(line), flush=True)
+    # every rank leaves together (rank 0 may still have been timing rows)
+    dist_barrier(device)
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.destroy_process_group()
 
 
 def e2e_arm(args, tensors, codes, scales, outs, calls, device):
