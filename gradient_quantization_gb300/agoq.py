@@ -59,6 +59,7 @@ def _lib_handle():
         L.agoq_wgrad_gemm_int4_f32out.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
         L.agoq_wgrad_gemm_int4_accum_fp8.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp, vp]
         L.agoq_device_status.argtypes = [vp]
+        L.agoq_test_wait_timeout.argtypes = [i64, vp]
         L.agoq_dbca_pp_bits.argtypes = [i32, i32, i32, vp]
         L.agoq_fwd_gemm_quant.argtypes = [vp, vp, i32, i32, i32, i32, vp, vp, vp, vp]
         for name in ("agoq_quant_act", "agoq_dequant_act", "agoq_grad_accum_fp8",
@@ -66,7 +67,7 @@ def _lib_handle():
                      "agoq_wgrad_gemm_int4_f32out", "agoq_device_status",
                      "agoq_wgrad_gemm_int4_accum_fp8", "agoq_grad_accum_fp8_mid",
                      "agoq_silu_backward", "agoq_rmsnorm_backward", "agoq_dbca_pp_bits",
-                     "agoq_fwd_gemm_quant"):
+                     "agoq_fwd_gemm_quant", "agoq_test_wait_timeout"):
             getattr(L, name).restype = i32
         _L = L
     return _L
@@ -311,6 +312,13 @@ def agoq_wgrad_gemm_int4_accum_fp8(dY, x_codes, x_scales, M, N, K, master, maste
                                                 _stream(stream)),
            "agoq_wgrad_gemm_int4_accum_fp8")
     return master, master_scales
+
+
+def agoq_test_wait_timeout(limit_cycles, stream=None):
+    """Launch the failure-path probe whose one pipeline wait gives up after
+    `limit_cycles` SM cycles (test-only; see include/agoq.h)."""
+    _check(lib().agoq_test_wait_timeout(int(limit_cycles), _stream(stream)),
+           "agoq_test_wait_timeout")
 
 
 def agoq_device_status(stream=None):

@@ -287,6 +287,11 @@ agoq_status agoq_fwd_gemm_quant(const void *x_bf16, const void *w_bf16, int T, i
                                            as_stream(stream)));
 }
 
+agoq_status agoq_test_wait_timeout(int64_t limit_cycles, void *stream) {
+    if (limit_cycles <= 0 || limit_cycles > 4000000000ll) return AGOQ_ERR_SHAPE;
+    return agoq::from_cuda(agoq::launch_wait_timeout_probe(limit_cycles, agoq::as_stream(stream)));
+}
+
 agoq_status agoq_device_status(void *stream) {
     unsigned status = 0, fwd = 0;
     if (agoq::read_and_clear_device_status(agoq::as_stream(stream), &status) != cudaSuccess ||

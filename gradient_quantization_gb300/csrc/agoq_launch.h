@@ -70,6 +70,8 @@ cudaError_t launch_wgrad_accum_fp8(const void *dY, const void *xc, const float *
                                    int K, void *master, float *master_scales, cudaStream_t st);
 cudaError_t launch_fwd_gemm_quant(const void *x, const void *w, int T, int N, int K, int bits,
                                   void *y, void *codes, float *scales, cudaStream_t st);
+// A kernel whose one pipeline wait runs out after `limit_cycles` (failure-path test).
+cudaError_t launch_wait_timeout_probe(long long limit_cycles, cudaStream_t st);
 // Read and clear the forward GEMM's status word (call after synchronising).
 cudaError_t read_and_clear_fwd_status(unsigned *status);
 // Synchronise `st`, read and clear the device status word (0 = no timeout).

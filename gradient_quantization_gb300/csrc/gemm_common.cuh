@@ -241,13 +241,14 @@ __device__ __forceinline__ uint64_t sw128_kmajor_desc(uint32_t saddr) {
 // final drains, which must run even after an abort.
 __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatile int *abort,
                                          unsigned *status, bool ignore_abort = false,
-                                         uint32_t hint_ns = 0) {
+                                         uint32_t hint_ns = 0,
+                                         long long limit_cycles = kWaitLimitCycles) {
     if (mbar_try_wait(bar, parity, hint_ns)) return true;
     const long long t0 = clock64();
     for (;;) {
         if (mbar_try_wait(bar, parity, hint_ns)) return true;
         if (!ignore_abort && *abort) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
+        if (clock64() - t0 > limit_cycles) {
             *abort = 1;
             atomicExch(status, kStatusTimeout);
             return false;

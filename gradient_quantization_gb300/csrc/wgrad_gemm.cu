@@ -40,6 +40,10 @@ cudaError_t launch_wgrad_accum_fp8(const void *dY, const void *xc, const float *
                : wg64::launch_accum_fp8(dY, xc, xs, M, N, K, master, master_scales, st);
 }
 
+cudaError_t launch_wait_timeout_probe(long long limit_cycles, cudaStream_t st) {
+    return wg128::launch_wait_timeout_probe(limit_cycles, st);
+}
+
 cudaError_t read_and_clear_device_status(cudaStream_t st, unsigned *status) {
     cudaError_t e = cudaStreamSynchronize(st);
     if (e != cudaSuccess) return e;

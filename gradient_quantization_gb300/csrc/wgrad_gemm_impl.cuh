@@ -690,6 +690,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
+// Failure-path probe: one thread waits, with the GEMM's bounded wait and a
+// caller-given limit, for the first phase of an mbarrier that nothing arrives
+// on; the wait runs out, records the timeout in this instance's status word
+// and the kernel returns.
+__global__ void wait_timeout_probe_kernel(long long limit_cycles) {
+    __shared__ uint64_t bar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    if (threadIdx.x == 0)
+        wait_bar(&bar, 0u, &abort_flag, &g_device_status, false, 0u, limit_cycles);
+}
+
 // ---------------------------------------------------------------- host side
 template <int EPI>
 cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, int N, int K,
@@ -755,6 +772,11 @@ cudaError_t launch_gemm(const void *dY, const void *xc, const float *xs, int M, 
 cudaError_t launch_accum_fp8(const void *dY, const void *xc, const float *xs, int M, int N, int K,
                              void *master, float *master_scales, cudaStream_t st) {
     return launch_impl<kEpiAccumFp8>(dY, xc, xs, M, N, K, master, master_scales, st);
+}
+
+cudaError_t launch_wait_timeout_probe(long long limit_cycles, cudaStream_t st) {
+    wait_timeout_probe_kernel<<<1, 32, 0, st>>>(limit_cycles);
+    return cudaGetLastError();
 }
 
 // Read and clear this instance's status word (the stream is synchronised).

@@ -282,6 +282,16 @@ agoq_status agoq_dbca_pp_bits(int stages, int microbatches, int base_bits, int *
  */
 agoq_status agoq_device_status(void *stream);
 
+/*
+ * Test-only export for the failure path: launches one thread that waits, with
+ * the GEMMs' bounded mbarrier wait, for a barrier phase that never completes.
+ * The wait gives up after `limit_cycles` SM clock cycles (0 < limit_cycles <=
+ * 4e9, else AGOQ_ERR_SHAPE), records a timeout in the status word and the
+ * kernel returns; the next agoq_device_status then reports AGOQ_ERR_TIMEOUT
+ * and the CUDA context stays usable.
+ */
+agoq_status agoq_test_wait_timeout(int64_t limit_cycles, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

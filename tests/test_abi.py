@@ -176,6 +176,13 @@ def test_fwd_gemm_quant_validation(L):
     assert fn(P(A), P(B), 128, 256, 64, 4, P(D), P(D + 256), P(F), None) == ALIAS
 
 
+def test_wait_timeout_probe_validation(L):
+    fn = L.agoq_test_wait_timeout
+    assert fn(0, None) == SHAPE
+    assert fn(-5, None) == SHAPE
+    assert fn(4000000001, None) == SHAPE
+
+
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(agoq, "LIB_PATH", str(tmp_path / "missing.so"))
     monkeypatch.setattr(agoq, "_L", None)
