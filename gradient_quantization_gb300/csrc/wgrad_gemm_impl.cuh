@@ -82,7 +82,16 @@ constexpr int kEpiBf16 = 0, kEpiF32 = 1, kEpiAccumFp8 = 2;
 
 constexpr int BM = 256, BN = 256, BK = AGOQ_GEMM_BK;
 constexpr int NA = AGOQ_GEMM_NA, NX = AGOQ_GEMM_NX, NB = AGOQ_GEMM_NB;
-constexpr int kChunk = BK * 128;                          // bytes of one 64-wide M/N chunk of a stage
+constexpr int kChunk = BK * 128;                          // bytes of one 64-wide M chunk of an A stage
+// The B (X-hat) ring is kept in sub-stages of BKB = BK / kBSplit k-rows, so the
+// dequantizers can run further ahead of the MMA in the same shared memory.
+#ifndef AGOQ_GEMM_BSPLIT
+#define AGOQ_GEMM_BSPLIT 1
+#endif
+constexpr int kBSplit = AGOQ_GEMM_BSPLIT;
+constexpr int BKB = BK / kBSplit;                          // k-rows of a B sub-stage
+constexpr int kChunkB = BKB * 128;                         // bytes of one 64-wide N chunk of it
+static_assert(BKB % 16 == 0 && BKB * kBSplit == BK, "B sub-stages are whole K-steps");
 constexpr int kTmaWarp = 0, kMmaWarp = 1, kTmaXWarp = 2, kDeqWarp0 = 3, kDeqWarps = 16;
 constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;   // 608
 #ifndef AGOQ_GEMM_PAIR
@@ -114,9 +123,9 @@ constexpr int kTileRows = BM * kPair;                      // output rows per ti
 constexpr int kBCols = BN / kPair;                         // X-hat columns this CTA holds
 constexpr int kWordsPerRow = kBCols / 8;                   // 4-bit code words per k-row
 constexpr int kRowsPerWarp = 32 / kWordsPerRow;            // k-rows a dequant warp covers at once
-constexpr int kDeqRows = BK / (kRowsPerWarp * kDeqWarps);  // code words per dequant thread per stage
-static_assert(kDeqRows >= 1 && kDeqRows * kRowsPerWarp * kDeqWarps == BK,
-              "every k-row of a stage is dequantized exactly once");
+constexpr int kDeqRows = BKB / (kRowsPerWarp * kDeqWarps); // code words per dequant thread per sub-stage
+static_assert(kDeqRows >= 1 && kDeqRows * kRowsPerWarp * kDeqWarps == BKB,
+              "every k-row of a sub-stage is dequantized exactly once");
 static_assert(NB >= 2, "the B ring must let dequantization run ahead of the MMA");
 static_assert(kDeqWarps == 16, "epilogue items: 4 TMEM lane quarters x 4 blocks of 128 columns");
 // A waiter may only be one phase behind the barrier it polls (a parity test
@@ -126,10 +135,10 @@ static_assert(kDeqWarps == 16, "epilogue items: 4 TMEM lane quarters x 4 blocks 
 // released the accumulator.  The pair-ready ring (CTA 0 only) has as many
 // slots as the relay can run ahead of the MMA: NA k-blocks when it waits for
 // the A stage only (its TMA producer needs the stages the MMA releases), or
-// min(NA, NB) when it also waits for the X-hat stage.
-constexpr int NP = AGOQ_PAIR_DIRECT_B ? NA : (NA < NB ? NA : NB);
+// min(NA, NB / kBSplit) when it also waits for the X-hat sub-stages.
+constexpr int NP = AGOQ_PAIR_DIRECT_B ? NA : (NA < NB / kBSplit ? NA : NB / kBSplit);
 constexpr int kAStage = BM * BK * 2;                      // 32 KiB of dY (BF16)
-constexpr int kBStage = kBCols * BK * 2;                  // this CTA's X-hat columns (BF16)
+constexpr int kBStage = kBCols * BKB * 2;                 // this CTA's X-hat columns (BF16), one sub-stage
 constexpr int kCStage = BK * kBCols / 2;                  // their packed codes
 constexpr int kSStage = BK * 4 * 4;                       // ... and 4-wide scale boxes
 static_assert(BK % 16 == 0 && BK >= 16 && BK <= 256, "k-block depth");
@@ -326,12 +335,14 @@ __device__ __forceinline__ void epilogue_item(uint32_t taddr, void *dW, float *m
 // of a tile overwrites the accumulator.  NK and BOTH are compile-time
 // constants so the issuing thread runs a straight line of MMA instructions
 // (a depth test in the loop measured 2-7% slower, hence one kernel per BK).
+//   a0: the A stage; kk0: its first K-step used here; b0: the B sub-stage.
 template <int NK, bool BOTH>
 __device__ __forceinline__ void issue_kblock_h(uint32_t tmem_base, uint32_t a0, uint32_t b0,
-                                               bool accumulate) {
+                                               int kk0, bool accumulate) {
 #pragma unroll
-    for (int kk = 0; kk < NK; ++kk) {
-        const uint64_t bdesc = sw128_desc(b0 + kk * 2048, kChunk, 1024);
+    for (int j = 0; j < NK; ++j) {
+        const int kk = kk0 + j;
+        const uint64_t bdesc = sw128_desc(b0 + j * 2048, kChunkB, 1024);
         const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
         const uint64_t adesc0 = sw128_desc(a0 + kk * 2048, kChunk, 1024);
         if constexpr (kPair > 1)
@@ -348,12 +359,12 @@ __device__ __forceinline__ void issue_kblock_h(uint32_t tmem_base, uint32_t a0, 
     }
 }
 template <int NK>
-__device__ __forceinline__ void issue_kblock(uint32_t tmem_base, uint32_t a0, uint32_t b0,
+__device__ __forceinline__ void issue_kblock(uint32_t tmem_base, uint32_t a0, uint32_t b0, int kk0,
                                              bool accumulate, bool both) {
     if (kPair == 1 || both)
-        issue_kblock_h<NK, true>(tmem_base, a0, b0, accumulate);
+        issue_kblock_h<NK, true>(tmem_base, a0, b0, kk0, accumulate);
     else
-        issue_kblock_h<NK, false>(tmem_base, a0, b0, accumulate);
+        issue_kblock_h<NK, false>(tmem_base, a0, b0, kk0, accumulate);
 }
 
 // dW (EPI kEpiBf16 / kEpiF32) or the FP8 master codes (kEpiAccumFp8, with
@@ -501,9 +512,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 tc_fence_after();
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const int sa = it % NA, sb = it % NB;
+                    const int sa = it % NA;
                     if (!wait_bar(&sh.full_a[sa], (it / NA) & 1u, sh.abort, &g_device_status) ||
-                        !wait_bar(&sh.full_b[sb], (it / NB) & 1u, sh.abort, &g_device_status) ||
                         (kPair > 1 &&
                          !(AGOQ_PAIR_CLUSTER_WAIT
                                ? wait_bar_cluster(&sh.pair_ready[it % NP], (it / NP) & 1u, sh.abort,
@@ -513,18 +523,29 @@ __global__ void __launch_bounds__(kThreads, 1)
                         ok = false;
                         break;
                     }
-                    tc_fence_after();
                     const uint32_t a0 = smem_u32(sh.a + sa * kAStage);
-                    const uint32_t b0 = smem_u32(sh.b + sb * kBStage);
-                    issue_kblock<BK / 16>(tmem_base, a0, b0, kb > 0, v1);
-                    issued = true;
-                    if constexpr (kPair > 1) {
-                        umma_commit_pair_multicast(&sh.empty_a[sa], 3);
-                        umma_commit_pair_multicast(&sh.empty_b[sb], 3);
-                    } else {
-                        umma_commit(&sh.empty_a[sa]);
-                        umma_commit(&sh.empty_b[sb]);
+#pragma unroll
+                    for (int sub = 0; sub < kBSplit; ++sub) {
+                        const uint32_t ib = it * kBSplit + sub;   // B sub-stage sequence number
+                        const int sb = ib % NB;
+                        if (!wait_bar(&sh.full_b[sb], (ib / NB) & 1u, sh.abort, &g_device_status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        issue_kblock<BKB / 16>(tmem_base, a0, smem_u32(sh.b + sb * kBStage),
+                                               sub * (BKB / 16), kb > 0, v1);
+                        issued = true;
+                        if constexpr (kPair > 1)
+                            umma_commit_pair_multicast(&sh.empty_b[sb], 3);
+                        else
+                            umma_commit(&sh.empty_b[sb]);
                     }
+                    if (!ok) break;
+                    if constexpr (kPair > 1)
+                        umma_commit_pair_multicast(&sh.empty_a[sa], 3);
+                    else
+                        umma_commit(&sh.empty_a[sa]);
                 }
                 if (!ok) break;
                 if constexpr (kPair > 1)
@@ -549,10 +570,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (int g = cluster_id; ok && g < num_groups; g += num_clusters) {
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const int sa = it % NA, sb = it % NB;
+                    const int sa = it % NA;
+                    const uint32_t ibl = it * kBSplit + kBSplit - 1;   // the k-block's last B sub-stage
                     if (!wait_bar(&sh.full_a[sa], (it / NA) & 1u, sh.abort, &g_device_status) ||
-                        (!kDirectB &&
-                         !wait_bar(&sh.full_b[sb], (it / NB) & 1u, sh.abort, &g_device_status))) {
+                        (!kDirectB && !wait_bar(&sh.full_b[ibl % NB], (ibl / NB) & 1u, sh.abort,
+                                                &g_device_status))) {
                         ok = false;
                         break;
                     }
@@ -577,7 +599,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             kPair > 1 ? mapa_shared(smem_u32(sh.full_b), 0) : smem_u32(sh.full_b);
         // The previous tile's epilogue runs once the B ring holds the first
         // stages of this tile (or all of them, for short K).
-        const int lead = (kblocks < NB ? kblocks : NB) - 1;
+        constexpr int kBBlocks = NB / kBSplit > 0 ? NB / kBSplit : 1;   // k-blocks the B ring holds
+        const int lead = (kblocks < kBBlocks ? kblocks : kBBlocks) - 1;
         auto epilogue = [&](int g, uint32_t t) -> bool {
             int m0, n0;
             tile_of(g, m0, n0);
@@ -627,43 +650,54 @@ __global__ void __launch_bounds__(kThreads, 1)
                         prefetch_l2(mscales + row * (N / 128) + n0 / 128 + ejb);
                     }
                 }
-                const int sx = it % NX, sb = it % NB;
+                const int sx = it % NX;
                 if (!warp_wait(&sh.full_x[sx], (it / NX) & 1u, sh.abort, &g_device_status)) { ok = false; break; }
                 const uint32_t *codes = reinterpret_cast<const uint32_t *>(sh.c + sx * kCStage);
                 const float *scales = sh.s + sx * (kSStage / 4);
-                uint32_t w[kDeqRows];
-                float sc[kDeqRows];
+                uint32_t w[kBSplit][kDeqRows];
+                float sc[kBSplit][kDeqRows];
 #pragma unroll
-                for (int i = 0; i < kDeqRows; ++i) {
-                    const int k = kRowsPerWarp * (d + kDeqWarps * i) + rsub;   // row of the stage
-                    w[i] = codes[k * kWordsPerRow + wc];
-                    sc[i] = scales[k * 4 + soff];
-                }
-                // The stage may be overwritten once the MMA has read it.
-                if (!warp_wait(&sh.empty_b[sb], ((it / NB) & 1u) ^ 1u, sh.abort, &g_device_status)) {
-                    ok = false;
-                    break;
-                }
-                uint8_t *btile = sh.b + sb * kBStage + chunk * kChunk;
+                for (int sub = 0; sub < kBSplit; ++sub) {
 #pragma unroll
-                for (int i = 0; i < kDeqRows; ++i) {
-                    const int k = kRowsPerWarp * (d + kDeqWarps * i) + rsub;
-                    const uint4 y = dequant_word(w[i], sc[i]);
-                    uint8_t *dst = btile + k * 128 + ((piece ^ (k & 7)) << 4);
-                    *reinterpret_cast<uint4 *>(dst) = y;
+                    for (int i = 0; i < kDeqRows; ++i) {
+                        // row of the X stage
+                        const int k = sub * BKB + kRowsPerWarp * (d + kDeqWarps * i) + rsub;
+                        w[sub][i] = codes[k * kWordsPerRow + wc];
+                        sc[sub][i] = scales[k * 4 + soff];
+                    }
                 }
-                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                __syncwarp();
+#pragma unroll
+                for (int sub = 0; sub < kBSplit; ++sub) {
+                    const uint32_t ib = it * kBSplit + sub;   // B sub-stage sequence number
+                    const int sb = ib % NB;
+                    // The sub-stage may be overwritten once the MMA has read it.
+                    if (!warp_wait(&sh.empty_b[sb], ((ib / NB) & 1u) ^ 1u, sh.abort,
+                                   &g_device_status)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t *btile = sh.b + sb * kBStage + chunk * kChunkB;
+#pragma unroll
+                    for (int i = 0; i < kDeqRows; ++i) {
+                        const int k = kRowsPerWarp * (d + kDeqWarps * i) + rsub;   // row of the sub-stage
+                        const uint4 y = dequant_word(w[sub][i], sc[sub][i]);
+                        uint8_t *dst = btile + k * 128 + ((piece ^ (k & 7)) << 4);
+                        *reinterpret_cast<uint4 *>(dst) = y;
+                    }
+                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                    __syncwarp();
+                    if (lane == 0) {
+                        if (kDirectB && rank != 0)
+                            mbar_arrive_remote(full_b0 + (uint32_t)sb * 8u);
+                        else
+                            mbar_arrive(&sh.full_b[sb]);
+                    }
+                }
+                if (!ok) break;
                 // The X stage is released only now: its codes have been consumed
                 // (the B stores depend on them), so no shared-memory load of it
                 // can still be in flight when the next TMA load overwrites it.
-                if (lane == 0) {
-                    if (kDirectB && rank != 0)
-                        mbar_arrive_remote(full_b0 + (uint32_t)sb * 8u);
-                    else
-                        mbar_arrive(&sh.full_b[sb]);
-                    mbar_arrive(&sh.empty_x[sx]);
-                }
+                if (lane == 0) mbar_arrive(&sh.empty_x[sx]);
                 if (kb == lead && prev >= 0 && !epilogue(prev, t - 1)) { ok = false; break; }
             }
             prev = g;
