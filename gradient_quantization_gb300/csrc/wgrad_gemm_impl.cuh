@@ -123,8 +123,16 @@ constexpr int kTileRows = BM * kPair;                      // output rows per ti
 constexpr int kBCols = BN / kPair;                         // X-hat columns this CTA holds
 constexpr int kWordsPerRow = kBCols / 8;                   // 4-bit code words per k-row
 constexpr int kRowsPerWarp = 32 / kWordsPerRow;            // k-rows a dequant warp covers at once
-constexpr int kDeqRows = BKB / (kRowsPerWarp * kDeqWarps); // code words per dequant thread per sub-stage
-static_assert(kDeqRows >= 1 && kDeqRows * kRowsPerWarp * kDeqWarps == BKB,
+// With AGOQ_GEMM_SUB_BY_WARP each B sub-stage is written by its own group of
+// kDeqWarps / kBSplit dequantizer warps (one wait, one fence and one arrive per
+// warp and k-block); otherwise every warp writes its rows of every sub-stage.
+#ifndef AGOQ_GEMM_SUB_BY_WARP
+#define AGOQ_GEMM_SUB_BY_WARP 0
+#endif
+constexpr bool kSubByWarp = AGOQ_GEMM_SUB_BY_WARP && kBSplit > 1;
+constexpr int kSubWarps = kSubByWarp ? kDeqWarps / kBSplit : kDeqWarps;   // writers of a sub-stage
+constexpr int kDeqRows = BKB / (kRowsPerWarp * kSubWarps); // code words per dequant thread per sub-stage
+static_assert(kDeqRows >= 1 && kDeqRows * kRowsPerWarp * kSubWarps == BKB,
               "every k-row of a sub-stage is dequantized exactly once");
 static_assert(NB >= 2, "the B ring must let dequantization run ahead of the MMA");
 static_assert(kDeqWarps == 16, "epilogue items: 4 TMEM lane quarters x 4 blocks of 128 columns");
@@ -215,6 +223,18 @@ __device__ __forceinline__ uint32_t word_of(const uint4 (&c)[8], int i) {
     return (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
 }
 
+// The epilogue of a tile runs after the dequantizers have written the B
+// stages of the next tile's first AGOQ_GEMM_LEAD + 1 k-blocks (-1: as many as
+// the B ring holds).
+#ifndef AGOQ_GEMM_LEAD
+#define AGOQ_GEMM_LEAD 0
+#endif
+// 1: the BF16 epilogue releases the accumulator before its global stores
+// (all 128 columns held in registers); 2: after storing the first 64 columns
+// (64 held); 0: after all stores.
+#ifndef AGOQ_EPI_EARLY_RELEASE
+#define AGOQ_EPI_EARLY_RELEASE 1
+#endif
 #ifndef AGOQ_ACCUM_LD_GROUP
 #define AGOQ_ACCUM_LD_GROUP 1
 #endif
@@ -422,7 +442,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.empty_x[s], kDeqWarps);
         }
         for (int s = 0; s < NB; ++s) {
-            mbar_init(&sh.full_b[s], kDirectB ? kDeqWarps * kPair : kDeqWarps);
+            mbar_init(&sh.full_b[s], kDirectB ? kSubWarps * kPair : kSubWarps);
             mbar_init(&sh.empty_b[s], 1);
         }
         for (int s = 0; s < NP; ++s) mbar_init(&sh.pair_ready[s], 1);
@@ -600,7 +620,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         // The previous tile's epilogue runs once the B ring holds the first
         // stages of this tile (or all of them, for short K).
         constexpr int kBBlocks = NB / kBSplit > 0 ? NB / kBSplit : 1;   // k-blocks the B ring holds
-        const int lead = (kblocks < kBBlocks ? kblocks : kBBlocks) - 1;
+        constexpr int kLead = AGOQ_GEMM_LEAD < 0 ? kBBlocks - 1 : AGOQ_GEMM_LEAD;
+        const int lead = kblocks - 1 < kLead ? kblocks - 1 : kLead;
         auto epilogue = [&](int g, uint32_t t) -> bool {
             int m0, n0;
             tile_of(g, m0, n0);
@@ -620,14 +641,59 @@ __global__ void __launch_bounds__(kThreads, 1)
                     mb.load(static_cast<const uint8_t *>(dW) + (size_t)row * N + col0,
                             mscales + (size_t)row * (N / 128) + col0 / 128);
             }
-            if (valid) epilogue_item<EPI>(etaddr, dW, mscales, row, col0, N, mb);
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) {
-                if (kPair > 1 && rank != 0)
-                    mbar_arrive_remote(tmem_empty0);
-                else
-                    mbar_arrive(sh.tmem_empty);
+            auto release = [&]() {   // the accumulator may be overwritten
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) {
+                    if (kPair > 1 && rank != 0)
+                        mbar_arrive_remote(tmem_empty0);
+                    else
+                        mbar_arrive(sh.tmem_empty);
+                }
+            };
+            if constexpr (EPI == kEpiBf16 && AGOQ_EPI_EARLY_RELEASE) {
+                // Read and round the item, storing the first kStoreEarly
+                // 32-column chunks at once and keeping the rest in registers;
+                // hand the accumulator back to the MMA, then store the rest
+                // while the next tile's MMAs run.
+                constexpr int kStoreEarly = AGOQ_EPI_EARLY_RELEASE == 1 ? 0 : 2;
+                constexpr int kHold = 4 - kStoreEarly;
+                uint32_t h[16 * kHold];
+                uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(dW) +
+                                                       (size_t)row * N + col0);
+                if (valid) {
+#pragma unroll
+                    for (int cc = 0; cc < 4; ++cc) {
+                        uint32_t v[32];
+                        tmem_ld32(etaddr + cc * 32, v);
+                        if (cc < kStoreEarly) {
+#pragma unroll
+                            for (int j = 0; j < 4; ++j) {
+                                uint32_t w4[4];
+#pragma unroll
+                                for (int i = 0; i < 4; ++i)
+                                    w4[i] = pack_bf16x2(__uint_as_float(v[8 * j + 2 * i]),
+                                                        __uint_as_float(v[8 * j + 2 * i + 1]));
+                                dst[4 * cc + j] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
+                            }
+                        } else {
+#pragma unroll
+                            for (int i = 0; i < 16; ++i)
+                                h[16 * (cc - kStoreEarly) + i] = pack_bf16x2(
+                                    __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
+                        }
+                    }
+                }
+                release();
+                if (valid) {
+#pragma unroll
+                    for (int j = 0; j < 4 * kHold; ++j)
+                        dst[4 * kStoreEarly + j] =
+                            make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+                }
+            } else {
+                if (valid) epilogue_item<EPI>(etaddr, dW, mscales, row, col0, N, mb);
+                release();
             }
             return true;
         };
@@ -654,20 +720,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!warp_wait(&sh.full_x[sx], (it / NX) & 1u, sh.abort, &g_device_status)) { ok = false; break; }
                 const uint32_t *codes = reinterpret_cast<const uint32_t *>(sh.c + sx * kCStage);
                 const float *scales = sh.s + sx * (kSStage / 4);
-                uint32_t w[kBSplit][kDeqRows];
-                float sc[kBSplit][kDeqRows];
+                // sub-stages this warp writes: all of them, or only its own
+                constexpr int kMySubs = kSubByWarp ? 1 : kBSplit;
+                const int sub0 = kSubByWarp ? d / kSubWarps : 0;
+                const int dd = kSubByWarp ? d % kSubWarps : d;   // the warp's index among the writers
+                uint32_t w[kMySubs][kDeqRows];
+                float sc[kMySubs][kDeqRows];
 #pragma unroll
-                for (int sub = 0; sub < kBSplit; ++sub) {
+                for (int js = 0; js < kMySubs; ++js) {
 #pragma unroll
                     for (int i = 0; i < kDeqRows; ++i) {
                         // row of the X stage
-                        const int k = sub * BKB + kRowsPerWarp * (d + kDeqWarps * i) + rsub;
-                        w[sub][i] = codes[k * kWordsPerRow + wc];
-                        sc[sub][i] = scales[k * 4 + soff];
+                        const int k = (sub0 + js) * BKB + kRowsPerWarp * (dd + kSubWarps * i) + rsub;
+                        w[js][i] = codes[k * kWordsPerRow + wc];
+                        sc[js][i] = scales[k * 4 + soff];
                     }
                 }
 #pragma unroll
-                for (int sub = 0; sub < kBSplit; ++sub) {
+                for (int js = 0; js < kMySubs; ++js) {
+                    const int sub = sub0 + js;
                     const uint32_t ib = it * kBSplit + sub;   // B sub-stage sequence number
                     const int sb = ib % NB;
                     // The sub-stage may be overwritten once the MMA has read it.
@@ -679,8 +750,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     uint8_t *btile = sh.b + sb * kBStage + chunk * kChunkB;
 #pragma unroll
                     for (int i = 0; i < kDeqRows; ++i) {
-                        const int k = kRowsPerWarp * (d + kDeqWarps * i) + rsub;   // row of the sub-stage
-                        const uint4 y = dequant_word(w[sub][i], sc[sub][i]);
+                        const int k = kRowsPerWarp * (dd + kSubWarps * i) + rsub;   // row of the sub-stage
+                        const uint4 y = dequant_word(w[js][i], sc[js][i]);
                         uint8_t *dst = btile + k * 128 + ((piece ^ (k & 7)) << 4);
                         *reinterpret_cast<uint4 *>(dst) = y;
                     }
