@@ -46,7 +46,7 @@
 #define AGOQ_NAIVE_MIXED_ADD 1
 #endif
 #ifndef AGOQ_REDUCE_MIN_CTAS
-#define AGOQ_REDUCE_MIN_CTAS 1
+#define AGOQ_REDUCE_MIN_CTAS 2
 #endif
 #ifndef AGOQ_REDUCE_COUNT_MIN_CTAS
 #define AGOQ_REDUCE_COUNT_MIN_CTAS 2
@@ -56,11 +56,11 @@
 #ifndef AGOQ_NAIVE_MAX
 #define AGOQ_NAIVE_MAX 1
 #endif
-// 1: with the naive count, the shard products are formed with packed binary32
-//    multiplies (two per instruction) and added with scalar round-to-nearest
-//    adds (measured faster there, slower without the count); 0: all scalar.
+// The shard products are formed with packed binary32 multiplies (two per
+// instruction) and added with scalar round-to-nearest adds: 2 in both reduce
+// kernels, 1 only in the one with the naive count, 0 nowhere.
 #ifndef AGOQ_REDUCE_PACKED_MUL
-#define AGOQ_REDUCE_PACKED_MUL 1
+#define AGOQ_REDUCE_PACKED_MUL 2
 #endif
 
 namespace agoq {
@@ -321,7 +321,7 @@ reduce_shards_kernel(
                 float e[16];
 #pragma unroll
                 for (int q = 0; q < 4; ++q) decode4(w4[q], e + 4 * q);
-                if constexpr (NAIVE && AGOQ_REDUCE_PACKED_MUL) {
+                if constexpr ((NAIVE && AGOQ_REDUCE_PACKED_MUL) || AGOQ_REDUCE_PACKED_MUL == 2) {
                     // products in packed pairs, each sum a scalar round-to-nearest add
                     const uint64_t sc2 = f32x2(sc[u], sc[u]);
 #pragma unroll
