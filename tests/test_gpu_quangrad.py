@@ -191,3 +191,37 @@ def test_reduce_count_is_set_not_accumulated(oracle):
     first = int(cnt.item())
     agoq.agoq_reduce_fp8_shards(G.dev(sh), G.dev(ss), W, n, naive_overflow_count=cnt)
     assert int(cnt.item()) == first == oracle.reduce_fp8_shards(sh, ss, W, n)[2]
+
+
+# ---------------------------------------------------------------- checkpoint / resume
+def test_accum_resume_from_saved_master_is_bit_identical(oracle, tmp_path):
+    """The FP8 master (codes + scales) is the whole state of the accumulation:
+    saving it to a file after 3 micro-batches, reloading it into fresh device
+    buffers and continuing with 5 more gives the same bits as 8 uninterrupted
+    micro-batches, and as the oracle."""
+    nblocks = 1031
+    n = nblocks * 128
+    grads = list(synthetic.quangrad_grads_np(seed=9, n=n, steps=8))
+    m = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    s = torch.zeros(nblocks, dtype=torch.float32, device="cuda")
+    for g in grads:
+        agoq.agoq_grad_accum_fp8(m, s, G.dev_bf16(g))
+    m2 = torch.zeros(n, dtype=torch.uint8, device="cuda")
+    s2 = torch.zeros(nblocks, dtype=torch.float32, device="cuda")
+    for g in grads[:3]:
+        agoq.agoq_grad_accum_fp8(m2, s2, G.dev_bf16(g))
+    path = tmp_path / "master.npz"
+    np.savez(path, codes=m2.cpu().numpy(), scales=s2.cpu().numpy())
+    del m2, s2
+    saved = np.load(path)
+    m3 = torch.from_numpy(saved["codes"]).cuda()
+    s3 = torch.from_numpy(saved["scales"]).cuda()
+    for g in grads[3:]:
+        agoq.agoq_grad_accum_fp8(m3, s3, G.dev_bf16(g))
+    assert np.array_equal(m3.cpu().numpy(), m.cpu().numpy())
+    assert np.array_equal(s3.cpu().numpy().view(np.uint32), s.cpu().numpy().view(np.uint32))
+    m_np, s_np = np.zeros(n, np.uint8), np.zeros(nblocks, np.float32)
+    for g in grads:
+        m_np, s_np = oracle.grad_accum_fp8(m_np, s_np, g)
+    assert np.array_equal(m.cpu().numpy(), m_np)
+    assert np.array_equal(s.cpu().numpy().view(np.uint32), s_np.view(np.uint32))
