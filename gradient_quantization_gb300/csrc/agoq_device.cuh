@@ -35,6 +35,38 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     return r;
 }
 
+// ---- packed binary32 pairs (sm_100+): two IEEE round-to-nearest operations
+// per instruction, bit-identical to the scalar __fadd_rn/__fsub_rn/__fmul_rn.
+__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
+    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
+}
+__device__ __forceinline__ uint64_t u32x2(uint32_t lo, uint32_t hi) {
+    return (static_cast<uint64_t>(hi) << 32) | lo;
+}
+__device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
+__device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
+__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
+    uint64_t d;
+    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+    return d;
+}
+// a*b + c per lane with a single rounding (fused multiply-add).
+__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
+    uint64_t d;
+    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+    return d;
+}
+
 // ---- E4M3 ------------------------------------------------------------------
 // Two binary32 values to two E4M3 codes, round to nearest even, saturating to
 // +-448; `lo` in bits 0-7.
@@ -100,12 +132,28 @@ __device__ __forceinline__ float e4m3_mul(uint32_t w, int i, float S, bool folde
 // underflow are far below the smallest E4M3 midpoint (2^-10) and give a signed
 // zero either way.  s subnormal takes the division; s == 0 (all-zero block)
 // gives zero codes.
+#ifndef AGOQ_E4M3_PACKED
+#define AGOQ_E4M3_PACKED 1
+#endif
 __device__ __forceinline__ uint2 e4m3_codes8(const float t[8], float s) {
     uint32_t c[4];
     if (s >= 0x1p-126f) {
         const float r = __frcp_rn(s);
         constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
         bool differ = false;
+#if AGOQ_E4M3_PACKED
+        // the same products in packed pairs (multiplies only: nothing to contract)
+        const uint64_t r2 = f32x2(r, r), dn2 = f32x2(kDown, kDown), up2 = f32x2(kUp, kUp);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) {
+            const uint64_t q2 = mul_f32x2(f32x2(t[2 * p], t[2 * p + 1]), r2);
+            const uint64_t a2 = mul_f32x2(q2, dn2), b2 = mul_f32x2(q2, up2);
+            const uint32_t lo = e4m3x2_from_f32(lo_f32(a2), hi_f32(a2));
+            const uint32_t hi = e4m3x2_from_f32(lo_f32(b2), hi_f32(b2));
+            differ |= lo != hi;
+            c[p] = lo;
+        }
+#else
 #pragma unroll
         for (int p = 0; p < 4; ++p) {
             const float qa = __fmul_rn(t[2 * p], r), qb = __fmul_rn(t[2 * p + 1], r);
@@ -114,6 +162,7 @@ __device__ __forceinline__ uint2 e4m3_codes8(const float t[8], float s) {
             differ |= lo != hi;
             c[p] = lo;
         }
+#endif
         if (differ) {
 #pragma unroll
             for (int p = 0; p < 4; ++p)
@@ -139,38 +188,6 @@ __device__ __forceinline__ float e4m3_round_f32(float t) {
     const uint32_t e = max(__float_as_uint(t) & 0x7F800000u, (uint32_t)(127 - 6) << 23);
     const float c = __uint_as_float(e + (20u << 23) + 0x00400000u);
     return __fsub_rn(__fadd_rn(t, c), c);
-}
-
-// ---- packed binary32 pairs (sm_100+): two IEEE round-to-nearest operations
-// per instruction, bit-identical to the scalar __fadd_rn/__fsub_rn/__fmul_rn.
-__device__ __forceinline__ uint64_t f32x2(float lo, float hi) {
-    return (static_cast<uint64_t>(__float_as_uint(hi)) << 32) | __float_as_uint(lo);
-}
-__device__ __forceinline__ uint64_t u32x2(uint32_t lo, uint32_t hi) {
-    return (static_cast<uint64_t>(hi) << 32) | lo;
-}
-__device__ __forceinline__ float lo_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v)); }
-__device__ __forceinline__ float hi_f32(uint64_t v) { return __uint_as_float(static_cast<uint32_t>(v >> 32)); }
-__device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t sub_f32x2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-__device__ __forceinline__ uint64_t mul_f32x2(uint64_t a, uint64_t b) {
-    uint64_t d;
-    asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
-    return d;
-}
-// a*b + c per lane with a single rounding (fused multiply-add).
-__device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c) {
-    uint64_t d;
-    asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
-    return d;
 }
 
 // Largest |value| of the BF16 pairs in w[0..N-1], as a binary32 (exact: the

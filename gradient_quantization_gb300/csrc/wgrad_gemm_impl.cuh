@@ -206,16 +206,22 @@ __device__ __forceinline__ void prefetch_l2(const void *p) {
 }
 
 // t_i = fl(fl(e4m3(c_i) * s) + acc_i) for the four E4M3 codes of word w and
-// four binary32 accumulator values (bit patterns).  Scalar __fmul_rn/__fadd_rn:
-// the two roundings must stay separate (a fused multiply-add gives a different
-// t, e.g. a signed zero where m and acc cancel).
+// four binary32 accumulator values (bit patterns).  The two roundings must
+// stay separate (a fused multiply-add gives a different t, e.g. a signed zero
+// where m and acc cancel): packed multiplies, scalar adds (a packed multiply
+// followed by a packed add was contracted into one rounding by the compiler).
 __device__ __forceinline__ void master_plus_acc4(uint32_t w, float s, const uint32_t *acc,
                                                  float t[4]) {
     float e[4];
     e4m3x2_to_f32(w & 0xFFFFu, e[0], e[1]);
     e4m3x2_to_f32(w >> 16, e[2], e[3]);
-#pragma unroll
-    for (int i = 0; i < 4; ++i) t[i] = __fadd_rn(__fmul_rn(e[i], s), __uint_as_float(acc[i]));
+    // products in packed pairs, each sum a scalar round-to-nearest add
+    const uint64_t s2 = f32x2(s, s);
+    const uint64_t p01 = mul_f32x2(f32x2(e[0], e[1]), s2), p23 = mul_f32x2(f32x2(e[2], e[3]), s2);
+    t[0] = __fadd_rn(lo_f32(p01), __uint_as_float(acc[0]));
+    t[1] = __fadd_rn(hi_f32(p01), __uint_as_float(acc[1]));
+    t[2] = __fadd_rn(lo_f32(p23), __uint_as_float(acc[2]));
+    t[3] = __fadd_rn(hi_f32(p23), __uint_as_float(acc[3]));
 }
 
 __device__ __forceinline__ uint32_t word_of(const uint4 (&c)[8], int i) {
