@@ -623,8 +623,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             kPair > 1 ? mapa_shared(smem_u32(sh.tmem_empty), 0) : smem_u32(sh.tmem_empty);
         const uint32_t full_b0 =
             kPair > 1 ? mapa_shared(smem_u32(sh.full_b), 0) : smem_u32(sh.full_b);
-        // The previous tile's epilogue runs once the B ring holds the first
-        // stages of this tile (or all of them, for short K).
+        // The previous tile's epilogue runs once this tile's first kLead + 1
+        // k-blocks of X-hat are written (fewer for short K).
         constexpr int kBBlocks = NB / kBSplit > 0 ? NB / kBSplit : 1;   // k-blocks the B ring holds
         constexpr int kLead = AGOQ_GEMM_LEAD < 0 ? kBBlocks - 1 : AGOQ_GEMM_LEAD;
         const int lead = kblocks - 1 < kLead ? kblocks - 1 : kLead;
