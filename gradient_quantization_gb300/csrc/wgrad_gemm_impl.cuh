@@ -33,13 +33,14 @@
 //               an arrive on CTA 0's B barrier (remote from CTA 1) and the
 //               release of the X stage (after its codes have been consumed).
 //               They also run the epilogue of the previous tile, once they
-//               have filled the B ring with the first stages of the next one
-//               (the MMA waits for the accumulator anyway): each warp takes
+//               have written the next tile's first k-block (the MMA waits
+//               for the accumulator anyway): each warp takes
 //               one 32-row x 128-column item of its CTA's accumulators (its
 //               TMEM lane quarter, warp % 4, and one of four 128-column
 //               blocks), reads it with tcgen05.ld, one output row per thread,
 //               and does one of
-//               - BF16 round-to-nearest-even and global stores;
+//               - BF16 round-to-nearest-even and global stores (the
+//                 accumulator is handed back before the stores);
 //               - the FP32 accumulator stored unrounded;
 //               - the QuanGrad accumulation into an FP8 master gradient
 //                 ("Lokale accumulatie", section 2.B): dequantize the 128
