@@ -271,6 +271,13 @@ def gpu_arm(args):
     dom_label, dom_bytes = calls[dom][0], calls[dom][1]
     achieved = dom_bytes / (per_call[dom] * 1e-3) / 1e9
     traffic = DOMINANT_TRAFFIC_BYTES.get(dom_label)
+    # the same launch alone, after an L2 flush that leaves no dirty lines (in the
+    # step it also writes back what the previous call left dirty in L2)
+    flushbuf = torch.zeros(256 << 20 >> 2, dtype=torch.float32, device=device)
+    cleanbuf = torch.ones(256 << 20 >> 2, dtype=torch.float32, device=device)
+    iso_ms = _time_launch(calls[dom][3], lambda: _flush_l2(flushbuf, cleanbuf), reps=7, warm=2)
+    del flushbuf, cleanbuf
+    iso_gbs = dom_bytes / (iso_ms * 1e-3) / 1e9
     kernels = {c[0]: {"us": round(per_call[i] * 1e3, 2),
                       "GB/s": round(c[1] / (per_call[i] * 1e-3) / 1e9, 1),
                       "Gelem/s": round(c[2] / (per_call[i] * 1e-3) / 1e9, 2),
@@ -313,7 +320,12 @@ def gpu_arm(args):
                          "peak": hbm_peak, "unit": "GB/s",
                          "frac": round(achieved / hbm_peak, 4), "peak_kind": peak_kind,
                          "bytes_per_launch": dom_bytes, "us_per_launch": round(per_call[dom] * 1e3, 2),
-                         "traffic": traffic},
+                         "traffic": traffic,
+                         "isolated": {"us_per_launch": round(iso_ms * 1e3, 2),
+                                      "achieved": round(iso_gbs, 1),
+                                      "frac": round(iso_gbs / hbm_peak, 4),
+                                      "timing": "median of 7 launches alone, each after an L2 "
+                                                "flush leaving no dirty lines"}},
             "kernels": kernels,
             "kernels_timing": "separate pass of %d steps with an event after every call; the "
                               "timed region (value) has events only at its ends" % ksteps,
