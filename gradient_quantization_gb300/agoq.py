@@ -322,5 +322,5 @@ def agoq_test_wait_timeout(limit_cycles, stream=None):
 
 
 def agoq_device_status(stream=None):
-    """Synchronise and check the device status word (raises AgoqError on a GEMM timeout)."""
+    """Synchronise and check the device status words (raises AgoqError if a pipeline wait timed out)."""
     _check(lib().agoq_device_status(_stream(stream)), "agoq_device_status")

@@ -11,9 +11,14 @@
 // rewritten in place by the same lane that read it.
 // Reduce: 8 lanes own a block, each lane 16 elements (one 16-byte load of
 // codes per shard), so a warp reads 4 adjacent blocks (512 contiguous bytes)
-// of every shard per load instruction; RUNROLL shards are loaded ahead.
+// of every shard per load instruction.  Two kernels feed that arithmetic: one
+// loads the codes into registers itself, RUNROLL shards ahead; the other
+// (used whenever the scale rows allow 16-byte bulk copies) has a producer warp
+// stream (tile, shard) stages into a shared-memory ring with bulk async
+// copies, so that far more bytes are in flight per SM than registers can hold.
 #include "agoq_device.cuh"
 #include "agoq_launch.h"
+#include "gemm_common.cuh"
 
 // Implementation choices, all bit-identical (selected by measurement):
 //   AGOQ_E4M3_DECODE_CVT   1: decode codes with cvt.f16x2.e4m3x2; 0: with integer bit moves
@@ -61,6 +66,30 @@
 // kernels, 1 only in the one with the naive count, 0 nowhere.
 #ifndef AGOQ_REDUCE_PACKED_MUL
 #define AGOQ_REDUCE_PACKED_MUL 2
+#endif
+// Shared-memory staged reduce: 1 selects it when the scale rows allow bulk
+// copies; consumer warps per CTA (each 4 blocks of a tile) without and with
+// the naive count, ring stages, shards per stage, and CTAs per SM.
+#ifndef AGOQ_REDUCE_STAGED
+#define AGOQ_REDUCE_STAGED 1
+#endif
+#ifndef AGOQ_RSTAGED_WARPS
+#define AGOQ_RSTAGED_WARPS 16
+#endif
+#ifndef AGOQ_RSTAGED_COUNT_WARPS
+#define AGOQ_RSTAGED_COUNT_WARPS 15
+#endif
+#ifndef AGOQ_RSTAGED_STAGES
+#define AGOQ_RSTAGED_STAGES 2
+#endif
+#ifndef AGOQ_RSTAGED_SHARDS
+#define AGOQ_RSTAGED_SHARDS 8
+#endif
+#ifndef AGOQ_RSTAGED_HINT
+#define AGOQ_RSTAGED_HINT 0
+#endif
+#ifndef AGOQ_RSTAGED_MIN_CTAS
+#define AGOQ_RSTAGED_MIN_CTAS 1
 #endif
 
 namespace agoq {
@@ -243,6 +272,141 @@ __device__ __forceinline__ void add_f16x2_f32(uint32_t h2, float c0, float c1, f
         : "r"(h2), "f"(c0), "f"(c1));
 }
 
+// One lane's share of the reduce of one block: 16 elements (one 16-byte load
+// of codes per shard), their binary32 running sums over the shards in rank
+// order and, with the naive count, the naive FP8 running sums.
+template <bool NAIVE>
+struct ReduceLane {
+    float acc[16];
+#if AGOQ_NAIVE_MIXED_ADD
+    uint32_t nvh[8];   // naive running sum, FP16 pairs
+#else
+    float nv[16];
+#endif
+#if AGOQ_NAIVE_MAX
+    float nmax[16];    // largest |naive sum| seen per element
+#else
+    uint32_t alive;
+#endif
+
+    __device__ __forceinline__ void clear() {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        if constexpr (NAIVE) {
+#if AGOQ_NAIVE_MAX
+#pragma unroll
+            for (int i = 0; i < 16; ++i) nmax[i] = 0.0f;
+#else
+            alive = 0xFFFFu;
+#endif
+        }
+    }
+
+    // Shard r (codes c, block scale sc): acc += fl(e4m3(c) * sc) element-wise,
+    // and the naive FP8 sum steps once.
+    __device__ __forceinline__ void add_shard(const uint4 &c, float sc, int r) {
+        const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
+        float e[16];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) decode4(w4[q], e + 4 * q);
+        if constexpr ((NAIVE && AGOQ_REDUCE_PACKED_MUL) || AGOQ_REDUCE_PACKED_MUL == 2) {
+            // products in packed pairs, each sum a scalar round-to-nearest add
+            const uint64_t sc2 = f32x2(sc, sc);
+#pragma unroll
+            for (int i = 0; i < 16; i += 2) {
+                const uint64_t p2 = mul_f32x2(f32x2(e[i], e[i + 1]), sc2);
+                acc[i] = __fadd_rn(acc[i], lo_f32(p2));
+                acc[i + 1] = __fadd_rn(acc[i + 1], hi_f32(p2));
+            }
+        } else {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(e[i], sc));
+        }
+        if constexpr (NAIVE) {
+#if AGOQ_NAIVE_MIXED_ADD
+            if (r == 0) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q) {
+                    nvh[2 * q] = e4m3x2_to_f16x2(w4[q] & 0xFFFFu);
+                    nvh[2 * q + 1] = e4m3x2_to_f16x2(w4[q] >> 16);
+                }
+            } else {
+#pragma unroll
+                for (int p = 0; p < 8; ++p) {
+                    float t0, t1;   // exact: both operands are E4M3 values
+                    add_f16x2_f32(nvh[p], e[2 * p], e[2 * p + 1], t0, t1);
+#if AGOQ_NAIVE_MAX
+                    nmax[2 * p] = fmaxf(nmax[2 * p], fabsf(t0));
+                    nmax[2 * p + 1] = fmaxf(nmax[2 * p + 1], fabsf(t1));
+#else
+                    if (fabsf(t0) > kE4M3Max) alive &= ~(1u << (2 * p));
+                    if (fabsf(t1) > kE4M3Max) alive &= ~(2u << (2 * p));
+#endif
+                    nvh[p] = e4m3x2_to_f16x2(e4m3x2_from_f32(t0, t1));
+                }
+            }
+#else
+            if (r == 0) {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) nv[i] = e[i];
+            } else {
+                float tt[16];
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                    tt[i] = __fadd_rn(nv[i], e[i]);   // exact: both are E4M3 values
+                    if (fabsf(tt[i]) > kE4M3Max) alive &= ~(1u << i);
+                }
+#if AGOQ_NAIVE_ROUND_CVT
+#pragma unroll
+                for (int i = 0; i < 16; i += 2)
+                    e4m3x2_to_f32(e4m3x2_from_f32(tt[i], tt[i + 1]), nv[i], nv[i + 1]);
+#else
+#pragma unroll
+                for (int i = 0; i < 16; ++i) nv[i] = e4m3_round_f32(tt[i]);
+#endif
+            }
+#endif
+        }
+    }
+
+    // All W shards are in: requantize with a fresh block scale (the block's 8
+    // lanes are an aligned octet of the warp, all of which call this), store
+    // the lane's 16 codes and, from the octet's first lane, the scale; count
+    // the lane's overflowed naive sums.  Every lane of the warp must call it.
+    __device__ __forceinline__ void finish(bool valid, uint4 *out16, float *out_scale, bool first,
+                                           unsigned long long &overflowed) {
+        float am = 0.0f;
+#pragma unroll
+        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(acc[i]));
+        am = octet_max(am);
+        const float snew = __fdiv_rn(am, kE4M3Max);
+        const uint2 lo = requant8(acc, snew);
+        const uint2 hi = requant8(acc + 8, snew);
+        if (valid) {
+            *out16 = make_uint4(lo.x, lo.y, hi.x, hi.y);
+            if (first) *out_scale = snew;
+            if constexpr (NAIVE) {
+#if AGOQ_NAIVE_MAX
+                int k = 0;
+#pragma unroll
+                for (int i = 0; i < 16; ++i) k += nmax[i] > kE4M3Max;
+                overflowed += (unsigned long long)k;
+#else
+                overflowed += (unsigned long long)__popc(~alive & 0xFFFFu);
+#endif
+            }
+        }
+    }
+};
+
+// Sum of the warp's overflow counts, added to *naive_count by lane 0.
+__device__ __forceinline__ void flush_count(unsigned long long overflowed,
+                                            unsigned long long *naive_count) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) overflowed += __shfl_xor_sync(kFull, overflowed, o);
+    if ((threadIdx.x & 31) == 0 && overflowed) atomicAdd(naive_count, overflowed);
+}
+
 //
 // Block indices are 32-bit (the launcher splits larger inputs); shard r of
 // block b is at shards[r * shard_vec + 8 b ...] and its scale at
@@ -283,21 +447,8 @@ reduce_shards_kernel(
         float sn[RUNROLL];
         load(base, 0, cn, sn);
         int ch = 0;
-        float acc[16];
-#if AGOQ_NAIVE_MIXED_ADD
-        uint32_t nvh[8];   // naive running sum, FP16 pairs
-#else
-        float nv[16];
-#endif
-#if AGOQ_NAIVE_MAX
-        float nmax[16];    // largest |naive sum| seen per element
-#pragma unroll
-        for (int i = 0; i < 16; ++i) nmax[i] = 0.0f;
-#else
-        uint32_t alive = 0xFFFFu;
-#endif
-#pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        ReduceLane<NAIVE> st;
+        st.clear();
         for (;;) {
             uint4 c[RUNROLL];
             float sc[RUNROLL];
@@ -317,113 +468,184 @@ reduce_shards_kernel(
             for (int u = 0; u < RUNROLL; ++u) {
                 const int r = ch * RUNROLL + u;
                 if (r >= W) break;
-                const uint32_t w4[4] = {c[u].x, c[u].y, c[u].z, c[u].w};
-                float e[16];
-#pragma unroll
-                for (int q = 0; q < 4; ++q) decode4(w4[q], e + 4 * q);
-                if constexpr ((NAIVE && AGOQ_REDUCE_PACKED_MUL) || AGOQ_REDUCE_PACKED_MUL == 2) {
-                    // products in packed pairs, each sum a scalar round-to-nearest add
-                    const uint64_t sc2 = f32x2(sc[u], sc[u]);
-#pragma unroll
-                    for (int i = 0; i < 16; i += 2) {
-                        const uint64_t p2 = mul_f32x2(f32x2(e[i], e[i + 1]), sc2);
-                        acc[i] = __fadd_rn(acc[i], lo_f32(p2));
-                        acc[i + 1] = __fadd_rn(acc[i + 1], hi_f32(p2));
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(e[i], sc[u]));
-                }
-                if constexpr (NAIVE) {
-#if AGOQ_NAIVE_MIXED_ADD
-                    if (r == 0) {
-#pragma unroll
-                        for (int q = 0; q < 4; ++q) {
-                            nvh[2 * q] = e4m3x2_to_f16x2(w4[q] & 0xFFFFu);
-                            nvh[2 * q + 1] = e4m3x2_to_f16x2(w4[q] >> 16);
-                        }
-                    } else {
-#pragma unroll
-                        for (int p = 0; p < 8; ++p) {
-                            float t0, t1;   // exact: both operands are E4M3 values
-                            add_f16x2_f32(nvh[p], e[2 * p], e[2 * p + 1], t0, t1);
-#if AGOQ_NAIVE_MAX
-                            nmax[2 * p] = fmaxf(nmax[2 * p], fabsf(t0));
-                            nmax[2 * p + 1] = fmaxf(nmax[2 * p + 1], fabsf(t1));
-#else
-                            if (fabsf(t0) > kE4M3Max) alive &= ~(1u << (2 * p));
-                            if (fabsf(t1) > kE4M3Max) alive &= ~(2u << (2 * p));
-#endif
-                            nvh[p] = e4m3x2_to_f16x2(e4m3x2_from_f32(t0, t1));
-                        }
-                    }
-#else
-                    if (r == 0) {
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) nv[i] = e[i];
-                    } else {
-                        float tt[16];
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) {
-                            tt[i] = __fadd_rn(nv[i], e[i]);   // exact: both are E4M3 values
-                            if (fabsf(tt[i]) > kE4M3Max) alive &= ~(1u << i);
-                        }
-#if AGOQ_NAIVE_ROUND_CVT
-#pragma unroll
-                        for (int i = 0; i < 16; i += 2)
-                            e4m3x2_to_f32(e4m3x2_from_f32(tt[i], tt[i + 1]), nv[i], nv[i + 1]);
-#else
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) nv[i] = e4m3_round_f32(tt[i]);
-#endif
-                    }
-#endif
-                }
+                st.add_shard(c[u], sc[u], r);
             }
             if (nch == 0) {
                 // all W shards of the block group are in: requantize and store
                 const int blk = base + oct;
-                const bool valid = blk < nblocks;
-                float am = 0.0f;
-#pragma unroll
-                for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(acc[i]));
-                am = octet_max(am);
-                const float snew = __fdiv_rn(am, kE4M3Max);
-                const uint2 lo = requant8(acc, snew);
-                const uint2 hi = requant8(acc + 8, snew);
-                if (valid) {
-                    out[(size_t)(unsigned)blk * 8 + t8] = make_uint4(lo.x, lo.y, hi.x, hi.y);
-                    if (t8 == 0) out_scales[blk] = snew;
-                    if constexpr (NAIVE) {
-#if AGOQ_NAIVE_MAX
-                        int k = 0;
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) k += nmax[i] > kE4M3Max;
-                        overflowed += (unsigned long long)k;
-#else
-                        overflowed += (unsigned long long)__popc(~alive & 0xFFFFu);
-#endif
-                    }
-                }
-#pragma unroll
-                for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
-#if AGOQ_NAIVE_MAX
-#pragma unroll
-                for (int i = 0; i < 16; ++i) nmax[i] = 0.0f;
-#else
-                alive = 0xFFFFu;
-#endif
+                st.finish(blk < nblocks, out + (size_t)(unsigned)blk * 8 + t8, out_scales + blk,
+                          t8 == 0, overflowed);
+                st.clear();
             }
             if (nbase >= nblocks) break;
             base = nbase;
             ch = nch;
         }
     }
-    if constexpr (NAIVE) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) overflowed += __shfl_xor_sync(kFull, overflowed, o);
-        if (lane == 0 && overflowed) atomicAdd(naive_count, overflowed);
+    if constexpr (NAIVE) flush_count(overflowed, naive_count);
+}
+
+// ---- the staged reduce ------------------------------------------------------
+// A CTA is kStWarps consumer warps and one producer warp (16 + 1 without the
+// naive count; 15 + 1 with it, so that the CTA is 16 warps and a thread may
+// hold 128 registers).  Work is cut into
+// tiles of kStTile blocks (a consumer warp owns 4 blocks of a tile, laid out as
+// in reduce_shards_kernel); the CTAs take tiles round-robin.  The producer
+// walks (tile, group of kStShards shards) items in the order the consumers
+// take them and copies each shard's codes (kStTile * 128 bytes) and scales
+// (kStTile * 4 bytes) with cp.async.bulk into the next free stage of a
+// kStStages-deep ring (one barrier wait per group of shards): full[s]
+// completes when both copies have landed, empty[s] when every consumer warp
+// has read the stage.  Every wait is time-limited: on expiry the wait records
+// a timeout in g_reduce_status and raises the CTA's abort flag, the warps stop,
+// and the producer waits (time-limited) for its copies still in flight before
+// the CTA exits.
+constexpr int kStStages = AGOQ_RSTAGED_STAGES;
+constexpr int kStShards = AGOQ_RSTAGED_SHARDS;          // shards per stage
+template <bool NAIVE>
+struct StagedShape {
+    static constexpr int kWarps = NAIVE ? AGOQ_RSTAGED_COUNT_WARPS : AGOQ_RSTAGED_WARPS;
+    static constexpr int kThreads = (kWarps + 1) * 32;
+    static constexpr int kTile = 4 * kWarps;
+    static constexpr int kCodeBytes = kStShards * kTile * 128;
+    static constexpr int kScaleBytes = kStShards * kTile * 4;
+    static constexpr size_t kSmem = (size_t)kStStages * (kCodeBytes + kScaleBytes + 16);
+    static_assert((kTile * 4) % 16 == 0, "a full tile's scales must be whole 16-byte units");
+};
+
+__device__ unsigned g_reduce_status;
+
+// Bulk copy of `bytes` (a multiple of 16) from global `src` to shared `dst`
+// (both 16-byte aligned), completing `bytes` transactions on `bar`.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t bytes,
+                                         uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(gemm::smem_u32(dst)), "l"(src), "r"(bytes), "r"(gemm::smem_u32(bar))
+        : "memory");
+}
+
+// shards: byte base; shard r of block b at shards + r * shard_bytes + 128 b.
+// Requires shard_scales 16-byte aligned, scale_stride and nblocks multiples of
+// 4 (so every scale copy is whole 16-byte units).
+template <bool NAIVE>
+__global__ void __launch_bounds__(StagedShape<NAIVE>::kThreads, AGOQ_RSTAGED_MIN_CTAS)
+reduce_shards_staged_kernel(
+    const uint8_t *__restrict__ shards, const float *__restrict__ shard_scales, int W,
+    int64_t shard_bytes, int64_t scale_stride, int nblocks, uint4 *__restrict__ out,
+    float *__restrict__ out_scales, unsigned long long *__restrict__ naive_count) {
+    using namespace gemm;
+    using Sh = StagedShape<NAIVE>;
+    constexpr int kStWarps = Sh::kWarps, kStTile = Sh::kTile;
+    constexpr int kStCodeBytes = Sh::kCodeBytes, kStScaleBytes = Sh::kScaleBytes;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint8_t *codes = smem;
+    float *scl = reinterpret_cast<float *>(smem + (size_t)kStStages * kStCodeBytes);
+    uint64_t *full =
+        reinterpret_cast<uint64_t *>(smem + (size_t)kStStages * (kStCodeBytes + kStScaleBytes));
+    uint64_t *empty = full + kStStages;
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kStWarps);
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
+    __syncthreads();
+    pdl_wait_and_release();
+    volatile int *abort = &abort_flag;
+    const int ntiles = (nblocks + kStTile - 1) / kStTile;
+
+    if (warp == kStWarps) {
+        // producer: one lane issues every copy
+        if (lane == 0) {
+            uint32_t issued = 0;
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+                const int b0 = tile * kStTile;
+                const int nb = nblocks - b0 < kStTile ? nblocks - b0 : kStTile;
+                const uint8_t *src_c = shards + (int64_t)b0 * 128;
+                const float *src_s = shard_scales + b0;
+                for (int r0 = 0; r0 < W; r0 += kStShards) {
+                    const int k = W - r0 < kStShards ? W - r0 : kStShards;
+                    if (issued >= (uint32_t)kStStages &&
+                        !wait_bar(&empty[stage], phase ^ 1u, abort, &g_reduce_status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_expect_tx(&full[stage], (uint32_t)(k * nb) * (128u + 4u));
+                    for (int j = 0; j < k; ++j) {
+                        bulk_g2s(codes + (size_t)stage * kStCodeBytes + (size_t)j * kStTile * 128,
+                                 src_c + (int64_t)(r0 + j) * shard_bytes, (uint32_t)nb * 128u,
+                                 &full[stage]);
+                        bulk_g2s(scl + ((size_t)stage * kStShards + j) * kStTile,
+                                 src_s + (int64_t)(r0 + j) * scale_stride, (uint32_t)nb * 4u,
+                                 &full[stage]);
+                    }
+                    ++issued;
+                    if (++stage == kStStages) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            // copies still in flight land before the CTA may exit
+            const uint32_t first = issued > (uint32_t)kStStages ? issued - kStStages : 0u;
+            for (uint32_t j = first; j < issued; ++j)
+                wait_bar(&full[j % kStStages], (j / kStStages) & 1u, abort, &g_reduce_status, true);
+        }
+        return;
+    }
+
+    // consumers
+    const int oct = lane >> 3, t8 = lane & 7;
+    const int lb = warp * 4 + oct;   // the lane's block within a tile
+    int stage = 0;
+    uint32_t phase = 0;
+    unsigned long long overflowed = 0;
+    bool ok = true;
+    for (int tile = blockIdx.x; ok && tile < ntiles; tile += gridDim.x) {
+        const int blk = tile * kStTile + lb;
+        ReduceLane<NAIVE> st;
+        st.clear();
+        for (int r0 = 0; r0 < W; r0 += kStShards) {
+            const int k = W - r0 < kStShards ? W - r0 : kStShards;
+            if (!warp_wait(&full[stage], phase, abort, &g_reduce_status, AGOQ_RSTAGED_HINT)) {
+                ok = false;
+                break;
+            }
+            mbar_try_wait(&full[stage], phase, 0);   // each lane observes the completed phase
+            const uint8_t *cs = codes + (size_t)stage * kStCodeBytes + (size_t)(warp * 32 + lane) * 16;
+            const float *ss = scl + (size_t)stage * kStShards * kStTile + lb;
+            uint4 c[kStShards];
+            float sc[kStShards];
+#pragma unroll
+            for (int j = 0; j < kStShards; ++j) {
+                if (j < k) {
+                    c[j] = *reinterpret_cast<const uint4 *>(cs + (size_t)j * kStTile * 128);
+                    sc[j] = ss[j * kStTile];
+                }
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[stage]);
+            if (++stage == kStStages) {
+                stage = 0;
+                phase ^= 1u;
+            }
+#pragma unroll
+            for (int j = 0; j < kStShards; ++j)
+                if (j < k) st.add_shard(c[j], sc[j], r0 + j);
+        }
+        if (!ok) break;
+        st.finish(blk < nblocks, out + (size_t)(unsigned)blk * 8 + t8, out_scales + blk, t8 == 0,
+                  overflowed);
+    }
+    if constexpr (NAIVE) flush_count(overflowed, naive_count);
 }
 
 template <typename K>
@@ -459,6 +681,58 @@ cudaError_t launch_grad_accum(void *master, float *master_scales, const void *gr
     }
 }
 
+namespace {
+// The staged reduce (the caller has zeroed naive_count); nblocks a multiple of 4.
+cudaError_t launch_reduce_staged(const void *shards, const float *shard_scales, int W, int64_t n,
+                                 void *out, float *out_scales, unsigned long long *naive_count,
+                                 cudaStream_t st) {
+    constexpr int64_t kMaxLaunchBlocks = int64_t(1) << 30;
+    static bool smem_set[2][kMaxDevices];
+    static int cache[2][kMaxDevices];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices) dev = 0;
+    const int which = naive_count ? 1 : 0;
+    auto kernel = naive_count ? reduce_shards_staged_kernel<true> : reduce_shards_staged_kernel<false>;
+    const int threads = naive_count ? StagedShape<true>::kThreads : StagedShape<false>::kThreads;
+    const int tile = naive_count ? StagedShape<true>::kTile : StagedShape<false>::kTile;
+    const size_t smem = naive_count ? StagedShape<true>::kSmem : StagedShape<false>::kSmem;
+    if (!smem_set[which][dev]) {
+        cudaError_t e =
+            cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        smem_set[which][dev] = true;
+    }
+    const int per_sm = resident_per_sm(kernel, threads, smem, cache[which]);
+    const int64_t nb_all = n / kBlock;
+    for (int64_t b0 = 0; b0 < nb_all; b0 += kMaxLaunchBlocks) {
+        const int64_t nb = nb_all - b0 < kMaxLaunchBlocks ? nb_all - b0 : kMaxLaunchBlocks;
+        const int64_t tiles = (nb + tile - 1) / tile;
+        int64_t grid = (int64_t)sm_count() * per_sm;
+        if (tiles < grid) grid = tiles;
+        const cudaError_t e = launch_pdl(
+            kernel, (int)grid, threads, smem, st, static_cast<const uint8_t *>(shards) + b0 * 128,
+            shard_scales + b0, W, n, nb_all, (int)nb, static_cast<uint4 *>(out) + b0 * 8,
+            out_scales + b0, naive_count);
+        if (e != cudaSuccess) return e;
+    }
+    return cudaSuccess;
+}
+}  // namespace
+
+cudaError_t read_and_clear_reduce_status(unsigned *status) {
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_reduce_status, sizeof v);
+    if (e != cudaSuccess) return e;
+    if (v) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_reduce_status, &zero, sizeof zero);
+        if (e != cudaSuccess) return e;
+    }
+    *status = v;
+    return cudaSuccess;
+}
+
 cudaError_t launch_reduce_shards(const void *shards, const float *shard_scales, int W, int64_t n,
                                  void *out, float *out_scales, unsigned long long *naive_count,
                                  cudaStream_t st) {
@@ -470,6 +744,9 @@ cudaError_t launch_reduce_shards(const void *shards, const float *shard_scales, 
         cudaError_t e = cudaMemsetAsync(naive_count, 0, sizeof(unsigned long long), st);
         if (e != cudaSuccess) return e;
     }
+    if (AGOQ_REDUCE_STAGED && nb_all % 4 == 0 &&
+        reinterpret_cast<uintptr_t>(shard_scales) % 16 == 0)
+        return launch_reduce_staged(shards, shard_scales, W, n, out, out_scales, naive_count, st);
     static int cache_count[kMaxDevices], cache_plain[kMaxDevices];
     auto kc = reduce_shards_kernel<true, AGOQ_REDUCE_COUNT_RUNROLL>;
     auto kp = reduce_shards_kernel<false, kRUnroll>;

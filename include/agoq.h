@@ -187,6 +187,9 @@ agoq_status agoq_grad_accum_fp8_mid(void *master_e4m3, float *master_scales,
  *     naive FP8 all-reduce -- the W FP8 values summed directly in rank order,
  *     the running sum rounded back to E4M3 after each add -- exceeds 448.
  *     The library zeroes it on `stream` before the reduce.
+ * When shard_scales is 16-byte aligned and n/128 is a multiple of 4, the
+ * reduce streams the shards through shared memory with time-limited pipeline
+ * waits (see agoq_device_status); the results are the same either way.
  */
 agoq_status agoq_reduce_fp8_shards(const void *shards_e4m3, const float *shard_scales, int W,
                                    int64_t n, void *out_e4m3, float *out_scales,
@@ -276,8 +279,9 @@ agoq_status agoq_dbca_pp_bits(int stages, int microbatches, int base_bits, int *
 /*
  * Synchronise `stream`, then read and clear the library's device-side status
  * words for the current device.  Returns AGOQ_ERR_TIMEOUT if a pipeline wait
- * of a GEMM (agoq_wgrad_gemm_int4*, agoq_fwd_gemm_quant) exceeded its time
- * limit since the last call (that GEMM's output is then incomplete),
+ * of a GEMM (agoq_wgrad_gemm_int4*, agoq_fwd_gemm_quant) or of the staged
+ * shard reduce (agoq_reduce_fp8_shards) exceeded its time limit since the last
+ * call (that call's output is then incomplete),
  * AGOQ_ERR_CUDA if the synchronisation failed, else AGOQ_OK.
  */
 agoq_status agoq_device_status(void *stream);

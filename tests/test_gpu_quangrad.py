@@ -122,8 +122,10 @@ def _oracle_shards(oracle, W, n, seed=3):
 
 
 @pytest.mark.parametrize("W", [1, 2, 3, 8, 13, 64])
-@pytest.mark.parametrize("nblocks", [1, 5, 37, 600])
+@pytest.mark.parametrize("nblocks", [1, 4, 5, 36, 37, 600, 1028])
 def test_reduce_parity(oracle, W, nblocks):
+    """Block counts that are multiples of 4 take the shared-memory staged kernel
+    (36 and 1028: a ragged last tile), the others the register-staged one."""
     n = nblocks * 128
     sh, ss = _oracle_shards(oracle, W, n, seed=3 + W)
     og = G.Guarded(n, torch.uint8)
@@ -138,6 +140,28 @@ def test_reduce_parity(oracle, W, nblocks):
     # without the count: same codes
     o2, s2 = agoq.agoq_reduce_fp8_shards(G.dev(sh), G.dev(ss), W, n)
     assert np.array_equal(o2.cpu().numpy(), wc)
+
+
+@pytest.mark.parametrize("W,nblocks", [(8, 600), (3, 36), (64, 100)])
+def test_reduce_staged_and_register_kernels_agree(oracle, W, nblocks):
+    """The same shards through both reduce kernels: scales on a 16-byte boundary
+    take the staged kernel (bulk copies), the same scales 4 bytes off it the
+    register-staged kernel; both equal the oracle, counts included."""
+    n = nblocks * 128
+    sh, ss = _oracle_shards(oracle, W, n, seed=40 + W)
+    wc, ws, wcnt = oracle.reduce_fp8_shards(sh, ss, W, n)
+    d_sh = G.dev(sh)
+    room = torch.zeros(ss.size + 4, dtype=torch.float32, device="cuda")
+    for off in (0, 1):
+        ss_dev = room[off:off + ss.size]
+        ss_dev.copy_(G.dev(ss))
+        assert (ss_dev.data_ptr() % 16 == 0) == (off == 0)
+        cnt = torch.full((1,), -1, dtype=torch.int64, device="cuda")
+        o, os_ = agoq.agoq_reduce_fp8_shards(d_sh, ss_dev, W, n, naive_overflow_count=cnt)
+        assert np.array_equal(o.cpu().numpy(), wc)
+        assert np.array_equal(os_.cpu().numpy().view(np.uint32), ws.view(np.uint32))
+        assert int(cnt.item()) == wcnt
+    agoq.agoq_device_status()   # raises if a pipeline wait timed out
 
 
 def test_reduce_edge_cases(oracle):
