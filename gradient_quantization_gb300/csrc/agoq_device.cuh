@@ -24,6 +24,15 @@ __device__ __forceinline__ void pdl_wait_and_release() {
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
+// Ask the L2 to start fetching [p, p + bytes) (p 16-byte aligned, bytes a
+// multiple of 16).  A hint with no effect on results: the L2 is the point of
+// coherence, so a line fetched before a preceding grid writes it is updated by
+// that write.  Kernels issue it for their first inputs before
+// pdl_wait_and_release, so that the fetch overlaps the preceding grid's tail.
+__device__ __forceinline__ void prefetch_l2(const void *p, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
 // ---- BF16 ------------------------------------------------------------------
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

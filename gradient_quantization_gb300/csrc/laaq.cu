@@ -42,6 +42,11 @@
 #ifndef AGOQ_SILU_FAST_EXP
 #define AGOQ_SILU_FAST_EXP 1
 #endif
+// Block groups per warp whose inputs are prefetched into L2 before the wait on
+// the preceding grid (0: none).
+#ifndef AGOQ_PDL_PREFETCH
+#define AGOQ_PDL_PREFETCH 1
+#endif
 #ifndef AGOQ_QUANT_PIPELINE
 #define AGOQ_QUANT_PIPELINE 1
 #endif
@@ -130,6 +135,21 @@ template <int BITS, int UNROLL>
 __global__ void __launch_bounds__(kThreads, AGOQ_QUANT_MIN_CTAS)
 laaq_quant_kernel(const uint4 *__restrict__ x, uint32_t *__restrict__ codes,
                   float *__restrict__ scales, int nblocks) {
+    if constexpr (AGOQ_PDL_PREFETCH > 0) {
+        // this warp's first groups of 4 * UNROLL blocks (256 bytes each)
+        const int w0 = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+        const int nw = (int)((gridDim.x * blockDim.x) >> 5);
+        if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+            for (int g = 0; g < AGOQ_PDL_PREFETCH; ++g) {
+                const int b0 = (w0 + g * nw) * (4 * UNROLL);
+                if (b0 < nblocks) {
+                    const int nb = nblocks - b0 < 4 * UNROLL ? nblocks - b0 : 4 * UNROLL;
+                    prefetch_l2(x + (size_t)(unsigned)b0 * 16, (uint32_t)nb * 256u);
+                }
+            }
+        }
+    }
     pdl_wait_and_release();
     constexpr int kWords = 4 * BITS;
     constexpr int kQmax = (1 << (BITS - 1)) - 1;
@@ -257,6 +277,24 @@ __global__ void __launch_bounds__(kThreads, AGOQ_DEQUANT_MIN_CTAS) laaq_dequant_
                                                                 const float *__restrict__ scales,
                                                                 uint4 *__restrict__ y,
                                                                 int nblocks) {
+    if constexpr (AGOQ_PDL_PREFETCH > 0) {
+        // codes and scales of this warp's first groups of 4 * UNROLL blocks
+        const int w0 = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+        const int nw = (int)((gridDim.x * blockDim.x) >> 5);
+        if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+            for (int g = 0; g < AGOQ_PDL_PREFETCH; ++g) {
+                const int b0 = (w0 + g * nw) * (4 * UNROLL);
+                if (b0 < nblocks) {
+                    const int nb = nblocks - b0 < 4 * UNROLL ? nblocks - b0 : 4 * UNROLL;
+                    prefetch_l2(codes + (size_t)(unsigned)b0 * (4 * BITS), (uint32_t)nb * (16u * BITS));
+                    // scales need only 4-byte alignment: prefetched when 16-byte aligned
+                    if (nb % 4 == 0 && (reinterpret_cast<uintptr_t>(scales + b0) & 15u) == 0)
+                        prefetch_l2(scales + b0, (uint32_t)nb * 4u);
+                }
+            }
+        }
+    }
     pdl_wait_and_release();
     const int lane = threadIdx.x & 31;
     const int oct = lane >> 3, j = lane & 7;
