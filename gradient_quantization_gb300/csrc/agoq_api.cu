@@ -293,12 +293,13 @@ agoq_status agoq_test_wait_timeout(int64_t limit_cycles, void *stream) {
 }
 
 agoq_status agoq_device_status(void *stream) {
-    unsigned status = 0, fwd = 0, red = 0;
+    unsigned status = 0, fwd = 0, red = 0, rms = 0;
     if (agoq::read_and_clear_device_status(agoq::as_stream(stream), &status) != cudaSuccess ||
         agoq::read_and_clear_fwd_status(&fwd) != cudaSuccess ||
-        agoq::read_and_clear_reduce_status(&red) != cudaSuccess)
+        agoq::read_and_clear_reduce_status(&red) != cudaSuccess ||
+        agoq::read_and_clear_rmsnorm_status(&rms) != cudaSuccess)
         return AGOQ_ERR_CUDA;
-    return (status || fwd || red) ? AGOQ_ERR_TIMEOUT : AGOQ_OK;
+    return (status || fwd || red || rms) ? AGOQ_ERR_TIMEOUT : AGOQ_OK;
 }
 
 }  // extern "C"

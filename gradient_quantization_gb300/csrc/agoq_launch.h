@@ -76,6 +76,8 @@ cudaError_t launch_wait_timeout_probe(long long limit_cycles, cudaStream_t st);
 cudaError_t read_and_clear_fwd_status(unsigned *status);
 // The same for the staged FP8 shard reduce.
 cudaError_t read_and_clear_reduce_status(unsigned *status);
+// The same for the TMA-staged RMSNorm weight-gradient kernel.
+cudaError_t read_and_clear_rmsnorm_status(unsigned *status);
 // Synchronise `st`, read and clear the device status word (0 = no timeout).
 cudaError_t read_and_clear_device_status(cudaStream_t st, unsigned *status);
 

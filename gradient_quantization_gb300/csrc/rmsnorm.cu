@@ -26,6 +26,7 @@
 
 #include "agoq_device.cuh"
 #include "agoq_launch.h"
+#include "gemm_common.cuh"
 
 namespace agoq {
 namespace {
@@ -43,6 +44,24 @@ constexpr int kDwCols = 128;                     // columns per slice (16 lanes 
 #define AGOQ_DW_UNROLL 4
 #endif
 constexpr int kDwUnroll = AGOQ_DW_UNROLL;        // rows in flight per half warp
+// dw through TMA-staged row tiles (when T, H and the alignments allow it):
+// kDwTileRows rows of a 128-column slice per stage, kDwStagesTma stages.
+#ifndef AGOQ_DW_TMA
+#define AGOQ_DW_TMA 1
+#endif
+#ifndef AGOQ_DW_TMA_STAGES
+#define AGOQ_DW_TMA_STAGES 8
+#endif
+#ifndef AGOQ_DW_TMA_CLUSTER
+#define AGOQ_DW_TMA_CLUSTER 8
+#endif
+constexpr int kDwTileRows = 32;
+constexpr int kDwTmaCluster = AGOQ_DW_TMA_CLUSTER;   // CTAs per slice (cluster along y)
+constexpr int kDwStagesTma = AGOQ_DW_TMA_STAGES;
+#ifndef AGOQ_DW_TMA_MIN_CTAS
+#define AGOQ_DW_TMA_MIN_CTAS 2
+#endif
+constexpr int kDwTmaThreads = kDwThreads + 32;   // 8 consumer warps + 1 producer warp
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     uint4 v;
@@ -401,12 +420,199 @@ __global__ void __launch_bounds__(kDwThreads, 2) rmsnorm_dw_kernel(
     cluster.sync();   // the other CTAs' csum stays alive until rank 0 has read it
 }
 
+__device__ unsigned g_rms_status;
+
+// Shared-memory layout of one stage of the TMA dw kernel (offsets 128-byte
+// aligned): dy [32][128] BF16, the slice's block records [32][16 BITS] bytes,
+// the scales of the 4-block group holding the slice [32][4], rstd [32].
+template <int BITS>
+struct DwTmaStage {
+    static constexpr int kDy = 0;
+    static constexpr int kCodes = kDwTileRows * 256;
+    static constexpr int kScales = kCodes + kDwTileRows * 16 * BITS;
+    static constexpr int kRstd = kScales + kDwTileRows * 16;
+    static constexpr int kBytes = kRstd + kDwTileRows * 4;
+    static constexpr uint32_t kTx = kBytes;
+    static_assert(kBytes % 128 == 0, "stages stay 128-byte aligned");
+};
+
+// dw[i] = sum_t dy[t][i] * xh[t][i] * r_t with the rows streamed by TMA: a
+// cluster of 8 CTAs per 128-column slice; CTA rank q takes the contiguous
+// 32-row tiles [q S/8, (q+1) S/8) of the S = T/32 tiles.  One producer lane
+// loads each tile (dy, codes and scales as 2-D tensor boxes, rstd as one bulk
+// copy) into a kDwStagesTma-deep ring; half warp h of the CTA sums rows h and
+// h + 16 of every tile, in row order, for its 8 columns (so each column's sum
+// is a chain of T/128 rows per half warp, then the 16 half warps and the 8
+// CTAs in fixed order, as in rmsnorm_dw_kernel).  Waits are time-limited: on
+// expiry g_rms_status records a timeout, the CTA stops (still joining the
+// cluster barriers) and the producer waits for its copies in flight.
+template <int BITS>
+__global__ void __launch_bounds__(kDwTmaThreads, AGOQ_DW_TMA_MIN_CTAS) rmsnorm_dw_tma_kernel(
+    const __grid_constant__ CUtensorMap map_dy, const __grid_constant__ CUtensorMap map_codes,
+    const __grid_constant__ CUtensorMap map_scales, const float *__restrict__ rstd, int64_t T,
+    float *__restrict__ dw) {
+    using namespace gemm;
+    using St = DwTmaStage<BITS>;
+    constexpr int kHalves = 2 * (kDwThreads / 32);                 // 16 consumer half warps
+    extern __shared__ __align__(128) uint8_t dwt_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(dwt_raw) + 127) & ~static_cast<uintptr_t>(127));
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kDwStagesTma * St::kBytes);
+    uint64_t *empty = full + kDwStagesTma;
+    __shared__ float part[kHalves][kDwCols];
+    __shared__ float csum[kDwCols];
+    __shared__ int abort_flag;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int rank = (int)cluster.block_rank();
+    const int b = blockIdx.x;                                       // slice = block b of each row
+    const int64_t tiles = T / kDwTileRows;
+    const int64_t tile0 = tiles * rank / kDwTmaCluster, tile1 = tiles * (rank + 1) / kDwTmaCluster;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kDwStagesTma; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kDwThreads / 32);
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_wait_and_release();
+    volatile int *abort = &abort_flag;
+    float acc[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = 0.0f;
+    const int half = lane >> 4, l16 = lane & 15, hw = 2 * warp + half;
+
+    if (warp == kDwThreads / 32) {
+        if (lane == 0) {
+            uint32_t it = 0;
+            for (int64_t tl = tile0; tl < tile1; ++tl, ++it) {
+                const int s = it % kDwStagesTma;
+                const uint32_t ph = (it / kDwStagesTma) & 1u;
+                if (it >= (uint32_t)kDwStagesTma &&
+                    !wait_bar(&empty[s], ph ^ 1u, abort, &g_rms_status))
+                    break;
+                uint8_t *st = smem + (size_t)s * St::kBytes;
+                const int y = (int)(tl * kDwTileRows);
+                mbar_expect_tx(&full[s], St::kTx);
+                tma_load_2d(st + St::kDy, &map_dy, &full[s], b * kDwCols, y);
+                tma_load_2d(st + St::kCodes, &map_codes, &full[s], b * 16 * BITS, y);
+                tma_load_2d(st + St::kScales, &map_scales, &full[s], b & ~3, y);
+                asm volatile(
+                    "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], "
+                    "%2, [%3];" ::"r"(smem_u32(st + St::kRstd)),
+                    "l"(rstd + (int64_t)y), "r"(kDwTileRows * 4), "r"(smem_u32(&full[s]))
+                    : "memory");
+            }
+            // copies still in flight land before the CTA may exit
+            const uint32_t first = it > (uint32_t)kDwStagesTma ? it - kDwStagesTma : 0u;
+            for (uint32_t j = first; j < it; ++j)
+                wait_bar(&full[j % kDwStagesTma], (j / kDwStagesTma) & 1u, abort, &g_rms_status,
+                         true);
+        }
+    } else {
+        uint32_t it = 0;
+        for (int64_t tl = tile0; tl < tile1; ++tl, ++it) {
+            const int s = it % kDwStagesTma;
+            if (!warp_wait(&full[s], (it / kDwStagesTma) & 1u, abort, &g_rms_status)) break;
+            mbar_try_wait(&full[s], (it / kDwStagesTma) & 1u, 0);   // each lane's own acquire
+            const uint8_t *st = smem + (size_t)s * St::kBytes;
+#pragma unroll
+            for (int rr = 0; rr < 2; ++rr) {
+                const int row = hw + kHalves * rr;                   // 0 .. 31
+                const float sc = reinterpret_cast<const float *>(st + St::kScales)[4 * row + (b & 3)];
+                const float r = reinterpret_cast<const float *>(st + St::kRstd)[row];
+                uint32_t lo, hi;
+                chunk_from_smem<BITS>(
+                    reinterpret_cast<const uint32_t *>(st + St::kCodes + row * 16 * BITS), l16, lo, hi);
+                const uint4 xh = dequantize_chunk<BITS>(lo, hi, sc);
+                const uint4 d = reinterpret_cast<const uint4 *>(st + St::kDy + row * 256)[l16];
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    acc[k] = __fadd_rn(acc[k], __fmul_rn(__fmul_rn(elem(d, k), elem(xh, k)), r));
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
+    }
+    if (warp < kDwThreads / 32) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) part[hw][8 * l16 + k] = acc[k];
+    }
+    __syncthreads();
+    if (threadIdx.x < kDwCols) {
+        float v = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kHalves; ++i) v = __fadd_rn(v, part[i][threadIdx.x]);
+        csum[threadIdx.x] = v;
+    }
+    cluster.sync();
+    if (rank == 0 && threadIdx.x < kDwCols) {
+        float v = 0.0f;
+        for (int q = 0; q < kDwTmaCluster; ++q)
+            v = __fadd_rn(v, cluster.map_shared_rank(csum, q)[threadIdx.x]);
+        dw[blockIdx.x * kDwCols + threadIdx.x] = v;
+    }
+    cluster.sync();   // the other CTAs' csum stays alive until rank 0 has read it
+}
+
 template <typename K>
 int rows_grid(K kernel, int64_t T) {
     static int per_sm[kMaxDevices];
     int64_t g = (int64_t)sm_count() * resident_per_sm(kernel, kRowThreads, 0, per_sm);
     if (T < g) g = T;
     return (int)(g > 0 ? g : 1);
+}
+
+// dw through rmsnorm_dw_tma_kernel: T a multiple of 32, H of 512, scales and
+// rstd 16-byte aligned (the caller has checked).
+template <int BITS>
+cudaError_t launch_dw_tma(const void *codes, const float *scales, const void *dy, const float *rstd,
+                          int64_t T, int H, float *dw, cudaStream_t st) {
+    using namespace gemm;
+    using Stg = DwTmaStage<BITS>;
+    const int nb = H / kBlock;
+    CUtensorMap m_dy, m_codes, m_scales;
+    if (!encode_2d(&m_dy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dy, (uint64_t)H, (uint64_t)T,
+                   (uint64_t)H * 2, kDwCols, kDwTileRows, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&m_codes, CU_TENSOR_MAP_DATA_TYPE_UINT8, codes, (uint64_t)nb * 16 * BITS,
+                   (uint64_t)T, (uint64_t)nb * 16 * BITS, 16 * BITS, kDwTileRows,
+                   CU_TENSOR_MAP_SWIZZLE_NONE) ||
+        !encode_2d(&m_scales, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, scales, (uint64_t)nb, (uint64_t)T,
+                   (uint64_t)nb * 4, 4, kDwTileRows, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    constexpr size_t smem = (size_t)kDwStagesTma * (Stg::kBytes + 16) + 128;
+    static bool attr_set[kMaxDevices];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev >= 0 && dev < kMaxDevices && !attr_set[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(rmsnorm_dw_tma_kernel<BITS>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (kDwTmaCluster > 8) {
+            e = cudaFuncSetAttribute(rmsnorm_dw_tma_kernel<BITS>,
+                                     cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+            if (e != cudaSuccess) return e;
+        }
+        attr_set[dev] = true;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(H / kDwCols, kDwTmaCluster, 1);
+    cfg.blockDim = dim3(kDwTmaThreads, 1, 1);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = kDwTmaCluster;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, rmsnorm_dw_tma_kernel<BITS>, m_dy, m_codes, m_scales, rstd, T,
+                              dw);
 }
 
 template <int BITS>
@@ -441,6 +647,10 @@ cudaError_t rmsnorm_bits(const void *codes, const float *scales, const void *dy,
                        static_cast<uint4 *>(dx), rstd);
     }
     if (e != cudaSuccess || !dw) return e;
+    if (AGOQ_DW_TMA && T % kDwTileRows == 0 && T / kDwTileRows <= INT32_MAX / kDwTileRows &&
+        H % 512 == 0 && reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
+        reinterpret_cast<uintptr_t>(rstd) % 16 == 0)
+        return launch_dw_tma<BITS>(codes, scales, dy, rstd, T, H, dw, st);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(H / kDwCols, kDwCluster, 1);
     cfg.blockDim = dim3(kDwThreads, 1, 1);
@@ -460,6 +670,19 @@ cudaError_t rmsnorm_bits(const void *codes, const float *scales, const void *dy,
 }
 
 }  // namespace
+
+cudaError_t read_and_clear_rmsnorm_status(unsigned *status) {
+    unsigned v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_rms_status, sizeof v);
+    if (e != cudaSuccess) return e;
+    if (v) {
+        const unsigned zero = 0;
+        e = cudaMemcpyToSymbol(g_rms_status, &zero, sizeof zero);
+        if (e != cudaSuccess) return e;
+    }
+    *status = v;
+    return cudaSuccess;
+}
 
 cudaError_t launch_rmsnorm_backward(const void *codes, const float *scales, const void *dy,
                                     const void *w, int64_t T, int64_t H, int bits, float eps,

@@ -136,7 +136,10 @@ agoq_status agoq_silu_backward(const void *codes, const float *scales, const voi
  * plus the output rounding.  H must be a multiple of 256 and at
  * most 8192, eps finite and >= 0 (AGOQ_ERR_SHAPE otherwise).  The input is read
  * once for dx and rstd; dw reads the codes and dy a second time.  Outputs must
- * not overlap the inputs or each other.
+ * not overlap the inputs or each other.  When T is a multiple of 32, H of 512,
+ * and scales and rstd are 16-byte aligned, dw streams its rows through shared
+ * memory by TMA with time-limited pipeline waits (see agoq_device_status); the
+ * bound above holds either way.
  */
 agoq_status agoq_rmsnorm_backward(const void *codes, const float *scales, const void *dy_bf16,
                                   const void *w_bf16, int64_t T, int64_t H, int bits, float eps,
@@ -279,9 +282,10 @@ agoq_status agoq_dbca_pp_bits(int stages, int microbatches, int base_bits, int *
 /*
  * Synchronise `stream`, then read and clear the library's device-side status
  * words for the current device.  Returns AGOQ_ERR_TIMEOUT if a pipeline wait
- * of a GEMM (agoq_wgrad_gemm_int4*, agoq_fwd_gemm_quant) or of the staged
- * shard reduce (agoq_reduce_fp8_shards) exceeded its time limit since the last
- * call (that call's output is then incomplete),
+ * of a GEMM (agoq_wgrad_gemm_int4*, agoq_fwd_gemm_quant), of the staged
+ * shard reduce (agoq_reduce_fp8_shards) or of the staged RMSNorm dw
+ * (agoq_rmsnorm_backward) exceeded its time limit since the last call (that
+ * call's output is then incomplete),
  * AGOQ_ERR_CUDA if the synchronisation failed, else AGOQ_OK.
  */
 agoq_status agoq_device_status(void *stream);

@@ -68,8 +68,12 @@ def _run(codes, scales, dy, w, T, H, bits, eps, want_dw=True):
 
 
 @pytest.mark.parametrize("bits", [4, 5, 6, 8])
-@pytest.mark.parametrize("T,H", [(1, 256), (7, 512), (33, 4096), (5, 5120), (70, 8192)])
+@pytest.mark.parametrize("T,H", [(1, 256), (7, 512), (33, 4096), (5, 5120), (70, 8192),
+                                 (32, 4096), (64, 512), (96, 5120), (320, 8192)])
 def test_rmsnorm_backward_parity(oracle, bits, T, H):
+    """T a multiple of 32 with H a multiple of 512 takes the TMA-staged dw
+    kernel (32 and 64 rows: some CTAs of a cluster get no tile); the other
+    shapes the register-buffered one."""
     eps = 1e-6
     codes, scales, dy, w = _inputs(oracle, T, H, bits, seed=T * 10 + bits)
     got = _run(codes, scales, dy, w, T, H, bits, eps)
@@ -115,6 +119,31 @@ def test_rmsnorm_backward_full_size(oracle):
     w = synthetic.bf16_bits_from_f32((1 + 0.1 * rng.standard_normal(H)).astype(np.float32))
     got = _run(c_np, s_np, dy, w, T, H, bits, eps)
     _check(oracle, c_np, s_np, dy, w, T, H, bits, eps, got)
+
+
+def test_rmsnorm_dw_tma_and_register_paths(oracle):
+    """The same rows through both dw kernels: rstd on a 16-byte boundary takes
+    the TMA-staged kernel, rstd 4 bytes off it the register-buffered one.  dx
+    and rstd come from the same row kernel (equal bits); both dw are within the
+    bound."""
+    T, H, bits, eps = 256, 1024, 5, 1e-6
+    codes, scales, dy, w = _inputs(oracle, T, H, bits, seed=44)
+    outs = []
+    for off in (0, 1):
+        room = torch.zeros(T + 4, dtype=torch.float32, device="cuda")
+        rstd = room[off:off + T]
+        assert (rstd.data_ptr() % 16 == 0) == (off == 0)
+        dx = torch.empty(T * H, dtype=torch.bfloat16, device="cuda")
+        dw = torch.empty(H, dtype=torch.float32, device="cuda")
+        agoq.agoq_rmsnorm_backward(G.dev(codes), G.dev(scales), G.dev_bf16(dy), G.dev_bf16(w), T,
+                                   H, bits, eps, dx, rstd, dw)
+        torch.cuda.synchronize()
+        got = (G.host_bits_bf16(dx), rstd.cpu().numpy().astype(np.float64),
+               dw.cpu().numpy().astype(np.float64))
+        _check(oracle, codes, scales, dy, w, T, H, bits, eps, got)
+        outs.append(got)
+    assert np.array_equal(outs[0][0], outs[1][0]) and np.array_equal(outs[0][1], outs[1][1])
+    agoq.agoq_device_status()   # raises if a pipeline wait timed out
 
 
 def test_rmsnorm_backward_guard_bands(oracle):
