@@ -216,6 +216,41 @@ __device__ __forceinline__ void chunk_from_smem(const uint32_t *rowcodes, int c,
 
 constexpr int kWarpRowThreads = 128;             // 4 warps per CTA, one row per warp at a time
 
+// 1: the row kernel forms the BF16 x BF16 products (xh^2, xh w, dy w) with the
+// mixed-precision fma.rn.f32.bf16 on the BF16 halves directly instead of
+// widening both operands first.  Each such product is exact in binary32, so
+// the sums and dx are the same bits either way.
+#ifndef AGOQ_RMS_MIXED
+#define AGOQ_RMS_MIXED 1
+#endif
+
+// d_k = fl(a_k * b_k + c_k) for the BF16 halves k = 0 (bits 0-15), 1 of a and b.
+__device__ __forceinline__ void fma_bf16x2_f32(uint32_t a, uint32_t b, float c0, float c1,
+                                               float &d0, float &d1) {
+    asm("{\n\t.reg .b16 al, ah, bl, bh;\n\tmov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+        "fma.rn.f32.bf16 %0, al, bl, %4;\n\tfma.rn.f32.bf16 %1, ah, bh, %5;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "r"(a), "r"(b), "f"(c0), "f"(c1));
+}
+
+// dw terms of one chunk: acc[k] += fl(fl(dy_k * xh_k) * r) for the 8 BF16
+// values of d (dy) and xh (the BF16 x BF16 product is exact in binary32).
+__device__ __forceinline__ void dw_accum8(float acc[8], const uint4 &d, const uint4 &xh, float r) {
+#if AGOQ_RMS_MIXED
+    const uint32_t dw4[4] = {d.x, d.y, d.z, d.w}, xw[4] = {xh.x, xh.y, xh.z, xh.w};
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        float q0, q1;
+        fma_bf16x2_f32(dw4[p], xw[p], -0.0f, -0.0f, q0, q1);
+        acc[2 * p] = __fadd_rn(acc[2 * p], __fmul_rn(q0, r));
+        acc[2 * p + 1] = __fadd_rn(acc[2 * p + 1], __fmul_rn(q1, r));
+    }
+#else
+#pragma unroll
+    for (int k = 0; k < 8; ++k) acc[k] = __fadd_rn(acc[k], __fmul_rn(__fmul_rn(elem(d, k), elem(xh, k)), r));
+#endif
+}
+
 // Shared-memory words of one warp's row stage: dy (H/8 x 16 B), the row's
 // codes (H*BITS/8 B, padded by 16 B so a 5/6-bit chunk read may touch the
 // next word) and its H/128 scales.
@@ -283,6 +318,9 @@ __global__ void __launch_bounds__(kWarpRowThreads) rmsnorm_backward_warp_rows_ke
         // Row sums in packed pairs with fused multiply-adds (a tolerance-
         // bounded result: fusing only removes roundings).
         uint64_t sxx2 = 0ull, sgx2 = 0ull;
+#if AGOQ_RMS_MIXED
+        float sxx0 = 0.0f, sxx1 = 0.0f;
+#endif
 #pragma unroll 4
         for (int k = 0; k < C; ++k) {
             const uint4 xh = xh_of(k);
@@ -292,13 +330,24 @@ __global__ void __launch_bounds__(kWarpRowThreads) rmsnorm_backward_warp_rows_ke
                            ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
+#if AGOQ_RMS_MIXED
+                // sxx += xh^2;  sgx += dy * (xh w): the same exact products as (dy w) xh
+                float v0, v1;
+                fma_bf16x2_f32(xw[p], xw[p], sxx0, sxx1, sxx0, sxx1);
+                fma_bf16x2_f32(xw[p], ww[p], -0.0f, -0.0f, v0, v1);
+                sgx2 = fma_f32x2(u32x2(dw4[p] << 16, dw4[p] & 0xFFFF0000u), f32x2(v0, v1), sgx2);
+#else
                 const uint64_t x2 = u32x2(xw[p] << 16, xw[p] & 0xFFFF0000u);
                 const uint64_t g2 = mul_f32x2(u32x2(dw4[p] << 16, dw4[p] & 0xFFFF0000u),
                                               u32x2(ww[p] << 16, ww[p] & 0xFFFF0000u));
                 sxx2 = fma_f32x2(x2, x2, sxx2);
                 sgx2 = fma_f32x2(g2, x2, sgx2);
+#endif
             }
         }
+#if AGOQ_RMS_MIXED
+        sxx2 = f32x2(sxx0, sxx1);
+#endif
         float sxx = __fadd_rn(lo_f32(sxx2), hi_f32(sxx2));
         float sgx = __fadd_rn(lo_f32(sgx2), hi_f32(sgx2));
 #pragma unroll
@@ -321,8 +370,14 @@ __global__ void __launch_bounds__(kWarpRowThreads) rmsnorm_backward_warp_rows_ke
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 const uint64_t x2 = u32x2(xw[p] << 16, xw[p] & 0xFFFF0000u);
+#if AGOQ_RMS_MIXED
+                float g0, g1;
+                fma_bf16x2_f32(dw4[p], ww[p], -0.0f, -0.0f, g0, g1);
+                const uint64_t g2 = f32x2(g0, g1);
+#else
                 const uint64_t g2 = mul_f32x2(u32x2(dw4[p] << 16, dw4[p] & 0xFFFF0000u),
                                               u32x2(ww[p] << 16, ww[p] & 0xFFFF0000u));
+#endif
                 // dx = r * g - xh * kk
                 const uint64_t d2 = fma_f32x2(r2, g2, mul_f32x2(x2, nkk2));
                 o[p] = pack_bf16x2(lo_f32(d2), hi_f32(d2));
@@ -395,9 +450,7 @@ __global__ void __launch_bounds__(kDwThreads, 2) rmsnorm_dw_kernel(
 #pragma unroll
         for (int u = 0; u < kDwUnroll; ++u) {
             const uint4 xh = dequantize_chunk<BITS>(cur.lo[u], cur.hi[u], cur.s[u]);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-                acc[k] = __fadd_rn(acc[k], __fmul_rn(__fmul_rn(elem(cur.d[u], k), elem(xh, k)), cur.r[u]));
+            dw_accum8(acc, cur.d[u], xh, cur.r[u]);
         }
         if (more) cur = nxt;
     }
@@ -528,9 +581,7 @@ __global__ void __launch_bounds__(kDwTmaThreads, AGOQ_DW_TMA_MIN_CTAS) rmsnorm_d
                     reinterpret_cast<const uint32_t *>(st + St::kCodes + row * 16 * BITS), l16, lo, hi);
                 const uint4 xh = dequantize_chunk<BITS>(lo, hi, sc);
                 const uint4 d = reinterpret_cast<const uint4 *>(st + St::kDy + row * 256)[l16];
-#pragma unroll
-                for (int k = 0; k < 8; ++k)
-                    acc[k] = __fadd_rn(acc[k], __fmul_rn(__fmul_rn(elem(d, k), elem(xh, k)), r));
+                dw_accum8(acc, d, xh, r);
             }
             __syncwarp();
             if (lane == 0) mbar_arrive(&empty[s]);
