@@ -131,6 +131,37 @@ def test_repeatable_and_stream_ordered(oracle):
     assert torch.equal(c1, c2) and torch.equal(s1, s2)
 
 
+def test_widths_on_two_streams_match_the_oracle(oracle):
+    """The bench's step layout: widths {4, 6} on one side stream and {5, 8} on
+    another, each quantizing then dequantizing its own buffers, forked from and
+    joined to the main stream; every output equals the oracle's."""
+    xbits = synthetic.laaq_activation_np(seed=5, tokens=96)
+    n = xbits.size
+    x = G.dev_bf16(xbits)
+    main = torch.cuda.current_stream()
+    side = [torch.cuda.Stream(), torch.cuda.Stream()]
+    out = {}
+    fork = torch.cuda.Event()
+    fork.record(main)
+    for st, widths in zip(side, ((4, 6), (5, 8))):
+        st.wait_event(fork)
+        with torch.cuda.stream(st):
+            for b in widths:
+                out[b] = agoq.agoq_quant_act(x, b)
+            for b in widths:
+                out[b] = out[b] + (agoq.agoq_dequant_act(out[b][0], out[b][1], n, b),)
+    for st in side:
+        join = torch.cuda.Event()
+        join.record(st)
+        main.wait_event(join)
+    torch.cuda.synchronize()
+    for b in WIDTHS:
+        want_c, want_s = oracle.quant_act(xbits.reshape(-1), b)
+        assert np.array_equal(out[b][0].cpu().numpy(), want_c)
+        assert np.array_equal(out[b][1].cpu().numpy().view(np.uint32), want_s.view(np.uint32))
+        assert np.array_equal(G.host_bits_bf16(out[b][2]), oracle.dequant_act(want_c, want_s, n, b))
+
+
 def test_errors_raise_and_touch_nothing():
     x = torch.zeros(200, dtype=torch.bfloat16, device="cuda")
     c = torch.full((64,), 7, dtype=torch.uint8, device="cuda")
