@@ -33,6 +33,24 @@
 #ifndef AGOQ_NAIVE_ROUND_CVT
 #define AGOQ_NAIVE_ROUND_CVT 1
 #endif
+// Shared-memory staged accumulation: 1 selects it when the master scales are
+// 16-byte aligned and the block count is a multiple of 4; consumer warps per
+// CTA, blocks per half warp and stage, ring stages, CTAs per SM.
+#ifndef AGOQ_ACCUM_STAGED
+#define AGOQ_ACCUM_STAGED 1
+#endif
+#ifndef AGOQ_ASTAGED_WARPS
+#define AGOQ_ASTAGED_WARPS 16
+#endif
+#ifndef AGOQ_ASTAGED_REP
+#define AGOQ_ASTAGED_REP 3
+#endif
+#ifndef AGOQ_ASTAGED_STAGES
+#define AGOQ_ASTAGED_STAGES 3
+#endif
+#ifndef AGOQ_ASTAGED_MIN_CTAS
+#define AGOQ_ASTAGED_MIN_CTAS 1
+#endif
 #ifndef AGOQ_ACCUM_PIPELINE
 #define AGOQ_ACCUM_PIPELINE 0
 #endif
@@ -179,6 +197,30 @@ __device__ __forceinline__ void add_in_format(float t[8], const uint4 &g) {
     }
 }
 
+// One lane's 8 elements of a block (every lane of the warp calls it, a half
+// warp per block): t = the master's products plus the gradient in the MID
+// format, the block's new scale (returned in snew) and the 8 new codes.
+template <int MID>
+__device__ __forceinline__ uint2 accum_block(const uint2 &mc, const uint4 &g, float s, float &snew) {
+    const float gv[8] = {bf16_lo(g.x), bf16_hi(g.x), bf16_lo(g.y), bf16_hi(g.y),
+                         bf16_lo(g.z), bf16_hi(g.z), bf16_lo(g.w), bf16_hi(g.w)};
+    float t[8];
+    decode_mul4(mc.x, s, t);
+    decode_mul4(mc.y, s, t + 4);
+    float am = 0.0f;
+    if constexpr (MID == kMidF32) {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) t[i] = __fadd_rn(t[i], gv[i]);
+    } else {
+        add_in_format<MID>(t, g);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(t[i]));
+    am = halfwarp_max(am);
+    snew = __fdiv_rn(am, kE4M3Max);
+    return requant8(t, snew);
+}
+
 template <int UNROLL, int MID>
 __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict__ master,
                                                               float *__restrict__ scales,
@@ -231,23 +273,8 @@ __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict_
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t blk = base + 2 * u + half;
-            const float gv[8] = {bf16_lo(g[u].x), bf16_hi(g[u].x), bf16_lo(g[u].y), bf16_hi(g[u].y),
-                                 bf16_lo(g[u].z), bf16_hi(g[u].z), bf16_lo(g[u].w), bf16_hi(g[u].w)};
-            float t[8];
-            decode_mul4(mc[u].x, s[u], t);
-            decode_mul4(mc[u].y, s[u], t + 4);
-            float am = 0.0f;
-            if constexpr (MID == kMidF32) {
-#pragma unroll
-                for (int i = 0; i < 8; ++i) t[i] = __fadd_rn(t[i], gv[i]);
-            } else {
-                add_in_format<MID>(t, g[u]);
-            }
-#pragma unroll
-            for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(t[i]));
-            am = halfwarp_max(am);
-            const float snew = __fdiv_rn(am, kE4M3Max);
-            const uint2 out = requant8(t, snew);
+            float snew;
+            const uint2 out = accum_block<MID>(mc[u], g[u], s[u], snew);
             if (blk < nblocks) {
                 master[blk * 16 + j] = out;
                 if (j == 0) scales[blk] = snew;
@@ -648,6 +675,115 @@ reduce_shards_staged_kernel(
     if constexpr (NAIVE) flush_count(overflowed, naive_count);
 }
 
+// ---- the staged accumulation ------------------------------------------------
+// A CTA is kAcWarps consumer warps and one producer warp.  Tiles of kAcTile
+// blocks go round-robin to the CTAs; the producer copies each tile's BF16
+// gradient, master codes and master scales with cp.async.bulk into a
+// kAcStages-deep ring, and half warp h takes blocks h, h + 2 kAcWarps, ... of
+// the tile (lane j: elements 8j .. 8j+7), loads them from shared memory,
+// releases the stage and writes the new codes and scale straight back over the
+// master (the producer never reads a tile twice, so the in-place update races
+// nothing).  The arithmetic is accum_block, as in grad_accum_kernel.  Waits are
+// time-limited (status in g_reduce_status, this file's pipeline status word).
+constexpr int kAcWarps = AGOQ_ASTAGED_WARPS;
+constexpr int kAcThreads = (kAcWarps + 1) * 32;
+constexpr int kAcRep = AGOQ_ASTAGED_REP;                 // blocks per half warp per stage
+constexpr int kAcTile = 2 * kAcWarps * kAcRep;
+constexpr int kAcStages = AGOQ_ASTAGED_STAGES;
+constexpr int kAcGradBytes = kAcTile * 256, kAcCodeBytes = kAcTile * 128;
+constexpr int kAcStageBytes = kAcGradBytes + kAcCodeBytes + kAcTile * 4;
+constexpr size_t kAcSmem = (size_t)kAcStages * (kAcStageBytes + 16);
+static_assert(kAcTile % 4 == 0 && kAcStageBytes % 16 == 0, "whole 16-byte copies");
+
+template <int MID>
+__global__ void __launch_bounds__(kAcThreads, AGOQ_ASTAGED_MIN_CTAS)
+grad_accum_staged_kernel(uint8_t *__restrict__ master, float *__restrict__ scales,
+                         const uint8_t *__restrict__ grad, int64_t nblocks) {
+    using namespace gemm;
+    extern __shared__ __align__(128) uint8_t smem[];
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + (size_t)kAcStages * kAcStageBytes);
+    uint64_t *empty = full + kAcStages;
+    __shared__ int abort_flag;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kAcStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kAcWarps);
+        }
+        abort_flag = 0;
+        asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    __syncthreads();
+    pdl_wait_and_release();
+    volatile int *abort = &abort_flag;
+    const int64_t ntiles = (nblocks + kAcTile - 1) / kAcTile;
+
+    if (warp == kAcWarps) {
+        if (lane == 0) {
+            uint32_t issued = 0;
+            int stage = 0;
+            uint32_t phase = 0;
+            for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+                if (issued >= (uint32_t)kAcStages &&
+                    !wait_bar(&empty[stage], phase ^ 1u, abort, &g_reduce_status))
+                    break;
+                const int64_t b0 = tile * kAcTile;
+                const uint32_t nb = (uint32_t)(nblocks - b0 < kAcTile ? nblocks - b0 : kAcTile);
+                uint8_t *st = smem + (size_t)stage * kAcStageBytes;
+                mbar_expect_tx(&full[stage], nb * (256u + 128u + 4u));
+                bulk_g2s(st, grad + b0 * 256, nb * 256u, &full[stage]);
+                bulk_g2s(st + kAcGradBytes, master + b0 * 128, nb * 128u, &full[stage]);
+                bulk_g2s(st + kAcGradBytes + kAcCodeBytes, scales + b0, nb * 4u, &full[stage]);
+                ++issued;
+                if (++stage == kAcStages) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+            const uint32_t first = issued > (uint32_t)kAcStages ? issued - kAcStages : 0u;
+            for (uint32_t j = first; j < issued; ++j)
+                wait_bar(&full[j % kAcStages], (j / kAcStages) & 1u, abort, &g_reduce_status, true);
+        }
+        return;
+    }
+
+    const int half = lane >> 4, j = lane & 15, hw = 2 * warp + half;
+    int stage = 0;
+    uint32_t phase = 0;
+    for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
+        if (!warp_wait(&full[stage], phase, abort, &g_reduce_status)) break;
+        mbar_try_wait(&full[stage], phase, 0);   // each lane observes the completed phase
+        const uint8_t *st = smem + (size_t)stage * kAcStageBytes;
+        uint2 mc[kAcRep];
+        uint4 g[kAcRep];
+        float sc[kAcRep];
+#pragma unroll
+        for (int r = 0; r < kAcRep; ++r) {
+            const int lb = hw + 2 * kAcWarps * r;
+            g[r] = reinterpret_cast<const uint4 *>(st)[lb * 16 + j];
+            mc[r] = reinterpret_cast<const uint2 *>(st + kAcGradBytes)[lb * 16 + j];
+            sc[r] = reinterpret_cast<const float *>(st + kAcGradBytes + kAcCodeBytes)[lb];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&empty[stage]);
+        if (++stage == kAcStages) {
+            stage = 0;
+            phase ^= 1u;
+        }
+        const int64_t b0 = tile * kAcTile;
+#pragma unroll
+        for (int r = 0; r < kAcRep; ++r) {
+            const int64_t blk = b0 + hw + 2 * kAcWarps * r;
+            float snew;
+            const uint2 out = accum_block<MID>(mc[r], g[r], sc[r], snew);
+            if (blk < nblocks) {
+                reinterpret_cast<uint2 *>(master)[blk * 16 + j] = out;
+                if (j == 0) scales[blk] = snew;
+            }
+        }
+    }
+}
+
 template <typename K>
 int resident_grid(K kernel, int *cache, int64_t work_ctas) {
     int64_t g = (int64_t)sm_count() * resident_per_sm(kernel, kThreads, 0, cache);
@@ -661,6 +797,27 @@ namespace {
 template <int MID>
 cudaError_t launch_grad_accum_mid(void *master, float *master_scales, const void *grad, int64_t n,
                                   cudaStream_t st) {
+    if (AGOQ_ACCUM_STAGED && (n / kBlock) % 4 == 0 &&
+        reinterpret_cast<uintptr_t>(master_scales) % 16 == 0) {
+        static bool smem_set[kMaxDevices];
+        static int cache_st[kMaxDevices];
+        int dev = 0;
+        cudaGetDevice(&dev);
+        if (dev < 0 || dev >= kMaxDevices) dev = 0;
+        auto ks = grad_accum_staged_kernel<MID>;
+        if (!smem_set[dev]) {
+            cudaError_t e =
+                cudaFuncSetAttribute(ks, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kAcSmem);
+            if (e != cudaSuccess) return e;
+            smem_set[dev] = true;
+        }
+        const int64_t nbs = n / kBlock, tiles = (nbs + kAcTile - 1) / kAcTile;
+        int64_t grid = (int64_t)sm_count() * resident_per_sm(ks, kAcThreads, kAcSmem, cache_st);
+        if (tiles < grid) grid = tiles;
+        return launch_pdl(ks, (int)(grid > 0 ? grid : 1), kAcThreads, kAcSmem, st,
+                          static_cast<uint8_t *>(master), master_scales,
+                          static_cast<const uint8_t *>(grad), nbs);
+    }
     constexpr int kUnroll = AGOQ_ACCUM_UNROLL;
     static int cache[kMaxDevices];
     const int64_t nb = n / kBlock;

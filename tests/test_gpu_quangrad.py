@@ -49,6 +49,30 @@ def test_accum_parity_over_steps(oracle, nblocks):
         assert np.array_equal(s.cpu().numpy().view(np.uint32), s_np.view(np.uint32))
 
 
+@pytest.mark.parametrize("nblocks", [4, 600])
+def test_accum_staged_and_register_kernels_agree(oracle, nblocks):
+    """The same accumulation through both kernels: master scales on a 16-byte
+    boundary take the staged kernel (bulk copies; 600 blocks leave a ragged
+    last tile), the same scales 4 bytes off it the register kernel; both give
+    the oracle's master bit for bit over three micro-batches."""
+    n = nblocks * 128
+    results = []
+    for off in (0, 1):
+        m = torch.zeros(n, dtype=torch.uint8, device="cuda")
+        room = torch.zeros(nblocks + 4, dtype=torch.float32, device="cuda")
+        ms = room[off:off + nblocks]
+        assert (ms.data_ptr() % 16 == 0) == (off == 0)
+        wm, ws = np.zeros(n, np.uint8), np.zeros(nblocks, np.float32)
+        for g in synthetic.quangrad_grads_np(seed=30 + nblocks, n=n, steps=3):
+            agoq.agoq_grad_accum_fp8(m, ms, G.dev_bf16(g))
+            wm, ws = oracle.grad_accum_fp8(wm, ws, g)
+        agoq.agoq_device_status()
+        assert np.array_equal(m.cpu().numpy(), wm)
+        assert np.array_equal(ms.cpu().numpy().view(np.uint32), ws.view(np.uint32))
+        results.append(m.cpu().numpy())
+    assert np.array_equal(results[0], results[1])
+
+
 def test_accum_edge_cases(oracle):
     rng = np.random.default_rng(5)
     blocks = []
