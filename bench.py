@@ -688,15 +688,16 @@ def rows_arm(device, hbm_peak, bf16_peak):
     # FP8 shard local reduce, 2^25 elements per shard
     n = synthetic.REDUCE_N
     for W in synthetic.REDUCE_WS:
-        sh = torch.randint(0, 126, (W, n), dtype=torch.uint8, device=device)
-        sh |= (torch.randint(0, 2, (W, n), dtype=torch.uint8, device=device) << 7)
-        ss = torch.rand((W, n // 128), device=device) * 1e-4
+        sh, ss = reduce_shards_torch(W, n, device)
         out = torch.empty(n, dtype=torch.uint8, device=device)
         outs = torch.empty(n // 128, dtype=torch.float32, device=device)
         cnt = torch.zeros(1, dtype=torch.int64, device=device)
         nbytes = (W + 1) * (n + (n // 128) * 4)
-        row("reduce_W%d_2^25" % W, nbytes, W * n,
-            _time_launch(lambda: agoq.agoq_reduce_fp8_shards(sh, ss, W, n, out, outs, cnt), flush))
+        ms = _time_launch(lambda: agoq.agoq_reduce_fp8_shards(sh, ss, W, n, out, outs, cnt), flush)
+        row("reduce_W%d_2^25" % W, nbytes, W * n, ms,
+            {"naive_overflow_count": int(cnt.item()),
+             "inputs": "shard r ~ N(0, sd 1e-2 j_r), j_r ~ U[0.5,2), seed 3 (torch generator), "
+                       "block-quantized to E4M3 by the library (absmax/448)"})
         row("reduce_W%d_2^25_nocount" % W, nbytes, W * n,
             _time_launch(lambda: agoq.agoq_reduce_fp8_shards(sh, ss, W, n, out, outs), flush))
         del sh, ss, out, outs
@@ -839,6 +840,22 @@ def reference_arm(args):
     print(json.dumps(line), flush=True)
 
 
+def reduce_shards_torch(W, n, device):
+    """The FP8 shard workload: shard r holds N(0, sd 1e-2 * j_r) values, j_r ~ U[0.5, 2)
+    (seed 3, torch generator), block-quantized to E4M3 by the library's own
+    accumulation into a zeroed master (the a4 requantization rule)."""
+    import torch
+    from gradient_quantization_gb300 import agoq, synthetic
+    vals = synthetic.reduce_shard_values_torch(seed=3, W=W, device=device, n=n)
+    sh = torch.zeros((W, n), dtype=torch.uint8, device=device)
+    ss = torch.zeros((W, n // 128), dtype=torch.float32, device=device)
+    for r in range(W):
+        agoq.agoq_grad_accum_fp8(sh[r], ss[r], vals[r])
+    del vals
+    torch.cuda.synchronize()
+    return sh, ss
+
+
 PROFILE_CASES = ("accum", "reduce8", "reduce8_nocount", "reduce64", "gemm", "gemm_accum", "silu",
                  "rmsnorm", "fwd_gemm")
 
@@ -859,9 +876,7 @@ def profile_case(name, launches=3):
             agoq.agoq_grad_accum_fp8(m, ms, g)
     elif name.startswith("reduce"):
         W, n = (64, 1 << 22) if name == "reduce64" else (8, 1 << 25)
-        sh = torch.randint(0, 126, (W, n), dtype=torch.uint8, device=dev)
-        sh |= (torch.randint(0, 2, (W, n), dtype=torch.uint8, device=dev) << 7)
-        ss = torch.rand((W, n // 128), device=dev) * 1e-4
+        sh, ss = reduce_shards_torch(W, n, dev)
         cnt = None if name.endswith("nocount") else torch.zeros(1, dtype=torch.int64, device=dev)
         for _ in range(launches):
             agoq.agoq_reduce_fp8_shards(sh, ss, W, n, naive_overflow_count=cnt)

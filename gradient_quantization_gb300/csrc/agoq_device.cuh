@@ -86,47 +86,13 @@ __device__ __forceinline__ uint32_t e4m3x2_from_f32(float lo, float hi) {
 }
 
 // Two E4M3 codes (bits 0-7 and 8-15 of v) to binary32, exactly (every E4M3
-// value is an FP16 value, and every FP16 value a binary32 value).  The FP16 to
-// binary32 step is either a conversion or, with AGOQ_F16_WIDEN_BY_ADD, the
-// mixed-precision addition f32(h) + (-0), which is exact and returns h's value
-// (including its signed zero) unchanged.
-#ifndef AGOQ_F16_WIDEN_BY_ADD
-#define AGOQ_F16_WIDEN_BY_ADD 0
-#endif
+// value is an FP16 value, and every FP16 value a binary32 value).
 __device__ __forceinline__ void e4m3x2_to_f32(uint32_t v, float &lo, float &hi) {
     uint32_t h2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)v));
-#if AGOQ_F16_WIDEN_BY_ADD
-    asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\t"
-        "add.rn.f32.f16 %0, a, 0f80000000;\n\tadd.rn.f32.f16 %1, b, 0f80000000;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(h2));
-#else
     asm("{\n\t.reg .f16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.f32.f16 %0, a;\n\tcvt.f32.f16 %1, b;\n\t}"
         : "=f"(lo), "=f"(hi)
         : "r"(h2));
-#endif
-}
-
-// Code i (bits 8i..8i+7) of a word of four E4M3 codes, as a binary32 whose
-// value is exactly e4m3(code) * 2^-120: the code's sign goes to bit 31 and its
-// 7 exponent/fraction bits to bits 26..20, which reads as a binary32 with the
-// E4M3 exponent field (bias 7 instead of 127) and fraction; E4M3 subnormals
-// land on binary32 subnormals with the same scaling.  Multiplying by 2^120, or
-// by a scale s pre-multiplied by 2^120, is therefore exact up to the single
-// rounding of the final product.
-__device__ __forceinline__ float e4m3_times_2m120(uint32_t w, int i) {
-    const uint32_t x = i == 3 ? w : (w << (24 - 8 * i));   // code i in bits 24..31
-    return __uint_as_float((x & 0x80000000u) | ((x >> 4) & 0x07F00000u));
-}
-
-constexpr float kTwo120 = 0x1p120f;
-
-// fl(e4m3(code) * s) for the codes of a word, with S = s * 2^120 precomputed
-// when s < 2^8 (so that S is exact) -- `folded` says which form `S` holds.
-__device__ __forceinline__ float e4m3_mul(uint32_t w, int i, float S, bool folded, float s) {
-    const float f = e4m3_times_2m120(w, i);
-    return folded ? __fmul_rn(f, S) : __fmul_rn(__fmul_rn(f, kTwo120), s);
 }
 
 // E4M3 codes of 8 values t[] requantized with block scale s = fl(absmax/448):
@@ -141,16 +107,12 @@ __device__ __forceinline__ float e4m3_mul(uint32_t w, int i, float S, bool folde
 // underflow are far below the smallest E4M3 midpoint (2^-10) and give a signed
 // zero either way.  s subnormal takes the division; s == 0 (all-zero block)
 // gives zero codes.
-#ifndef AGOQ_E4M3_PACKED
-#define AGOQ_E4M3_PACKED 1
-#endif
 __device__ __forceinline__ uint2 e4m3_codes8(const float t[8], float s) {
     uint32_t c[4];
     if (s >= 0x1p-126f) {
         const float r = __frcp_rn(s);
         constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
         bool differ = false;
-#if AGOQ_E4M3_PACKED
         // the same products in packed pairs (multiplies only: nothing to contract)
         const uint64_t r2 = f32x2(r, r), dn2 = f32x2(kDown, kDown), up2 = f32x2(kUp, kUp);
 #pragma unroll
@@ -162,16 +124,6 @@ __device__ __forceinline__ uint2 e4m3_codes8(const float t[8], float s) {
             differ |= lo != hi;
             c[p] = lo;
         }
-#else
-#pragma unroll
-        for (int p = 0; p < 4; ++p) {
-            const float qa = __fmul_rn(t[2 * p], r), qb = __fmul_rn(t[2 * p + 1], r);
-            const uint32_t lo = e4m3x2_from_f32(__fmul_rn(qa, kDown), __fmul_rn(qb, kDown));
-            const uint32_t hi = e4m3x2_from_f32(__fmul_rn(qa, kUp), __fmul_rn(qb, kUp));
-            differ |= lo != hi;
-            c[p] = lo;
-        }
-#endif
         if (differ) {
 #pragma unroll
             for (int p = 0; p < 4; ++p)
@@ -187,28 +139,12 @@ __device__ __forceinline__ uint2 e4m3_codes8(const float t[8], float s) {
     return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
 }
 
-// Round an exactly representable binary32 sum of two E4M3 values (|t| <= 448)
-// to the nearest E4M3 value, ties to even, staying in binary32: with
-// c = 1.5 * 2^(e+20), where 2^e <= |t| < 2^(e+1) (e clamped below at -6, the
-// E4M3 subnormal spacing being 2^-9), fl(t + c) keeps exactly the bits of t at
-// and above 2^(e-3) -- the E4M3 spacing -- rounding the rest to nearest even
-// (c's own bits there are even); subtracting c is exact.
-__device__ __forceinline__ float e4m3_round_f32(float t) {
-    const uint32_t e = max(__float_as_uint(t) & 0x7F800000u, (uint32_t)(127 - 6) << 23);
-    const float c = __uint_as_float(e + (20u << 23) + 0x00400000u);
-    return __fsub_rn(__fadd_rn(t, c), c);
-}
-
 // Largest |value| of the BF16 pairs in w[0..N-1], as a binary32 (exact: the
-// maximum of BF16 magnitudes is a BF16 value).  With AGOQ_ABSMAX_XORSIGN,
-// max.xorsign.abs compares magnitudes directly (its sign bit, the XOR of the
-// inputs', is masked once at the end) instead of masking every word first.
-#ifndef AGOQ_ABSMAX_XORSIGN
-#define AGOQ_ABSMAX_XORSIGN 1
-#endif
+// maximum of BF16 magnitudes is a BF16 value).  max.xorsign.abs compares
+// magnitudes directly; its sign bit, the XOR of the inputs', is masked once at
+// the end.
 template <int N>
 __device__ __forceinline__ float bf16_absmax(const uint32_t *w) {
-#if AGOQ_ABSMAX_XORSIGN
     uint32_t m = w[0];
 #pragma unroll
     for (int i = 1; i < N; ++i) {
@@ -217,15 +153,6 @@ __device__ __forceinline__ float bf16_absmax(const uint32_t *w) {
         m = r;
     }
     m &= 0x7FFF7FFFu;
-#else
-    uint32_t m = w[0] & 0x7FFF7FFFu;
-#pragma unroll
-    for (int i = 1; i < N; ++i) {
-        uint32_t r;
-        asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(m), "r"(w[i] & 0x7FFF7FFFu));
-        m = r;
-    }
-#endif
     return fmaxf(bf16_lo(m), bf16_hi(m));
 }
 
@@ -436,11 +363,8 @@ __host__ __device__ constexpr uint32_t packed_hi(uint32_t v) {
 // bit then turns offset binary into two's complement.  The low 22 bits of
 // 0x4B400000 are zero, so the right shift of a field that straddles bit 32
 // splits t into the constant's and the field's parts exactly.
-// 1: the shifted additions are written as integer multiply-adds, which the
+// The shifted additions are written as integer multiply-adds, which the
 // compiler can place on the FMA pipe (measured faster than shifts and adds).
-#ifndef AGOQ_PACK_MAD
-#define AGOQ_PACK_MAD 1
-#endif
 template <int BITS>
 __device__ __forceinline__ void pack_biased8(const uint32_t t[8], uint32_t &lo, uint32_t &hi) {
     constexpr uint32_t kC = 0x4B400000u;
@@ -451,14 +375,9 @@ __device__ __forceinline__ void pack_biased8(const uint32_t t[8], uint32_t &lo, 
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int pos = i * BITS;
-#if AGOQ_PACK_MAD
         // integer multiply-adds (power-of-two multipliers)
         if (pos < 32) asm("mad.lo.u32 %0, %1, %2, %0;" : "+r"(l) : "r"(t[i]), "r"(1u << pos));
         if (pos >= 32) asm("mad.lo.u32 %0, %1, %2, %0;" : "+r"(h) : "r"(t[i]), "r"(1u << (pos - 32)));
-#else
-        if (pos < 32) l += t[i] << pos;
-        if (pos >= 32) h += t[i] << (pos - 32);
-#endif
         else if (pos + BITS > 32) h += t[i] >> (32 - pos);
     }
     lo = l ^ kSLo;
@@ -508,25 +427,22 @@ __device__ __forceinline__ void load_chunk(const uint32_t *rec, int c, uint32_t 
 
 // The 8 fields of a chunk as biased binary32 words: word i holds
 // 0x4B000000 + (code_i + 2^(BITS-1)), whose value is 2^23 + code_i + 2^(BITS-1)
-// (field_value's bias trick).  With AGOQ_DEQUANT_PRMT, 4- and 8-bit fields
-// are moved into place by byte permutes: the sign bits of a whole word are
+// (field_value's bias trick).  4- and 8-bit fields are moved into place by
+// byte permutes: the sign bits of a whole word are
 // flipped at once, the nibbles of 4-bit fields are first spread over the
 // bytes of two words (even and odd fields), and one permute per field puts
 // its byte below the constant bytes 00 00 4B.
-#ifndef AGOQ_DEQUANT_PRMT
-#define AGOQ_DEQUANT_PRMT 1
-#endif
 template <int BITS>
 __device__ __forceinline__ void biased_words8(uint32_t lo, uint32_t hi, uint32_t wv[8]) {
     constexpr uint32_t kHigh = 0x4B000000u;
-    if constexpr (AGOQ_DEQUANT_PRMT && BITS == 8) {
+    if constexpr (BITS == 8) {
         const uint32_t a = lo ^ 0x80808080u, b = hi ^ 0x80808080u;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             wv[i] = __byte_perm(a, kHigh, 0x7650 + i);
             wv[4 + i] = __byte_perm(b, kHigh, 0x7650 + i);
         }
-    } else if constexpr (AGOQ_DEQUANT_PRMT && BITS == 4) {
+    } else if constexpr (BITS == 4) {
         const uint32_t a = lo ^ 0x88888888u;
         const uint32_t even = a & 0x0F0F0F0Fu, odd = (a >> 4) & 0x0F0F0F0Fu;
 #pragma unroll

@@ -12,103 +12,13 @@
 // Reduce: 8 lanes own a block, each lane 16 elements (one 16-byte load of
 // codes per shard), so a warp reads 4 adjacent blocks (512 contiguous bytes)
 // of every shard per load instruction.  Two kernels feed that arithmetic: one
-// loads the codes into registers itself, RUNROLL shards ahead; the other
+// loads the codes into registers itself, several shards ahead; the other
 // (used whenever the scale rows allow 16-byte bulk copies) has a producer warp
-// stream (tile, shard) stages into a shared-memory ring with bulk async
+// stream (tile, shard group) stages into a shared-memory ring with bulk async
 // copies, so that far more bytes are in flight per SM than registers can hold.
 #include "agoq_device.cuh"
 #include "agoq_launch.h"
 #include "gemm_common.cuh"
-
-// Implementation choices, all bit-identical (selected by measurement):
-//   AGOQ_E4M3_DECODE_CVT   1: decode codes with cvt.f16x2.e4m3x2; 0: with integer bit moves
-//   AGOQ_E4M3_REQUANT_FAST 1: reciprocal + bracketing check; 0: IEEE division per value
-//   AGOQ_NAIVE_ROUND_CVT   1: round the naive sum through an E4M3 cvt; 0: in binary32
-#ifndef AGOQ_E4M3_DECODE_CVT
-#define AGOQ_E4M3_DECODE_CVT 1
-#endif
-#ifndef AGOQ_E4M3_REQUANT_FAST
-#define AGOQ_E4M3_REQUANT_FAST 1
-#endif
-#ifndef AGOQ_NAIVE_ROUND_CVT
-#define AGOQ_NAIVE_ROUND_CVT 1
-#endif
-// Shared-memory staged accumulation: 1 selects it when the master scales are
-// 16-byte aligned and the block count is a multiple of 4; consumer warps per
-// CTA, blocks per half warp and stage, ring stages, CTAs per SM.
-#ifndef AGOQ_ACCUM_STAGED
-#define AGOQ_ACCUM_STAGED 1
-#endif
-#ifndef AGOQ_ASTAGED_WARPS
-#define AGOQ_ASTAGED_WARPS 16
-#endif
-#ifndef AGOQ_ASTAGED_REP
-#define AGOQ_ASTAGED_REP 3
-#endif
-#ifndef AGOQ_ASTAGED_STAGES
-#define AGOQ_ASTAGED_STAGES 3
-#endif
-#ifndef AGOQ_ASTAGED_MIN_CTAS
-#define AGOQ_ASTAGED_MIN_CTAS 1
-#endif
-#ifndef AGOQ_ACCUM_PIPELINE
-#define AGOQ_ACCUM_PIPELINE 0
-#endif
-#ifndef AGOQ_ACCUM_UNROLL
-#define AGOQ_ACCUM_UNROLL 4
-#endif
-#ifndef AGOQ_REDUCE_RUNROLL
-#define AGOQ_REDUCE_RUNROLL 8
-#endif
-#ifndef AGOQ_REDUCE_COUNT_RUNROLL
-#define AGOQ_REDUCE_COUNT_RUNROLL 4
-#endif
-// 1: the naive FP8 running sum is kept as FP16 pairs (every E4M3 value is an
-//    FP16 value) and added with the mixed add.rn.f32.f16; 0: kept in binary32.
-#ifndef AGOQ_NAIVE_MIXED_ADD
-#define AGOQ_NAIVE_MIXED_ADD 1
-#endif
-#ifndef AGOQ_REDUCE_MIN_CTAS
-#define AGOQ_REDUCE_MIN_CTAS 2
-#endif
-#ifndef AGOQ_REDUCE_COUNT_MIN_CTAS
-#define AGOQ_REDUCE_COUNT_MIN_CTAS 2
-#endif
-// 1: the overflow test keeps the largest |naive sum| of each element and
-//    compares it with 448 once per block; 0: a flag per element and step.
-#ifndef AGOQ_NAIVE_MAX
-#define AGOQ_NAIVE_MAX 1
-#endif
-// The shard products are formed with packed binary32 multiplies (two per
-// instruction) and added with scalar round-to-nearest adds: 2 in both reduce
-// kernels, 1 only in the one with the naive count, 0 nowhere.
-#ifndef AGOQ_REDUCE_PACKED_MUL
-#define AGOQ_REDUCE_PACKED_MUL 2
-#endif
-// Shared-memory staged reduce: 1 selects it when the scale rows allow bulk
-// copies; consumer warps per CTA (each 4 blocks of a tile) without and with
-// the naive count, ring stages, shards per stage, and CTAs per SM.
-#ifndef AGOQ_REDUCE_STAGED
-#define AGOQ_REDUCE_STAGED 1
-#endif
-#ifndef AGOQ_RSTAGED_WARPS
-#define AGOQ_RSTAGED_WARPS 16
-#endif
-#ifndef AGOQ_RSTAGED_COUNT_WARPS
-#define AGOQ_RSTAGED_COUNT_WARPS 15
-#endif
-#ifndef AGOQ_RSTAGED_STAGES
-#define AGOQ_RSTAGED_STAGES 2
-#endif
-#ifndef AGOQ_RSTAGED_SHARDS
-#define AGOQ_RSTAGED_SHARDS 8
-#endif
-#ifndef AGOQ_RSTAGED_HINT
-#define AGOQ_RSTAGED_HINT 0
-#endif
-#ifndef AGOQ_RSTAGED_MIN_CTAS
-#define AGOQ_RSTAGED_MIN_CTAS 1
-#endif
 
 namespace agoq {
 namespace {
@@ -124,45 +34,13 @@ __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
     return v;
 }
 
-// Requantize 8 binary32 values with the block scale s (see e4m3_codes8).
-__device__ __forceinline__ uint2 requant8(const float t[8], float s) {
-#if AGOQ_E4M3_REQUANT_FAST
-    return e4m3_codes8(t, s);
-#else
-    if (s == 0.0f) return make_uint2(0u, 0u);
-    uint32_t c[4];
-#pragma unroll
-    for (int p = 0; p < 4; ++p)
-        c[p] = e4m3x2_from_f32(__fdiv_rn(t[2 * p], s), __fdiv_rn(t[2 * p + 1], s));
-    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-#endif
-}
-
 // fl(e4m3(code_i) * s) for the 4 codes of word w.
 __device__ __forceinline__ void decode_mul4(uint32_t w, float s, float v[4]) {
-#if AGOQ_E4M3_DECODE_CVT
     float e[4];
     e4m3x2_to_f32(w & 0xFFFFu, e[0], e[1]);
     e4m3x2_to_f32(w >> 16, e[2], e[3]);
 #pragma unroll
     for (int i = 0; i < 4; ++i) v[i] = __fmul_rn(e[i], s);
-#else
-    const bool folded = s < 256.0f;
-    const float S = folded ? __fmul_rn(s, kTwo120) : s;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) v[i] = e4m3_mul(w, i, S, folded, s);
-#endif
-}
-
-// The E4M3 values of the 4 codes of word w (exact).
-__device__ __forceinline__ void decode4(uint32_t w, float e[4]) {
-#if AGOQ_E4M3_DECODE_CVT
-    e4m3x2_to_f32(w & 0xFFFFu, e[0], e[1]);
-    e4m3x2_to_f32(w >> 16, e[2], e[3]);
-#else
-#pragma unroll
-    for (int i = 0; i < 4; ++i) e[i] = __fmul_rn(e4m3_times_2m120(w, i), kTwo120);
-#endif
 }
 
 // Intermediate formats of the accumulation: MID 0 binary32 (t = fl(m + g));
@@ -218,9 +96,12 @@ __device__ __forceinline__ uint2 accum_block(const uint2 &mc, const uint4 &g, fl
     for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(t[i]));
     am = halfwarp_max(am);
     snew = __fdiv_rn(am, kE4M3Max);
-    return requant8(t, snew);
+    return e4m3_codes8(t, snew);
 }
 
+// The register-staged accumulation (master scales not 16-byte aligned, or a
+// block count that is not a multiple of 4): each half warp keeps UNROLL blocks
+// in flight.
 template <int UNROLL, int MID>
 __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict__ master,
                                                               float *__restrict__ scales,
@@ -232,10 +113,13 @@ __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict_
     const int64_t warp = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
     const int64_t stride = nwarps * (2 * UNROLL);
-    auto load = [&](int64_t b0, uint2 (&mc)[UNROLL], float (&s)[UNROLL], uint4 (&g)[UNROLL]) {
+    for (int64_t base = warp * (2 * UNROLL); base < nblocks; base += stride) {
+        uint2 mc[UNROLL];
+        uint4 g[UNROLL];
+        float s[UNROLL];
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
-            const int64_t blk = b0 + 2 * u + half;
+            const int64_t blk = base + 2 * u + half;
             if (blk < nblocks) {
                 mc[u] = master[blk * 16 + j];
                 s[u] = scales[blk];
@@ -246,30 +130,6 @@ __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict_
                 g[u] = make_uint4(0u, 0u, 0u, 0u);
             }
         }
-    };
-#if AGOQ_ACCUM_PIPELINE
-    // The next group's loads are issued before this group's arithmetic (each
-    // lane reads and rewrites only its own master words, so reading ahead is safe).
-    uint2 mcn[UNROLL];
-    float sn[UNROLL];
-    uint4 gn[UNROLL];
-    load(warp * (2 * UNROLL), mcn, sn, gn);
-#endif
-    for (int64_t base = warp * (2 * UNROLL); base < nblocks; base += stride) {
-        uint2 mc[UNROLL];
-        uint4 g[UNROLL];
-        float s[UNROLL];
-#if AGOQ_ACCUM_PIPELINE
-#pragma unroll
-        for (int u = 0; u < UNROLL; ++u) {
-            mc[u] = mcn[u];
-            s[u] = sn[u];
-            g[u] = gn[u];
-        }
-        load(base + stride, mcn, sn, gn);
-#else
-        load(base, mc, s, g);
-#endif
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             const int64_t blk = base + 2 * u + half;
@@ -283,11 +143,24 @@ __global__ void __launch_bounds__(kThreads) grad_accum_kernel(uint2 *__restrict_
     }
 }
 
+// ---- the local reduce: per-lane arithmetic -----------------------------------
+
 // Two E4M3 codes (bits 0-15 of v) to an FP16 pair, exactly.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t v) {
     uint32_t h2;
     asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)v));
     return h2;
+}
+
+// An FP16 pair to a binary32 pair held in one 64-bit register (half 0 in the
+// low word), exactly.
+__device__ __forceinline__ uint64_t f16x2_to_f32x2(uint32_t h2) {
+    uint64_t d;
+    asm("{\n\t.reg .f16 a, b;\n\t.reg .f32 x, y;\n\tmov.b32 {a, b}, %1;\n\t"
+        "cvt.f32.f16 x, a;\n\tcvt.f32.f16 y, b;\n\tmov.b64 %0, {x, y};\n\t}"
+        : "=l"(d)
+        : "r"(h2));
+    return d;
 }
 
 // d_k = fl(f32(half k of h2) + c_k): binary32 additions of an FP16 operand.
@@ -299,100 +172,114 @@ __device__ __forceinline__ void add_f16x2_f32(uint32_t h2, float c0, float c1, f
         : "r"(h2), "f"(c0), "f"(c1));
 }
 
+// max(|a|, |b|, |c|).
+__device__ __forceinline__ float max3_abs(float a, float b, float c) {
+    float d;
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // One lane's share of the reduce of one block: 16 elements (one 16-byte load
 // of codes per shard), their binary32 running sums over the shards in rank
 // order and, with the naive count, the naive FP8 running sums.
+//
+// The running sums are kept as binary32 pairs.  A shard's products are formed
+// as fma(e4m3(c), s, +0) on pairs: that is fl(e4m3(c) * s) except that an
+// exactly -0 product becomes +0, which changes nothing here -- the sums start
+// at +0 and a binary32 sum is -0 only if both operands are, so no running sum
+// is ever -0 and adding +0 or -0 to it gives the same value.  (A multiply
+// would be equivalent too, but a packed multiply followed by a packed add has
+// been seen contracted into one fused operation by the assembler; a fused
+// multiply-add with +0 is not a multiply.)  Each sum is then fl(acc + p), a
+// packed round-to-nearest add.
+//
+// The naive FP8 sum (one shared scale, summed in the code domain) is kept as
+// FP16 pairs (every E4M3 value is an FP16 value): step r forms the exact sum
+// t = n + e4m3(c_r) in binary32 (mixed FP16 + binary32 add; both operands are
+// E4M3 values, so the sum is exact), keeps the largest |t| seen per element
+// (an element overflows iff that maximum exceeds 448, which is the first
+// overflow's test; later steps cannot undo it), and rounds t to E4M3 through a
+// saturating cvt.  Shards are taken two at a time so that one three-input
+// maximum covers both steps of an element.
 template <bool NAIVE>
 struct ReduceLane {
-    float acc[16];
-#if AGOQ_NAIVE_MIXED_ADD
-    uint32_t nvh[8];   // naive running sum, FP16 pairs
-#else
-    float nv[16];
-#endif
-#if AGOQ_NAIVE_MAX
-    float nmax[16];    // largest |naive sum| seen per element
-#else
-    uint32_t alive;
-#endif
+    uint64_t acc[8];   // binary32 running sums, elements (2p, 2p+1)
+    uint32_t nvh[8];   // naive running sums, FP16 pairs
+    float nmax[16];    // largest |exact naive sum| seen per element
 
     __device__ __forceinline__ void clear() {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = 0.0f;
+        for (int p = 0; p < 8; ++p) acc[p] = 0ull;
         if constexpr (NAIVE) {
-#if AGOQ_NAIVE_MAX
 #pragma unroll
             for (int i = 0; i < 16; ++i) nmax[i] = 0.0f;
-#else
-            alive = 0xFFFFu;
-#endif
         }
     }
 
-    // Shard r (codes c, block scale sc): acc += fl(e4m3(c) * sc) element-wise,
-    // and the naive FP8 sum steps once.
-    __device__ __forceinline__ void add_shard(const uint4 &c, float sc, int r) {
-        const uint32_t w4[4] = {c.x, c.y, c.z, c.w};
-        float e[16];
+    // Pair p (elements 2p, 2p+1) of one shard: its codes as an FP16 pair h and
+    // a binary32 pair e, and its products added to the running sums.
+    __device__ __forceinline__ void decode_add(const uint4 &c, uint64_t s2, int p, uint32_t &h,
+                                               uint64_t &e) {
+        const uint32_t w = p < 2 ? c.x : p < 4 ? c.y : p < 6 ? c.z : c.w;
+        h = e4m3x2_to_f16x2((p & 1) ? w >> 16 : w & 0xFFFFu);
+        e = f16x2_to_f32x2(h);
+        acc[p] = add_f32x2(acc[p], fma_f32x2(e, s2, 0ull));
+    }
+
+    // One naive step of pair p with the shard values e (binary32 pair): returns
+    // the exact sums t0, t1 and rounds them to E4M3 (nearest even, saturating).
+    __device__ __forceinline__ void naive_step(int p, uint64_t e, float &t0, float &t1) {
+        add_f16x2_f32(nvh[p], lo_f32(e), hi_f32(e), t0, t1);
+        nvh[p] = e4m3x2_to_f16x2(e4m3x2_from_f32(t0, t1));
+    }
+
+    // One shard; `first` says it is rank 0.
+    __device__ __forceinline__ void add(const uint4 &c, float sc, bool first) {
+        const uint64_t s2 = f32x2(sc, sc);
 #pragma unroll
-        for (int q = 0; q < 4; ++q) decode4(w4[q], e + 4 * q);
-        if constexpr ((NAIVE && AGOQ_REDUCE_PACKED_MUL) || AGOQ_REDUCE_PACKED_MUL == 2) {
-            // products in packed pairs, each sum a scalar round-to-nearest add
-            const uint64_t sc2 = f32x2(sc, sc);
-#pragma unroll
-            for (int i = 0; i < 16; i += 2) {
-                const uint64_t p2 = mul_f32x2(f32x2(e[i], e[i + 1]), sc2);
-                acc[i] = __fadd_rn(acc[i], lo_f32(p2));
-                acc[i + 1] = __fadd_rn(acc[i + 1], hi_f32(p2));
-            }
-        } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) acc[i] = __fadd_rn(acc[i], __fmul_rn(e[i], sc));
-        }
-        if constexpr (NAIVE) {
-#if AGOQ_NAIVE_MIXED_ADD
-            if (r == 0) {
-#pragma unroll
-                for (int q = 0; q < 4; ++q) {
-                    nvh[2 * q] = e4m3x2_to_f16x2(w4[q] & 0xFFFFu);
-                    nvh[2 * q + 1] = e4m3x2_to_f16x2(w4[q] >> 16);
-                }
-            } else {
-#pragma unroll
-                for (int p = 0; p < 8; ++p) {
-                    float t0, t1;   // exact: both operands are E4M3 values
-                    add_f16x2_f32(nvh[p], e[2 * p], e[2 * p + 1], t0, t1);
-#if AGOQ_NAIVE_MAX
+        for (int p = 0; p < 8; ++p) {
+            uint32_t h;
+            uint64_t e;
+            decode_add(c, s2, p, h, e);
+            if constexpr (NAIVE) {
+                if (first) {
+                    nvh[p] = h;
+                } else {
+                    float t0, t1;
+                    naive_step(p, e, t0, t1);
                     nmax[2 * p] = fmaxf(nmax[2 * p], fabsf(t0));
                     nmax[2 * p + 1] = fmaxf(nmax[2 * p + 1], fabsf(t1));
-#else
-                    if (fabsf(t0) > kE4M3Max) alive &= ~(1u << (2 * p));
-                    if (fabsf(t1) > kE4M3Max) alive &= ~(2u << (2 * p));
-#endif
-                    nvh[p] = e4m3x2_to_f16x2(e4m3x2_from_f32(t0, t1));
                 }
             }
-#else
-            if (r == 0) {
+        }
+    }
+
+    // Two consecutive shards a, b (a of rank 0 if `first`).  Elements are
+    // independent, so each pair takes a then b before the next pair.
+    __device__ __forceinline__ void add2(const uint4 &ca, float sa, const uint4 &cb, float sb,
+                                         bool first) {
+        const uint64_t sa2 = f32x2(sa, sa), sb2 = f32x2(sb, sb);
 #pragma unroll
-                for (int i = 0; i < 16; ++i) nv[i] = e[i];
-            } else {
-                float tt[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i) {
-                    tt[i] = __fadd_rn(nv[i], e[i]);   // exact: both are E4M3 values
-                    if (fabsf(tt[i]) > kE4M3Max) alive &= ~(1u << i);
+        for (int p = 0; p < 8; ++p) {
+            uint32_t ha, hb;
+            uint64_t ea, eb;
+            decode_add(ca, sa2, p, ha, ea);
+            decode_add(cb, sb2, p, hb, eb);
+            if constexpr (NAIVE) {
+                if (first) {
+                    nvh[p] = ha;
+                    float t0, t1;
+                    naive_step(p, eb, t0, t1);
+                    nmax[2 * p] = fmaxf(nmax[2 * p], fabsf(t0));
+                    nmax[2 * p + 1] = fmaxf(nmax[2 * p + 1], fabsf(t1));
+                } else {
+                    float a0, a1, b0, b1;
+                    naive_step(p, ea, a0, a1);
+                    naive_step(p, eb, b0, b1);
+                    nmax[2 * p] = max3_abs(nmax[2 * p], a0, b0);
+                    nmax[2 * p + 1] = max3_abs(nmax[2 * p + 1], a1, b1);
                 }
-#if AGOQ_NAIVE_ROUND_CVT
-#pragma unroll
-                for (int i = 0; i < 16; i += 2)
-                    e4m3x2_to_f32(e4m3x2_from_f32(tt[i], tt[i + 1]), nv[i], nv[i + 1]);
-#else
-#pragma unroll
-                for (int i = 0; i < 16; ++i) nv[i] = e4m3_round_f32(tt[i]);
-#endif
             }
-#endif
         }
     }
 
@@ -402,29 +289,44 @@ struct ReduceLane {
     // the lane's overflowed naive sums.  Every lane of the warp must call it.
     __device__ __forceinline__ void finish(bool valid, uint4 *out16, float *out_scale, bool first,
                                            unsigned long long &overflowed) {
-        float am = 0.0f;
+        float t[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) am = fmaxf(am, fabsf(acc[i]));
+        for (int p = 0; p < 8; ++p) {
+            t[2 * p] = lo_f32(acc[p]);
+            t[2 * p + 1] = hi_f32(acc[p]);
+        }
+        // |max| of the 16 sums as a tree of three-input maxima
+        float m[5];
+#pragma unroll
+        for (int i = 0; i < 5; ++i) m[i] = max3_abs(t[3 * i], t[3 * i + 1], t[3 * i + 2]);
+        float am = max3_abs(max3_abs(m[0], m[1], m[2]), max3_abs(m[3], m[4], t[15]), 0.0f);
         am = octet_max(am);
         const float snew = __fdiv_rn(am, kE4M3Max);
-        const uint2 lo = requant8(acc, snew);
-        const uint2 hi = requant8(acc + 8, snew);
+        const uint2 lo = e4m3_codes8(t, snew);
+        const uint2 hi = e4m3_codes8(t + 8, snew);
         if (valid) {
             *out16 = make_uint4(lo.x, lo.y, hi.x, hi.y);
             if (first) *out_scale = snew;
             if constexpr (NAIVE) {
-#if AGOQ_NAIVE_MAX
                 int k = 0;
 #pragma unroll
                 for (int i = 0; i < 16; ++i) k += nmax[i] > kE4M3Max;
                 overflowed += (unsigned long long)k;
-#else
-                overflowed += (unsigned long long)__popc(~alive & 0xFFFFu);
-#endif
             }
         }
     }
 };
+
+// Shards c[0..k-1] of a group whose first shard has rank r0, two at a time.
+template <bool NAIVE, int KMAX>
+__device__ __forceinline__ void add_group(ReduceLane<NAIVE> &st, const uint4 (&c)[KMAX],
+                                          const float (&sc)[KMAX], int k, int r0) {
+#pragma unroll
+    for (int j = 0; j < KMAX; j += 2) {
+        if (j + 1 < k) st.add2(c[j], sc[j], c[j + 1], sc[j + 1], r0 + j == 0);
+        else if (j < k) st.add(c[j], sc[j], r0 + j == 0);
+    }
+}
 
 // Sum of the warp's overflow counts, added to *naive_count by lane 0.
 __device__ __forceinline__ void flush_count(unsigned long long overflowed,
@@ -434,12 +336,15 @@ __device__ __forceinline__ void flush_count(unsigned long long overflowed,
     if ((threadIdx.x & 31) == 0 && overflowed) atomicAdd(naive_count, overflowed);
 }
 
-//
-// Block indices are 32-bit (the launcher splits larger inputs); shard r of
-// block b is at shards[r * shard_vec + 8 b ...] and its scale at
-// shard_scales[r * scale_stride + b].
+// ---- the register-staged reduce ---------------------------------------------
+// Used when the scale rows are not 16-byte aligned or n/128 is not a multiple
+// of 4.  Block indices are 32-bit (the launcher splits larger inputs); shard r
+// of block b is at shards[r * shard_vec + 8 b ...] and its scale at
+// shard_scales[r * scale_stride + b].  Each warp keeps the loads of its next
+// (block group, chunk of RUNROLL shards) in flight while it accumulates the
+// current chunk.
 template <bool NAIVE, int RUNROLL>
-__global__ void __launch_bounds__(kThreads, NAIVE ? AGOQ_REDUCE_COUNT_MIN_CTAS : AGOQ_REDUCE_MIN_CTAS)
+__global__ void __launch_bounds__(kThreads, 2)
 reduce_shards_kernel(
     const uint4 *__restrict__ shards, const float *__restrict__ shard_scales, int W,
     int64_t shard_vec, int64_t scale_stride, int nblocks, uint4 *__restrict__ out,
@@ -468,8 +373,6 @@ reduce_shards_kernel(
     unsigned long long overflowed = 0;
     int base = warp * 4;
     if (base < nblocks) {
-        // The loads of the next (block group, shard chunk) are always in flight
-        // while the current chunk is accumulated.
         uint4 cn[RUNROLL];
         float sn[RUNROLL];
         load(base, 0, cn, sn);
@@ -491,12 +394,8 @@ reduce_shards_kernel(
                 nbase = base + stride;
             }
             if (nbase < nblocks) load(nbase, nch, cn, sn);
-#pragma unroll
-            for (int u = 0; u < RUNROLL; ++u) {
-                const int r = ch * RUNROLL + u;
-                if (r >= W) break;
-                st.add_shard(c[u], sc[u], r);
-            }
+            const int k = W - ch * RUNROLL < RUNROLL ? W - ch * RUNROLL : RUNROLL;
+            add_group<NAIVE, RUNROLL>(st, c, sc, k, ch * RUNROLL);
             if (nch == 0) {
                 // all W shards of the block group are in: requantize and store
                 const int blk = base + oct;
@@ -515,23 +414,22 @@ reduce_shards_kernel(
 // ---- the staged reduce ------------------------------------------------------
 // A CTA is kStWarps consumer warps and one producer warp (16 + 1 without the
 // naive count; 15 + 1 with it, so that the CTA is 16 warps and a thread may
-// hold 128 registers).  Work is cut into
-// tiles of kStTile blocks (a consumer warp owns 4 blocks of a tile, laid out as
-// in reduce_shards_kernel); the CTAs take tiles round-robin.  The producer
-// walks (tile, group of kStShards shards) items in the order the consumers
-// take them and copies each shard's codes (kStTile * 128 bytes) and scales
-// (kStTile * 4 bytes) with cp.async.bulk into the next free stage of a
-// kStStages-deep ring (one barrier wait per group of shards): full[s]
-// completes when both copies have landed, empty[s] when every consumer warp
-// has read the stage.  Every wait is time-limited: on expiry the wait records
-// a timeout in g_reduce_status and raises the CTA's abort flag, the warps stop,
-// and the producer waits (time-limited) for its copies still in flight before
-// the CTA exits.
-constexpr int kStStages = AGOQ_RSTAGED_STAGES;
-constexpr int kStShards = AGOQ_RSTAGED_SHARDS;          // shards per stage
+// hold 128 registers).  Work is cut into tiles of kStTile blocks (a consumer
+// warp owns 4 blocks of a tile, laid out as in reduce_shards_kernel); the CTAs
+// take tiles round-robin.  The producer walks (tile, group of kStShards shards)
+// items in the order the consumers take them and copies each shard's codes
+// (kStTile * 128 bytes) and scales (kStTile * 4 bytes) with cp.async.bulk into
+// the next free stage of a kStStages-deep ring (one barrier wait per group of
+// shards): full[s] completes when both copies have landed, empty[s] when every
+// consumer warp has read the stage.  Every wait is time-limited: on expiry the
+// wait records a timeout in g_reduce_status and raises the CTA's abort flag,
+// the warps stop, and the producer waits (time-limited) for its copies still
+// in flight before the CTA exits.
+constexpr int kStStages = 2;
+constexpr int kStShards = 8;          // shards per stage
 template <bool NAIVE>
 struct StagedShape {
-    static constexpr int kWarps = NAIVE ? AGOQ_RSTAGED_COUNT_WARPS : AGOQ_RSTAGED_WARPS;
+    static constexpr int kWarps = NAIVE ? 15 : 16;
     static constexpr int kThreads = (kWarps + 1) * 32;
     static constexpr int kTile = 4 * kWarps;
     static constexpr int kCodeBytes = kStShards * kTile * 128;
@@ -556,7 +454,7 @@ __device__ __forceinline__ void bulk_g2s(void *dst, const void *src, uint32_t by
 // Requires shard_scales 16-byte aligned, scale_stride and nblocks multiples of
 // 4 (so every scale copy is whole 16-byte units).
 template <bool NAIVE>
-__global__ void __launch_bounds__(StagedShape<NAIVE>::kThreads, AGOQ_RSTAGED_MIN_CTAS)
+__global__ void __launch_bounds__(StagedShape<NAIVE>::kThreads, 1)
 reduce_shards_staged_kernel(
     const uint8_t *__restrict__ shards, const float *__restrict__ shard_scales, int W,
     int64_t shard_bytes, int64_t scale_stride, int nblocks, uint4 *__restrict__ out,
@@ -642,31 +540,51 @@ reduce_shards_staged_kernel(
         st.clear();
         for (int r0 = 0; r0 < W; r0 += kStShards) {
             const int k = W - r0 < kStShards ? W - r0 : kStShards;
-            if (!warp_wait(&full[stage], phase, abort, &g_reduce_status, AGOQ_RSTAGED_HINT)) {
+            if (!warp_wait(&full[stage], phase, abort, &g_reduce_status)) {
                 ok = false;
                 break;
             }
             mbar_try_wait(&full[stage], phase, 0);   // each lane observes the completed phase
             const uint8_t *cs = codes + (size_t)stage * kStCodeBytes + (size_t)(warp * 32 + lane) * 16;
             const float *ss = scl + (size_t)stage * kStShards * kStTile + lb;
-            uint4 c[kStShards];
-            float sc[kStShards];
-#pragma unroll
-            for (int j = 0; j < kStShards; ++j) {
-                if (j < k) {
-                    c[j] = *reinterpret_cast<const uint4 *>(cs + (size_t)j * kStTile * 128);
-                    sc[j] = ss[j * kStTile];
-                }
+            // Shards are read from the stage two at a time, the next pair's
+            // loads issued before the current pair is added; the stage is
+            // released once its last loads are issued (the arrive orders them).
+            uint4 c0 = *reinterpret_cast<const uint4 *>(cs);
+            float s0 = ss[0];
+            uint4 c1 = make_uint4(0u, 0u, 0u, 0u);
+            float s1 = 0.0f;
+            if (k > 1) {
+                c1 = *reinterpret_cast<const uint4 *>(cs + (size_t)kStTile * 128);
+                s1 = ss[kStTile];
             }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stage]);
+#pragma unroll
+            for (int j = 0; j < kStShards; j += 2) {
+                if (j >= k) break;
+                uint4 n0 = c0, n1 = c1;
+                float t0 = s0, t1 = s1;
+                if (j + 2 < k) {
+                    n0 = *reinterpret_cast<const uint4 *>(cs + (size_t)(j + 2) * kStTile * 128);
+                    t0 = ss[(j + 2) * kStTile];
+                    if (j + 3 < k) {
+                        n1 = *reinterpret_cast<const uint4 *>(cs + (size_t)(j + 3) * kStTile * 128);
+                        t1 = ss[(j + 3) * kStTile];
+                    }
+                } else {
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&empty[stage]);
+                }
+                if (j + 1 < k) st.add2(c0, s0, c1, s1, r0 + j == 0);
+                else st.add(c0, s0, r0 + j == 0);
+                c0 = n0;
+                c1 = n1;
+                s0 = t0;
+                s1 = t1;
+            }
             if (++stage == kStStages) {
                 stage = 0;
                 phase ^= 1u;
             }
-#pragma unroll
-            for (int j = 0; j < kStShards; ++j)
-                if (j < k) st.add_shard(c[j], sc[j], r0 + j);
         }
         if (!ok) break;
         st.finish(blk < nblocks, out + (size_t)(unsigned)blk * 8 + t8, out_scales + blk, t8 == 0,
@@ -685,18 +603,18 @@ reduce_shards_staged_kernel(
 // master (the producer never reads a tile twice, so the in-place update races
 // nothing).  The arithmetic is accum_block, as in grad_accum_kernel.  Waits are
 // time-limited (status in g_reduce_status, this file's pipeline status word).
-constexpr int kAcWarps = AGOQ_ASTAGED_WARPS;
+constexpr int kAcWarps = 16;
 constexpr int kAcThreads = (kAcWarps + 1) * 32;
-constexpr int kAcRep = AGOQ_ASTAGED_REP;                 // blocks per half warp per stage
+constexpr int kAcRep = 3;                               // blocks per half warp per stage
 constexpr int kAcTile = 2 * kAcWarps * kAcRep;
-constexpr int kAcStages = AGOQ_ASTAGED_STAGES;
+constexpr int kAcStages = 3;
 constexpr int kAcGradBytes = kAcTile * 256, kAcCodeBytes = kAcTile * 128;
 constexpr int kAcStageBytes = kAcGradBytes + kAcCodeBytes + kAcTile * 4;
 constexpr size_t kAcSmem = (size_t)kAcStages * (kAcStageBytes + 16);
 static_assert(kAcTile % 4 == 0 && kAcStageBytes % 16 == 0, "whole 16-byte copies");
 
 template <int MID>
-__global__ void __launch_bounds__(kAcThreads, AGOQ_ASTAGED_MIN_CTAS)
+__global__ void __launch_bounds__(kAcThreads, 1)
 grad_accum_staged_kernel(uint8_t *__restrict__ master, float *__restrict__ scales,
                          const uint8_t *__restrict__ grad, int64_t nblocks) {
     using namespace gemm;
@@ -797,8 +715,7 @@ namespace {
 template <int MID>
 cudaError_t launch_grad_accum_mid(void *master, float *master_scales, const void *grad, int64_t n,
                                   cudaStream_t st) {
-    if (AGOQ_ACCUM_STAGED && (n / kBlock) % 4 == 0 &&
-        reinterpret_cast<uintptr_t>(master_scales) % 16 == 0) {
+    if ((n / kBlock) % 4 == 0 && reinterpret_cast<uintptr_t>(master_scales) % 16 == 0) {
         static bool smem_set[kMaxDevices];
         static int cache_st[kMaxDevices];
         int dev = 0;
@@ -818,7 +735,7 @@ cudaError_t launch_grad_accum_mid(void *master, float *master_scales, const void
                           static_cast<uint8_t *>(master), master_scales,
                           static_cast<const uint8_t *>(grad), nbs);
     }
-    constexpr int kUnroll = AGOQ_ACCUM_UNROLL;
+    constexpr int kUnroll = 4;
     static int cache[kMaxDevices];
     const int64_t nb = n / kBlock;
     auto k = grad_accum_kernel<kUnroll, MID>;
@@ -893,7 +810,7 @@ cudaError_t read_and_clear_reduce_status(unsigned *status) {
 cudaError_t launch_reduce_shards(const void *shards, const float *shard_scales, int W, int64_t n,
                                  void *out, float *out_scales, unsigned long long *naive_count,
                                  cudaStream_t st) {
-    constexpr int kRUnroll = AGOQ_REDUCE_RUNROLL;
+    constexpr int kRUnroll = 8, kRUnrollCount = 4;
     constexpr int64_t kMaxLaunchBlocks = int64_t(1) << 30;
     const int64_t nb_all = n / kBlock;
     const int64_t per_cta = 4 * (kThreads / 32);
@@ -901,11 +818,10 @@ cudaError_t launch_reduce_shards(const void *shards, const float *shard_scales, 
         cudaError_t e = cudaMemsetAsync(naive_count, 0, sizeof(unsigned long long), st);
         if (e != cudaSuccess) return e;
     }
-    if (AGOQ_REDUCE_STAGED && nb_all % 4 == 0 &&
-        reinterpret_cast<uintptr_t>(shard_scales) % 16 == 0)
+    if (nb_all % 4 == 0 && reinterpret_cast<uintptr_t>(shard_scales) % 16 == 0)
         return launch_reduce_staged(shards, shard_scales, W, n, out, out_scales, naive_count, st);
     static int cache_count[kMaxDevices], cache_plain[kMaxDevices];
-    auto kc = reduce_shards_kernel<true, AGOQ_REDUCE_COUNT_RUNROLL>;
+    auto kc = reduce_shards_kernel<true, kRUnrollCount>;
     auto kp = reduce_shards_kernel<false, kRUnroll>;
     for (int64_t b0 = 0; b0 < nb_all; b0 += kMaxLaunchBlocks) {
         const int64_t nb = nb_all - b0 < kMaxLaunchBlocks ? nb_all - b0 : kMaxLaunchBlocks;
