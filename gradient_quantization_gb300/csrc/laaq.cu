@@ -19,49 +19,13 @@
 #include "agoq_device.cuh"
 #include "agoq_launch.h"
 
-#ifndef AGOQ_QUANT_UNROLL
-#define AGOQ_QUANT_UNROLL 2
-#endif
-#ifndef AGOQ_DEQUANT_UNROLL
-#define AGOQ_DEQUANT_UNROLL 2
-#endif
-#ifndef AGOQ_QUANT_MIN_CTAS
-#define AGOQ_QUANT_MIN_CTAS 3
-#endif
-// 1: each warp issues the loads of its next group of blocks before the
-// arithmetic of the current one (register double buffering).
-#ifndef AGOQ_SILU_UNROLL
-#define AGOQ_SILU_UNROLL 1
-#endif
-#ifndef AGOQ_SILU_MIN_CTAS
-#define AGOQ_SILU_MIN_CTAS 4
-#endif
-#ifndef AGOQ_SILU_Y_MIN_CTAS
-#define AGOQ_SILU_Y_MIN_CTAS 3
-#endif
-#ifndef AGOQ_SILU_FAST_EXP
-#define AGOQ_SILU_FAST_EXP 1
-#endif
-// Block groups per warp whose inputs are prefetched into L2 before the wait on
-// the preceding grid (0: none).
-#ifndef AGOQ_PDL_PREFETCH
-#define AGOQ_PDL_PREFETCH 1
-#endif
-#ifndef AGOQ_QUANT_PIPELINE
-#define AGOQ_QUANT_PIPELINE 1
-#endif
-#ifndef AGOQ_DEQUANT_MIN_CTAS
-#define AGOQ_DEQUANT_MIN_CTAS 1
-#endif
-// 1: codes of 4, 5 and 6 bits are rounded with a biased constant and packed by
-// shifted additions (pack_biased8) instead of masks and shifts.
-#ifndef AGOQ_PACK_BIASED
-#define AGOQ_PACK_BIASED 1
-#endif
-// 1: block scales fl(absmax / qmax) by bf16_div_qmax instead of IEEE division.
-#ifndef AGOQ_SCALE_MARKSTEIN
-#define AGOQ_SCALE_MARKSTEIN 1
-#endif
+// Measured choices: quantize 2 block groups per warp in flight with the next
+// group's loads issued before the current group's arithmetic (3 CTAs of 256
+// threads per SM); dequantize 2 groups per warp, software-pipelined; SiLU
+// backward 1 group (4 CTAs per SM, 3 with the recomputed forward output); one
+// block group per warp prefetched into L2 before the wait on the preceding grid.
+constexpr int kQuantUnroll = 2, kDequantUnroll = 2, kSiluUnroll = 1;
+constexpr int kQuantMinCtas = 3, kSiluMinCtas = 4, kSiluYMinCtas = 3;
 
 
 namespace agoq {
@@ -132,28 +96,21 @@ __device__ __forceinline__ void store_chunk_set(uint32_t *rec, int j, int set, u
 // Block indices are 32-bit: the launcher splits inputs of more than
 // kMaxLaunchBlocks blocks into several launches.
 template <int BITS, int UNROLL>
-__global__ void __launch_bounds__(kThreads, AGOQ_QUANT_MIN_CTAS)
+__global__ void __launch_bounds__(kThreads, kQuantMinCtas)
 laaq_quant_kernel(const uint4 *__restrict__ x, uint32_t *__restrict__ codes,
                   float *__restrict__ scales, int nblocks) {
-    if constexpr (AGOQ_PDL_PREFETCH > 0) {
-        // this warp's first groups of 4 * UNROLL blocks (256 bytes each)
-        const int w0 = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-        const int nw = (int)((gridDim.x * blockDim.x) >> 5);
-        if ((threadIdx.x & 31) == 0) {
-#pragma unroll
-            for (int g = 0; g < AGOQ_PDL_PREFETCH; ++g) {
-                const int b0 = (w0 + g * nw) * (4 * UNROLL);
-                if (b0 < nblocks) {
-                    const int nb = nblocks - b0 < 4 * UNROLL ? nblocks - b0 : 4 * UNROLL;
-                    prefetch_l2(x + (size_t)(unsigned)b0 * 16, (uint32_t)nb * 256u);
-                }
-            }
+    {
+        // this warp's first group of 4 * UNROLL blocks (256 bytes each)
+        const int b0 = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * (4 * UNROLL);
+        if ((threadIdx.x & 31) == 0 && b0 < nblocks) {
+            const int nb = nblocks - b0 < 4 * UNROLL ? nblocks - b0 : 4 * UNROLL;
+            prefetch_l2(x + (size_t)(unsigned)b0 * 16, (uint32_t)nb * 256u);
         }
     }
     pdl_wait_and_release();
     constexpr int kWords = 4 * BITS;
     constexpr int kQmax = (1 << (BITS - 1)) - 1;
-    constexpr bool kBiased = AGOQ_PACK_BIASED && BITS < 8;
+    constexpr bool kBiased = BITS < 8;
     constexpr int kBias = kBiased ? (1 << (BITS - 1)) : 0;
     const int lane = threadIdx.x & 31;
     const int oct = lane >> 3, j = lane & 7;
@@ -173,19 +130,12 @@ laaq_quant_kernel(const uint4 *__restrict__ x, uint32_t *__restrict__ codes,
             }
         }
     };
-#if AGOQ_QUANT_PIPELINE
     // The next group's loads are issued before this group's arithmetic.
     uint4 va[UNROLL], vb[UNROLL];
     load_group(warp * (4 * UNROLL), va, vb);
-#endif
     for (int base = warp * (4 * UNROLL); base < nblocks; base += stride) {
-#if AGOQ_QUANT_PIPELINE
         uint4 na[UNROLL], nb[UNROLL];
         load_group(base + stride, na, nb);
-#else
-        uint4 va[UNROLL], vb[UNROLL];
-        load_group(base, va, vb);
-#endif
         uint32_t w[UNROLL][8];
         float s[UNROLL];
         bool fast = true;
@@ -194,11 +144,7 @@ laaq_quant_kernel(const uint4 *__restrict__ x, uint32_t *__restrict__ codes,
             w[u][0] = va[u].x; w[u][1] = va[u].y; w[u][2] = va[u].z; w[u][3] = va[u].w;
             w[u][4] = vb[u].x; w[u][5] = vb[u].y; w[u][6] = vb[u].z; w[u][7] = vb[u].w;
             const float am = octet_max(bf16_absmax<8>(w[u]));
-#if AGOQ_SCALE_MARKSTEIN
             s[u] = bf16_div_qmax<kQmax>(am);               // +0 for an all-zero block
-#else
-            s[u] = __fdiv_rn(am, (float)kQmax);
-#endif
             fast &= s[u] >= 0x1p-96f;
         }
         uint32_t cb[UNROLL][16];
@@ -234,13 +180,11 @@ laaq_quant_kernel(const uint4 *__restrict__ x, uint32_t *__restrict__ codes,
             store_chunk_set<BITS>(rec, j, 1, lo, hi, valid);
             if (valid && j == 0) scales[blk] = s[u];
         }
-#if AGOQ_QUANT_PIPELINE
 #pragma unroll
         for (int u = 0; u < UNROLL; ++u) {
             va[u] = na[u];
             vb[u] = nb[u];
         }
-#endif
     }
 }
 
@@ -273,26 +217,19 @@ struct DequantBatch {
 // Software-pipelined: the next batch's code and scale loads are issued before
 // the current batch is converted and stored, so loads stay in flight.
 template <int BITS, int UNROLL>
-__global__ void __launch_bounds__(kThreads, AGOQ_DEQUANT_MIN_CTAS) laaq_dequant_kernel(const uint32_t *__restrict__ codes,
+__global__ void __launch_bounds__(kThreads, 1) laaq_dequant_kernel(const uint32_t *__restrict__ codes,
                                                                 const float *__restrict__ scales,
                                                                 uint4 *__restrict__ y,
                                                                 int nblocks) {
-    if constexpr (AGOQ_PDL_PREFETCH > 0) {
-        // codes and scales of this warp's first groups of 4 * UNROLL blocks
-        const int w0 = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
-        const int nw = (int)((gridDim.x * blockDim.x) >> 5);
-        if ((threadIdx.x & 31) == 0) {
-#pragma unroll
-            for (int g = 0; g < AGOQ_PDL_PREFETCH; ++g) {
-                const int b0 = (w0 + g * nw) * (4 * UNROLL);
-                if (b0 < nblocks) {
-                    const int nb = nblocks - b0 < 4 * UNROLL ? nblocks - b0 : 4 * UNROLL;
-                    prefetch_l2(codes + (size_t)(unsigned)b0 * (4 * BITS), (uint32_t)nb * (16u * BITS));
-                    // scales need only 4-byte alignment: prefetched when 16-byte aligned
-                    if (nb % 4 == 0 && (reinterpret_cast<uintptr_t>(scales + b0) & 15u) == 0)
-                        prefetch_l2(scales + b0, (uint32_t)nb * 4u);
-                }
-            }
+    {
+        // codes and scales of this warp's first group of 4 * UNROLL blocks
+        const int b0 = (int)((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * (4 * UNROLL);
+        if ((threadIdx.x & 31) == 0 && b0 < nblocks) {
+            const int nb = nblocks - b0 < 4 * UNROLL ? nblocks - b0 : 4 * UNROLL;
+            prefetch_l2(codes + (size_t)(unsigned)b0 * (4 * BITS), (uint32_t)nb * (16u * BITS));
+            // scales need only 4-byte alignment: prefetched when 16-byte aligned
+            if (nb % 4 == 0 && (reinterpret_cast<uintptr_t>(scales + b0) & 15u) == 0)
+                prefetch_l2(scales + b0, (uint32_t)nb * 4u);
         }
     }
     pdl_wait_and_release();
@@ -327,7 +264,6 @@ __global__ void __launch_bounds__(kThreads, AGOQ_DEQUANT_MIN_CTAS) laaq_dequant_
 // values xh of a chunk and the matching upstream gradients dy, in binary32:
 //   sigma = 1 / (1 + exp(-xh));  silu'(xh) = sigma * (1 + xh * (1 - sigma));
 //   dx = bf16(dy * silu'(xh));   y = bf16(xh * sigma)  (the recomputed forward output).
-#if AGOQ_SILU_FAST_EXP
 // e^-x as 2^(-x log2 e) by the hardware's approximate base-2 exponential, and
 // the approximate reciprocal (each within a few binary32 ulps; subnormal
 // results flush to zero, which leaves sigma at 1 or 0 where they occur).
@@ -341,14 +277,12 @@ __device__ __forceinline__ float rcp_approx(float a) {
     asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(a));
     return r;
 }
-#endif
 
 template <bool WITH_Y>
 __device__ __forceinline__ void silu_backward_chunk(uint4 xh, uint4 dy, uint4 &dx, uint4 &y) {
     const uint32_t xw[4] = {xh.x, xh.y, xh.z, xh.w};
     const uint32_t dw[4] = {dy.x, dy.y, dy.z, dy.w};
     uint32_t o[4], yo[4];
-#if AGOQ_SILU_FAST_EXP
     constexpr float kNegLog2e = -1.4426950408889634f;
     const uint64_t nl2e = f32x2(kNegLog2e, kNegLog2e), one = f32x2(1.0f, 1.0f);
 #pragma unroll
@@ -367,23 +301,6 @@ __device__ __forceinline__ void silu_backward_chunk(uint4 xh, uint4 dy, uint4 &d
             yo[p] = pack_bf16x2(lo_f32(yy), hi_f32(yy));
         }
     }
-#else
-#pragma unroll
-    for (int p = 0; p < 4; ++p) {
-        float r[2], yy[2];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const float x = h ? bf16_hi(xw[p]) : bf16_lo(xw[p]);
-            const float d = h ? bf16_hi(dw[p]) : bf16_lo(dw[p]);
-            const float sg = __frcp_rn(__fadd_rn(1.0f, expf(-x)));
-            const float g = __fmul_rn(sg, __fadd_rn(1.0f, __fmul_rn(x, __fsub_rn(1.0f, sg))));
-            r[h] = __fmul_rn(d, g);
-            yy[h] = __fmul_rn(x, sg);
-        }
-        o[p] = pack_bf16x2(r[0], r[1]);
-        if constexpr (WITH_Y) yo[p] = pack_bf16x2(yy[0], yy[1]);
-    }
-#endif
     dx = make_uint4(o[0], o[1], o[2], o[3]);
     if constexpr (WITH_Y) y = make_uint4(yo[0], yo[1], yo[2], yo[3]);
 }
@@ -393,7 +310,7 @@ __device__ __forceinline__ void silu_backward_chunk(uint4 xh, uint4 dy, uint4 &d
 // the next batch's code, scale and gradient loads are issued before the
 // current batch's arithmetic.
 template <int BITS, int UNROLL, bool WITH_Y>
-__global__ void __launch_bounds__(kThreads, WITH_Y ? AGOQ_SILU_Y_MIN_CTAS : AGOQ_SILU_MIN_CTAS) laaq_silu_backward_kernel(
+__global__ void __launch_bounds__(kThreads, WITH_Y ? kSiluYMinCtas : kSiluMinCtas) laaq_silu_backward_kernel(
     const uint32_t *__restrict__ codes, const float *__restrict__ scales,
     const uint4 *__restrict__ dy, uint4 *__restrict__ dx, uint4 *__restrict__ y,
     int nblocks) {
@@ -470,7 +387,7 @@ constexpr int64_t kMaxLaunchBlocks = int64_t(1) << 30;
 
 template <int BITS>
 cudaError_t quant_bits(const void *x, int64_t nblocks, void *codes, float *scales, cudaStream_t st) {
-    constexpr int kU = AGOQ_QUANT_UNROLL;
+    constexpr int kU = kQuantUnroll;
     static int cache[kMaxDevices];
     auto k = laaq_quant_kernel<BITS, kU>;
     const int64_t per_cta = 4 * kU * (kThreads / 32);
@@ -488,7 +405,7 @@ cudaError_t quant_bits(const void *x, int64_t nblocks, void *codes, float *scale
 template <int BITS>
 cudaError_t dequant_bits(const void *codes, const float *scales, int64_t nblocks, void *y,
                          cudaStream_t st) {
-    constexpr int kU = AGOQ_DEQUANT_UNROLL;
+    constexpr int kU = kDequantUnroll;
     static int cache[kMaxDevices];
     auto k = laaq_dequant_kernel<BITS, kU>;
     const int64_t per_cta = 4 * kU * (kThreads / 32);
@@ -506,7 +423,7 @@ cudaError_t dequant_bits(const void *codes, const float *scales, int64_t nblocks
 template <int BITS, bool WITH_Y>
 cudaError_t silu_backward_bits(const void *codes, const float *scales, const void *dy,
                                int64_t nblocks, void *dx, void *y, cudaStream_t st) {
-    constexpr int kU = AGOQ_SILU_UNROLL;
+    constexpr int kU = kSiluUnroll;
     static int cache[kMaxDevices];
     auto k = laaq_silu_backward_kernel<BITS, kU, WITH_Y>;
     const int64_t per_cta = 4 * kU * (kThreads / 32);

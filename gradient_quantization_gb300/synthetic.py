@@ -8,8 +8,13 @@ the oracle, the bench uses the library.
 
 Two families of generators share each recipe:
 
-* ``*_np`` functions use ``numpy.random.default_rng(seed)`` (PCG64) and return
-  BF16 bit patterns as ``numpy.uint16``; the draw order is part of the recipe.
+* ``*_np`` functions use numpy's PCG64 and return BF16 bit patterns as
+  ``numpy.uint16``.  A tensor is drawn in chunks of ``CHUNK`` consecutive
+  elements; chunk c of tensor t comes from its own stream,
+  ``PCG64(SeedSequence(seed, spawn_key=(t, c)))``, and within a chunk the
+  values are drawn first, then the outlier mask.  The chunks are independent,
+  so full-size tensors are drawn by several threads at once (numpy releases
+  the GIL while it draws) with the same result as one thread.
 * ``*_torch`` functions draw the same distributions on a torch device with a
   seeded ``torch.Generator``; they serve full-size runs, where the host would
   spend minutes drawing numbers.  Their values differ from the numpy ones.
@@ -19,6 +24,9 @@ LAAQ section of "AGoQ: Activation and Gradient Quantization for
 Memory-Efficient Distributed Training of LLMs" quantizes (RMSNorm and SiLU
 inputs); no real activations or weights are used.
 """
+import concurrent.futures as _cf
+import os
+
 import numpy as np
 import torch
 
@@ -45,60 +53,91 @@ def bf16_tensor_from_bits(bits: np.ndarray) -> torch.Tensor:
 
 
 # ---------------------------------------------------------------- numpy recipes
-def outlier_normal_np(rng, n, p=1e-3, factor=20.0):
-    """N(0,1) float32 draws, then a Bernoulli(p) mask (drawn after the values)
-    whose entries are multiplied by ``factor``."""
+CHUNK = 1 << 22   # elements per independently seeded chunk
+
+
+def chunk_rng(seed, tensor, chunk):
+    """The PCG64 generator of chunk ``chunk`` of tensor ``tensor`` under ``seed``."""
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(seed, spawn_key=(tensor, chunk))))
+
+
+def draw_bf16_np(seed, tensor, n, draw):
+    """BF16 bit patterns [n] of one tensor: ``draw(rng, size)`` returns the float32
+    values of one chunk; chunks are drawn (and rounded to BF16) in parallel."""
+    out = np.empty(n, np.uint16)
+    nchunks = (n + CHUNK - 1) // CHUNK
+
+    def one(c):
+        lo = c * CHUNK
+        hi = min(n, lo + CHUNK)
+        out[lo:hi] = bf16_bits_from_f32(draw(chunk_rng(seed, tensor, c), hi - lo))
+
+    if nchunks <= 1:
+        for c in range(nchunks):
+            one(c)
+    else:
+        with _cf.ThreadPoolExecutor(max_workers=min(nchunks, os.cpu_count() or 1)) as ex:
+            list(ex.map(one, range(nchunks)))
+    return out
+
+
+def outlier_normal_np(rng, n, p=1e-3, factor=20.0, sd=1.0):
+    """sd * N(0,1) float32 draws, then a Bernoulli(p) mask (drawn after the
+    values) whose entries are multiplied by ``factor``."""
     x = rng.standard_normal(n, dtype=np.float32)
+    if sd != 1.0:
+        x *= np.float32(sd)
     mask = rng.random(n, dtype=np.float32) < p
     x[mask] *= np.float32(factor)
     return x
 
 
 def laaq_activation_np(seed=0, tokens=LAAQ_INT4_SHAPE[0], hidden=LAAQ_INT4_SHAPE[1]):
-    """BF16 activation [tokens x hidden]: N(0,1) with 0.1% of entries x20."""
-    rng = np.random.default_rng(seed)
-    return bf16_bits_from_f32(outlier_normal_np(rng, tokens * hidden)).reshape(tokens, hidden)
+    """BF16 activation [tokens x hidden]: N(0,1) with 0.1% of entries x20 (tensor 0)."""
+    return draw_bf16_np(seed, 0, tokens * hidden, outlier_normal_np).reshape(tokens, hidden)
 
 
 def dbca_activations_np(seed=1, tokens=DBCA_RMSNORM_SHAPE[0], hidden=DBCA_RMSNORM_SHAPE[1],
                         ffn=DBCA_SILU_SHAPE[1]):
-    """(RMSNorm input [tokens x hidden], SiLU input [tokens x ffn]), Student-t nu=4, BF16."""
-    rng = np.random.default_rng(seed)
-    a = rng.standard_t(4, tokens * hidden).astype(np.float32)
-    b = rng.standard_t(4, tokens * ffn).astype(np.float32)
-    return (bf16_bits_from_f32(a).reshape(tokens, hidden),
-            bf16_bits_from_f32(b).reshape(tokens, ffn))
+    """(RMSNorm input [tokens x hidden] (tensor 0), SiLU input [tokens x ffn] (tensor 1)),
+    Student-t nu=4, BF16."""
+    t4 = lambda rng, m: rng.standard_t(4, m).astype(np.float32)   # noqa: E731
+    return (draw_bf16_np(seed, 0, tokens * hidden, t4).reshape(tokens, hidden),
+            draw_bf16_np(seed, 1, tokens * ffn, t4).reshape(tokens, ffn))
+
+
+def quangrad_grad_np(seed=2, step=0, n=QUANGRAD_N):
+    """Micro-batch ``step`` (tensor ``step``): N(0, sd 1e-3), 0.01% of entries x1000, BF16."""
+    draw = lambda rng, m: outlier_normal_np(rng, m, p=1e-4, factor=1000.0, sd=1e-3)   # noqa: E731
+    return draw_bf16_np(seed, step, n, draw)
 
 
 def quangrad_grads_np(seed=2, n=QUANGRAD_N, steps=QUANGRAD_STEPS):
-    """Yield ``steps`` BF16 micro-batch gradients: N(0, sd 1e-3), 0.01% of entries x1000."""
-    rng = np.random.default_rng(seed)
-    for _ in range(steps):
-        g = rng.standard_normal(n, dtype=np.float32) * np.float32(1e-3)
-        mask = rng.random(n, dtype=np.float32) < 1e-4
-        g[mask] *= np.float32(1000.0)
-        yield bf16_bits_from_f32(g)
+    """Yield the ``steps`` BF16 micro-batch gradients in order."""
+    for k in range(steps):
+        yield quangrad_grad_np(seed, k, n)
 
 
 def reduce_shard_values_np(seed=3, W=8, n=REDUCE_N):
-    """BF16 values of W shards [W][n]: shard r is N(0, sd 1e-2 * j_r), j_r ~ U[0.5, 2)
-    drawn first for all shards.  The caller block-quantizes each shard to FP8."""
-    rng = np.random.default_rng(seed)
-    j = rng.uniform(0.5, 2.0, W).astype(np.float32)
+    """BF16 values of W shards [W][n]: shard r (tensor r + 1) is N(0, sd 1e-2 * j_r),
+    with the factors j_r ~ U[0.5, 2) drawn first, from tensor 0's stream.  The
+    caller block-quantizes each shard to FP8."""
+    j = chunk_rng(seed, 0, 0).uniform(0.5, 2.0, W).astype(np.float32)
     out = np.empty((W, n), np.uint16)
     for r in range(W):
-        v = rng.standard_normal(n, dtype=np.float32) * np.float32(1e-2) * j[r]
-        out[r] = bf16_bits_from_f32(v)
+        sd = np.float32(np.float32(1e-2) * j[r])
+        out[r] = draw_bf16_np(seed, r + 1, n,
+                              lambda rng, m, sd=sd: rng.standard_normal(m, dtype=np.float32) * sd)
     return out
 
 
 def wgrad_inputs_np(seed=4, M=WGRAD_M, N=WGRAD_N, K=WGRAD_K):
-    """(dY BF16 [K x M] ~ N(0, sd 1e-2), X BF16 [K x N] ~ N(0,1) with 0.1% x20).
-    The caller quantizes X with the 4-bit LAAQ rule."""
-    rng = np.random.default_rng(seed)
-    dy = rng.standard_normal(K * M, dtype=np.float32) * np.float32(1e-2)
-    x = outlier_normal_np(rng, K * N)
-    return bf16_bits_from_f32(dy).reshape(K, M), bf16_bits_from_f32(x).reshape(K, N)
+    """(dY BF16 [K x M] ~ N(0, sd 1e-2) (tensor 0), X BF16 [K x N] ~ N(0,1) with
+    0.1% x20 (tensor 1)).  The caller quantizes X with the 4-bit LAAQ rule."""
+    dy = draw_bf16_np(seed, 0, K * M,
+                      lambda rng, m: rng.standard_normal(m, dtype=np.float32) * np.float32(1e-2))
+    x = draw_bf16_np(seed, 1, K * N, outlier_normal_np)
+    return dy.reshape(K, M), x.reshape(K, N)
 
 
 def wgrad_exact_sum_inputs_np(seed=5, M=WGRAD_M, N=WGRAD_N, K=WGRAD_K):

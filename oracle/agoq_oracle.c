@@ -28,6 +28,11 @@
  * round-to-nearest-even; the file must be compiled with -ffp-contract=off and
  * without fast-math so that no multiply-add is fused.
  *
+ * The outer loops over blocks (or rows, or sampled entries) carry OpenMP
+ * pragmas.  Every iteration writes only its own outputs and the naive overflow
+ * count is a sum, so the single-threaded build (pragmas ignored) and the
+ * all-core build (-fopenmp) compute the same bits; a test compares them.
+ *
  * Parity pins: every function here is pinned by tests under tests/ (codec
  * sweeps against library casts, exact-rational brute force, closed forms and
  * invariants).  No function in this file is "parity unpinned".
@@ -36,6 +41,9 @@
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
 
 #define OR_BLOCK 128
 
@@ -200,6 +208,7 @@ int or_quant_act(const uint16_t *x, int64_t n, int bits, uint8_t *codes, float *
         return OR_BAD_ARG;
     const int32_t qmax = (1 << (bits - 1)) - 1;
     const int64_t rec_bytes = 16 * (int64_t)bits;
+#pragma omp parallel for schedule(static)
     for (int64_t b = 0; b < n / OR_BLOCK; ++b) {
         const uint16_t *xb = x + b * OR_BLOCK;
         uint8_t *rec = codes + b * rec_bytes;
@@ -236,6 +245,7 @@ int or_dequant_act(const uint8_t *codes, const float *scales, int64_t n, int bit
     if (!or_bits_ok(bits) || n < 0 || n % OR_BLOCK)
         return OR_BAD_ARG;
     const int64_t rec_bytes = 16 * (int64_t)bits;
+#pragma omp parallel for schedule(static)
     for (int64_t b = 0; b < n / OR_BLOCK; ++b) {
         const uint8_t *rec = codes + b * rec_bytes;
         float s = scales[b];
@@ -262,6 +272,7 @@ int or_silu_backward(const uint8_t *codes, const float *scales, const uint16_t *
     if (!or_bits_ok(bits) || n < 0 || n % OR_BLOCK)
         return OR_BAD_ARG;
     const int64_t rec_bytes = 16 * (int64_t)bits;
+#pragma omp parallel for schedule(static)
     for (int64_t b = 0; b < n / OR_BLOCK; ++b) {
         const uint8_t *rec = codes + b * rec_bytes;
         float s = scales[b];
@@ -350,8 +361,9 @@ int or_grad_accum_fp8(uint8_t *master, float *master_scales, const uint16_t *gra
 {
     if (n < 0 || n % OR_BLOCK)
         return OR_BAD_ARG;
-    float t[OR_BLOCK];
+#pragma omp parallel for schedule(static)
     for (int64_t b = 0; b < n / OR_BLOCK; ++b) {
+        float t[OR_BLOCK];
         uint8_t *cb = master + b * OR_BLOCK;
         float s = master_scales[b];
         for (int i = 0; i < OR_BLOCK; ++i) {
@@ -382,8 +394,9 @@ int or_grad_accum_fp8_mid(uint8_t *master, float *master_scales, const uint16_t 
     if (n < 0 || n % OR_BLOCK || (mid != 1 && mid != 2))
         return OR_BAD_ARG;
     const int p = mid == 1 ? 8 : 11, emin = mid == 1 ? -126 : -14, emax = mid == 1 ? 127 : 15;
-    float t[OR_BLOCK];
+#pragma omp parallel for schedule(static)
     for (int64_t b = 0; b < n / OR_BLOCK; ++b) {
+        float t[OR_BLOCK];
         uint8_t *cb = master + b * OR_BLOCK;
         float s = master_scales[b];
         for (int i = 0; i < OR_BLOCK; ++i) {
@@ -417,8 +430,9 @@ int or_reduce_fp8_shards(const uint8_t *shards, const float *shard_scales, int W
         return OR_BAD_ARG;
     const int64_t nb = n / OR_BLOCK;
     uint64_t overflow = 0;
-    float acc[OR_BLOCK];
+#pragma omp parallel for schedule(static) reduction(+ : overflow)
     for (int64_t b = 0; b < nb; ++b) {
+        float acc[OR_BLOCK];
         for (int i = 0; i < OR_BLOCK; ++i)
             acc[i] = 0.0f;
         for (int r = 0; r < W; ++r) {
@@ -472,9 +486,11 @@ int or_wgrad_gemm_int4_f64(const uint16_t *dY, const uint8_t *xc, const float *x
     double *xhat = (double *)malloc(sizeof(double) * (size_t)K * (size_t)N);
     if (!xhat)
         return OR_BAD_ARG;
+#pragma omp parallel for schedule(static)
     for (int64_t k = 0; k < K; ++k)
         for (int64_t j = 0; j < N; ++j)
             xhat[k * N + j] = or_xhat(xc, xs, N, k, j);
+#pragma omp parallel for schedule(static)
     for (int64_t i = 0; i < M; ++i)
         for (int64_t j = 0; j < N; ++j) {
             double acc = 0.0;
@@ -494,10 +510,12 @@ int or_wgrad_gemm_int4_f64_entries(const uint16_t *dY, const uint8_t *xc, const 
 {
     if (M <= 0 || N <= 0 || K <= 0 || N % OR_BLOCK || count < 0)
         return OR_BAD_ARG;
+    for (int64_t e = 0; e < count; ++e)
+        if (rows[e] < 0 || rows[e] >= M || cols[e] < 0 || cols[e] >= N)
+            return OR_BAD_ARG;
+#pragma omp parallel for schedule(dynamic, 16)
     for (int64_t e = 0; e < count; ++e) {
         int64_t i = rows[e], j = cols[e];
-        if (i < 0 || i >= M || j < 0 || j >= N)
-            return OR_BAD_ARG;
         double acc = 0.0;
         for (int64_t k = 0; k < K; ++k)
             acc += (double)or_bf16_to_f32(dY[k * M + i]) * or_xhat(xc, xs, N, k, j);
@@ -516,8 +534,9 @@ int or_grad_accum_fp8_f32(uint8_t *master, float *master_scales, const float *gr
 {
     if (n < 0 || n % OR_BLOCK)
         return OR_BAD_ARG;
-    float t[OR_BLOCK];
+#pragma omp parallel for schedule(static)
     for (int64_t b = 0; b < n / OR_BLOCK; ++b) {
+        float t[OR_BLOCK];
         uint8_t *cb = master + b * OR_BLOCK;
         float s = master_scales[b];
         for (int i = 0; i < OR_BLOCK; ++i) {
@@ -626,4 +645,14 @@ void or_e4m3_to_f32_array(const uint8_t *src, float *dst, int64_t n)
 {
     for (int64_t i = 0; i < n; ++i)
         dst[i] = or_e4m3_to_f32(src[i]);
+}
+
+/* Threads the loops above may use: 1 in the single-threaded build.            */
+int or_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
 }

@@ -1,4 +1,6 @@
-"""Compile the CPU oracle (TEST INFRASTRUCTURE) into oracle/libagoq_oracle.so.
+"""Compile the CPU oracle (TEST INFRASTRUCTURE) into oracle/libagoq_oracle.so
+and, where the compiler supports OpenMP, an all-core build of the same source
+into oracle/libagoq_oracle_omp.so.
 
 The flags matter: -ffp-contract=off keeps every multiply and add a separately
 rounded binary32 operation (aarch64 GCC fuses them by default), and no
@@ -12,22 +14,37 @@ import sys
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "agoq_oracle.c")
 LIB = os.path.join(HERE, "libagoq_oracle.so")
+LIB_OMP = os.path.join(HERE, "libagoq_oracle_omp.so")
 
 CFLAGS = ["-O2", "-ffp-contract=off", "-fno-fast-math", "-std=c11", "-fPIC", "-shared",
           "-Wall", "-Wextra"]
 
 
+def _compile(target, extra, force):
+    if (not force and os.path.exists(target)
+            and os.path.getmtime(target) >= max(os.path.getmtime(SRC), os.path.getmtime(__file__))):
+        return target
+    tmp = target + ".tmp%d" % os.getpid()
+    subprocess.run(["gcc", *CFLAGS, *extra, "-o", tmp, SRC, "-lm"], check=True)
+    os.replace(tmp, target)
+    return target
+
+
 def build(force: bool = False) -> str:
-    """Build the oracle library if it is missing or older than its source."""
-    if (not force and os.path.exists(LIB)
-            and os.path.getmtime(LIB) >= os.path.getmtime(SRC)):
-        return LIB
-    tmp = LIB + ".tmp%d" % os.getpid()
-    cmd = ["gcc", *CFLAGS, "-o", tmp, SRC, "-lm"]
-    subprocess.run(cmd, check=True)
-    os.replace(tmp, LIB)
+    """Build the single-threaded oracle library (and, if possible, the all-core
+    one) if missing or older than the source; return the single-threaded path."""
+    _compile(LIB, ["-Wno-unknown-pragmas"], force)
+    build_omp(force)
     return LIB
 
 
+def build_omp(force: bool = False):
+    """The all-core build (OpenMP), or None if the compiler cannot build it."""
+    try:
+        return _compile(LIB_OMP, ["-fopenmp"], force)
+    except (subprocess.CalledProcessError, OSError):
+        return None
+
+
 if __name__ == "__main__":
-    print(build(force="--force" in sys.argv))
+    print(build(force="--force" in sys.argv), build_omp())

@@ -19,14 +19,20 @@ from . import build as _build
 
 BLOCK = 128
 
-_lib = None
+_libs = {}
 
 
-def lib():
-    """Load (building first if needed) the oracle shared library."""
-    global _lib
-    if _lib is None:
+def lib(parallel=False):
+    """Load (building first if needed) the oracle shared library: the
+    single-threaded build, or with ``parallel`` the all-core (OpenMP) build of
+    the same source, which computes the same bits."""
+    key = bool(parallel)
+    if key not in _libs:
         path = _build.build()
+        if parallel:
+            path = _build.build_omp()
+            if path is None:
+                raise RuntimeError("the all-core oracle build is not available (no OpenMP)")
         L = ctypes.CDLL(path)
         vp, i64, i32 = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         L.or_quant_act.argtypes = [vp, i64, i32, vp, vp]
@@ -46,17 +52,28 @@ def lib():
         L.or_f32_to_bf16_array.argtypes = [vp, vp, i64]
         L.or_f32_to_e4m3_array.argtypes = [vp, vp, i64]
         L.or_e4m3_to_f32_array.argtypes = [vp, vp, i64]
+        L.or_threads.argtypes = []
         for name in ("or_quant_act", "or_dequant_act", "or_grad_accum_fp8",
                      "or_reduce_fp8_shards", "or_wgrad_gemm_int4_f64",
                      "or_wgrad_gemm_int4_f64_entries", "or_grad_accum_fp8_f32",
                      "or_wgrad_accum_fp8", "or_grad_accum_fp8_mid", "or_silu_backward",
-                     "or_rmsnorm_backward", "or_fwd_gemm_quant"):
+                     "or_rmsnorm_backward", "or_fwd_gemm_quant", "or_threads"):
             getattr(L, name).restype = ctypes.c_int
         for name in ("or_f32_to_bf16_array", "or_f32_to_e4m3_array", "or_e4m3_to_f32_array",
                      "or_round_format_array"):
             getattr(L, name).restype = None
-        _lib = L
-    return _lib
+        _libs[key] = L
+    return _libs[key]
+
+
+def parallel_available():
+    """Whether the all-core build could be made."""
+    return _build.build_omp() is not None
+
+
+def threads(parallel=False):
+    """Threads the oracle's loops use (1 for the single-threaded build)."""
+    return int(lib(parallel).or_threads())
 
 
 def _ptr(a):
@@ -108,39 +125,43 @@ def e4m3_to_f32(c):
 
 
 # --- the path ------------------------------------------------------------
-def quant_act(x_bf16, bits):
+def quant_act(x_bf16, bits, parallel=False):
     """LAAQ quantize: BF16 bit patterns [n] -> (codes uint8 [n/128*16*bits], scales f32 [n/128])."""
     x = _contig(x_bf16, np.uint16).reshape(-1)
     n = x.size
     codes = np.empty(n // BLOCK * record_bytes(bits), np.uint8)
     scales = np.empty(n // BLOCK, np.float32)
-    _check(lib().or_quant_act(_ptr(x), n, bits, _ptr(codes), _ptr(scales)), "quant_act")
+    _check(lib(parallel).or_quant_act(_ptr(x), n, bits, _ptr(codes), _ptr(scales)), "quant_act")
     return codes, scales
 
 
-def dequant_act(codes, scales, n, bits):
+def dequant_act(codes, scales, n, bits, parallel=False):
     """LAAQ dequantize: packed codes + scales -> BF16 bit patterns [n]."""
     codes = _contig(codes, np.uint8).reshape(-1)
     scales = _contig(scales, np.float32).reshape(-1)
     if codes.size < n // BLOCK * record_bytes(bits) or scales.size < n // BLOCK:
         raise ValueError("codes/scales too short for n")
     y = np.empty(n, np.uint16)
-    _check(lib().or_dequant_act(_ptr(codes), _ptr(scales), n, bits, _ptr(y)), "dequant_act")
+    _check(lib(parallel).or_dequant_act(_ptr(codes), _ptr(scales), n, bits, _ptr(y)), "dequant_act")
     return y
 
 
-def grad_accum_fp8(master, master_scales, grad_bf16):
-    """QuanGrad local accumulation; returns new (master, scales), inputs untouched."""
-    m = _contig(master, np.uint8).reshape(-1).copy()
-    s = _contig(master_scales, np.float32).reshape(-1).copy()
+def grad_accum_fp8(master, master_scales, grad_bf16, parallel=False, in_place=False):
+    """QuanGrad local accumulation; returns new (master, scales), inputs untouched
+    (with ``in_place`` the contiguous uint8/float32 arrays given are updated and
+    returned)."""
+    m = _contig(master, np.uint8).reshape(-1)
+    s = _contig(master_scales, np.float32).reshape(-1)
+    if not in_place:
+        m, s = m.copy(), s.copy()
     g = _contig(grad_bf16, np.uint16).reshape(-1)
     if g.size != m.size or s.size != m.size // BLOCK:
         raise ValueError("shape mismatch")
-    _check(lib().or_grad_accum_fp8(_ptr(m), _ptr(s), _ptr(g), m.size), "grad_accum_fp8")
+    _check(lib(parallel).or_grad_accum_fp8(_ptr(m), _ptr(s), _ptr(g), m.size), "grad_accum_fp8")
     return m, s
 
 
-def reduce_fp8_shards(shards, shard_scales, W, n, count_naive=True):
+def reduce_fp8_shards(shards, shard_scales, W, n, count_naive=True, parallel=False):
     """Local reduce over W shard-major shards; returns (codes, scales, naive_overflow or None)."""
     sh = _contig(shards, np.uint8).reshape(-1)
     ss = _contig(shard_scales, np.float32).reshape(-1)
@@ -149,7 +170,7 @@ def reduce_fp8_shards(shards, shard_scales, W, n, count_naive=True):
     out = np.empty(n, np.uint8)
     outs = np.empty(n // BLOCK, np.float32)
     cnt = np.zeros(1, np.uint64)
-    _check(lib().or_reduce_fp8_shards(_ptr(sh), _ptr(ss), W, n, _ptr(out), _ptr(outs),
+    _check(lib(parallel).or_reduce_fp8_shards(_ptr(sh), _ptr(ss), W, n, _ptr(out), _ptr(outs),
                                        _ptr(cnt) if count_naive else None),
            "reduce_fp8_shards")
     return out, outs, (int(cnt[0]) if count_naive else None)
@@ -168,7 +189,25 @@ def wgrad_gemm_int4_f64(dY_bf16, x_codes, x_scales, M, N, K):
     return out
 
 
-def wgrad_gemm_int4_f64_entries(dY_bf16, x_codes, x_scales, M, N, K, rows, cols):
+def wgrad_gemm_int4_f64_matmul(dY_bf16, x_codes, x_scales, M, N, K, absolute=False):
+    """The binary64 product dW = dY^T Xhat [M][N] for full-size shapes: Xhat is the
+    oracle's own LAAQ 4-bit dequantization (dequant_act, BF16) of X, both operands
+    are widened to binary64 and a library binary64 matrix product forms the sums
+    (any summation order: the binary64 rounding error, about 1e-16 relative, is
+    far below every tolerance it serves).  With ``absolute`` the product of the
+    absolute values, sum_k |dY[k][i]| |Xhat[k][j]|, the scale of the binary32
+    summation error bound."""
+    dY = _contig(dY_bf16, np.uint16).reshape(K, M)
+    xh = dequant_act(x_codes, x_scales, K * N, 4, parallel=parallel_available()).reshape(K, N)
+    a = bf16_to_f32(dY).astype(np.float64)
+    b = bf16_to_f32(xh).astype(np.float64)
+    if absolute:
+        np.abs(a, out=a)
+        np.abs(b, out=b)
+    return a.T @ b
+
+
+def wgrad_gemm_int4_f64_entries(dY_bf16, x_codes, x_scales, M, N, K, rows, cols, parallel=False):
     """Binary64 entries dW[rows[e], cols[e]] of the same product."""
     dY = _contig(dY_bf16, np.uint16).reshape(-1)
     xc = _contig(x_codes, np.uint8).reshape(-1)
@@ -176,7 +215,7 @@ def wgrad_gemm_int4_f64_entries(dY_bf16, x_codes, x_scales, M, N, K, rows, cols)
     r = _contig(np.asarray(rows, np.int32), np.int32)
     c = _contig(np.asarray(cols, np.int32), np.int32)
     out = np.empty(r.size, np.float64)
-    _check(lib().or_wgrad_gemm_int4_f64_entries(_ptr(dY), _ptr(xc), _ptr(xs), M, N, K,
+    _check(lib(parallel).or_wgrad_gemm_int4_f64_entries(_ptr(dY), _ptr(xc), _ptr(xs), M, N, K,
                                                 _ptr(r), _ptr(c), r.size, _ptr(out)),
            "wgrad_gemm_int4_f64_entries")
     return out

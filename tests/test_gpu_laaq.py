@@ -94,33 +94,6 @@ def test_edge_and_midpoint_blocks(oracle, bits):
     _parity(oracle, x, bits)
 
 
-@pytest.mark.parametrize("bits", WIDTHS)
-def test_full_size_dbca_sampled_blocks(oracle, bits):
-    """The 8192 x 4096 and 8192 x 11008 Student-t tensors at full size, in the
-    launch configuration the bench times; 4096 sampled blocks of each checked
-    against the oracle, plus code-range and finiteness over every block."""
-    a, b = synthetic.dbca_activations_torch(seed=1)
-    for x in (a, b):
-        n = x.numel()
-        nb = n // 128
-        codes, scales = agoq.agoq_quant_act(x, bits)
-        y = agoq.agoq_dequant_act(codes, scales, n, bits)
-        torch.cuda.synchronize()
-        blocks = G.sample_blocks(nb, 4096, seed=bits)
-        xs = G.gather_blocks(x.view(torch.int16), blocks, 128).numpy().view(np.uint16)
-        want_c, want_s = oracle.quant_act(xs.reshape(-1), bits)
-        got_c = G.gather_blocks(codes, blocks, 16 * bits).numpy()
-        got_s = scales.cpu().numpy()[blocks]
-        assert np.array_equal(got_s.view(np.uint32), want_s.view(np.uint32))
-        assert np.array_equal(got_c.reshape(-1), want_c)
-        want_y = oracle.dequant_act(want_c, want_s, xs.size, bits)
-        got_y = G.gather_blocks(y.view(torch.int16), blocks, 128).numpy().view(np.uint16)
-        assert np.array_equal(got_y.reshape(-1), want_y)
-        assert torch.isfinite(scales).all() and bool((scales >= 0).all())
-        assert torch.isfinite(y.float()).all()
-        del codes, scales, y
-
-
 def test_repeatable_and_stream_ordered(oracle):
     x = G.dev_bf16(synthetic.laaq_activation_np(seed=2, tokens=64))
     s = torch.cuda.Stream()

@@ -8,31 +8,6 @@ from gradient_quantization_gb300 import agoq, synthetic
 from tests import gpu_util as G
 
 pytestmark = pytest.mark.gpu
-E4M3 = torch.float8_e4m3fn
-
-
-def torch_block_e4m3(vals):
-    """Block-128 FP8 quantization of a BF16 CUDA tensor [n] with torch ops (test
-    input preparation only): scale = absmax/448, codes = E4M3(value/scale)."""
-    t = vals.float().view(-1, 128)
-    amax = t.abs().amax(dim=1)
-    s = amax / 448.0
-    q = torch.where(amax[:, None] > 0, t / torch.where(s > 0, s, 1.0)[:, None],
-                    torch.zeros_like(t)).clamp(-448.0, 448.0)
-    return q.to(E4M3).view(torch.uint8).reshape(-1), s
-
-
-def torch_naive_overflow_count(shards):
-    """Naive FP8 rank-order sum of [W][n] E4M3 codes, counted with torch (test restatement)."""
-    W = shards.shape[0]
-    acc = shards[0].view(E4M3).float()
-    alive = torch.ones_like(acc, dtype=torch.bool)
-    for r in range(1, W):
-        t = acc + shards[r].view(E4M3).float()
-        alive &= t.abs() <= 448.0
-        acc = t.clamp(-448.0, 448.0).to(E4M3).float()
-    return int((~alive).sum().item())
-
 
 # ---------------------------------------------------------------- accumulation
 @pytest.mark.parametrize("nblocks", [1, 3, 33, 1031, 1 << 10])
@@ -96,31 +71,6 @@ def test_accum_edge_cases(oracle):
         wm, ws = oracle.grad_accum_fp8(mm, ss, g0)
         assert np.array_equal(m.cpu().numpy(), wm)
         assert np.array_equal(s.cpu().numpy().view(np.uint32), ws.view(np.uint32))
-
-
-def test_accum_full_size_sampled_chain(oracle):
-    """2^30-element master, 8 micro-batches at full size in the bench's launch
-    configuration; 2048 sampled blocks followed through all 8 steps by the oracle,
-    and every code checked for NaN after each step."""
-    n = synthetic.QUANGRAD_N
-    nb = n // 128
-    blocks = G.sample_blocks(nb, 2048, seed=7)
-    m = torch.zeros(n, dtype=torch.uint8, device="cuda")
-    s = torch.zeros(nb, dtype=torch.float32, device="cuda")
-    om = np.zeros(blocks.size * 128, np.uint8)
-    osc = np.zeros(blocks.size, np.float32)
-    for step in range(synthetic.QUANGRAD_STEPS):
-        g = synthetic.quangrad_grad_torch(seed=2, step=step)
-        agoq.agoq_grad_accum_fp8(m, s, g)
-        gs = G.gather_blocks(g.view(torch.int16), blocks, 128).numpy().view(np.uint16).reshape(-1)
-        om, osc = oracle.grad_accum_fp8(om, osc, gs)
-        torch.cuda.synchronize()
-        got_m = G.gather_blocks(m, blocks, 128).numpy().reshape(-1)
-        got_s = s.cpu().numpy()[blocks]
-        assert np.array_equal(got_m, om), "step %d" % step
-        assert np.array_equal(got_s.view(np.uint32), osc.view(np.uint32)), "step %d" % step
-        assert int(((m & 0x7F) == 0x7F).sum().item()) == 0
-        del g
 
 
 def test_accum_guard_bands(oracle):
@@ -197,38 +147,16 @@ def test_reduce_edge_cases(oracle):
     sh[0, 128:256] = 0x80; sh[1:, 128:256] = 0           # block 1: -0 and +0
     ss = rng.uniform(1e-8, 1e3, (W, n // 128)).astype(np.float32)
     ss[:, 2] = 2.0 ** -140                               # block 2: subnormal shard scales
+    # block 3: scale 2^-149, so codes below 1 in magnitude give products that
+    # underflow to a signed zero (a negative one in shard 0 must still leave +0)
+    ss[:, 3] = 2.0 ** -149
+    sh[0, 384:448] = 0x80 | rng.integers(1, 0x38, 64)    # -(2^-9 .. <1)
     cnt = torch.zeros(1, dtype=torch.int64, device="cuda")
     o, os_ = agoq.agoq_reduce_fp8_shards(G.dev(sh), G.dev(ss), W, n, naive_overflow_count=cnt)
     wc, ws, wcnt = oracle.reduce_fp8_shards(sh, ss, W, n)
     assert np.array_equal(o.cpu().numpy(), wc)
     assert np.array_equal(os_.cpu().numpy().view(np.uint32), ws.view(np.uint32))
     assert int(cnt.item()) == wcnt
-
-
-@pytest.mark.parametrize("W", [8, 64])
-def test_reduce_full_size_sampled(oracle, W):
-    """W shards of 2^25 elements at full size in the bench's launch configuration:
-    1024 sampled blocks against the oracle, the naive-overflow count against a
-    torch restatement over every element."""
-    n = synthetic.REDUCE_N
-    nb = n // 128
-    vals = synthetic.reduce_shard_values_torch(seed=3, W=W)
-    sh = torch.empty((W, n), dtype=torch.uint8, device="cuda")
-    ss = torch.empty((W, nb), dtype=torch.float32, device="cuda")
-    for r in range(W):
-        sh[r], ss[r] = torch_block_e4m3(vals[r])
-    del vals
-    cnt = torch.zeros(1, dtype=torch.int64, device="cuda")
-    out, outs = agoq.agoq_reduce_fp8_shards(sh, ss, W, n, naive_overflow_count=cnt)
-    torch.cuda.synchronize()
-    blocks = G.sample_blocks(nb, 1024, seed=W)
-    sub_sh = np.stack([G.gather_blocks(sh[r], blocks, 128).numpy().reshape(-1) for r in range(W)])
-    sub_ss = np.stack([ss[r].cpu().numpy()[blocks] for r in range(W)])
-    wc, ws, _ = oracle.reduce_fp8_shards(sub_sh, sub_ss, W, blocks.size * 128, count_naive=False)
-    assert np.array_equal(G.gather_blocks(out, blocks, 128).numpy().reshape(-1), wc)
-    assert np.array_equal(outs.cpu().numpy()[blocks].view(np.uint32), ws.view(np.uint32))
-    want = torch_naive_overflow_count(sh)
-    assert int(cnt.item()) == want and want > 0
 
 
 def test_reduce_count_is_set_not_accumulated(oracle):
