@@ -16,21 +16,35 @@ Every width quantizes its own copy of each input tensor, and every dequantize
 reads codes written at least 247 MB of HBM traffic earlier; one step moves
 2.7 GB, so no call finds its input in the L2 (126 MB) from another call.
 
+The timed region is a window of exactly K steps (barrier and synchronize on
+both sides, CUDA events at its ends), repeated until the windows last at least
+one second together; value comes from the median window (max over ranks) and
+the windows' spread is reported.
+
 Also reported:
   roofline      the dominant kernel's algorithmic GB/s (CUDA events around each
                 launch on the launching stream) against the measured HBM copy peak;
   e2e           the same step with inputs copied from pinned host memory and all
-                outputs copied back inside the timed region;
-  cpu_baseline  the CPU oracle timed on a bounded sample of the same workload;
-  rows          each other kernel of the path on its own workload (QuanGrad
-                accumulation of 2^30 elements, FP8 shard reduce W=8/64 of 2^25,
-                INT4-fused weight-gradient GEMM 11008x4096x8192, the 2048x4096
-                4-bit round trip), L2 flushed before each timed launch (a 256 MB
-                buffer written, then another 256 MB read, so the launch starts
-                from a cold L2 holding no dirty lines).
+                outputs copied back inside the timed region, and the same plan
+                with the kernels left out (the host link's share);
+  cpu_baseline  the CPU oracle on the host cores: its all-core (OpenMP) build on
+                the full workload where it fits the time budget, and the
+                single-threaded build on a bounded sample;
+  rows          each other kernel of the path on its own workload, L2 flushed
+                before each timed launch (a 256 MB buffer written, then another
+                256 MB read, so the launch starts from a cold L2 holding no dirty
+                lines): the 2048x4096 4-bit round trip (single launches and a
+                100-call CUDA graph), the DBCA-PP tensors' 4-bit calls in 100-call
+                graphs and the 16-call step as a graph, QuanGrad accumulation of
+                2^30 elements over the 8 micro-batches from a zeroed master, the
+                FP8 shard reduce W=8/64 of 2^25 with and without the naive count,
+                the INT4-fused weight-gradient GEMM 11008x4096x8192, its fused
+                accumulation, the forward GEMM with quantized output and the
+                SiLU/RMSNorm backward recompute.
 
 --impl reference times the CPU oracle (the plain restatement the kernels are
-checked against) on a bounded sample of the same workload.
+checked against), all-core build, on the same workload (all 8192 token rows
+when a step fits the time budget, else a bounded sample).
 Launch: python bench.py [--gpus N --steps K --warmup W]; for N > 1 under
 torch.distributed.run, one rank per GPU, each rank running the workload on its
 own GPU (weak scaling, no collective on the data path).
@@ -53,15 +67,9 @@ METRIC = "HBM GB/s and Gelem/s per quant kernel; fraction of GB300 HBM/tensor pe
 NOMINAL_HBM_GBS = 8000.0
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
-# dram__bytes_read.sum + dram__bytes_write.sum per launch, from the ncu captures
-# summarised in profiles/ (laaq_quant_b5_dbca_8192x4096_8192x11008.md,
-# laaq_dequant_b8_silu_8192x11008.md); valid only while those kernels are
-# unchanged -- remove an entry when its kernel changes.
-DOMINANT_TRAFFIC_BYTES = {
-    "quant_b5_silu_in": 180403200 + 9767680,
-    "quant_b5_rmsnorm_in": 67147008 + 2065664,
-    "dequant_b8_silu_in": 93009408 + 121078016,
-}
+# Least total length of the timed region: the K-step window is repeated until
+# the windows together last at least this long.
+MIN_TIMED_S = 1.0
 
 
 def act_bytes(n, bits):
@@ -258,20 +266,30 @@ def gpu_arm(args):
     sampler = ClockSampler(uuid) if rank == 0 else None
     time.sleep(0.3 if sampler else 0)
 
-    # Timed region: K steps with events only at its ends, so that consecutive
-    # kernels keep their programmatic-dependent-launch overlap.
+    # Timed region: windows of exactly K steps, each bracketed by a barrier and
+    # a synchronize, with events only at the window's ends (so that consecutive
+    # kernels keep their programmatic-dependent-launch overlap).  The window is
+    # repeated until the windows last MIN_TIMED_S together; value is the median
+    # window (max over ranks), and the spread is reported.
     stream = torch.cuda.current_stream(device)
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    dist_barrier(device)
-    torch.cuda.synchronize()
+    windows = []
     t_wall0 = time.time()
-    start.record(stream)
-    for k in range(args.steps):
-        step()
-    stop.record(stream)
-    torch.cuda.synchronize()
-    dist_barrier(device)
-    elapsed_ms = start.elapsed_time(stop)
+    while True:
+        dist_barrier(device)
+        torch.cuda.synchronize()
+        start.record(stream)
+        for k in range(args.steps):
+            step()
+        stop.record(stream)
+        torch.cuda.synchronize()
+        dist_barrier(device)
+        windows.append(start.elapsed_time(stop))
+        # the same stopping decision on every rank
+        if max_over_ranks(sum(windows), device) >= MIN_TIMED_S * 1e3 or len(windows) >= 10000:
+            break
+    windows = [max_over_ranks(w, device) for w in windows]
+    elapsed_ms = statistics.median(windows)
     # the same steps on one stream, for comparison
     one_ms = None
     if len(groups) > 1:
@@ -306,7 +324,7 @@ def gpu_arm(args):
         time.sleep(0.25)
         sampler.stop()
         clocks = sampler.summary(t_wall0 - 0.05, t_wall1 + 0.3)
-    max_ms = max_over_ranks(elapsed_ms, device)
+    max_ms = elapsed_ms
     total_bytes = sum_over_ranks(step_bytes * args.steps, device)
     total_elems = sum_over_ranks(step_elems * args.steps, device)
     value = total_bytes / (max_ms * 1e-3) / 1e9
@@ -316,7 +334,7 @@ def gpu_arm(args):
     dom = max(range(len(calls)), key=lambda i: per_call[i])
     dom_label, dom_bytes = calls[dom][0], calls[dom][1]
     achieved = dom_bytes / (per_call[dom] * 1e-3) / 1e9
-    traffic = DOMINANT_TRAFFIC_BYTES.get(dom_label)
+    traffic = None   # DRAM counters come from ncu captures, not from this run
     # the same launch alone, after an L2 flush that leaves no dirty lines (in the
     # step it also writes back what the previous call left dirty in L2)
     flushbuf = torch.zeros(256 << 20 >> 2, dtype=torch.float32, device=device)
@@ -352,6 +370,13 @@ def gpu_arm(args):
             "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(max_ms / args.steps, 4), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "dtypes": {"input": "bf16", "codes": "int4/int5/int6/int8", "scales": "f32",
+                       "arithmetic": "f32", "output": "bf16"},
+            "windows": {"count": len(windows), "steps_each": args.steps,
+                        "timed_region_s": round(sum(windows) / 1e3, 3),
+                        "median_ms": round(statistics.median(windows), 4),
+                        "min_ms": round(min(windows), 4), "max_ms": round(max(windows), 4),
+                        "value_from": "median window"},
             "gelem_per_s": round(gelem, 2),
             "frac_of_measured_hbm": round(value / world / hbm_peak, 4),
             "frac_of_nominal_hbm": round(value / world / NOMINAL_HBM_GBS, 4),
@@ -379,7 +404,7 @@ def gpu_arm(args):
             "kernels_timing": "separate pass of %d steps with an event after every call; the "
                               "timed region (value) has events only at its ends" % ksteps,
             "e2e": e2e,
-            "gpu_launches": len(calls) * args.steps,
+            "gpu_launches": len(calls) * args.steps * len(windows),
             "gpu_launches_per_step": len(calls),
             "clocks": clocks,
             "cpu_baseline": cpu,
@@ -428,7 +453,7 @@ def e2e_arm(args, tensors, codes, scales, outs, calls, device):
     plan = [("q", name, b) for b in WIDTHS for name in names] + \
            [("d", name, b) for b in WIDTHS for name in names]
 
-    def one():
+    def one(kernels=True):
         in_ready = {}
         with torch.cuda.stream(s_in):
             for name in names:
@@ -445,13 +470,15 @@ def e2e_arm(args, tensors, codes, scales, outs, calls, device):
                     s_comp.wait_event(in_ready[name])
                     if copied_out[k] is not None:
                         s_comp.wait_event(copied_out[k])
-                    agoq.agoq_quant_act(dev_in[name], b, codes[k], scales[k], stream=s_comp)
+                    if kernels:
+                        agoq.agoq_quant_act(dev_in[name], b, codes[k], scales[k], stream=s_comp)
                     last_quant[name] = ev()
                     last_quant[name].record(s_comp)
                     done = last_quant[name]
                 else:
-                    agoq.agoq_dequant_act(codes[k], scales[k], outs[k].numel(), b, outs[k],
-                                          stream=s_comp)
+                    if kernels:
+                        agoq.agoq_dequant_act(codes[k], scales[k], outs[k].numel(), b, outs[k],
+                                              stream=s_comp)
                     done = ev()
                     done.record(s_comp)
                 s_out = s_outs[(WIDTHS.index(b) * len(names) + names.index(name)) % len(s_outs)]
@@ -487,26 +514,15 @@ def e2e_arm(args, tensors, codes, scales, outs, calls, device):
     ms = max_over_ranks(a.elapsed_time(b), device)
     total = sum_over_ranks(step_bytes * steps, device)
 
-    # The same host<->device copies alone (no kernels), on the same streams: the
-    # host link's bound for this step.
-    def copies():
-        with torch.cuda.stream(s_in):
-            for name in names:
-                dev_in[name].copy_(host_in[name], non_blocking=True)
-        for i, k in enumerate(codes):
-            s_out = s_outs[i % len(s_outs)]
-            with torch.cuda.stream(s_out):
-                hc, hs, ho = host_out[k]
-                hc.copy_(codes[k], non_blocking=True)
-                hs.copy_(scales[k], non_blocking=True)
-                ho.copy_(outs[k], non_blocking=True)
-    copies()
+    # The same plan with the kernels left out: the same copies on the same
+    # streams with the same event dependencies, i.e. the host link's share.
+    one(kernels=False)
     torch.cuda.synchronize()
     a.record(s_comp)
     for st in [s_in] + s_outs:
         st.wait_event(a)
     for _ in range(steps):
-        copies()
+        one(kernels=False)
     for st in [s_in] + s_outs:
         e = ev()
         e.record(st)
@@ -518,8 +534,8 @@ def e2e_arm(args, tensors, codes, scales, outs, calls, device):
             "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
             "ms_per_step": round(ms / steps, 3), "steps": steps,
             "copies_only_ms_per_step": round(copy_ms, 3),
-            "overlap": "copies in, kernels and copies out (4 streams) overlapped; the step is "
-                       "bound by the host link (copies alone take copies_only_ms_per_step)"}
+            "overlap": "copies in, kernels and copies out (4 streams) overlapped; "
+                       "copies_only_ms_per_step runs the same plan without the kernels"}
 
 
 def allreduce_arm(device, world, reps=10, warm=3):
@@ -634,6 +650,65 @@ def rows_arm(device, hbm_peak, bf16_peak):
         del graph
     del x, c, s, y, xs_c, cs_c, ss_c, ys_c
 
+    # The DBCA-PP activations (8192 x 4096 and 8192 x 11008): 100 back-to-back
+    # 4-bit calls in one CUDA graph over 2 rotating copies of each tensor (every
+    # copy is larger than L2, or 2 x 67 MB for the smaller tensor), and the
+    # 16-call step on one stream captured as a graph (10 steps per replay).
+    xa, xb = synthetic.dbca_activations_torch(seed=1, device=device)
+    for label, xt in (("rmsnorm_in_8192x4096", xa), ("silu_in_8192x11008", xb)):
+        n = xt.numel()
+        k = 2
+        xs_c = [xt.clone() for _ in range(k)]
+        cs_c = [torch.empty(n // 2, dtype=torch.uint8, device=device) for _ in range(k)]
+        ss_c = [torch.empty(n // 128, dtype=torch.float32, device=device) for _ in range(k)]
+        ys_c = [torch.empty_like(xt) for _ in range(k)]
+        for name, fn in (("dbca_int4_quant_%s_graph100" % label,
+                          lambda i: agoq.agoq_quant_act(xs_c[i % k], 4, cs_c[i % k], ss_c[i % k])),
+                         ("dbca_int4_dequant_%s_graph100" % label,
+                          lambda i: agoq.agoq_dequant_act(cs_c[i % k], ss_c[i % k], n, 4,
+                                                          ys_c[i % k]))):
+            for i in range(k):
+                fn(i)
+            torch.cuda.synchronize()
+            graph = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(graph):
+                for i in range(100):
+                    fn(i)
+            ms = _time_launch(graph.replay, flush, reps=3, warm=1) / 100
+            row(name, act_bytes(n, 4), n, ms, {"calls_per_graph": 100, "rotating_copies": k})
+            del graph
+        del xs_c, cs_c, ss_c, ys_c
+    # the 16-call step: quantize both tensors at 4/5/6/8 bits, then dequantize
+    xin, cod, sca, out = {}, {}, {}, {}
+    for name, xt in (("a", xa), ("b", xb)):
+        for bits in WIDTHS:
+            xin[name, bits] = xt.clone()
+            cod[name, bits] = torch.empty(xt.numel() // 128 * 16 * bits, dtype=torch.uint8,
+                                          device=device)
+            sca[name, bits] = torch.empty(xt.numel() // 128, dtype=torch.float32, device=device)
+            out[name, bits] = torch.empty_like(xt)
+
+    def dbca_step():
+        for bits in WIDTHS:
+            for name in ("a", "b"):
+                agoq.agoq_quant_act(xin[name, bits], bits, cod[name, bits], sca[name, bits])
+        for bits in WIDTHS:
+            for name in ("a", "b"):
+                agoq.agoq_dequant_act(cod[name, bits], sca[name, bits], xin[name, bits].numel(),
+                                      bits, out[name, bits])
+    dbca_step()
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for _ in range(10):
+            dbca_step()
+    step_bytes = sum(2 * act_bytes(xt.numel(), bits) for xt in (xa, xb) for bits in WIDTHS)
+    ms = _time_launch(graph.replay, flush, reps=5, warm=1) / 10
+    row("dbca_step_16_calls_graph", step_bytes,
+        sum(2 * xt.numel() for xt in (xa, xb) for _ in WIDTHS), ms,
+        {"calls_per_step": 16, "steps_per_graph": 10, "stream": "one"})
+    del graph, xin, cod, sca, out, xa, xb
+
     # SiLU backward recomputed from the 4-bit SiLU input (8192 x 11008)
     xs_ = synthetic.dbca_activations_torch(seed=1, device=device)[1]
     n = xs_.numel()
@@ -670,20 +745,40 @@ def rows_arm(device, hbm_peak, bf16_peak):
         {"note": "algorithmic bytes read the input once; dw reads codes and dy a second time"})
     del c, s, dy, dx
 
-    # QuanGrad accumulation, 2^30 elements
+    # QuanGrad accumulation, 2^30 elements: the 8 micro-batches of the workload
+    # into a zeroed master, each step timed after an L2 flush; the chain is run
+    # 3 times from zero, and each step's median and the mean over steps reported
     n = synthetic.QUANGRAD_N
     m = torch.zeros(n, dtype=torch.uint8, device=device)
     ms_ = torch.zeros(n // 128, dtype=torch.float32, device=device)
-    g = synthetic.quangrad_grad_torch(seed=2, step=0, device=device)
-    agoq.agoq_grad_accum_fp8(m, ms_, g)
+    grads = [synthetic.quangrad_grad_torch(seed=2, step=k, device=device)
+             for k in range(synthetic.QUANGRAD_STEPS)]
     nbytes = n * 4 + (n // 128) * 8
-    row("quangrad_accum_2^30", nbytes, n,
-        _time_launch(lambda: agoq.agoq_grad_accum_fp8(m, ms_, g), flush, reps=5, warm=1))
+    def chain(acc, label, extra_note=""):
+        acc(grads[0])   # warm-up
+        step_ms = [[] for _ in grads]
+        for _ in range(3):
+            m.zero_()
+            ms_.zero_()
+            for k, g in enumerate(grads):
+                flush()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record()
+                acc(g)
+                b.record()
+                b.synchronize()
+                step_ms[k].append(a.elapsed_time(b))
+        med = [statistics.median(t) for t in step_ms]
+        row(label, nbytes, n, sum(med) / len(med),
+            {"steps": len(med), "per_step_us": [round(t * 1e3, 1) for t in med],
+             "timing": "mean over the 8 micro-batches of each step's median of 3 chains from a "
+                       "zeroed master" + extra_note})
+
+    chain(lambda g: agoq.agoq_grad_accum_fp8(m, ms_, g), "quangrad_accum_2^30")
     for mid, label in ((agoq.MID_BF16, "bf16"), (agoq.MID_FP16, "fp16")):
-        row("quangrad_accum_%smid_2^30" % label, nbytes, n,
-            _time_launch(lambda mid=mid: agoq.agoq_grad_accum_fp8_mid(m, ms_, g, mid), flush,
-                         reps=5, warm=1))
-    del m, ms_, g
+        chain(lambda g, mid=mid: agoq.agoq_grad_accum_fp8_mid(m, ms_, g, mid),
+              "quangrad_accum_%smid_2^30" % label)
+    del m, ms_, grads
 
     # FP8 shard local reduce, 2^25 elements per shard
     n = synthetic.REDUCE_N
@@ -772,23 +867,43 @@ def rows_arm(device, hbm_peak, bf16_peak):
 
 
 # ----------------------------------------------------------------------- CPU oracle
-def _oracle_step(O, a, b):
+def _oracle_step(O, a, b, parallel=False):
     for x in (a, b):
         flat = x.reshape(-1)
         for bits in WIDTHS:
-            c, s = O.quant_act(flat, bits)
-            O.dequant_act(c, s, flat.size, bits)
+            c, s = O.quant_act(flat, bits, parallel=parallel)
+            O.dequant_act(c, s, flat.size, bits, parallel=parallel)
 
 
-def cpu_sample(target_s):
-    """The workload restricted to its first R token rows, R chosen for ~target_s of oracle work."""
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), or None."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except OSError:
+        pass
+    return None
+
+
+def cpu_sample(target_s, parallel=False):
+    """The workload restricted to its first R token rows, R chosen for about
+    target_s of oracle work (all 8192 rows if they fit)."""
     from gradient_quantization_gb300 import synthetic
     from oracle import oracle as O
-    O.lib()
-    rows = 16
+    O.lib(parallel)
+    rows = 64 if parallel else 16
     a, b = synthetic.dbca_activations_np(seed=1, tokens=rows)
     t0 = time.perf_counter()
-    _oracle_step(O, a, b)
+    _oracle_step(O, a, b, parallel)
     dt = time.perf_counter() - t0
     rows = int(max(16, min(8192, rows * target_s / max(dt, 1e-6))))
     a, b = synthetic.dbca_activations_np(seed=1, tokens=rows)
@@ -797,33 +912,53 @@ def cpu_sample(target_s):
     return O, a, b, rows, nbytes, nelems
 
 
-def cpu_baseline(target_s):
-    O, a, b, rows, nbytes, nelems = cpu_sample(target_s)
+def _cpu_leg(target_s, parallel):
+    O, a, b, rows, nbytes, nelems = cpu_sample(target_s, parallel)
     t0 = time.perf_counter()
-    _oracle_step(O, a, b)
+    _oracle_step(O, a, b, parallel)
     dt = time.perf_counter() - t0
-    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-            "gelem_per_s": round(nelems / dt / 1e9, 5), "seconds": round(dt, 2),
-            "sample": "first %d of 8192 token rows of both tensors, quantize+dequantize at 4/5/6/8 "
-                      "bits (single-threaded C oracle)" % rows}
+    what = ("all 8192 token rows" if rows == 8192 else "first %d of 8192 token rows" % rows)
+    return {"value": round(nbytes / dt / 1e9, 4), "unit": "GB/s", "cores": O.threads(parallel),
+            "kind": "oracle", "gelem_per_s": round(nelems / dt / 1e9, 5), "seconds": round(dt, 2),
+            "sample": "%s of both tensors, quantize+dequantize at 4/5/6/8 bits (%s C oracle)"
+                      % (what, "all-core OpenMP" if parallel else "single-threaded")}
+
+
+def cpu_baseline(target_s):
+    """The oracle on the host cores: the all-core build (the line's value) and the
+    single-threaded build, each on a sample sized for about target_s."""
+    from oracle import oracle as O
+    single = _cpu_leg(target_s / 2, False)
+    if O.parallel_available():
+        line = _cpu_leg(target_s / 2, True)
+        line["single_thread"] = single
+    else:
+        line = single
+    line["cpu_model"] = cpu_model()
+    line["host_cores"] = len(os.sched_getaffinity(0))
+    return line
 
 
 def reference_arm(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return
+    from oracle import oracle as O
+    parallel = O.parallel_available()
     # keep the whole reference run within about three minutes of host time
     per_step = min(args.ref_step_seconds, 180.0 / (args.steps + args.warmup))
-    O, a, b, rows, nbytes, nelems = cpu_sample(per_step)
+    O, a, b, rows, nbytes, nelems = cpu_sample(per_step, parallel)
     for _ in range(args.warmup):
-        _oracle_step(O, a, b)
+        _oracle_step(O, a, b, parallel)
     t0 = time.perf_counter()
     for _ in range(args.steps):
-        _oracle_step(O, a, b)
+        _oracle_step(O, a, b, parallel)
     dt = time.perf_counter() - t0
     value = nbytes * args.steps / dt / 1e9
-    sample = ("first %d of 8192 token rows of both tensors per step, quantize+dequantize at "
-              "4/5/6/8 bits (single-threaded C oracle)" % rows)
+    cores = O.threads(parallel)
+    what = ("all 8192 token rows" if rows == 8192 else "first %d of 8192 token rows" % rows)
+    sample = ("%s of both tensors per step, quantize+dequantize at 4/5/6/8 bits (%s C oracle)"
+              % (what, "all-core OpenMP" if parallel else "single-threaded"))
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
             "ms_per_step": round(dt / args.steps * 1e3, 2), "higher_is_better": True,
@@ -831,9 +966,9 @@ def reference_arm(args):
             "gelem_per_s": round(nelems * args.steps / dt / 1e9, 5),
             "config": {"workload": "DBCA-PP activations: RMSNorm in BF16[8192x4096] + SiLU in "
                                    "BF16[8192x11008], Student-t nu=4, quantize+dequantize at 4/5/6/8 bits",
-                       "sample_rows": rows, "parallelism": "single host thread"},
-            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": sample},
+                       "sample_rows": rows, "parallelism": "%d host threads" % cores},
+            "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
+                             "kind": "oracle", "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
