@@ -202,9 +202,9 @@ agoq_status agoq_reduce_fp8_shards(const void *shards_e4m3, const float *shard_s
 static agoq_status wgrad_common(const void *dY, const void *xc, const float *xs, int M, int N,
                                 int K, void *dW, bool f32_out, void *stream) {
     using namespace agoq;
-    if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 512 || K % 64) return AGOQ_ERR_SHAPE;
+    if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 64) return AGOQ_ERR_SHAPE;
     if (!dY || !xc || !xs || !dW) return AGOQ_ERR_NULL;
-    if (!aligned(dY, 16) || !aligned(xc, 16) || !aligned(xs, 16) || !aligned(dW, 16))
+    if (!aligned(dY, 16) || !aligned(xc, 16) || !aligned(xs, 4) || !aligned(dW, 16))
         return AGOQ_ERR_ALIGN;
     const uint64_t dyb = 2ull * K * M, xcb = (uint64_t)K * N / 2, xsb = (uint64_t)K * (N / 128) * 4;
     const uint64_t dwb = (uint64_t)M * N * (f32_out ? 4 : 2);
@@ -229,9 +229,9 @@ agoq_status agoq_wgrad_gemm_int4_accum_fp8(const void *dY_bf16, const void *x_co
                                            void *master_e4m3, float *master_scales,
                                            void *stream) {
     using namespace agoq;
-    if (M <= 0 || N <= 0 || K <= 0 || M % 256 || N % 512 || K % 64) return AGOQ_ERR_SHAPE;
+    if (M <= 0 || N <= 0 || K <= 0 || M % 128 || N % 128 || K % 64) return AGOQ_ERR_SHAPE;
     if (!dY_bf16 || !x_codes || !x_scales || !master_e4m3 || !master_scales) return AGOQ_ERR_NULL;
-    if (!aligned(dY_bf16, 16) || !aligned(x_codes, 16) || !aligned(x_scales, 16) ||
+    if (!aligned(dY_bf16, 16) || !aligned(x_codes, 16) || !aligned(x_scales, 4) ||
         !aligned(master_e4m3, 16) || !aligned(master_scales, 4))
         return AGOQ_ERR_ALIGN;
     const uint64_t dyb = 2ull * K * M, xcb = (uint64_t)K * N / 2, xsb = (uint64_t)K * (N / 128) * 4;

@@ -1,12 +1,8 @@
 // fwd_gemm.cu -- the forward GEMM with fused LAAQ quantization, 128-deep
 // k-blocks (K a multiple of 128), and the entry points that pick an instance
 // by K (the kernel itself is in fwd_gemm_impl.cuh).
-#ifndef AGOQ_FWD_BK
 #define AGOQ_FWD_BK 128
-#endif
-#ifndef AGOQ_FWD_STAGES
 #define AGOQ_FWD_STAGES 3
-#endif
 #define AGOQ_FWD_INSTANCE fwd128
 #include "fwd_gemm_impl.cuh"
 

@@ -7,9 +7,9 @@
 //   Y[t][n] = bf16(fl32(sum_k X[t][k] * W[n][k]))     X [T][K], W [N][K], BF16
 //   codes, scales = LAAQ b-bit quantization of Y (128-column blocks of each row)
 //
-// Blackwell design (sm_103a), persistent, one CTA per SM; with AGOQ_FWD_PAIR
-// (the default) the two CTAs of a cluster of two form a tcgen05 CTA pair on
-// 256 x 256 output tiles, both operands K-major:
+// Blackwell design (sm_103a), persistent, one CTA per SM; the two CTAs of a
+// cluster of two form a tcgen05 CTA pair on 256 x 256 output tiles, both
+// operands K-major:
 //   warp 0      TMA producer: per BK-deep k-block, this CTA's 128 rows of X
 //               and its 128 of the tile's 256 rows of W (64-wide boxes with
 //               the 128-byte swizzle) into an NS-stage ring;
@@ -28,8 +28,6 @@
 //               as the LAAQ quantizer) and stores the packed record and the
 //               scale.  CTA 1's warps release an accumulator with a remote
 //               arrive on CTA 0's barrier.
-// Without AGOQ_FWD_PAIR each CTA works alone on 128 x 256 tiles (M=128 MMAs,
-// all 256 W rows loaded locally; it needs BK = 64, AGOQ_FWD_STAGES = 4 to fit).
 // Every mbarrier wait is time-limited (status word, CTA abort flag, drains); the
 // two CTAs of a pair meet at a cluster barrier before either frees TMEM.
 #pragma once
@@ -47,20 +45,18 @@ using namespace gemm;
 // agoq_device_status).
 __device__ unsigned g_fwd_status;
 
-// With AGOQ_FWD_PAIR (the default) the two CTAs of a cluster of two form a
-// tcgen05 CTA pair on 256 x 256 tiles: each CTA loads 128 rows of X and 128
-// of the tile's 256 rows of W, and CTA 0 issues pair MMAs (M = 256, N = 256)
-// that read both CTAs' shared memory, so each SM streams half of the W tile
-// from L2 and reads half as many B bytes from shared memory per MMA.  CTA 1
-// publishes each landed stage to CTA 0 with a remote mbarrier arrive.
-#ifndef AGOQ_FWD_PAIR
-#define AGOQ_FWD_PAIR 1
-#endif
+// The two CTAs of a cluster of two form a tcgen05 CTA pair on 256 x 256
+// tiles: each CTA loads 128 rows of X and 128 of the tile's 256 rows of W, and
+// CTA 0 issues pair MMAs (M = 256, N = 256) that read both CTAs' shared memory,
+// so each SM streams half of the W tile from L2 and reads half as many B bytes
+// from shared memory per MMA (a single-CTA design on 128 x 256 tiles measured
+// slower).  CTA 1 publishes each landed stage to CTA 0 with a remote mbarrier
+// arrive.
 // AGOQ_FWD_BK (k-block depth) and AGOQ_FWD_STAGES (ring depth) are set by the
 // translation unit that includes this file (fwd_gemm.cu: BK = 128 for K a
 // multiple of 128; fwd_gemm_k64.cu: BK = 64 for the other multiples of 64),
 // and AGOQ_FWD_INSTANCE names the instance's namespace.
-constexpr int kPair = AGOQ_FWD_PAIR ? 2 : 1;
+constexpr int kPair = 2;
 constexpr int BM = 128, BN = 256, BK = AGOQ_FWD_BK, NS = AGOQ_FWD_STAGES;
 constexpr int kTileRows = BM * kPair;                     // output rows per tile
 constexpr int kBRows = BN / kPair;                        // W rows this CTA loads per tile
@@ -79,17 +75,11 @@ constexpr uint32_t kTmemCols = 512;
 static_assert(BK % 64 == 0, "k-blocks are whole 64-wide swizzle atoms");
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
-#ifndef AGOQ_FWD_BAND
-#define AGOQ_FWD_BAND 16
-#endif
-#ifndef AGOQ_FWD_STREAM_STORES
-#define AGOQ_FWD_STREAM_STORES 1
-#endif
-
 // Tile order: bands of kBand consecutive N-panels; within a band the tiles run
 // N-fastest, then M, so the CTAs working at the same time share a few W panels
-// and X row blocks (a working set that stays in L2).
-constexpr int kBand = AGOQ_FWD_BAND;
+// and X row blocks (a working set that stays in L2; bands of 4, 8 or 32
+// measured slower).
+constexpr int kBand = 16;
 
 __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int &m0, int &n0) {
     const int band = tile / (kBand * num_m);
@@ -99,18 +89,16 @@ __device__ __forceinline__ void tile_coords(int tile, int num_m, int num_n, int 
     n0 = (band * kBand + r % nb) * BN;
 }
 
+// Streaming (evict-first) store of the outputs, which no later part of the
+// kernel reads.
 __device__ __forceinline__ void st_stream16(void *p, uint4 v) {
-#if AGOQ_FWD_STREAM_STORES
     asm volatile("st.global.cs.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z),
                  "r"(v.w)
                  : "memory");
-#else
-    *static_cast<uint4 *>(p) = v;
-#endif
 }
 
-// kind::f16, BF16 A and B, FP32 D, both K-major, M = 128 per CTA (256 for a
-// pair), N = 256.
+// kind::f16, BF16 A and B, FP32 D, both K-major, M = 256 (128 rows from each
+// CTA of the pair), N = 256.
 constexpr uint32_t kIdescK = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) |
                              ((uint32_t)(kTileRows >> 4) << 24);
 
@@ -153,7 +141,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     // pair) holds rows m0 + 128 rank .. +127 and loads W rows
     // n0 + kBRows rank .. + kBRows - 1.  Rows at or past T read as zeros and
     // are not stored.
-    const int rank = kPair > 1 ? (int)cluster_ctarank() : 0;
+    const int rank = (int)cluster_ctarank();
     const int cid = (int)(blockIdx.x / kPair), ncl = (int)(gridDim.x / kPair);
     const int num_m = (T + kTileRows - 1) / kTileRows, num_n = N / BN;
     const int num_tiles = num_m * num_n, kblocks = K / BK;
@@ -173,24 +161,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kMmaWarp) {
-        if constexpr (kPair > 1) {
-            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                             smem_u32(tmem_addr)),
-                         "r"(kTmemCols)
-                         : "memory");
-            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-        } else {
-            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                             smem_u32(tmem_addr)),
-                         "r"(kTmemCols)
-                         : "memory");
-            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-        }
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(tmem_addr)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if constexpr (kPair > 1) cluster_sync_all();   // the peer's barriers are initialised
+    cluster_sync_all();   // the peer's barriers are initialised
     const uint32_t tmem_base = *tmem_addr;
 
     if (warp == kTmaWarp) {
@@ -232,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
                     const int s = it % NS;
                     if (!wait_bar(&full[s], (it / NS) & 1u, abort, status) ||
-                        (kPair > 1 && !wait_bar(&ready[s], (it / NS) & 1u, abort, status))) {
+                        !wait_bar(&ready[s], (it / NS) & 1u, abort, status)) {
                         ok = false;
                         break;
                     }
@@ -244,31 +224,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint64_t adesc = sw128_kmajor_desc(a0 + (kk >> 2) * kAAtom + 32 * (kk & 3));
                         const uint64_t bdesc = sw128_kmajor_desc(b0 + (kk >> 2) * kBAtom + 32 * (kk & 3));
                         const uint32_t acc = (kb > 0 || kk > 0) ? 1u : 0u;
-                        if constexpr (kPair > 1)
-                            umma_bf16_pair(tmem_base + buf * BN, adesc, bdesc, kIdescK, acc);
-                        else
-                            umma_bf16(tmem_base + buf * BN, adesc, bdesc, kIdescK, acc);
+                        umma_bf16_pair(tmem_base + buf * BN, adesc, bdesc, kIdescK, acc);
                     }
                     issued = true;
-                    if constexpr (kPair > 1)
-                        umma_commit_pair_multicast(&empty[s], 3);
-                    else
-                        umma_commit(&empty[s]);
+                    umma_commit_pair_multicast(&empty[s], 3);
                 }
                 if (!ok) break;
-                if constexpr (kPair > 1)
-                    umma_commit_pair_multicast(&tfull[buf], 3);
-                else
-                    umma_commit(&tfull[buf]);
+                umma_commit_pair_multicast(&tfull[buf], 3);
             }
             if (issued) {
-                if constexpr (kPair > 1)
-                    umma_commit_pair(drain);
-                else
-                    umma_commit(drain);
+                umma_commit_pair(drain);
                 wait_bar(drain, 0u, abort, status, true);
             }
-        } else if (lane == 0 && kPair > 1) {
+        } else if (lane == 0) {
             // Relay (CTA 1): each landed stage is announced to CTA 0.
             const uint32_t ready0 = mapa_shared(smem_u32(ready), 0);
             uint32_t it = 0;
@@ -289,7 +257,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         constexpr int kQmax = (1 << (BITS - 1)) - 1;
         const int q = warp & 3;
         const int rec_per_row = N / kBlock;
-        const uint32_t tempty0 = kPair > 1 ? mapa_shared(smem_u32(tempty), 0) : smem_u32(tempty);
+        const uint32_t tempty0 = mapa_shared(smem_u32(tempty), 0);
         uint32_t t = 0;
         for (int tile = cid; tile < num_tiles; tile += ncl, ++t) {
             const int buf = t & 1;
@@ -370,7 +338,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) {
-                if (kPair > 1 && rank != 0)
+                if (rank != 0)
                     mbar_arrive_remote(tempty0 + (uint32_t)buf * 8u);
                 else
                     mbar_arrive(&tempty[buf]);
@@ -383,17 +351,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     // Neither CTA of a pair frees TMEM or exits while the other may still
     // arrive on its barriers or have the pair's MMAs read its shared memory.
-    if constexpr (kPair > 1) cluster_sync_all();
+    cluster_sync_all();
     if (warp == kMmaWarp) {
         __syncwarp();
-        if constexpr (kPair > 1)
-            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                         "r"(kTmemCols)
-                         : "memory");
-        else
-            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                         "r"(kTmemCols)
-                         : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(kTmemCols)
+                     : "memory");
     }
 }
 
@@ -417,12 +380,6 @@ cudaError_t launch_bits(const void *x, const void *w, int T, int N, int K, void 
         attr_set[dev] = true;
     }
     const int num_tiles = ((T + kTileRows - 1) / kTileRows) * (N / BN);
-    if constexpr (kPair == 1) {
-        const int grid = num_tiles < sm_count() ? num_tiles : sm_count();
-        kernel<<<grid, kThreads, kSmemBytes, st>>>(m_x, m_w, T, N, K, static_cast<uint16_t *>(y),
-                                                   static_cast<uint32_t *>(codes), scales);
-        return cudaGetLastError();
-    }
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;

@@ -150,21 +150,13 @@ __device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
     asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
     return r;
 }
-// Arrive on an mbarrier of another CTA of the cluster: with
-// AGOQ_REMOTE_ARRIVE_CLUSTER a release at cluster scope, otherwise the
-// instruction's default release semantics (measured far cheaper on GB300; the
-// data that the arrival publishes is read by the tensor core's asynchronous
-// proxy, which the writer's proxy fence already ordered).
-#ifndef AGOQ_REMOTE_ARRIVE_CLUSTER
-#define AGOQ_REMOTE_ARRIVE_CLUSTER 0
-#endif
+// Arrive on an mbarrier of another CTA of the cluster, with the instruction's
+// default release semantics (a release at cluster scope measured far more
+// expensive on GB300; the data that the arrival publishes is read by the
+// tensor core's asynchronous proxy, which the writer's proxy fence already
+// ordered).
 __device__ __forceinline__ void mbar_arrive_remote(uint32_t raddr) {
-#if AGOQ_REMOTE_ARRIVE_CLUSTER
-    asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(raddr)
-                 : "memory");
-#else
     asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(raddr) : "memory");
-#endif
 }
 // This CTA's rank in its cluster.
 __device__ __forceinline__ uint32_t cluster_ctarank() {

@@ -1,18 +1,12 @@
 // wgrad_gemm.cu -- the weight-gradient GEMM with 128-deep k-blocks (K a
 // multiple of 128), and the entry points that pick an instance by K (the
 // kernel itself is in wgrad_gemm_impl.cuh).
-#ifndef AGOQ_GEMM_BK
+// Ring depths (k-blocks): A 2, B 2, X 3 -- what the shared memory holds at
+// this depth.
 #define AGOQ_GEMM_BK 128
-#endif
-#ifndef AGOQ_GEMM_NA
 #define AGOQ_GEMM_NA 2
-#endif
-#ifndef AGOQ_GEMM_NB
 #define AGOQ_GEMM_NB 2
-#endif
-#ifndef AGOQ_GEMM_NX
 #define AGOQ_GEMM_NX 3
-#endif
 #define AGOQ_WGRAD_NS wg128
 #include "wgrad_gemm_impl.cuh"
 

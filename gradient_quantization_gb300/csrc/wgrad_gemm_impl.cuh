@@ -6,10 +6,9 @@
 //
 //   dW[M][N] = sum_k dY[k][m] * Xhat[k][n],  Xhat = bf16(fl32(code * scale))
 //
-// Blackwell design (sm_103a): one CTA per SM; with AGOQ_GEMM_PAIR (the
-// default) the two CTAs of a cluster of two form a tcgen05 CTA pair that is
-// persistent over 512 x 256 output tiles (256 rows per CTA, as two 128-row
-// halves).  Per BK-deep k-block each CTA has three shared-memory rings:
+// Blackwell design (sm_103a): one CTA per SM; the two CTAs of a cluster of
+// two form a tcgen05 CTA pair that is persistent over 512 x 256 output tiles
+// (256 rows per CTA, as two 128-row halves).  Per BK-deep k-block each CTA has three shared-memory rings:
 //   A ring (NA stages)  its 256 dY rows x BK, four 64-wide boxes with the
 //                       128-byte swizzle, loaded by TMA (rows past M read as
 //                       zeros and are not multiplied);
@@ -47,9 +46,6 @@
 //                 E4M3 master codes of the row block, add the FP32
 //                 accumulator, take the block absmax, requantize in place with
 //                 the new scale.  The BF16 dW never exists.
-// Without AGOQ_GEMM_PAIR each CTA works alone on 256 x 256 tiles with the
-// same roles (M=128 MMAs of cta_group::1, all 256 X-hat columns dequantized
-// locally).
 // Every mbarrier wait has a time limit: on expiry the kernel records a code in
 // g_device_status, raises a CTA-wide abort flag, lets in-flight copies and
 // MMAs drain (with a limit), frees its TMEM and returns; both CTAs of a pair
@@ -83,58 +79,28 @@ constexpr int kEpiBf16 = 0, kEpiF32 = 1, kEpiAccumFp8 = 2;
 
 constexpr int BM = 256, BN = 256, BK = AGOQ_GEMM_BK;
 constexpr int NA = AGOQ_GEMM_NA, NX = AGOQ_GEMM_NX, NB = AGOQ_GEMM_NB;
-constexpr int kChunk = BK * 128;                          // bytes of one 64-wide M chunk of an A stage
-// The B (X-hat) ring is kept in sub-stages of BKB = BK / kBSplit k-rows, so the
-// dequantizers can run further ahead of the MMA in the same shared memory.
-#ifndef AGOQ_GEMM_BSPLIT
-#define AGOQ_GEMM_BSPLIT 1
-#endif
-constexpr int kBSplit = AGOQ_GEMM_BSPLIT;
-constexpr int BKB = BK / kBSplit;                          // k-rows of a B sub-stage
-constexpr int kChunkB = BKB * 128;                         // bytes of one 64-wide N chunk of it
-static_assert(BKB % 16 == 0 && BKB * kBSplit == BK, "B sub-stages are whole K-steps");
+constexpr int kChunk = BK * 128;   // bytes of one 64-wide M (A) or N (B) chunk of a stage
 constexpr int kTmaWarp = 0, kMmaWarp = 1, kTmaXWarp = 2, kDeqWarp0 = 3, kDeqWarps = 16;
 constexpr int kThreads = (kDeqWarp0 + kDeqWarps) * 32;   // 608
-#ifndef AGOQ_GEMM_PAIR
-#define AGOQ_GEMM_PAIR 1
-#endif
-// 1: CTA 0 waits for the peer's arrivals with cluster-scope acquire; 0: with
-// the default (CTA-scope) acquire of mbarrier.try_wait.
-#ifndef AGOQ_PAIR_CLUSTER_WAIT
-#define AGOQ_PAIR_CLUSTER_WAIT 0
-#endif
-// 1: the peer's dequantizer warps arrive directly on CTA 0's full_b barrier
-// (which then counts both CTAs' warps) and the relay only forwards the A
-// stage; 0: the relay forwards both.
-#ifndef AGOQ_PAIR_DIRECT_B
-#define AGOQ_PAIR_DIRECT_B 1
-#endif
-constexpr bool kDirectB = AGOQ_GEMM_PAIR && AGOQ_PAIR_DIRECT_B;
-// With AGOQ_GEMM_PAIR the two CTAs of a cluster of two form a tcgen05 CTA
-// pair working on one 512 x 256 tile: each CTA holds 256 rows of dY (two
-// 128-row halves) and dequantizes only its 128 of the 256 X-hat columns; CTA
-// 0 issues pair MMAs (M = 256, N = 256) that read the A rows and the B columns
-// of both CTAs and accumulate each CTA's rows in its own TMEM.  Per output
-// element this halves the dequantization work and the shared-memory traffic
-// of the B operand.  The peer's producers publish a k-block to the issuing
-// CTA through one remote mbarrier arrive (a relay thread), and every MMA
-// commit is multicast to both CTAs' release barriers.
-constexpr int kPair = AGOQ_GEMM_PAIR ? 2 : 1;             // CTAs per tile
+// The two CTAs of a cluster of two form a tcgen05 CTA pair working on one
+// 512 x 256 tile: each CTA holds 256 rows of dY (two 128-row halves) and
+// dequantizes only its 128 of the 256 X-hat columns; CTA 0 issues pair MMAs
+// (M = 256, N = 256) that read the A rows and the B columns of both CTAs and
+// accumulate each CTA's rows in its own TMEM.  Per output element this halves
+// the dequantization work and the shared-memory traffic of the B operand (a
+// single-CTA design with 256 x 256 tiles measured slower: its dequantizers
+// were the limit).  CTA 1's relay thread publishes each landed A stage to CTA
+// 0 with one remote mbarrier arrive, its dequantizer warps arrive directly on
+// CTA 0's B barrier, and every MMA commit is multicast to both CTAs' release
+// barriers.
+constexpr int kPair = 2;                                   // CTAs per tile
 constexpr int kTileRows = BM * kPair;                      // output rows per tile
 constexpr int kBCols = BN / kPair;                         // X-hat columns this CTA holds
 constexpr int kWordsPerRow = kBCols / 8;                   // 4-bit code words per k-row
 constexpr int kRowsPerWarp = 32 / kWordsPerRow;            // k-rows a dequant warp covers at once
-// With AGOQ_GEMM_SUB_BY_WARP each B sub-stage is written by its own group of
-// kDeqWarps / kBSplit dequantizer warps (one wait, one fence and one arrive per
-// warp and k-block); otherwise every warp writes its rows of every sub-stage.
-#ifndef AGOQ_GEMM_SUB_BY_WARP
-#define AGOQ_GEMM_SUB_BY_WARP 0
-#endif
-constexpr bool kSubByWarp = AGOQ_GEMM_SUB_BY_WARP && kBSplit > 1;
-constexpr int kSubWarps = kSubByWarp ? kDeqWarps / kBSplit : kDeqWarps;   // writers of a sub-stage
-constexpr int kDeqRows = BKB / (kRowsPerWarp * kSubWarps); // code words per dequant thread per sub-stage
-static_assert(kDeqRows >= 1 && kDeqRows * kRowsPerWarp * kSubWarps == BKB,
-              "every k-row of a sub-stage is dequantized exactly once");
+constexpr int kDeqRows = BK / (kRowsPerWarp * kDeqWarps); // code words per dequant thread per stage
+static_assert(kDeqRows >= 1 && kDeqRows * kRowsPerWarp * kDeqWarps == BK,
+              "every k-row of a stage is dequantized exactly once");
 static_assert(NB >= 2, "the B ring must let dequantization run ahead of the MMA");
 static_assert(kDeqWarps == 16, "epilogue items: 4 TMEM lane quarters x 4 blocks of 128 columns");
 // A waiter may only be one phase behind the barrier it polls (a parity test
@@ -142,12 +108,11 @@ static_assert(kDeqWarps == 16, "epilogue items: 4 TMEM lane quarters x 4 blocks 
 // on by all of its consumers for every phase in order, and tmem_full(t + 1)
 // cannot complete before every dequant warp has waited for tmem_full(t) and
 // released the accumulator.  The pair-ready ring (CTA 0 only) has as many
-// slots as the relay can run ahead of the MMA: NA k-blocks when it waits for
-// the A stage only (its TMA producer needs the stages the MMA releases), or
-// min(NA, NB / kBSplit) when it also waits for the X-hat sub-stages.
-constexpr int NP = AGOQ_PAIR_DIRECT_B ? NA : (NA < NB / kBSplit ? NA : NB / kBSplit);
+// slots as the relay can run ahead of the MMA: NA k-blocks (the relay waits
+// for the A stage only, whose TMA producer needs the stages the MMA releases).
+constexpr int NP = NA;
 constexpr int kAStage = BM * BK * 2;                      // 32 KiB of dY (BF16)
-constexpr int kBStage = kBCols * BKB * 2;                 // this CTA's X-hat columns (BF16), one sub-stage
+constexpr int kBStage = kBCols * BK * 2;                  // this CTA's X-hat columns (BF16)
 constexpr int kCStage = BK * kBCols / 2;                  // their packed codes
 constexpr int kSStage = BK * 4 * 4;                       // ... and 4-wide scale boxes
 static_assert(BK % 16 == 0 && BK >= 16 && BK <= 256, "k-block depth");
@@ -159,15 +124,12 @@ constexpr int kNumBars = 2 * NA + 2 * NX + 2 * NB + NP + 3;
 constexpr int kOffMisc = kOffBar + 8 * kNumBars;
 constexpr int kSmemBytes = kOffMisc + 16 + 1024;          // + slack for 1024-byte alignment
 constexpr uint32_t kTmemCols = 512;
-#ifndef AGOQ_GEMM_PREFETCH_LEAD
-#define AGOQ_GEMM_PREFETCH_LEAD 8
-#endif
-constexpr int kPrefetchLead = AGOQ_GEMM_PREFETCH_LEAD;   // k-blocks between master prefetch and use
+constexpr int kPrefetchLead = 8;   // k-blocks between master prefetch and use
 
 static_assert(kSmemBytes <= 232448, "shared memory budget");
 
 // Instruction descriptor: kind::f16, BF16 A and B, FP32 D, A and B MN-major,
-// M = 128 per CTA (256 for a pair), N = 256.
+// M = 256 (128 rows from each CTA of the pair), N = 256.
 constexpr uint32_t kIdesc = (1u << 4) | (1u << 7) | (1u << 10) | (1u << 15) | (1u << 16) |
                             ((uint32_t)(BN >> 3) << 17) | ((uint32_t)((128 * kPair) >> 4) << 24);
 
@@ -230,26 +192,6 @@ __device__ __forceinline__ uint32_t word_of(const uint4 (&c)[8], int i) {
     return (i & 3) == 0 ? v.x : (i & 3) == 1 ? v.y : (i & 3) == 2 ? v.z : v.w;
 }
 
-// The epilogue of a tile runs after the dequantizers have written the B
-// stages of the next tile's first AGOQ_GEMM_LEAD + 1 k-blocks (-1: as many as
-// the B ring holds).
-#ifndef AGOQ_GEMM_LEAD
-#define AGOQ_GEMM_LEAD 0
-#endif
-// 1: the BF16 epilogue releases the accumulator before its global stores
-// (all 128 columns held in registers); 2: after storing the first 64 columns
-// (64 held); 0: after all stores.
-#ifndef AGOQ_EPI_EARLY_RELEASE
-#define AGOQ_EPI_EARLY_RELEASE 1
-#endif
-#ifndef AGOQ_ACCUM_LD_GROUP
-#define AGOQ_ACCUM_LD_GROUP 1
-#endif
-#ifndef AGOQ_ACCUM_EARLY_LOAD
-#define AGOQ_ACCUM_EARLY_LOAD 0
-#endif
-constexpr int kLdGroup = AGOQ_ACCUM_LD_GROUP;   // TMEM loads issued per wait
-
 // The 128 E4M3 master codes and the scale of one row block, loaded before the
 // accumulator is ready (the loads do not depend on it).
 struct MasterBlock {
@@ -269,53 +211,45 @@ struct MasterBlock {
 // (already loaded), `codes`/`scale` where the new ones go.  The first pass
 // forms t = fl(fl(e4m3(c) * s) + acc), takes the block absmax and writes t
 // back over the accumulator in TMEM; the second pass reads t and requantizes
-// with the new scale.  TMEM loads go in pairs behind one wait.
+// with the new scale.
 __device__ __forceinline__ void accum_fp8_block(uint32_t taddr, const MasterBlock &mb,
                                                 uint8_t *codes, float *scale) {
     uint4 *mc = reinterpret_cast<uint4 *>(codes);
     float am = 0.0f;
 #pragma unroll
-    for (int cc = 0; cc < 8; cc += kLdGroup) {
-        uint32_t v[kLdGroup][16];
+    for (int cc = 0; cc < 8; ++cc) {
+        uint32_t v[16];
         __syncwarp();
-#pragma unroll
-        for (int h = 0; h < kLdGroup; ++h) tmem_ld16_nowait(taddr + (cc + h) * 16, v[h]);
+        tmem_ld16_nowait(taddr + cc * 16, v);
         tmem_wait_ld();
+        float t[16];
 #pragma unroll
-        for (int h = 0; h < kLdGroup; ++h) {
-            float t[16];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                master_plus_acc4(word_of(mb.c, (cc + h) * 4 + w), mb.s, v[h] + 4 * w, t + 4 * w);
-                am = fmaxf(am, fmaxf(fmaxf(fabsf(t[4 * w]), fabsf(t[4 * w + 1])),
-                                     fmaxf(fabsf(t[4 * w + 2]), fabsf(t[4 * w + 3]))));
-            }
-            tmem_st16(taddr + (cc + h) * 16, t);
+        for (int w = 0; w < 4; ++w) {
+            master_plus_acc4(word_of(mb.c, cc * 4 + w), mb.s, v + 4 * w, t + 4 * w);
+            am = fmaxf(am, fmaxf(fmaxf(fabsf(t[4 * w]), fabsf(t[4 * w + 1])),
+                                 fmaxf(fabsf(t[4 * w + 2]), fabsf(t[4 * w + 3]))));
         }
+        tmem_st16(taddr + cc * 16, t);
     }
     asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
     const float snew = __fdiv_rn(am, kE4M3Max);
 #pragma unroll
-    for (int cc = 0; cc < 8; cc += kLdGroup) {
-        uint32_t v[kLdGroup][16];
+    for (int cc = 0; cc < 8; ++cc) {
+        uint32_t v[16];
         __syncwarp();   // lanes may have left the fast requantization path; tcgen05.ld is .aligned
-#pragma unroll
-        for (int h = 0; h < kLdGroup; ++h) tmem_ld16_nowait(taddr + (cc + h) * 16, v[h]);
+        tmem_ld16_nowait(taddr + cc * 16, v);
         tmem_wait_ld();
+        uint32_t o[4];
 #pragma unroll
-        for (int h = 0; h < kLdGroup; ++h) {
-            uint32_t o[4];
+        for (int p = 0; p < 2; ++p) {
+            float t[8];
 #pragma unroll
-            for (int p = 0; p < 2; ++p) {
-                float t[8];
-#pragma unroll
-                for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(v[h][8 * p + i]);
-                const uint2 q = e4m3_codes8(t, snew);
-                o[2 * p] = q.x;
-                o[2 * p + 1] = q.y;
-            }
-            mc[cc + h] = make_uint4(o[0], o[1], o[2], o[3]);
+            for (int i = 0; i < 8; ++i) t[i] = __uint_as_float(v[8 * p + i]);
+            const uint2 q = e4m3_codes8(t, snew);
+            o[2 * p] = q.x;
+            o[2 * p + 1] = q.y;
         }
+        mc[cc] = make_uint4(o[0], o[1], o[2], o[3]);
     }
     *scale = snew;
 }
@@ -357,50 +291,47 @@ __device__ __forceinline__ void epilogue_item(uint32_t taddr, void *dW, float *m
     }
 }
 
-// The MMAs of one k-block: NK K-steps of 16, each for the M-halves (the
+// The MMAs of one k-block: BK/16 K-steps of 16, each for the M-halves (the
 // second only when BOTH) sharing the K-step's B descriptor; the first K-step
-// of a tile overwrites the accumulator.  NK and BOTH are compile-time
-// constants so the issuing thread runs a straight line of MMA instructions
-// (a depth test in the loop measured 2-7% slower, hence one kernel per BK).
-//   a0: the A stage; kk0: its first K-step used here; b0: the B sub-stage.
-template <int NK, bool BOTH>
+// of a tile overwrites the accumulator.  The depth is a compile-time constant
+// so the issuing thread runs a straight line of MMA instructions (a depth test
+// in the loop measured 2-7% slower, hence one kernel per BK).
+//   a0: the A stage; b0: the B stage.
+template <bool BOTH>
 __device__ __forceinline__ void issue_kblock_h(uint32_t tmem_base, uint32_t a0, uint32_t b0,
-                                               int kk0, bool accumulate) {
+                                               bool accumulate) {
 #pragma unroll
-    for (int j = 0; j < NK; ++j) {
-        const int kk = kk0 + j;
-        const uint64_t bdesc = sw128_desc(b0 + j * 2048, kChunkB, 1024);
+    for (int kk = 0; kk < BK / 16; ++kk) {
+        const uint64_t bdesc = sw128_desc(b0 + kk * 2048, kChunk, 1024);
         const uint32_t acc = (accumulate || kk > 0) ? 1u : 0u;
-        const uint64_t adesc0 = sw128_desc(a0 + kk * 2048, kChunk, 1024);
-        if constexpr (kPair > 1)
-            umma_bf16_pair(tmem_base, adesc0, bdesc, kIdesc, acc);
-        else
-            umma_bf16(tmem_base, adesc0, bdesc, kIdesc, acc);
-        if constexpr (BOTH) {
-            const uint64_t adesc1 = sw128_desc(a0 + 2 * kChunk + kk * 2048, kChunk, 1024);
-            if constexpr (kPair > 1)
-                umma_bf16_pair(tmem_base + 256, adesc1, bdesc, kIdesc, acc);
-            else
-                umma_bf16(tmem_base + 256, adesc1, bdesc, kIdesc, acc);
-        }
+        umma_bf16_pair(tmem_base, sw128_desc(a0 + kk * 2048, kChunk, 1024), bdesc, kIdesc, acc);
+        if constexpr (BOTH)
+            umma_bf16_pair(tmem_base + 256, sw128_desc(a0 + 2 * kChunk + kk * 2048, kChunk, 1024),
+                           bdesc, kIdesc, acc);
     }
 }
-template <int NK>
-__device__ __forceinline__ void issue_kblock(uint32_t tmem_base, uint32_t a0, uint32_t b0, int kk0,
+__device__ __forceinline__ void issue_kblock(uint32_t tmem_base, uint32_t a0, uint32_t b0,
                                              bool accumulate, bool both) {
-    if (kPair == 1 || both)
-        issue_kblock_h<NK, true>(tmem_base, a0, b0, kk0, accumulate);
+    if (both)
+        issue_kblock_h<true>(tmem_base, a0, b0, accumulate);
     else
-        issue_kblock_h<NK, false>(tmem_base, a0, b0, kk0, accumulate);
+        issue_kblock_h<false>(tmem_base, a0, b0, accumulate);
 }
 
 // dW (EPI kEpiBf16 / kEpiF32) or the FP8 master codes (kEpiAccumFp8, with
-// their scales in `mscales`) are [M][N] row-major.
-template <int EPI>
+// their scales in `mscales`) are [M][N] row-major.  M and N are multiples of
+// 128: rows past M of the last tile read as zeros and are not stored, and when
+// N is not a multiple of 256 the last tile's second 128-column block (codes
+// and scales read as zeros) is not stored.  With TMA_SCALES the X scales come
+// through the X ring by TMA (a scale row is then a multiple of 16 bytes: N a
+// multiple of 512); otherwise the X producer warp reads them from `xs` into
+// the same shared-memory slots.
+template <int EPI, bool TMA_SCALES>
 __global__ void __launch_bounds__(kThreads, 1)
     wgrad_gemm_int4_kernel(const __grid_constant__ CUtensorMap map_dy,
                            const __grid_constant__ CUtensorMap map_xc,
-                           const __grid_constant__ CUtensorMap map_xs, void *__restrict__ dW,
+                           const __grid_constant__ CUtensorMap map_xs,
+                           const float *__restrict__ xs, void *__restrict__ dW,
                            float *__restrict__ mscales, int M, int N, int K) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
@@ -424,12 +355,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     sh.tmem_addr = reinterpret_cast<uint32_t *>(smem + kOffMisc);
     sh.abort = reinterpret_cast<volatile int *>(smem + kOffMisc + 4);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_tiles = N / BN, kblocks = K / BK;   // K is a multiple of BK
+    const int n_tiles = (N + BN - 1) / BN, kblocks = K / BK;   // K is a multiple of BK
     // Tile g covers rows m0 .. m0 + kTileRows - 1 and columns n0 .. n0 + 255;
     // this CTA (rank in the pair) holds rows half_row(h) .. +127 of M-half h
     // and X-hat columns n0 + rank * kBCols .. + kBCols - 1.  Rows at or past M
     // (the second half of the last tile) are neither multiplied nor stored.
-    const int rank = kPair > 1 ? (int)cluster_ctarank() : 0;
+    const int rank = (int)cluster_ctarank();
     const int cluster_id = (int)(blockIdx.x / kPair), num_clusters = (int)(gridDim.x / kPair);
     const int m_tiles = (M + kTileRows - 1) / kTileRows, num_groups = m_tiles * n_tiles;
     auto tile_of = [&](int g, int &m0, int &n0) {
@@ -437,7 +368,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         n0 = (g % n_tiles) * BN;
     };
     auto half_row = [&](int m0, int h) { return m0 + h * 128 * kPair + 128 * rank; };
+    // some row of the pair's M-half h lies below M (its MMAs are issued)
     auto half_valid = [&](int m0, int h) { return m0 + h * 128 * kPair < M; };
+    // this CTA's rows of M-half h, and the 128-column block at col0, are stored
+    auto item_valid = [&](int m0, int h, int col0) { return half_row(m0, h) < M && col0 < N; };
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NA; ++s) {
@@ -449,7 +383,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_init(&sh.empty_x[s], kDeqWarps);
         }
         for (int s = 0; s < NB; ++s) {
-            mbar_init(&sh.full_b[s], kDirectB ? kSubWarps * kPair : kSubWarps);
+            mbar_init(&sh.full_b[s], kDeqWarps * kPair);   // every dequantizer warp of the pair
             mbar_init(&sh.empty_b[s], 1);
         }
         for (int s = 0; s < NP; ++s) mbar_init(&sh.pair_ready[s], 1);
@@ -460,66 +394,111 @@ __global__ void __launch_bounds__(kThreads, 1)
         asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     }
     if (warp == kMmaWarp) {
-        if constexpr (kPair > 1) {
-            asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                             smem_u32(sh.tmem_addr)),
-                         "r"(kTmemCols)
-                         : "memory");
-            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
-        } else {
-            asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                             smem_u32(sh.tmem_addr)),
-                         "r"(kTmemCols)
-                         : "memory");
-            asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-        }
+        asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                         smem_u32(sh.tmem_addr)),
+                     "r"(kTmemCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
     }
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
-    if constexpr (kPair > 1) cluster_sync_all();   // the peer's barriers are initialised
+    cluster_sync_all();   // the peer's barriers are initialised
     const uint32_t tmem_base = *sh.tmem_addr;
 
-    if (warp == kTmaWarp || warp == kTmaXWarp) {
-        // Producers: warp 0 fills the A ring, warp 2 the X ring.
+    if (warp == kTmaWarp) {
+        // Producer of the A ring (one lane).
         if (lane == 0) {
-            const bool is_a = warp == kTmaWarp;
-            const int depth = is_a ? NA : NX;
-            uint64_t *full = is_a ? sh.full_a : sh.full_x;
-            uint64_t *empty = is_a ? sh.empty_a : sh.empty_x;
             uint32_t it = 0;
             bool ok = true;
             for (int g = cluster_id; ok && g < num_groups; g += num_clusters) {
                 int m0, n0;
                 tile_of(g, m0, n0);
-                const int cb = n0 + rank * kBCols;   // first X-hat column of this CTA
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const int s = it % depth;
-                    const uint32_t ph = (it / depth) & 1u;
-                    if (!wait_bar(&empty[s], ph ^ 1u, sh.abort, &g_device_status)) { ok = false; break; }
+                    const int s = it % NA;
+                    const uint32_t ph = (it / NA) & 1u;
+                    if (!wait_bar(&sh.empty_a[s], ph ^ 1u, sh.abort, &g_device_status)) { ok = false; break; }
                     const int k0 = kb * BK;
-                    if (is_a) {
-                        const int halves = (kPair == 1 || half_valid(m0, 1)) ? 2 : 1;
-                        mbar_expect_tx(&full[s], halves * (kAStage / 2));
-                        for (int h = 0; h < halves; ++h) {
+                    const int halves = half_valid(m0, 1) ? 2 : 1;
+                    mbar_expect_tx(&sh.full_a[s], halves * (kAStage / 2));
+                    for (int h = 0; h < halves; ++h) {
 #pragma unroll
-                            for (int c = 0; c < 2; ++c)
-                                tma_load_2d(sh.a + s * kAStage + (2 * h + c) * kChunk, &map_dy,
-                                            &full[s], half_row(m0, h) + 64 * c, k0);
-                        }
-                    } else {
-                        mbar_expect_tx(&full[s], kCStage + kSStage);
-                        tma_load_2d(sh.c + s * kCStage, &map_xc, &full[s], cb / 2, k0);
-                        tma_load_2d(sh.s + s * (kSStage / 4), &map_xs, &full[s], (cb / 128) & ~3, k0);
+                        for (int c = 0; c < 2; ++c)
+                            tma_load_2d(sh.a + s * kAStage + (2 * h + c) * kChunk, &map_dy,
+                                        &sh.full_a[s], half_row(m0, h) + 64 * c, k0);
                     }
                 }
             }
             // Drain: every issued load lands before the CTA may exit (a no-op
             // unless the pipeline was aborted).  Iteration it-1-d was the last
-            // load into stage (it-1-d) % depth.
-            for (int d = 0; d < depth && d < (int)it; ++d) {
+            // load into stage (it-1-d) % NA.
+            for (int d = 0; d < NA && d < (int)it; ++d) {
                 const uint32_t last = it - 1 - d;
-                wait_bar(&full[last % depth], (last / depth) & 1u, sh.abort, &g_device_status, true);
+                wait_bar(&sh.full_a[last % NA], (last / NA) & 1u, sh.abort, &g_device_status, true);
+            }
+        }
+    } else if (warp == kTmaXWarp) {
+        // Producer of the X ring: lane 0 waits for the stage and issues the TMA
+        // loads of the codes (and, with TMA_SCALES, of the 4-wide scale box);
+        // without TMA_SCALES the warp's lanes read this CTA's scale of each
+        // k-row from global memory into the stage's scale slots, and the
+        // arrive that follows (after __syncwarp) publishes them with the codes.
+        // The scales of k-block (g, kb): lane l holds k-rows l, l + 32, ...;
+        // zeros past N (where the codes read as zeros too).
+        constexpr int kScPerLane = BK / 32;
+        static_assert(BK % 32 == 0, "every k-row of a stage gets its scale");
+        auto load_scales = [&](int g, int kb, float (&v)[kScPerLane]) {
+            int m0, n0;
+            tile_of(g, m0, n0);
+            const int cb = n0 + rank * kBCols;
+#pragma unroll
+            for (int i = 0; i < kScPerLane; ++i)
+                v[i] = cb < N ? __ldg(xs + (size_t)(kb * BK + lane + 32 * i) * (N / 128) + cb / 128)
+                              : 0.0f;
+        };
+        float vsc[kScPerLane];
+        if (!TMA_SCALES && cluster_id < num_groups) load_scales(cluster_id, 0, vsc);
+        uint32_t it = 0;
+        bool ok = true;
+        for (int g = cluster_id; ok && g < num_groups; g += num_clusters) {
+            int m0, n0;
+            tile_of(g, m0, n0);
+            const int cb = n0 + rank * kBCols;   // first X-hat column of this CTA
+            for (int kb = 0; kb < kblocks; ++kb, ++it) {
+                const int s = it % NX;
+                const uint32_t ph = (it / NX) & 1u;
+                float cur[kScPerLane];
+                if (!TMA_SCALES) {
+                    // this k-block's scales are in registers; the next one's
+                    // loads are issued before the wait for the stage
+#pragma unroll
+                    for (int i = 0; i < kScPerLane; ++i) cur[i] = vsc[i];
+                    if (kb + 1 < kblocks)
+                        load_scales(g, kb + 1, vsc);
+                    else if (g + num_clusters < num_groups)
+                        load_scales(g + num_clusters, 0, vsc);
+                }
+                if (!warp_wait(&sh.empty_x[s], ph ^ 1u, sh.abort, &g_device_status)) { ok = false; break; }
+                const int k0 = kb * BK;
+                if (!TMA_SCALES) {
+                    float *dst = sh.s + s * (kSStage / 4) + ((cb / 128) & 3);
+#pragma unroll
+                    for (int i = 0; i < kScPerLane; ++i) dst[4 * (lane + 32 * i)] = cur[i];
+                    __syncwarp();
+                }
+                if (lane == 0) {
+                    mbar_expect_tx(&sh.full_x[s], kCStage + (TMA_SCALES ? kSStage : 0));
+                    tma_load_2d(sh.c + s * kCStage, &map_xc, &sh.full_x[s], cb / 2, k0);
+                    if (TMA_SCALES)
+                        tma_load_2d(sh.s + s * (kSStage / 4), &map_xs, &sh.full_x[s],
+                                    (cb / 128) & ~3, k0);
+                }
+            }
+        }
+        if (lane == 0) {
+            for (int d = 0; d < NX && d < (int)it; ++d) {
+                const uint32_t last = it - 1 - d;
+                wait_bar(&sh.full_x[last % NX], (last / NX) & 1u, sh.abort, &g_device_status, true);
             }
         }
     } else if (warp == kMmaWarp) {
@@ -531,77 +510,45 @@ __global__ void __launch_bounds__(kThreads, 1)
                 int m0, n0;
                 tile_of(g, m0, n0);
                 const bool v1 = half_valid(m0, 1);
-                if (!(kPair > 1 && AGOQ_PAIR_CLUSTER_WAIT
-                          ? wait_bar_cluster(sh.tmem_empty, (t & 1u) ^ 1u, sh.abort, &g_device_status)
-                          : wait_bar(sh.tmem_empty, (t & 1u) ^ 1u, sh.abort, &g_device_status))) {
+                if (!wait_bar(sh.tmem_empty, (t & 1u) ^ 1u, sh.abort, &g_device_status)) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const int sa = it % NA;
+                    const int sa = it % NA, sb = it % NB;
                     if (!wait_bar(&sh.full_a[sa], (it / NA) & 1u, sh.abort, &g_device_status) ||
-                        (kPair > 1 &&
-                         !(AGOQ_PAIR_CLUSTER_WAIT
-                               ? wait_bar_cluster(&sh.pair_ready[it % NP], (it / NP) & 1u, sh.abort,
-                                                  &g_device_status)
-                               : wait_bar(&sh.pair_ready[it % NP], (it / NP) & 1u, sh.abort,
-                                          &g_device_status)))) {
+                        !wait_bar(&sh.pair_ready[it % NP], (it / NP) & 1u, sh.abort,
+                                  &g_device_status) ||
+                        !wait_bar(&sh.full_b[sb], (it / NB) & 1u, sh.abort, &g_device_status)) {
                         ok = false;
                         break;
                     }
-                    const uint32_t a0 = smem_u32(sh.a + sa * kAStage);
-#pragma unroll
-                    for (int sub = 0; sub < kBSplit; ++sub) {
-                        const uint32_t ib = it * kBSplit + sub;   // B sub-stage sequence number
-                        const int sb = ib % NB;
-                        if (!wait_bar(&sh.full_b[sb], (ib / NB) & 1u, sh.abort, &g_device_status)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        issue_kblock<BKB / 16>(tmem_base, a0, smem_u32(sh.b + sb * kBStage),
-                                               sub * (BKB / 16), kb > 0, v1);
-                        issued = true;
-                        if constexpr (kPair > 1)
-                            umma_commit_pair_multicast(&sh.empty_b[sb], 3);
-                        else
-                            umma_commit(&sh.empty_b[sb]);
-                    }
-                    if (!ok) break;
-                    if constexpr (kPair > 1)
-                        umma_commit_pair_multicast(&sh.empty_a[sa], 3);
-                    else
-                        umma_commit(&sh.empty_a[sa]);
+                    tc_fence_after();
+                    issue_kblock(tmem_base, smem_u32(sh.a + sa * kAStage),
+                                 smem_u32(sh.b + sb * kBStage), kb > 0, v1);
+                    issued = true;
+                    umma_commit_pair_multicast(&sh.empty_b[sb], 3);
+                    umma_commit_pair_multicast(&sh.empty_a[sa], 3);
                 }
                 if (!ok) break;
-                if constexpr (kPair > 1)
-                    umma_commit_pair_multicast(sh.tmem_full, 3);
-                else
-                    umma_commit(sh.tmem_full);
+                umma_commit_pair_multicast(sh.tmem_full, 3);
             }
             // Drain: all MMAs issued so far complete before TMEM is freed.
             if (issued) {
-                if constexpr (kPair > 1)
-                    umma_commit_pair(sh.drain);
-                else
-                    umma_commit(sh.drain);
+                umma_commit_pair(sh.drain);
                 wait_bar(sh.drain, 0u, sh.abort, &g_device_status, true);
             }
-        } else if (lane == 0 && kPair > 1) {
+        } else if (lane == 0) {
             // Relay (CTA 1 of a pair): once this CTA's A stage of a k-block
-            // has landed (and, without kDirectB, its X-hat stage is written),
-            // tell the issuing CTA with one remote arrive.
+            // has landed, tell the issuing CTA with one remote arrive (its
+            // dequantizer warps arrive on CTA 0's B barrier themselves).
             const uint32_t ready0 = mapa_shared(smem_u32(sh.pair_ready), 0);
             uint32_t it = 0;
             bool ok = true;
             for (int g = cluster_id; ok && g < num_groups; g += num_clusters) {
                 for (int kb = 0; kb < kblocks; ++kb, ++it) {
-                    const int sa = it % NA;
-                    const uint32_t ibl = it * kBSplit + kBSplit - 1;   // the k-block's last B sub-stage
-                    if (!wait_bar(&sh.full_a[sa], (it / NA) & 1u, sh.abort, &g_device_status) ||
-                        (!kDirectB && !wait_bar(&sh.full_b[ibl % NB], (ibl / NB) & 1u, sh.abort,
-                                                &g_device_status))) {
+                    if (!wait_bar(&sh.full_a[it % NA], (it / NA) & 1u, sh.abort, &g_device_status)) {
                         ok = false;
                         break;
                     }
@@ -620,30 +567,20 @@ __global__ void __launch_bounds__(kThreads, 1)
         // half_row(eh) + 32q + lane, columns n0 + 128*ejb .. +127.
         const int q = warp & 3, item = d >> 2, eh = item >> 1, ejb = item & 1;
         const uint32_t etaddr = tmem_base + ((uint32_t)(32 * q) << 16) + eh * 256 + ejb * 128;
-        const uint32_t tmem_empty0 =
-            kPair > 1 ? mapa_shared(smem_u32(sh.tmem_empty), 0) : smem_u32(sh.tmem_empty);
-        const uint32_t full_b0 =
-            kPair > 1 ? mapa_shared(smem_u32(sh.full_b), 0) : smem_u32(sh.full_b);
-        // The previous tile's epilogue runs once this tile's first kLead + 1
-        // k-blocks of X-hat are written (fewer for short K).
-        constexpr int kBBlocks = NB / kBSplit > 0 ? NB / kBSplit : 1;   // k-blocks the B ring holds
-        constexpr int kLead = AGOQ_GEMM_LEAD < 0 ? kBBlocks - 1 : AGOQ_GEMM_LEAD;
-        const int lead = kblocks - 1 < kLead ? kblocks - 1 : kLead;
+        const uint32_t tmem_empty0 = mapa_shared(smem_u32(sh.tmem_empty), 0);
+        const uint32_t full_b0 = mapa_shared(smem_u32(sh.full_b), 0);
+        // The previous tile's epilogue runs once this tile's first k-block of
+        // X-hat is written (measured: waiting for more of the ring, or running
+        // it before, was slower).
         auto epilogue = [&](int g, uint32_t t) -> bool {
             int m0, n0;
             tile_of(g, m0, n0);
-            const bool valid = half_valid(m0, eh);   // the same for the whole warp
             const int row = half_row(m0, eh) + 32 * q + lane, col0 = n0 + ejb * 128;
+            const bool valid = item_valid(m0, eh, col0);   // the same for the whole warp
             MasterBlock mb;
-            if constexpr (EPI == kEpiAccumFp8 && AGOQ_ACCUM_EARLY_LOAD) {
-                // the master block's loads overlap the wait for the accumulator
-                if (valid)
-                    mb.load(static_cast<const uint8_t *>(dW) + (size_t)row * N + col0,
-                            mscales + (size_t)row * (N / 128) + col0 / 128);
-            }
             if (!warp_wait(sh.tmem_full, t & 1u, sh.abort, &g_device_status)) return false;
             tc_fence_after();
-            if constexpr (EPI == kEpiAccumFp8 && !AGOQ_ACCUM_EARLY_LOAD) {
+            if constexpr (EPI == kEpiAccumFp8) {
                 if (valid)
                     mb.load(static_cast<const uint8_t *>(dW) + (size_t)row * N + col0,
                             mscales + (size_t)row * (N / 128) + col0 / 128);
@@ -652,20 +589,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) {
-                    if (kPair > 1 && rank != 0)
+                    if (rank != 0)
                         mbar_arrive_remote(tmem_empty0);
                     else
                         mbar_arrive(sh.tmem_empty);
                 }
             };
-            if constexpr (EPI == kEpiBf16 && AGOQ_EPI_EARLY_RELEASE) {
-                // Read and round the item, storing the first kStoreEarly
-                // 32-column chunks at once and keeping the rest in registers;
-                // hand the accumulator back to the MMA, then store the rest
-                // while the next tile's MMAs run.
-                constexpr int kStoreEarly = AGOQ_EPI_EARLY_RELEASE == 1 ? 0 : 2;
-                constexpr int kHold = 4 - kStoreEarly;
-                uint32_t h[16 * kHold];
+            if constexpr (EPI == kEpiBf16) {
+                // Read and round the whole item into registers, hand the
+                // accumulator back to the MMA, then store while the next tile's
+                // MMAs run.
+                uint32_t h[64];
                 uint4 *dst = reinterpret_cast<uint4 *>(static_cast<uint16_t *>(dW) +
                                                        (size_t)row * N + col0);
                 if (valid) {
@@ -673,30 +607,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int cc = 0; cc < 4; ++cc) {
                         uint32_t v[32];
                         tmem_ld32(etaddr + cc * 32, v);
-                        if (cc < kStoreEarly) {
 #pragma unroll
-                            for (int j = 0; j < 4; ++j) {
-                                uint32_t w4[4];
-#pragma unroll
-                                for (int i = 0; i < 4; ++i)
-                                    w4[i] = pack_bf16x2(__uint_as_float(v[8 * j + 2 * i]),
-                                                        __uint_as_float(v[8 * j + 2 * i + 1]));
-                                dst[4 * cc + j] = make_uint4(w4[0], w4[1], w4[2], w4[3]);
-                            }
-                        } else {
-#pragma unroll
-                            for (int i = 0; i < 16; ++i)
-                                h[16 * (cc - kStoreEarly) + i] = pack_bf16x2(
-                                    __uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-                        }
+                        for (int i = 0; i < 16; ++i)
+                            h[16 * cc + i] =
+                                pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
                     }
                 }
                 release();
                 if (valid) {
 #pragma unroll
-                    for (int j = 0; j < 4 * kHold; ++j)
-                        dst[4 * kStoreEarly + j] =
-                            make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+                    for (int j = 0; j < 16; ++j)
+                        dst[j] = make_uint4(h[4 * j], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
                 }
             } else {
                 if (valid) epilogue_item<EPI>(etaddr, dW, mscales, row, col0, N, mb);
@@ -716,7 +637,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if constexpr (EPI == kEpiAccumFp8) {
                     // Pull this thread's master block of the tile into L2 a few
                     // k-blocks before its epilogue needs it.
-                    if (half_valid(m0, eh) &&
+                    if (item_valid(m0, eh, n0 + ejb * 128) &&
                         kb == (kblocks > kPrefetchLead ? kblocks - kPrefetchLead : 0)) {
                         const size_t row = (size_t)(half_row(m0, eh) + 32 * q + lane);
                         prefetch_l2(static_cast<const uint8_t *>(dW) + row * N + n0 + ejb * 128);
@@ -727,56 +648,41 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!warp_wait(&sh.full_x[sx], (it / NX) & 1u, sh.abort, &g_device_status)) { ok = false; break; }
                 const uint32_t *codes = reinterpret_cast<const uint32_t *>(sh.c + sx * kCStage);
                 const float *scales = sh.s + sx * (kSStage / 4);
-                // sub-stages this warp writes: all of them, or only its own
-                constexpr int kMySubs = kSubByWarp ? 1 : kBSplit;
-                const int sub0 = kSubByWarp ? d / kSubWarps : 0;
-                const int dd = kSubByWarp ? d % kSubWarps : d;   // the warp's index among the writers
-                uint32_t w[kMySubs][kDeqRows];
-                float sc[kMySubs][kDeqRows];
+                uint32_t w[kDeqRows];
+                float sc[kDeqRows];
 #pragma unroll
-                for (int js = 0; js < kMySubs; ++js) {
-#pragma unroll
-                    for (int i = 0; i < kDeqRows; ++i) {
-                        // row of the X stage
-                        const int k = (sub0 + js) * BKB + kRowsPerWarp * (dd + kSubWarps * i) + rsub;
-                        w[js][i] = codes[k * kWordsPerRow + wc];
-                        sc[js][i] = scales[k * 4 + soff];
-                    }
+                for (int i = 0; i < kDeqRows; ++i) {
+                    const int k = kRowsPerWarp * (d + kDeqWarps * i) + rsub;   // row of the stage
+                    w[i] = codes[k * kWordsPerRow + wc];
+                    sc[i] = scales[k * 4 + soff];
                 }
-#pragma unroll
-                for (int js = 0; js < kMySubs; ++js) {
-                    const int sub = sub0 + js;
-                    const uint32_t ib = it * kBSplit + sub;   // B sub-stage sequence number
-                    const int sb = ib % NB;
-                    // The sub-stage may be overwritten once the MMA has read it.
-                    if (!warp_wait(&sh.empty_b[sb], ((ib / NB) & 1u) ^ 1u, sh.abort,
-                                   &g_device_status)) {
-                        ok = false;
-                        break;
-                    }
-                    uint8_t *btile = sh.b + sb * kBStage + chunk * kChunkB;
-#pragma unroll
-                    for (int i = 0; i < kDeqRows; ++i) {
-                        const int k = kRowsPerWarp * (dd + kSubWarps * i) + rsub;   // row of the sub-stage
-                        const uint4 y = dequant_word(w[js][i], sc[js][i]);
-                        uint8_t *dst = btile + k * 128 + ((piece ^ (k & 7)) << 4);
-                        *reinterpret_cast<uint4 *>(dst) = y;
-                    }
-                    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-                    __syncwarp();
-                    if (lane == 0) {
-                        if (kDirectB && rank != 0)
-                            mbar_arrive_remote(full_b0 + (uint32_t)sb * 8u);
-                        else
-                            mbar_arrive(&sh.full_b[sb]);
-                    }
+                const int sb = it % NB;
+                // The B stage may be overwritten once the MMA has read it.
+                if (!warp_wait(&sh.empty_b[sb], ((it / NB) & 1u) ^ 1u, sh.abort, &g_device_status)) {
+                    ok = false;
+                    break;
                 }
-                if (!ok) break;
+                uint8_t *btile = sh.b + sb * kBStage + chunk * kChunk;
+#pragma unroll
+                for (int i = 0; i < kDeqRows; ++i) {
+                    const int k = kRowsPerWarp * (d + kDeqWarps * i) + rsub;
+                    const uint4 y = dequant_word(w[i], sc[i]);
+                    uint8_t *dst = btile + k * 128 + ((piece ^ (k & 7)) << 4);
+                    *reinterpret_cast<uint4 *>(dst) = y;
+                }
+                asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+                __syncwarp();
+                if (lane == 0) {
+                    if (rank != 0)
+                        mbar_arrive_remote(full_b0 + (uint32_t)sb * 8u);
+                    else
+                        mbar_arrive(&sh.full_b[sb]);
+                }
                 // The X stage is released only now: its codes have been consumed
                 // (the B stores depend on them), so no shared-memory load of it
                 // can still be in flight when the next TMA load overwrites it.
                 if (lane == 0) mbar_arrive(&sh.empty_x[sx]);
-                if (kb == lead && prev >= 0 && !epilogue(prev, t - 1)) { ok = false; break; }
+                if (kb == 0 && prev >= 0 && !epilogue(prev, t - 1)) { ok = false; break; }
             }
             prev = g;
         }
@@ -788,17 +694,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     // Neither CTA of a pair leaves (or frees TMEM) while the other may still
     // arrive on its barriers or have the pair's MMAs read its shared memory.
-    if constexpr (kPair > 1) cluster_sync_all();
+    cluster_sync_all();
     if (warp == kMmaWarp) {
         __syncwarp();
-        if constexpr (kPair > 1)
-            asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                         "r"(kTmemCols)
-                         : "memory");
-        else
-            asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
-                         "r"(kTmemCols)
-                         : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(tmem_base),
+                     "r"(kTmemCols)
+                     : "memory");
     }
 }
 
@@ -820,18 +721,21 @@ __global__ void wait_timeout_probe_kernel(long long limit_cycles) {
 }
 
 // ---------------------------------------------------------------- host side
-template <int EPI>
+template <int EPI, bool TMA_SCALES>
 cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, int N, int K,
                         void *dW, float *mscales, cudaStream_t st) {
     CUtensorMap m_dy, m_xc, m_xs;
     if (!encode_2d(&m_dy, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, dY, (uint64_t)M, (uint64_t)K,
                    (uint64_t)M * 2, 64, BK, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !encode_2d(&m_xc, CU_TENSOR_MAP_DATA_TYPE_UINT8, xc, (uint64_t)N / 2, (uint64_t)K,
-                   (uint64_t)N / 2, kBCols / 2, BK, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-        !encode_2d(&m_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xs, (uint64_t)N / 128, (uint64_t)K,
-                   (uint64_t)(N / 128) * 4, 4, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
+                   (uint64_t)N / 2, kBCols / 2, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
         return cudaErrorInvalidValue;
-    auto kernel = wgrad_gemm_int4_kernel<EPI>;
+    if (!TMA_SCALES)
+        m_xs = m_xc;   // unused by this instance
+    else if (!encode_2d(&m_xs, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, xs, (uint64_t)N / 128, (uint64_t)K,
+                        (uint64_t)(N / 128) * 4, 4, BK, CU_TENSOR_MAP_SWIZZLE_NONE))
+        return cudaErrorInvalidValue;
+    auto kernel = wgrad_gemm_int4_kernel<EPI, TMA_SCALES>;
     static bool attr_set[kMaxDevices];
     int dev = 0;
     cudaGetDevice(&dev);
@@ -841,12 +745,7 @@ cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, 
         if (e != cudaSuccess) return e;
         attr_set[dev] = true;
     }
-    const int groups = ((M + kTileRows - 1) / kTileRows) * (N / BN);
-    if constexpr (kPair == 1) {
-        const int grid = groups < sm_count() ? groups : sm_count();
-        kernel<<<grid, kThreads, kSmemBytes, st>>>(m_dy, m_xc, m_xs, dW, mscales, M, N, K);
-        return cudaGetLastError();
-    }
+    const int groups = ((M + kTileRows - 1) / kTileRows) * ((N + BN - 1) / BN);
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(kThreads);
     cfg.dynamicSmemBytes = kSmemBytes;
@@ -870,20 +769,29 @@ cudaError_t launch_impl(const void *dY, const void *xc, const float *xs, int M, 
     }
     const int clusters = (dev >= 0 && dev < kMaxDevices) ? resident[dev] : sm_count() / kPair;
     cfg.gridDim = dim3((groups < clusters ? groups : clusters) * kPair);
-    return cudaLaunchKernelEx(&cfg, kernel, m_dy, m_xc, m_xs, dW, mscales, M, N, K);
+    return cudaLaunchKernelEx(&cfg, kernel, m_dy, m_xc, m_xs, xs, dW, mscales, M, N, K);
+}
+
+// Scales by TMA when a scale row is a multiple of 16 bytes and 16-byte aligned.
+template <int EPI>
+cudaError_t launch_any(const void *dY, const void *xc, const float *xs, int M, int N, int K,
+                       void *dW, float *mscales, cudaStream_t st) {
+    const bool tma = (N / 128) % 4 == 0 && (reinterpret_cast<uintptr_t>(xs) & 15u) == 0;
+    return tma ? launch_impl<EPI, true>(dY, xc, xs, M, N, K, dW, mscales, st)
+               : launch_impl<EPI, false>(dY, xc, xs, M, N, K, dW, mscales, st);
 }
 
 }  // namespace
 
 cudaError_t launch_gemm(const void *dY, const void *xc, const float *xs, int M, int N, int K,
                         void *dW, bool f32_out, cudaStream_t st) {
-    return f32_out ? launch_impl<kEpiF32>(dY, xc, xs, M, N, K, dW, nullptr, st)
-                   : launch_impl<kEpiBf16>(dY, xc, xs, M, N, K, dW, nullptr, st);
+    return f32_out ? launch_any<kEpiF32>(dY, xc, xs, M, N, K, dW, nullptr, st)
+                   : launch_any<kEpiBf16>(dY, xc, xs, M, N, K, dW, nullptr, st);
 }
 
 cudaError_t launch_accum_fp8(const void *dY, const void *xc, const float *xs, int M, int N, int K,
                              void *master, float *master_scales, cudaStream_t st) {
-    return launch_impl<kEpiAccumFp8>(dY, xc, xs, M, N, K, master, master_scales, st);
+    return launch_any<kEpiAccumFp8>(dY, xc, xs, M, N, K, master, master_scales, st);
 }
 
 cudaError_t launch_wait_timeout_probe(long long limit_cycles, cudaStream_t st) {

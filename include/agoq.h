@@ -154,6 +154,13 @@ agoq_status agoq_rmsnorm_backward(const void *codes, const float *scales, const 
  *   master_scales : in/out, n/128 FP32 scales.
  *   grad_bf16     : in, n BF16 micro-batch gradient values (must not overlap the master).
  * The page dequantizes to FP16/BF16; this library keeps the sum in FP32.
+ * When master_scales is 16-byte aligned and n/128 is a multiple of 4, the
+ * blocks stream through shared memory with time-limited pipeline waits (see
+ * agoq_device_status; the results are the same either way).  If such a wait
+ * runs out, the update stops part-way: some blocks of the master then hold the
+ * new sum and others the old one, and the old values of the updated blocks are
+ * gone.  A caller that must be able to recover from AGOQ_ERR_TIMEOUT keeps a
+ * copy of the master (codes and scales) from before the call.
  */
 agoq_status agoq_grad_accum_fp8(void *master_e4m3, float *master_scales, const void *grad_bf16,
                                 int64_t n, void *stream);
@@ -209,9 +216,12 @@ agoq_status agoq_reduce_fp8_shards(const void *shards_e4m3, const float *shard_s
  *   x_codes  : in, [K][N/2] bytes: row k is agoq_quant_act(bits=4) of X row k.
  *   x_scales : in, FP32 [K][N/128].
  *   dW_bf16  : out, BF16 [M][N] row-major.
- *   M must be a multiple of 256, N of 512 (so that a row of scales spans a
- *   multiple of 16 bytes) and K of 64, all > 0 (AGOQ_ERR_SHAPE otherwise).
- *   The dY tile loads need dY 16-byte aligned; all pointers must be.
+ *   M and N must be multiples of 128 and K of 64, all > 0 (AGOQ_ERR_SHAPE
+ *   otherwise).  dY, x_codes and dW must be 16-byte aligned, x_scales 4-byte
+ *   aligned (AGOQ_ERR_ALIGN).  When N is a multiple of 512 and x_scales is
+ *   16-byte aligned the scales are staged by TMA with the codes; otherwise the
+ *   kernel reads them directly.  Pipeline waits are time-limited: see
+ *   agoq_device_status.
  */
 agoq_status agoq_wgrad_gemm_int4(const void *dY_bf16, const void *x_codes, const float *x_scales,
                                  int M, int N, int K, void *dW_bf16, void *stream);
@@ -283,9 +293,11 @@ agoq_status agoq_dbca_pp_bits(int stages, int microbatches, int base_bits, int *
  * Synchronise `stream`, then read and clear the library's device-side status
  * words for the current device.  Returns AGOQ_ERR_TIMEOUT if a pipeline wait
  * of a GEMM (agoq_wgrad_gemm_int4*, agoq_fwd_gemm_quant), of the staged
- * shard reduce (agoq_reduce_fp8_shards) or of the staged RMSNorm dw
+ * shard reduce (agoq_reduce_fp8_shards), of the staged QuanGrad accumulation
+ * (agoq_grad_accum_fp8, agoq_grad_accum_fp8_mid) or of the staged RMSNorm dw
  * (agoq_rmsnorm_backward) exceeded its time limit since the last call (that
- * call's output is then incomplete),
+ * call's output is then incomplete; for the in-place accumulations the master
+ * is left partly updated),
  * AGOQ_ERR_CUDA if the synchronisation failed, else AGOQ_OK.
  */
 agoq_status agoq_device_status(void *stream);

@@ -139,12 +139,15 @@ def test_reduce_validation(L):
 
 def test_gemm_validation(L):
     for fn in (L.agoq_wgrad_gemm_int4, L.agoq_wgrad_gemm_int4_f32out):
+        # M and N multiples of 128, K of 64
         assert fn(P(A), P(B), P(C), 100, 512, 64, P(C + (1 << 24)), None) == SHAPE
-        assert fn(P(A), P(B), P(C), 256, 256, 64, P(C + (1 << 24)), None) == SHAPE
+        assert fn(P(A), P(B), P(C), 256, 192, 64, P(C + (1 << 24)), None) == SHAPE
         assert fn(P(A), P(B), P(C), 256, 512, 32, P(C + (1 << 24)), None) == SHAPE
         assert fn(P(A), P(B), P(C), 0, 512, 64, P(C + (1 << 24)), None) == SHAPE
         assert fn(None, P(B), P(C), 256, 512, 64, P(C + (1 << 24)), None) == NULL
-        assert fn(P(A), P(B), P(C + 4), 256, 512, 64, P(C + (1 << 24)), None) == ALIGN
+        # scales need 4-byte alignment, the other pointers 16
+        assert fn(P(A), P(B), P(C + 2), 256, 512, 64, P(C + (1 << 24)), None) == ALIGN
+        assert fn(P(A + 8), P(B), P(C), 256, 512, 64, P(C + (1 << 24)), None) == ALIGN
         assert fn(P(A), P(B), P(C), 256, 512, 64, P(A), None) == ALIAS
 
 
@@ -153,6 +156,7 @@ def test_gemm_accum_validation(L):
     D = C + (1 << 24)
     E = C + (1 << 26)
     assert fn(P(A), P(B), P(C), 100, 512, 64, P(D), P(E), None) == SHAPE
+    assert fn(P(A), P(B), P(C), 384, 320, 64, P(D), P(E), None) == SHAPE
     assert fn(P(A), P(B), P(C), 256, 512, 0, P(D), P(E), None) == SHAPE
     assert fn(P(A), P(B), P(C), 256, 512, 64, None, P(E), None) == NULL
     assert fn(P(A), P(B), P(C), 256, 512, 64, P(D), None, None) == NULL

@@ -41,10 +41,15 @@ def _abs_terms(oracle, dy, xc, xs, M, N, K):
 
 
 # K a multiple of 128 runs the 128-deep instance, the other multiples of 64 the
-# 64-deep one; M = 256 and 768 leave the second half of a 512-row pair tile empty.
+# 64-deep one; M = 256 and 768 leave the second half of a 512-row pair tile empty,
+# M = 128 and 384 also the second CTA's rows of a half; N = 128, 384, 640 end on a
+# half-filled 256-column tile and (with N = 768) take the kernel that reads the
+# scales without TMA (a scale row that is not a multiple of 16 bytes).
 @pytest.mark.parametrize("M,N,K", [(256, 512, 64), (256, 512, 128), (512, 1024, 192),
                                    (768, 512, 320), (2560, 4096, 64), (512, 1024, 384),
-                                   (768, 512, 640), (2560, 4096, 128)])
+                                   (768, 512, 640), (2560, 4096, 128),
+                                   (128, 128, 64), (384, 640, 192), (128, 384, 128),
+                                   (640, 768, 320), (1152, 1408, 256)])
 def test_gemm_matches_fp64_product(oracle, M, N, K):
     dy, xc, xs = _inputs(oracle, M, N, K)
     dyd, xcd, xsd = G.dev_bf16(dy), G.dev(xc), G.dev(xs)
@@ -82,5 +87,21 @@ def test_repeatable_across_calls(oracle):
     args = (G.dev_bf16(dy), G.dev(xc), G.dev(xs), M, N, K)
     a = agoq.agoq_wgrad_gemm_int4(*args)
     b = agoq.agoq_wgrad_gemm_int4(*args)
+    agoq.agoq_device_status()
+    assert torch.equal(a, b)
+
+
+def test_unaligned_scales_take_the_direct_path(oracle):
+    """Scales 4 bytes off a 16-byte boundary (N a multiple of 512, which would
+    otherwise load them by TMA): same results as the aligned call."""
+    M, N, K = 512, 1024, 128
+    dy, xc, xs = _inputs(oracle, M, N, K, seed=13)
+    room = torch.zeros(xs.size + 4, dtype=torch.float32, device="cuda")
+    xs_off = room[1:1 + xs.size]
+    xs_off.copy_(G.dev(xs))
+    assert xs_off.data_ptr() % 16 == 4
+    args = (G.dev_bf16(dy), G.dev(xc))
+    a = agoq.agoq_wgrad_gemm_int4_f32out(*args, G.dev(xs), M, N, K)
+    b = agoq.agoq_wgrad_gemm_int4_f32out(*args, xs_off, M, N, K)
     agoq.agoq_device_status()
     assert torch.equal(a, b)

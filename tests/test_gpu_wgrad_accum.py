@@ -60,7 +60,8 @@ def _assert_same(got, want):
 
 
 @pytest.mark.parametrize("M,N,K", [(256, 512, 64), (256, 512, 320), (512, 1024, 128),
-                                   (768, 1536, 192), (768, 1536, 384)])
+                                   (768, 1536, 192), (768, 1536, 384),
+                                   (128, 128, 64), (384, 640, 192), (640, 384, 128)])
 def test_exact_sums_match_oracle_bitwise(oracle, M, N, K):
     dy, xc, xs = _exact_inputs(oracle, M, N, K, seed=50 + K)
     master, scales = _master(oracle, M * N, seed=60 + M, sd=2.0)
