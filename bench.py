@@ -743,7 +743,14 @@ def rows_arm(device, hbm_peak, bf16_peak):
         _time_launch(lambda: agoq.agoq_rmsnorm_backward(c, s, dy, wt, T, H, 4, 1e-6, dx, rstd,
                                                         dwt), flush),
         {"note": "algorithmic bytes read the input once; dw reads codes and dy a second time"})
-    del c, s, dy, dx
+    ws = torch.empty(agoq.agoq_rmsnorm_backward_workspace_bytes(H), dtype=torch.uint8,
+                     device=device)
+    row("rmsnorm_backward_dx_dw_single_read_b4_8192x4096", base + 4 * H, n,
+        _time_launch(lambda: agoq.agoq_rmsnorm_backward_ws(c, s, dy, wt, T, H, 4, 1e-6, ws, dx,
+                                                           rstd, dwt), flush),
+        {"note": "one read of the input; dw from per-CTA partial sums in a workspace",
+         "workspace_bytes": ws.numel()})
+    del c, s, dy, dx, ws
 
     # QuanGrad accumulation, 2^30 elements: the 8 micro-batches of the workload
     # into a zeroed master, each step timed after an L2 flush; the chain is run
@@ -992,7 +999,7 @@ def reduce_shards_torch(W, n, device):
 
 
 PROFILE_CASES = ("accum", "reduce8", "reduce8_nocount", "reduce64", "gemm", "gemm_accum", "silu",
-                 "rmsnorm", "fwd_gemm")
+                 "rmsnorm", "rmsnorm_ws", "fwd_gemm")
 
 
 def profile_case(name, launches=3):
@@ -1041,14 +1048,19 @@ def profile_case(name, launches=3):
         dy = torch.randn(n, device=dev).to(torch.bfloat16)
         for _ in range(launches):
             agoq.agoq_silu_backward(c, s, dy, n, 4)
-    elif name == "rmsnorm":
+    elif name in ("rmsnorm", "rmsnorm_ws"):
         x = synthetic.dbca_activations_torch(seed=1, device=dev)[0]
         T, H = x.shape
         c, s = agoq.agoq_quant_act(x, 4)
         dy = torch.randn(T * H, device=dev).to(torch.bfloat16)
         w = torch.ones(H, device=dev).to(torch.bfloat16)
+        ws = torch.empty(agoq.agoq_rmsnorm_backward_workspace_bytes(H), dtype=torch.uint8,
+                         device=dev)
         for _ in range(launches):
-            agoq.agoq_rmsnorm_backward(c, s, dy, w, T, H, 4, 1e-6)
+            if name == "rmsnorm":
+                agoq.agoq_rmsnorm_backward(c, s, dy, w, T, H, 4, 1e-6)
+            else:
+                agoq.agoq_rmsnorm_backward_ws(c, s, dy, w, T, H, 4, 1e-6, ws)
     else:
         raise SystemExit("unknown profile case %r (choose from %s)" % (name, ", ".join(PROFILE_CASES)))
     torch.cuda.synchronize()

@@ -53,6 +53,10 @@ def _lib_handle():
         L.agoq_silu_backward.argtypes = [vp, vp, vp, i64, i32, vp, vp, vp]
         L.agoq_rmsnorm_backward.argtypes = [vp, vp, vp, vp, i64, i64, i32, ctypes.c_float, vp,
                                             vp, vp, vp]
+        L.agoq_rmsnorm_backward_ws.argtypes = [vp, vp, vp, vp, i64, i64, i32, ctypes.c_float, vp,
+                                               vp, vp, vp, i64, vp]
+        L.agoq_rmsnorm_backward_workspace_bytes.argtypes = [i64]
+        L.agoq_rmsnorm_backward_workspace_bytes.restype = i64
         L.agoq_grad_accum_fp8_mid.argtypes = [vp, vp, vp, i64, i32, vp]
         L.agoq_reduce_fp8_shards.argtypes = [vp, vp, i32, i64, vp, vp, vp, vp]
         L.agoq_wgrad_gemm_int4.argtypes = [vp, vp, vp, i32, i32, i32, vp, vp]
@@ -66,7 +70,8 @@ def _lib_handle():
                      "agoq_reduce_fp8_shards", "agoq_wgrad_gemm_int4",
                      "agoq_wgrad_gemm_int4_f32out", "agoq_device_status",
                      "agoq_wgrad_gemm_int4_accum_fp8", "agoq_grad_accum_fp8_mid",
-                     "agoq_silu_backward", "agoq_rmsnorm_backward", "agoq_dbca_pp_bits",
+                     "agoq_silu_backward", "agoq_rmsnorm_backward", "agoq_rmsnorm_backward_ws",
+                     "agoq_dbca_pp_bits",
                      "agoq_fwd_gemm_quant", "agoq_test_wait_timeout"):
             getattr(L, name).restype = i32
         _L = L
@@ -202,6 +207,35 @@ def agoq_rmsnorm_backward(codes, scales, dy, w, T, H, bits, eps, dx=None, rstd=N
     _check(lib().agoq_rmsnorm_backward(_ptr(codes), _ptr(scales), _ptr(dy), _ptr(w), T, H, bits,
                                        float(eps), _ptr(dx), _ptr(rstd), _ptr(dw),
                                        _stream(stream)), "agoq_rmsnorm_backward")
+    return dx, rstd, dw
+
+
+def agoq_rmsnorm_backward_workspace_bytes(H):
+    """Bytes of scratch agoq_rmsnorm_backward_ws needs for rows of H elements."""
+    return int(lib().agoq_rmsnorm_backward_workspace_bytes(int(H)))
+
+
+def agoq_rmsnorm_backward_ws(codes, scales, dy, w, T, H, bits, eps, workspace, dx=None, rstd=None,
+                             dw=None, stream=None):
+    """The RMSNorm backward in one read of the input (H <= 4096), dw included; `workspace`
+    is a CUDA tensor of at least agoq_rmsnorm_backward_workspace_bytes(H) bytes.
+    Returns (dx, rstd, dw)."""
+    _need(codes, torch.uint8, "codes")
+    _need(scales, torch.float32, "scales")
+    _need(dy, torch.bfloat16, "dy")
+    _need(w, torch.bfloat16, "w")
+    dev = dy.device
+    if dx is None:
+        dx = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if rstd is None:
+        rstd = torch.empty(T, dtype=torch.float32, device=dev)
+    if dw is None:
+        dw = torch.empty(H, dtype=torch.float32, device=dev)
+    nbytes = workspace.numel() * workspace.element_size()
+    _check(lib().agoq_rmsnorm_backward_ws(_ptr(codes), _ptr(scales), _ptr(dy), _ptr(w), T, H, bits,
+                                          float(eps), _ptr(dx), _ptr(rstd), _ptr(dw),
+                                          _ptr(workspace), nbytes, _stream(stream)),
+           "agoq_rmsnorm_backward_ws")
     return dx, rstd, dw
 
 

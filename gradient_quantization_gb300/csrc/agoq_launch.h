@@ -58,6 +58,15 @@ cudaError_t launch_silu_backward(const void *codes, const float *scales, const v
 cudaError_t launch_rmsnorm_backward(const void *codes, const float *scales, const void *dy,
                                     const void *w, int64_t T, int64_t H, int bits, float eps,
                                     void *dx, float *rstd, float *dw, cudaStream_t st);
+// The same in one read of the input (H <= rmsnorm_fused_max_h()): dx, rstd and
+// per-CTA dw partial sums in `partials` (rmsnorm_fused_partials() x H floats),
+// then dw from them in a fixed order.
+cudaError_t launch_rmsnorm_backward_fused(const void *codes, const float *scales, const void *dy,
+                                          const void *w, int64_t T, int64_t H, int bits, float eps,
+                                          void *dx, float *rstd, float *dw, float *partials,
+                                          cudaStream_t st);
+int rmsnorm_fused_partials();
+int rmsnorm_fused_max_h();
 // mid: intermediate format of the sum (0 binary32, 1 BF16, 2 FP16).
 cudaError_t launch_grad_accum(void *master, float *master_scales, const void *grad, int64_t n,
                               int mid, cudaStream_t st);

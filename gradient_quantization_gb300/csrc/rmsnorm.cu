@@ -40,27 +40,15 @@ constexpr int kRowBlocks = 2;                    // 128-element blocks per octet
 constexpr int kDwThreads = 256;                  // 8 warps
 constexpr int kDwCluster = 8;                    // CTAs per cluster (ranks along y)
 constexpr int kDwCols = 128;                     // columns per slice (16 lanes x 8)
-#ifndef AGOQ_DW_UNROLL
-#define AGOQ_DW_UNROLL 4
-#endif
-constexpr int kDwUnroll = AGOQ_DW_UNROLL;        // rows in flight per half warp
+constexpr int kDwUnroll = 4;                     // rows in flight per half warp
 // dw through TMA-staged row tiles (when T, H and the alignments allow it):
-// kDwTileRows rows of a 128-column slice per stage, kDwStagesTma stages.
-#ifndef AGOQ_DW_TMA
-#define AGOQ_DW_TMA 1
-#endif
-#ifndef AGOQ_DW_TMA_STAGES
-#define AGOQ_DW_TMA_STAGES 8
-#endif
-#ifndef AGOQ_DW_TMA_CLUSTER
-#define AGOQ_DW_TMA_CLUSTER 8
-#endif
+// kDwTileRows rows of a 128-column slice per stage, kDwStagesTma stages,
+// kDwTmaCluster CTAs per slice (4, 6, 9 and 12 stages and clusters of 4, 12 or
+// 16 CTAs measured slower than 8 and 8).
 constexpr int kDwTileRows = 32;
-constexpr int kDwTmaCluster = AGOQ_DW_TMA_CLUSTER;   // CTAs per slice (cluster along y)
-constexpr int kDwStagesTma = AGOQ_DW_TMA_STAGES;
-#ifndef AGOQ_DW_TMA_MIN_CTAS
-#define AGOQ_DW_TMA_MIN_CTAS 2
-#endif
+constexpr int kDwTmaCluster = 8;                 // CTAs per slice (cluster along y)
+constexpr int kDwStagesTma = 8;
+constexpr int kDwTmaMinCtas = 2;
 constexpr int kDwTmaThreads = kDwThreads + 32;   // 8 consumer warps + 1 producer warp
 
 __device__ __forceinline__ uint4 ld_stream(const uint4 *p) {
@@ -216,13 +204,10 @@ __device__ __forceinline__ void chunk_from_smem(const uint32_t *rowcodes, int c,
 
 constexpr int kWarpRowThreads = 128;             // 4 warps per CTA, one row per warp at a time
 
-// 1: the row kernel forms the BF16 x BF16 products (xh^2, xh w, dy w) with the
+// The row kernels form the BF16 x BF16 products (xh^2, xh w, dy w) with the
 // mixed-precision fma.rn.f32.bf16 on the BF16 halves directly instead of
 // widening both operands first.  Each such product is exact in binary32, so
-// the sums and dx are the same bits either way.
-#ifndef AGOQ_RMS_MIXED
-#define AGOQ_RMS_MIXED 1
-#endif
+// the sums and dx are the same bits either way (measured faster).
 
 // d_k = fl(a_k * b_k + c_k) for the BF16 halves k = 0 (bits 0-15), 1 of a and b.
 __device__ __forceinline__ void fma_bf16x2_f32(uint32_t a, uint32_t b, float c0, float c1,
@@ -236,7 +221,6 @@ __device__ __forceinline__ void fma_bf16x2_f32(uint32_t a, uint32_t b, float c0,
 // dw terms of one chunk: acc[k] += fl(fl(dy_k * xh_k) * r) for the 8 BF16
 // values of d (dy) and xh (the BF16 x BF16 product is exact in binary32).
 __device__ __forceinline__ void dw_accum8(float acc[8], const uint4 &d, const uint4 &xh, float r) {
-#if AGOQ_RMS_MIXED
     const uint32_t dw4[4] = {d.x, d.y, d.z, d.w}, xw[4] = {xh.x, xh.y, xh.z, xh.w};
 #pragma unroll
     for (int p = 0; p < 4; ++p) {
@@ -245,10 +229,6 @@ __device__ __forceinline__ void dw_accum8(float acc[8], const uint4 &d, const ui
         acc[2 * p] = __fadd_rn(acc[2 * p], __fmul_rn(q0, r));
         acc[2 * p + 1] = __fadd_rn(acc[2 * p + 1], __fmul_rn(q1, r));
     }
-#else
-#pragma unroll
-    for (int k = 0; k < 8; ++k) acc[k] = __fadd_rn(acc[k], __fmul_rn(__fmul_rn(elem(d, k), elem(xh, k)), r));
-#endif
 }
 
 // Shared-memory words of one warp's row stage: dy (H/8 x 16 B), the row's
@@ -318,9 +298,7 @@ __global__ void __launch_bounds__(kWarpRowThreads) rmsnorm_backward_warp_rows_ke
         // Row sums in packed pairs with fused multiply-adds (a tolerance-
         // bounded result: fusing only removes roundings).
         uint64_t sxx2 = 0ull, sgx2 = 0ull;
-#if AGOQ_RMS_MIXED
         float sxx0 = 0.0f, sxx1 = 0.0f;
-#endif
 #pragma unroll 4
         for (int k = 0; k < C; ++k) {
             const uint4 xh = xh_of(k);
@@ -330,24 +308,14 @@ __global__ void __launch_bounds__(kWarpRowThreads) rmsnorm_backward_warp_rows_ke
                            ww[4] = {wv.x, wv.y, wv.z, wv.w};
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
-#if AGOQ_RMS_MIXED
                 // sxx += xh^2;  sgx += dy * (xh w): the same exact products as (dy w) xh
                 float v0, v1;
                 fma_bf16x2_f32(xw[p], xw[p], sxx0, sxx1, sxx0, sxx1);
                 fma_bf16x2_f32(xw[p], ww[p], -0.0f, -0.0f, v0, v1);
                 sgx2 = fma_f32x2(u32x2(dw4[p] << 16, dw4[p] & 0xFFFF0000u), f32x2(v0, v1), sgx2);
-#else
-                const uint64_t x2 = u32x2(xw[p] << 16, xw[p] & 0xFFFF0000u);
-                const uint64_t g2 = mul_f32x2(u32x2(dw4[p] << 16, dw4[p] & 0xFFFF0000u),
-                                              u32x2(ww[p] << 16, ww[p] & 0xFFFF0000u));
-                sxx2 = fma_f32x2(x2, x2, sxx2);
-                sgx2 = fma_f32x2(g2, x2, sgx2);
-#endif
             }
         }
-#if AGOQ_RMS_MIXED
         sxx2 = f32x2(sxx0, sxx1);
-#endif
         float sxx = __fadd_rn(lo_f32(sxx2), hi_f32(sxx2));
         float sgx = __fadd_rn(lo_f32(sgx2), hi_f32(sgx2));
 #pragma unroll
@@ -370,14 +338,9 @@ __global__ void __launch_bounds__(kWarpRowThreads) rmsnorm_backward_warp_rows_ke
 #pragma unroll
             for (int p = 0; p < 4; ++p) {
                 const uint64_t x2 = u32x2(xw[p] << 16, xw[p] & 0xFFFF0000u);
-#if AGOQ_RMS_MIXED
                 float g0, g1;
                 fma_bf16x2_f32(dw4[p], ww[p], -0.0f, -0.0f, g0, g1);
                 const uint64_t g2 = f32x2(g0, g1);
-#else
-                const uint64_t g2 = mul_f32x2(u32x2(dw4[p] << 16, dw4[p] & 0xFFFF0000u),
-                                              u32x2(ww[p] << 16, ww[p] & 0xFFFF0000u));
-#endif
                 // dx = r * g - xh * kk
                 const uint64_t d2 = fma_f32x2(r2, g2, mul_f32x2(x2, nkk2));
                 o[p] = pack_bf16x2(lo_f32(d2), hi_f32(d2));
@@ -500,7 +463,7 @@ struct DwTmaStage {
 // expiry g_rms_status records a timeout, the CTA stops (still joining the
 // cluster barriers) and the producer waits for its copies in flight.
 template <int BITS>
-__global__ void __launch_bounds__(kDwTmaThreads, AGOQ_DW_TMA_MIN_CTAS) rmsnorm_dw_tma_kernel(
+__global__ void __launch_bounds__(kDwTmaThreads, kDwTmaMinCtas) rmsnorm_dw_tma_kernel(
     const __grid_constant__ CUtensorMap map_dy, const __grid_constant__ CUtensorMap map_codes,
     const __grid_constant__ CUtensorMap map_scales, const float *__restrict__ rstd, int64_t T,
     float *__restrict__ dw) {
@@ -698,7 +661,7 @@ cudaError_t rmsnorm_bits(const void *codes, const float *scales, const void *dy,
                        static_cast<uint4 *>(dx), rstd);
     }
     if (e != cudaSuccess || !dw) return e;
-    if (AGOQ_DW_TMA && T % kDwTileRows == 0 && T / kDwTileRows <= INT32_MAX / kDwTileRows &&
+    if (T % kDwTileRows == 0 && T / kDwTileRows <= INT32_MAX / kDwTileRows &&
         H % 512 == 0 && reinterpret_cast<uintptr_t>(scales) % 16 == 0 &&
         reinterpret_cast<uintptr_t>(rstd) % 16 == 0)
         return launch_dw_tma<BITS>(codes, scales, dy, rstd, T, H, dw, st);
@@ -718,6 +681,279 @@ cudaError_t rmsnorm_bits(const void *codes, const float *scales, const void *dy,
     return cudaLaunchKernelEx(&cfg, rmsnorm_dw_kernel<BITS>, static_cast<const uint32_t *>(codes),
                               scales, static_cast<const uint4 *>(dy),
                               static_cast<const float *>(rstd), T, H, dw);
+}
+
+// ---- single-pass backward: dx, rstd and the dw partial sums in one read ----
+// A row group of 128 threads (4 warps) takes one row at a time; thread i of the
+// group holds chunks i, i + 128, ... (CPT of them, 8 columns each) of the row,
+// so its dequantized input, dy and w stay in registers from the row sums to dx
+// and the dw terms (the input is dequantized once).  A CTA is two row groups:
+// CTA p of G takes rows 2p + g, 2p + g + 2G, ... in group g, the next row's
+// loads in flight while the current one is computed.  The two row sums are
+// reduced with shuffles, then over the group's 4 warps in shared memory in
+// warp order (one CTA barrier per row; the buffers alternate by row).  Each
+// thread adds its columns' dw terms fma(dy * xh, r, sum) (the BF16 x BF16
+// product is exact; one rounding per term) in row order; at the
+// end group 1's sums are added to group 0's and written as the CTA's row of
+// `partials` [G][H].  rmsnorm_dw_partials_kernel then adds the G rows in a
+// fixed order: eight contiguous ranges of ceil(G/8) rows, each summed in row
+// order, then the eight range sums in order.  Every dw sum is therefore a chain
+// of at most ceil(T/2G) + 1 + ceil(G/8) + 8 additions, and the result does not
+// depend on the schedule.
+constexpr int kFusedThreads = 256, kFusedGroup = 128, kFusedMaxH = 4096;
+constexpr int kFusedPartials = 304;              // G at most: the workspace is G x H floats
+constexpr int kFusedL2Ahead = 3;                 // rows asked of the L2 ahead of the loads
+
+template <int BITS, int CPT>
+__global__ void __launch_bounds__(kFusedThreads, 2) rmsnorm_backward_fused_kernel(
+    const uint32_t *__restrict__ codes, const float *__restrict__ scales,
+    const uint4 *__restrict__ dy, const uint4 *__restrict__ w, int64_t T, int H, float eps,
+    uint4 *__restrict__ dx, float *__restrict__ rstd, float *__restrict__ partials) {
+    pdl_wait_and_release();
+    constexpr int kWords = 4 * BITS;
+    __shared__ float red[2][2][2][kFusedGroup / 32];   // [group][row parity][sum][warp]
+    __shared__ __align__(16) float comb[kFusedMaxH];   // group 1's dw sums at the end
+    const int g = threadIdx.x / kFusedGroup, i = threadIdx.x % kFusedGroup;
+    const int lane = threadIdx.x & 31, wg = i >> 5;
+    const int nch = H / 8, nb = H / kBlock;
+    const bool full = nch == kFusedGroup * CPT;        // every thread has CPT chunks
+    // 1/H when H is a power of two (then x * (1/H) is x / H exactly), else 0
+    const float inv_h = (H & (H - 1)) == 0 ? 1.0f / (float)H : 0.0f;
+    uint4 wv[CPT];
+    uint64_t acc[CPT][4];                               // dw sums, column pairs
+#pragma unroll
+    for (int k = 0; k < CPT; ++k) {
+        const int c = i + kFusedGroup * k;
+        wv[k] = full || c < nch ? __ldg(w + c) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) acc[k][p] = 0ull;
+    }
+    struct RowIn {
+        uint4 d[CPT];
+        uint32_t lo[CPT], hi[CPT];
+        float s[CPT];
+    };
+    // Row t's inputs (zeros for chunks past H or a row past T).
+    auto load = [&](int64_t t, RowIn &in) {
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            const int c = i + kFusedGroup * k;
+            if (t < T && (full || c < nch)) {
+                const int64_t blk = t * nb + c / 16;
+                load_chunk<BITS>(codes + blk * kWords, c % 16, in.lo[k], in.hi[k]);
+                in.s[k] = __ldg(scales + blk);
+                in.d[k] = ld_stream(dy + t * nch + c);
+            } else {
+                in.lo[k] = in.hi[k] = 0u;
+                in.s[k] = 0.0f;
+                in.d[k] = make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+    };
+    const int64_t stride = 2 * (int64_t)gridDim.x;
+    // One thread of each group asks the L2 for a row's dy and codes
+    // kFusedL2Ahead rows before its loads are issued (a hint: no effect on results).
+    auto l2_ahead = [&](int64_t t) {
+        if (i == 0 && t < T) {
+            prefetch_l2(dy + t * nch, (uint32_t)H * 2u);
+            prefetch_l2(codes + t * nb * kWords, (uint32_t)(H / 8) * BITS);
+        }
+    };
+    // Row t of this group from `in`; every thread of the CTA calls it for every
+    // row pair (its barrier), with t past T for a group without a row.
+    auto process = [&](const RowIn &in, int64_t t, int par) {
+        uint4 xh[CPT];
+        float sxx0 = 0.0f, sxx1 = 0.0f;
+        uint64_t sgx2 = 0ull;
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            xh[k] = dequantize_chunk<BITS>(in.lo[k], in.hi[k], in.s[k]);
+            const uint32_t xw[4] = {xh[k].x, xh[k].y, xh[k].z, xh[k].w};
+            const uint32_t dw4[4] = {in.d[k].x, in.d[k].y, in.d[k].z, in.d[k].w};
+            const uint32_t ww[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+#pragma unroll
+            for (int p = 0; p < 4; ++p) {
+                // sxx += xh^2;  sgx += dy * (xh w) (exact BF16 x BF16 products)
+                float v0, v1;
+                fma_bf16x2_f32(xw[p], xw[p], sxx0, sxx1, sxx0, sxx1);
+                fma_bf16x2_f32(xw[p], ww[p], -0.0f, -0.0f, v0, v1);
+                sgx2 = fma_f32x2(u32x2(dw4[p] << 16, dw4[p] & 0xFFFF0000u), f32x2(v0, v1), sgx2);
+            }
+        }
+        float sxx = __fadd_rn(sxx0, sxx1);
+        float sgx = __fadd_rn(lo_f32(sgx2), hi_f32(sgx2));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            sxx = __fadd_rn(sxx, __shfl_xor_sync(kFull, sxx, o));
+            sgx = __fadd_rn(sgx, __shfl_xor_sync(kFull, sgx, o));
+        }
+        if (lane == 0) {
+            red[g][par][0][wg] = sxx;
+            red[g][par][1][wg] = sgx;
+        }
+        __syncthreads();
+        sxx = red[g][par][0][0];
+        sgx = red[g][par][1][0];
+#pragma unroll
+        for (int q = 1; q < kFusedGroup / 32; ++q) {
+            sxx = __fadd_rn(sxx, red[g][par][0][q]);
+            sgx = __fadd_rn(sgx, red[g][par][1][q]);
+        }
+        const float mxx = inv_h != 0.0f ? __fmul_rn(sxx, inv_h) : __fdiv_rn(sxx, (float)H);
+        const float mgx = inv_h != 0.0f ? __fmul_rn(sgx, inv_h) : __fdiv_rn(sgx, (float)H);
+        const float r = __frcp_rn(__fsqrt_rn(__fadd_rn(mxx, eps)));
+        const float kk = __fmul_rn(__fmul_rn(__fmul_rn(r, r), r), mgx);
+        if (t < T) {
+            if (i == 0) rstd[t] = r;
+            const uint64_t r2 = f32x2(r, r), nkk2 = f32x2(-kk, -kk);
+#pragma unroll
+            for (int k = 0; k < CPT; ++k) {
+                const int c = i + kFusedGroup * k;
+                if (!full && c >= nch) continue;
+                const uint32_t xw[4] = {xh[k].x, xh[k].y, xh[k].z, xh[k].w};
+                const uint32_t dw4[4] = {in.d[k].x, in.d[k].y, in.d[k].z, in.d[k].w};
+                const uint32_t ww[4] = {wv[k].x, wv[k].y, wv[k].z, wv[k].w};
+                uint32_t o[4];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    // dx = r * g - xh * kk, g = dy * w
+                    float g0, g1, q0, q1;
+                    fma_bf16x2_f32(dw4[p], ww[p], -0.0f, -0.0f, g0, g1);
+                    const uint64_t x2 = u32x2(xw[p] << 16, xw[p] & 0xFFFF0000u);
+                    const uint64_t d2 = fma_f32x2(r2, f32x2(g0, g1), mul_f32x2(x2, nkk2));
+                    o[p] = pack_bf16x2(lo_f32(d2), hi_f32(d2));
+                    // dw += (dy xh) r, the exact product scaled and added in one rounding
+                    fma_bf16x2_f32(dw4[p], xw[p], -0.0f, -0.0f, q0, q1);
+                    acc[k][p] = fma_f32x2(f32x2(q0, q1), r2, acc[k][p]);
+                }
+                dx[t * nch + c] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    };
+    RowIn ra, rb;
+    const int64_t first = 2 * (int64_t)blockIdx.x + g;
+#pragma unroll
+    for (int a = 0; a <= kFusedL2Ahead; ++a) l2_ahead(first + a * stride);
+    load(first, ra);
+    // Rows alternate between the two input buffers (no copies); both groups
+    // run the same row pairs.
+    int par = 0;
+    for (int64_t b0 = 2 * (int64_t)blockIdx.x; b0 < T; b0 += 2 * stride) {
+        l2_ahead(b0 + g + (kFusedL2Ahead + 1) * stride);
+        load(b0 + g + stride, rb);
+        process(ra, b0 + g, par);
+        par ^= 1;
+        if (b0 + stride >= T) break;
+        l2_ahead(b0 + g + (kFusedL2Ahead + 2) * stride);
+        load(b0 + g + 2 * stride, ra);
+        process(rb, b0 + g + stride, par);
+        par ^= 1;
+    }
+    // group 0's sums + group 1's sums -> this CTA's partial row
+    __syncthreads();
+    if (g == 1) {
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            const int c = i + kFusedGroup * k;
+            if (full || c < nch) {
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    comb[8 * c + 2 * p] = lo_f32(acc[k][p]);
+                    comb[8 * c + 2 * p + 1] = hi_f32(acc[k][p]);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (g == 0) {
+        float4 *prow = reinterpret_cast<float4 *>(partials + (size_t)blockIdx.x * H);
+#pragma unroll
+        for (int k = 0; k < CPT; ++k) {
+            const int c = i + kFusedGroup * k;
+            if (full || c < nch) {
+                float v[8];
+#pragma unroll
+                for (int p = 0; p < 4; ++p) {
+                    v[2 * p] = __fadd_rn(lo_f32(acc[k][p]), comb[8 * c + 2 * p]);
+                    v[2 * p + 1] = __fadd_rn(hi_f32(acc[k][p]), comb[8 * c + 2 * p + 1]);
+                }
+                prow[2 * c] = make_float4(v[0], v[1], v[2], v[3]);
+                prow[2 * c + 1] = make_float4(v[4], v[5], v[6], v[7]);
+            }
+        }
+    }
+}
+
+// dw[col] from the G partial rows in a fixed order: a CTA takes 32 columns;
+// warp q sums rows q*R .. q*R + R - 1 (R = ceil(G/8)) in row order, then the
+// eight warp sums are added in warp order.
+constexpr int kPartialsWarps = 8;
+__global__ void __launch_bounds__(32 * kPartialsWarps) rmsnorm_dw_partials_kernel(
+    const float *__restrict__ partials, int G, int H, float *__restrict__ dw) {
+    pdl_wait_and_release();
+    __shared__ float wsum[kPartialsWarps][32];
+    const int lane = threadIdx.x & 31, q = threadIdx.x >> 5;
+    const int col = blockIdx.x * 32 + lane;       // H is a multiple of 256
+    const int R = (G + kPartialsWarps - 1) / kPartialsWarps;
+    const int p0 = q * R, p1 = p0 + R < G ? p0 + R : G;
+    float s = 0.0f;
+    int p = p0;
+    for (; p + 8 <= p1; p += 8) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) v[j] = __ldg(partials + (size_t)(p + j) * H + col);
+#pragma unroll
+        for (int j = 0; j < 8; ++j) s = __fadd_rn(s, v[j]);
+    }
+    for (; p < p1; ++p) s = __fadd_rn(s, __ldg(partials + (size_t)p * H + col));
+    wsum[q][lane] = s;
+    __syncthreads();
+    if (q == 0) {
+        float tot = wsum[0][lane];
+#pragma unroll
+        for (int k = 1; k < kPartialsWarps; ++k) tot = __fadd_rn(tot, wsum[k][lane]);
+        dw[col] = tot;
+    }
+}
+
+// G: as many CTAs as are resident at once (at most kFusedPartials), so that
+// every CTA runs in one wave; G depends on the GPU, so dw's order of additions
+// (and last bits) is fixed per GPU model.
+template <int BITS>
+cudaError_t rmsnorm_fused_bits(const void *codes, const float *scales, const void *dy,
+                               const void *w, int64_t T, int H, float eps, void *dx, float *rstd,
+                               float *dw, float *partials, cudaStream_t st) {
+    const int cpt = (H / 8 + kFusedGroup - 1) / kFusedGroup;   // chunks per thread
+    static int cache[4][kMaxDevices];
+    int per_sm = 1;
+    switch (cpt) {
+        case 1: per_sm = resident_per_sm(rmsnorm_backward_fused_kernel<BITS, 1>, kFusedThreads, 0, cache[0]); break;
+        case 2: per_sm = resident_per_sm(rmsnorm_backward_fused_kernel<BITS, 2>, kFusedThreads, 0, cache[1]); break;
+        case 3: per_sm = resident_per_sm(rmsnorm_backward_fused_kernel<BITS, 3>, kFusedThreads, 0, cache[2]); break;
+        default: per_sm = resident_per_sm(rmsnorm_backward_fused_kernel<BITS, 4>, kFusedThreads, 0, cache[3]); break;
+    }
+    int64_t G = (T + 1) / 2;
+    const int64_t resident = (int64_t)sm_count() * per_sm;
+    if (G > resident) G = resident;
+    if (G > kFusedPartials) G = kFusedPartials;
+    cudaError_t e = cudaSuccess;
+    if (G > 0) {
+        auto args = [&](auto kernel) {
+            return launch_pdl(kernel, (int)G, kFusedThreads, 0, st,
+                              static_cast<const uint32_t *>(codes), scales,
+                              static_cast<const uint4 *>(dy), static_cast<const uint4 *>(w), T, H,
+                              eps, static_cast<uint4 *>(dx), rstd, partials);
+        };
+        switch (cpt) {
+            case 1: e = args(rmsnorm_backward_fused_kernel<BITS, 1>); break;
+            case 2: e = args(rmsnorm_backward_fused_kernel<BITS, 2>); break;
+            case 3: e = args(rmsnorm_backward_fused_kernel<BITS, 3>); break;
+            default: e = args(rmsnorm_backward_fused_kernel<BITS, 4>); break;
+        }
+        if (e != cudaSuccess) return e;
+    }
+    return launch_pdl(rmsnorm_dw_partials_kernel, H / 32, 32 * kPartialsWarps, 0, st,
+                      static_cast<const float *>(partials), (int)G, H, dw);
 }
 
 }  // namespace
@@ -746,5 +982,23 @@ cudaError_t launch_rmsnorm_backward(const void *codes, const float *scales, cons
         default: return cudaErrorInvalidValue;
     }
 }
+
+// Single-pass form (H <= 4096): `partials` holds rmsnorm_fused_partials() x H
+// floats of scratch.
+cudaError_t launch_rmsnorm_backward_fused(const void *codes, const float *scales, const void *dy,
+                                          const void *w, int64_t T, int64_t H, int bits, float eps,
+                                          void *dx, float *rstd, float *dw, float *partials,
+                                          cudaStream_t st) {
+    switch (bits) {
+        case 4: return rmsnorm_fused_bits<4>(codes, scales, dy, w, T, (int)H, eps, dx, rstd, dw, partials, st);
+        case 5: return rmsnorm_fused_bits<5>(codes, scales, dy, w, T, (int)H, eps, dx, rstd, dw, partials, st);
+        case 6: return rmsnorm_fused_bits<6>(codes, scales, dy, w, T, (int)H, eps, dx, rstd, dw, partials, st);
+        case 8: return rmsnorm_fused_bits<8>(codes, scales, dy, w, T, (int)H, eps, dx, rstd, dw, partials, st);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+int rmsnorm_fused_partials() { return kFusedPartials; }
+int rmsnorm_fused_max_h() { return kFusedMaxH; }
 
 }  // namespace agoq

@@ -146,6 +146,40 @@ agoq_status agoq_rmsnorm_backward(const void *codes, const float *scales, const 
                                   void *dx_bf16, float *rstd, float *dw, void *stream);
 
 /*
+ * Bytes of scratch agoq_rmsnorm_backward_ws needs for rows of H elements (the
+ * same for every T): 304 * H * 4 for H <= 4096, 0 for larger H (which takes the
+ * two-pass path of agoq_rmsnorm_backward), -1 if H is not a multiple of 256 in
+ * 256 .. 8192.
+ */
+int64_t agoq_rmsnorm_backward_workspace_bytes(int64_t H);
+
+/*
+ * The same backward as agoq_rmsnorm_backward, with dw (required here), in ONE
+ * read of the input for H <= 4096: a group of 128 threads takes a row, keeps its
+ * dequantized input, dy and w in registers from the row sums through dx, and
+ * adds the row's dw terms dy * xh * rstd to per-thread sums; each of the G
+ * CTAs (as many as are resident at once, at most 304) writes its sums as one row
+ * of the workspace, and a second small kernel adds those rows in a fixed order
+ * (eight contiguous ranges, each in row order, then the range sums in order)
+ * into dw.  Results are deterministic on a given GPU model; each dw sum is a
+ * chain of at most ceil(T/2G) + 1 + ceil(G/8) + 8 binary32 additions, and dx
+ * and rstd obey the bounds stated for agoq_rmsnorm_backward.
+ *   workspace       : caller-owned device scratch, 16-byte aligned, of at least
+ *                     agoq_rmsnorm_backward_workspace_bytes(H) bytes (else
+ *                     AGOQ_ERR_SHAPE); contents on entry are ignored and on
+ *                     return unspecified; it must not overlap any argument.
+ *   workspace_bytes : its size in bytes.
+ * Other arguments, rules and errors as agoq_rmsnorm_backward; dw NULL is
+ * AGOQ_ERR_NULL.  For H > 4096 (workspace size 0) the call is
+ * agoq_rmsnorm_backward.  Calls that share a workspace must not overlap in time
+ * on the GPU.
+ */
+agoq_status agoq_rmsnorm_backward_ws(const void *codes, const float *scales, const void *dy_bf16,
+                                     const void *w_bf16, int64_t T, int64_t H, int bits, float eps,
+                                     void *dx_bf16, float *rstd, float *dw, void *workspace,
+                                     int64_t workspace_bytes, void *stream);
+
+/*
  * QuanGrad local accumulation (AGoQ section 2.B, "Lokale accumulatie"), IN
  * PLACE on an FP8 master gradient.  Per block of 128:
  *   m_i = fl32(e4m3(c_i) * scale);  t_i = fl32(m_i + g_i);

@@ -37,7 +37,9 @@ def _inputs(oracle, T, H, bits, seed):
     return codes, scales, dy, w
 
 
-def _check(oracle, codes, scales, dy, w, T, H, bits, eps, got):
+def _check(oracle, codes, scales, dy, w, T, H, bits, eps, got, dw_chain=None):
+    """dw_chain: the longest chain of binary32 additions in a dw sum (default:
+    the two-pass kernels' T/64 + 24)."""
     gdx, grstd, gdw = got
     ex_dx, ex_r, ex_dw = oracle.rmsnorm_backward(codes, scales, dy, w, T, H, bits, eps)
     xh = _f64(oracle.dequant_act(codes, scales, T * H, bits)).reshape(T, H)
@@ -56,7 +58,8 @@ def _check(oracle, codes, scales, dy, w, T, H, bits, eps, got):
     assert np.mean(got_dx == oracle.round_format(ex_dx, MID_BF16).reshape(T, H)) >= 0.99
     if gdw is not None:
         terms = np.abs(_f64(dy).reshape(T, H) * xh * r).sum(axis=0)
-        assert np.all(np.abs(gdw - ex_dw) <= terms * (dr + (T / 64 + 24) * U) + 1e-38)
+        chain = T / 64 + 24 if dw_chain is None else dw_chain
+        assert np.all(np.abs(gdw - ex_dw) <= terms * (dr + chain * U) + 1e-38)
 
 
 def _run(codes, scales, dy, w, T, H, bits, eps, want_dw=True):
@@ -155,3 +158,86 @@ def test_rmsnorm_backward_guard_bands(oracle):
     agoq.agoq_rmsnorm_backward(G.dev(codes), G.dev(scales), G.dev_bf16(dy), G.dev_bf16(w), T, H,
                                6, 1e-6, dxg.view, rg.view[:T], wg.view)
     assert dxg.intact() and rg.intact() and wg.intact()
+
+
+# ---------------------------------------------------------------- single read
+def _ws_chain(T):
+    """Longest dw addition chain of the single-read path: ceil(T / 2G) rows per
+    thread, the two row groups, ceil(G / 8) partial rows per range, the eight
+    range sums; G <= min(304, ceil(T / 2)) partial rows (as many CTAs as fit at
+    once), and the chain is longest for the largest G when T >= 2G."""
+    worst = 0
+    for G_ in range(1, min(304, (T + 1) // 2) + 1):
+        worst = max(worst, -(-T // (2 * G_)) + 1 + -(-G_ // 8) + 8)
+    return worst
+
+
+def _run_ws(codes, scales, dy, w, T, H, bits, eps, ws=None):
+    if ws is None:
+        ws = torch.empty(max(agoq.agoq_rmsnorm_backward_workspace_bytes(H), 16), dtype=torch.uint8,
+                         device="cuda")
+    dx, rstd, dw = agoq.agoq_rmsnorm_backward_ws(G.dev(codes), G.dev(scales), G.dev_bf16(dy),
+                                                 G.dev_bf16(w), T, H, bits, eps, ws)
+    torch.cuda.synchronize()
+    return (G.host_bits_bf16(dx), rstd.cpu().numpy().astype(np.float64),
+            dw.cpu().numpy().astype(np.float64))
+
+
+@pytest.mark.parametrize("bits", [4, 5, 6, 8])
+@pytest.mark.parametrize("T,H", [(1, 256), (7, 512), (33, 4096), (2, 1280), (64, 3072),
+                                 (609, 1024), (1000, 4096), (5, 8192)])
+def test_rmsnorm_backward_ws_parity(oracle, bits, T, H):
+    """One read of the input: 1 to 4 chunks of 8 columns per thread (H up to
+    4096), more rows than 2 x 304 (several rows per thread), odd T (a row group
+    with no last row); H = 8192 takes the two-pass kernels."""
+    eps = 1e-6
+    codes, scales, dy, w = _inputs(oracle, T, H, bits, seed=T * 7 + bits + H)
+    got = _run_ws(codes, scales, dy, w, T, H, bits, eps)
+    chain = _ws_chain(T) if H <= 4096 else None
+    _check(oracle, codes, scales, dy, w, T, H, bits, eps, got, dw_chain=chain)
+
+
+def test_rmsnorm_backward_ws_deterministic_and_close_to_two_pass(oracle):
+    """Repeatable bits; the row sums are added in another order than in the
+    two-pass kernels, so rstd agrees to a few ulps and dx nearly everywhere; dw
+    within the bound of its chain."""
+    T, H = 1500, 4096
+    codes, scales, dy, w = _inputs(oracle, T, H, 4, seed=77)
+    a = _run_ws(codes, scales, dy, w, T, H, 4, 1e-6)
+    b = _run_ws(codes, scales, dy, w, T, H, 4, 1e-6)
+    assert all(np.array_equal(x, y) for x, y in zip(a, b))
+    c = _run(codes, scales, dy, w, T, H, 4, 1e-6)
+    assert np.all(np.abs(a[1] - c[1]) <= 2 * (H / 2 + 8) * U * c[1])
+    assert np.mean(a[0] == c[0]) >= 0.99
+    _check(oracle, codes, scales, dy, w, T, H, 4, 1e-6, a, dw_chain=_ws_chain(T))
+
+
+def test_rmsnorm_backward_ws_full_size(oracle):
+    """The DBCA-PP RMSNorm input (8192 x 4096) at 4 bits, single read; every
+    output against the oracle."""
+    T, H, bits, eps = 8192, 4096, 4, 1e-6
+    x = synthetic.dbca_activations_np(seed=1)[0].reshape(-1)
+    codes, scales = oracle.quant_act(x, bits, parallel=oracle.parallel_available())
+    rng = np.random.default_rng(21)
+    dy = synthetic.bf16_bits_from_f32(rng.standard_normal(T * H).astype(np.float32))
+    w = synthetic.bf16_bits_from_f32((1 + 0.1 * rng.standard_normal(H)).astype(np.float32))
+    got = _run_ws(codes, scales, dy, w, T, H, bits, eps)
+    _check(oracle, codes, scales, dy, w, T, H, bits, eps, got, dw_chain=_ws_chain(T))
+
+
+def test_rmsnorm_backward_ws_guard_bands_and_arguments(oracle):
+    T, H = 37, 1024
+    codes, scales, dy, w = _inputs(oracle, T, H, 5, seed=38)
+    need = agoq.agoq_rmsnorm_backward_workspace_bytes(H)
+    assert need == 304 * H * 4
+    dxg = G.Guarded(2 * T * H, torch.bfloat16)
+    rg = G.Guarded(4 * 40, torch.float32)
+    wg = G.Guarded(4 * H, torch.float32)
+    ws = G.Guarded(need, torch.uint8)
+    agoq.agoq_rmsnorm_backward_ws(G.dev(codes), G.dev(scales), G.dev_bf16(dy), G.dev_bf16(w), T, H,
+                                  5, 1e-6, ws.view, dxg.view, rg.view[:T], wg.view)
+    assert dxg.intact() and rg.intact() and wg.intact() and ws.intact()
+    small = torch.empty(need - 16, dtype=torch.uint8, device="cuda")
+    with pytest.raises(agoq.AgoqError):
+        agoq.agoq_rmsnorm_backward_ws(G.dev(codes), G.dev(scales), G.dev_bf16(dy), G.dev_bf16(w),
+                                      T, H, 5, 1e-6, small)
