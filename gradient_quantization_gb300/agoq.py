@@ -55,6 +55,8 @@ def _lib_handle():
                                             vp, vp, vp]
         L.agoq_rmsnorm_backward_ws.argtypes = [vp, vp, vp, vp, i64, i64, i32, ctypes.c_float, vp,
                                                vp, vp, vp, i64, vp]
+        L.agoq_rmsnorm_backward_noalloc.argtypes = [vp, vp, vp, vp, i64, i64, i32, ctypes.c_float,
+                                                    vp, vp, vp, vp]
         L.agoq_rmsnorm_backward_workspace_bytes.argtypes = [i64]
         L.agoq_rmsnorm_backward_workspace_bytes.restype = i64
         L.agoq_grad_accum_fp8_mid.argtypes = [vp, vp, vp, i64, i32, vp]
@@ -71,6 +73,7 @@ def _lib_handle():
                      "agoq_wgrad_gemm_int4_f32out", "agoq_device_status",
                      "agoq_wgrad_gemm_int4_accum_fp8", "agoq_grad_accum_fp8_mid",
                      "agoq_silu_backward", "agoq_rmsnorm_backward", "agoq_rmsnorm_backward_ws",
+                     "agoq_rmsnorm_backward_noalloc",
                      "agoq_dbca_pp_bits",
                      "agoq_fwd_gemm_quant", "agoq_test_wait_timeout"):
             getattr(L, name).restype = i32
@@ -236,6 +239,21 @@ def agoq_rmsnorm_backward_ws(codes, scales, dy, w, T, H, bits, eps, workspace, d
                                           float(eps), _ptr(dx), _ptr(rstd), _ptr(dw),
                                           _ptr(workspace), nbytes, _stream(stream)),
            "agoq_rmsnorm_backward_ws")
+    return dx, rstd, dw
+
+
+def agoq_rmsnorm_backward_noalloc(codes, scales, dy, w, T, H, bits, eps, dx, rstd, dw,
+                                  stream=None):
+    """agoq_rmsnorm_backward_ws with the library's own static scratch (H <= 4096), for
+    callers that cannot allocate device memory at the call: every output is
+    caller-provided and the call allocates nothing."""
+    _need(codes, torch.uint8, "codes")
+    _need(scales, torch.float32, "scales")
+    _need(dy, torch.bfloat16, "dy")
+    _need(w, torch.bfloat16, "w")
+    _check(lib().agoq_rmsnorm_backward_noalloc(_ptr(codes), _ptr(scales), _ptr(dy), _ptr(w), T, H,
+                                               bits, float(eps), _ptr(dx), _ptr(rstd), _ptr(dw),
+                                               _stream(stream)), "agoq_rmsnorm_backward_noalloc")
     return dx, rstd, dw
 
 

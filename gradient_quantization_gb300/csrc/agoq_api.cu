@@ -188,6 +188,39 @@ agoq_status agoq_rmsnorm_backward_ws(const void *codes, const float *scales, con
                                                    as_stream(stream)));
 }
 
+agoq_status agoq_rmsnorm_backward_noalloc(const void *codes, const float *scales,
+                                          const void *dy_bf16, const void *w_bf16, int64_t T,
+                                          int64_t H, int bits, float eps, void *dx_bf16,
+                                          float *rstd, float *dw, void *stream) {
+    using namespace agoq;
+    if (!bits_ok(bits)) return AGOQ_ERR_BITS;
+    if (T < 0 || H <= 0 || H % 256 || H > rmsnorm_fused_max_h() || !(eps >= 0.0f) ||
+        eps > 3.0e38f)
+        return AGOQ_ERR_SHAPE;
+    if (!dw) return AGOQ_ERR_NULL;
+    if (T == 0) {
+        if (!aligned(dw, 4)) return AGOQ_ERR_ALIGN;
+        return from_cuda(cudaMemsetAsync(dw, 0, 4ull * H, as_stream(stream)));
+    }
+    if (!codes || !scales || !dy_bf16 || !w_bf16 || !dx_bf16 || !rstd) return AGOQ_ERR_NULL;
+    if (!aligned(codes, 16) || !aligned(scales, 4) || !aligned(dy_bf16, 16) ||
+        !aligned(w_bf16, 16) || !aligned(dx_bf16, 16) || !aligned(rstd, 4) || !aligned(dw, 4))
+        return AGOQ_ERR_ALIGN;
+    const uint64_t n = (uint64_t)T * H, nb = n / kBlockElems;
+    const uint64_t cb = nb * 16 * bits, sb = nb * 4, vb = 2 * n, wb = 2ull * H;
+    const uint64_t rb = 4ull * T, db = 4ull * H;
+    const void *in[4] = {codes, scales, dy_bf16, w_bf16};
+    const uint64_t inb[4] = {cb, sb, vb, wb};
+    for (int i = 0; i < 4; ++i)
+        if (overlap(dx_bf16, vb, in[i], inb[i]) || overlap(rstd, rb, in[i], inb[i]) ||
+            overlap(dw, db, in[i], inb[i]))
+            return AGOQ_ERR_ALIAS;
+    if (overlap(dx_bf16, vb, rstd, rb) || overlap(dx_bf16, vb, dw, db) || overlap(rstd, rb, dw, db))
+        return AGOQ_ERR_ALIAS;
+    return from_cuda(launch_rmsnorm_backward_noalloc(codes, scales, dy_bf16, w_bf16, T, H, bits,
+                                                     eps, dx_bf16, rstd, dw, as_stream(stream)));
+}
+
 agoq_status agoq_grad_accum_fp8(void *master_e4m3, float *master_scales, const void *grad_bf16,
                                 int64_t n, void *stream) {
     return agoq_grad_accum_fp8_mid(master_e4m3, master_scales, grad_bf16, n, AGOQ_MID_FP32, stream);

@@ -67,6 +67,11 @@ cudaError_t launch_rmsnorm_backward_fused(const void *codes, const float *scales
                                           cudaStream_t st);
 int rmsnorm_fused_partials();
 int rmsnorm_fused_max_h();
+// The single-read form with the library's own static scratch (H <= rmsnorm_fused_max_h()).
+cudaError_t launch_rmsnorm_backward_noalloc(const void *codes, const float *scales, const void *dy,
+                                            const void *w, int64_t T, int64_t H, int bits,
+                                            float eps, void *dx, float *rstd, float *dw,
+                                            cudaStream_t st);
 // mid: intermediate format of the sum (0 binary32, 1 BF16, 2 FP16).
 cudaError_t launch_grad_accum(void *master, float *master_scales, const void *grad, int64_t n,
                               int mid, cudaStream_t st);

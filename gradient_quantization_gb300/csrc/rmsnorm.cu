@@ -23,6 +23,7 @@
 // rank order through distributed shared memory.  No global scratch, no
 // atomics: dw is deterministic.
 #include <cooperative_groups.h>
+#include <mutex>
 
 #include "agoq_device.cuh"
 #include "agoq_launch.h"
@@ -1000,5 +1001,51 @@ cudaError_t launch_rmsnorm_backward_fused(const void *codes, const float *scales
 
 int rmsnorm_fused_partials() { return kFusedPartials; }
 int rmsnorm_fused_max_h() { return kFusedMaxH; }
+
+// ---- the same single-read backward without a caller-provided workspace ----
+// For callers that cannot allocate device memory at the point of the call (a
+// framework's custom-operator hook that must not touch the allocator, code
+// running while device memory is locked down or accounted by someone else, a
+// plain C caller without an allocator of its own), the partial-sum scratch is
+// this file-scope array instead of a workspace argument.  It holds the partial
+// rows of the largest case the entry point accepts (rows of up to kFusedMaxH =
+// 4096 elements: kFusedPartials x 4096 floats, about 5 MB), and every GPU that
+// loads the library keeps it until the process exits.
+static __device__ __align__(256) float g_rms_noalloc_scratch[kFusedPartials * kFusedMaxH];
+
+// The array's device address, looked up once per device (with that device
+// current) on the first call; the name of the array in host code is only a
+// stand-in for the symbol and must not be handed to a kernel.
+static cudaError_t noalloc_scratch(float **out) {
+    static std::mutex lock;
+    static float *addr[kMaxDevices];
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+    std::lock_guard<std::mutex> hold(lock);
+    if (!addr[dev]) {
+        void *p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_rms_noalloc_scratch);
+        if (e != cudaSuccess) return e;
+        addr[dev] = static_cast<float *>(p);
+    }
+    *out = addr[dev];
+    return cudaSuccess;
+}
+
+// The caller has checked H <= kFusedMaxH.  Every CTA writes its whole partial
+// row before the second kernel reads it, so nothing in the array needs to
+// start at zero; the array is shared by all calls on a device.
+cudaError_t launch_rmsnorm_backward_noalloc(const void *codes, const float *scales, const void *dy,
+                                            const void *w, int64_t T, int64_t H, int bits,
+                                            float eps, void *dx, float *rstd, float *dw,
+                                            cudaStream_t st) {
+    float *scratch = nullptr;
+    cudaError_t e = noalloc_scratch(&scratch);
+    if (e != cudaSuccess) return e;
+    return launch_rmsnorm_backward_fused(codes, scales, dy, w, T, H, bits, eps, dx, rstd, dw,
+                                         scratch, st);
+}
 
 }  // namespace agoq

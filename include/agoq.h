@@ -180,6 +180,31 @@ agoq_status agoq_rmsnorm_backward_ws(const void *codes, const float *scales, con
                                      int64_t workspace_bytes, void *stream);
 
 /*
+ * agoq_rmsnorm_backward_ws without the workspace argument, for callers that
+ * cannot allocate device memory where they call it: a hook inside another
+ * framework's allocator-free path, code running while device memory is
+ * reserved or accounted by someone else, or a plain C caller with no device
+ * allocator of its own.  The page has no counterpart: it is a packaging of the
+ * single-read kernel above.  The scratch that workspace would hold is a
+ * static array inside the library, sized for the largest rows it accepts:
+ * H must be a multiple of 256 and at most 4096 (AGOQ_ERR_SHAPE beyond that;
+ * about 5 MB per GPU, held from the first use of the library on that GPU until
+ * the process exits).  The library allocates nothing in this call.  The first
+ * call on each device looks up the array's device address (with that device
+ * current), so make that first call before capturing a stream into a graph.
+ * All calls on a device share the array: calls that may run at the same time
+ * on the GPU (on different streams without ordering between them) race and
+ * give wrong dw; order them, or use agoq_rmsnorm_backward_ws with separate
+ * workspaces.  Nothing in the array needs to start at zero (every call writes
+ * the part it reads).  Arguments, results and the other errors as
+ * agoq_rmsnorm_backward_ws; dw NULL is AGOQ_ERR_NULL.
+ */
+agoq_status agoq_rmsnorm_backward_noalloc(const void *codes, const float *scales,
+                                          const void *dy_bf16, const void *w_bf16, int64_t T,
+                                          int64_t H, int bits, float eps, void *dx_bf16,
+                                          float *rstd, float *dw, void *stream);
+
+/*
  * QuanGrad local accumulation (AGoQ section 2.B, "Lokale accumulatie"), IN
  * PLACE on an FP8 master gradient.  Per block of 128:
  *   m_i = fl32(e4m3(c_i) * scale);  t_i = fl32(m_i + g_i);
