@@ -102,17 +102,21 @@ __device__ __forceinline__ void e4m3x2_to_f32(uint32_t v, float &lo, float &hi) 
 // within 3 * 2^-24 |t/s| of the binary32 quotient (plus a negligible absolute
 // term if subnormal).  The codes of fl(q * (1 - 2^-20)) and fl(q * (1 + 2^-20))
 // bracket that quotient on both sides; E4M3 rounding is monotonic, so when the
-// two codes agree they equal the quotient's code.  If any pair disagrees the
-// eight quotients are recomputed with IEEE division.  Values whose products
+// two codes agree they equal the quotient's code.  Only the values whose two
+// codes disagree (a quotient at or next to an E4M3 rounding boundary) are
+// recomputed with IEEE division.  Such values are not rare when t has few
+// significant bits: t/s is then close to 448 times a ratio of short integers,
+// and on the gradient workload about one BF16-valued sum in 200 lands within
+// 2^-20 of a boundary (one binary32 sum in 2000), so a per-value fallback keeps
+// most lanes of a warp on the fast path.  Values whose products
 // underflow are far below the smallest E4M3 midpoint (2^-10) and give a signed
 // zero either way.  s subnormal takes the division; s == 0 (all-zero block)
 // gives zero codes.
 __device__ __forceinline__ uint2 e4m3_codes8(const float t[8], float s) {
-    uint32_t c[4];
     if (s >= 0x1p-126f) {
         const float r = __frcp_rn(s);
         constexpr float kDown = 1.0f - 0x1p-20f, kUp = 1.0f + 0x1p-20f;
-        bool differ = false;
+        uint32_t c[2] = {0u, 0u}, d[2] = {0u, 0u};   // codes; nonzero byte: bracket differs
         // the same products in packed pairs (multiplies only: nothing to contract)
         const uint64_t r2 = f32x2(r, r), dn2 = f32x2(kDown, kDown), up2 = f32x2(kUp, kUp);
 #pragma unroll
@@ -121,22 +125,29 @@ __device__ __forceinline__ uint2 e4m3_codes8(const float t[8], float s) {
             const uint64_t a2 = mul_f32x2(q2, dn2), b2 = mul_f32x2(q2, up2);
             const uint32_t lo = e4m3x2_from_f32(lo_f32(a2), hi_f32(a2));
             const uint32_t hi = e4m3x2_from_f32(lo_f32(b2), hi_f32(b2));
-            differ |= lo != hi;
-            c[p] = lo;
+            c[p >> 1] |= lo << (16 * (p & 1));
+            d[p >> 1] |= (lo ^ hi) << (16 * (p & 1));
         }
-        if (differ) {
+        if (d[0] | d[1]) {
 #pragma unroll
-            for (int p = 0; p < 4; ++p)
-                c[p] = e4m3x2_from_f32(__fdiv_rn(t[2 * p], s), __fdiv_rn(t[2 * p + 1], s));
+            for (int k = 0; k < 8; ++k) {
+                const int sh = 8 * (k & 3);
+                if ((d[k >> 2] >> sh) & 0xFFu) {
+                    const uint32_t code = e4m3x2_from_f32(__fdiv_rn(t[k], s), 0.0f);
+                    c[k >> 2] = (c[k >> 2] & ~(0xFFu << sh)) | (code << sh);
+                }
+            }
         }
-    } else if (s > 0.0f) {
+        return make_uint2(c[0], c[1]);
+    }
+    if (s > 0.0f) {
+        uint32_t c[4];
 #pragma unroll
         for (int p = 0; p < 4; ++p)
             c[p] = e4m3x2_from_f32(__fdiv_rn(t[2 * p], s), __fdiv_rn(t[2 * p + 1], s));
-    } else {
-        return make_uint2(0u, 0u);
+        return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
     }
-    return make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    return make_uint2(0u, 0u);
 }
 
 // Largest |value| of the BF16 pairs in w[0..N-1], as a binary32 (exact: the
