@@ -56,7 +56,7 @@ const char *agoq_status_string(agoq_status s) {
         case AGOQ_ERR_ALIGN: return "AGOQ_ERR_ALIGN: pointer not aligned as required";
         case AGOQ_ERR_ALIAS: return "AGOQ_ERR_ALIAS: an output overlaps an input";
         case AGOQ_ERR_CUDA: return "AGOQ_ERR_CUDA: CUDA runtime error";
-        case AGOQ_ERR_TIMEOUT: return "AGOQ_ERR_TIMEOUT: a GEMM pipeline wait gave up";
+        case AGOQ_ERR_TIMEOUT: return "AGOQ_ERR_TIMEOUT: a pipeline wait gave up";
         case AGOQ_ERR_FORMAT: return "AGOQ_ERR_FORMAT: unsupported intermediate format";
     }
     return "AGOQ_ERR_UNKNOWN";

@@ -55,7 +55,7 @@ typedef enum {
     AGOQ_ERR_ALIGN = 4,   /* pointer not aligned as required */
     AGOQ_ERR_ALIAS = 5,   /* an output overlaps an input */
     AGOQ_ERR_CUDA = 6,    /* the CUDA runtime reported an error at launch */
-    AGOQ_ERR_TIMEOUT = 7, /* a GEMM pipeline wait gave up (see agoq_device_status) */
+    AGOQ_ERR_TIMEOUT = 7, /* a pipeline wait gave up (see agoq_device_status) */
     AGOQ_ERR_FORMAT = 8   /* unsupported intermediate format (agoq_grad_accum_fp8_mid) */
 } agoq_status;
 
