@@ -105,3 +105,23 @@ def test_unaligned_scales_take_the_direct_path(oracle):
     b = agoq.agoq_wgrad_gemm_int4_f32out(*args, xs_off, M, N, K)
     agoq.agoq_device_status()
     assert torch.equal(a, b)
+
+
+def test_output_16_byte_aligned_takes_the_narrow_stores(oracle):
+    """An output 16 bytes off a 32-byte boundary is written with 16-byte stores
+    instead of 32-byte ones: the same bits as a 32-byte-aligned output, for the
+    BF16 and the FP32 result (two tile rows and columns, a partial last tile)."""
+    M, N, K = 640, 384, 128
+    dy, xc, xs = _inputs(oracle, M, N, K, seed=14)
+    args = (G.dev_bf16(dy), G.dev(xc), G.dev(xs), M, N, K)
+    for dtype, fn in ((torch.bfloat16, agoq.agoq_wgrad_gemm_int4),
+                      (torch.float32, agoq.agoq_wgrad_gemm_int4_f32out)):
+        esz = torch.empty(0, dtype=dtype).element_size()
+        room = torch.zeros(M * N + 64 // esz, dtype=dtype, device="cuda")
+        off = room[16 // esz:16 // esz + M * N].view(M, N)
+        assert off.data_ptr() % 32 == 16
+        want = fn(*args)
+        fn(*args, off)
+        agoq.agoq_device_status()
+        assert torch.equal(off, want), str(dtype)
+        assert not room[:16 // esz].any() and not room[16 // esz + M * N:].any()

@@ -190,3 +190,21 @@ def test_full_size_gaussian_sampled_blocks(oracle):
     got = (G.gather_blocks(m, blocks, 128).numpy().reshape(-1),
            G.gather_blocks(s, blocks, 1).numpy().reshape(-1))
     _check_within_bound(oracle, dy, xc, xs, M, N, K, m0, s0, got, blocks=blocks)
+
+
+def test_master_16_byte_aligned_takes_the_narrow_accesses(oracle):
+    """Master codes 16 bytes off a 32-byte boundary are read and written with
+    16-byte accesses instead of 32-byte ones: the same codes and scales."""
+    M, N, K = 640, 384, 128
+    dy, xc, xs = _gauss_inputs(oracle, M, N, K, seed=31)
+    master, scales = _master(oracle, M * N, seed=32, sd=0.05)
+    want = _run(dy, xc, xs, M, N, K, master, scales)
+    room = torch.zeros(M * N + 64, dtype=torch.uint8, device="cuda")
+    m_off = room[16:16 + M * N]
+    assert m_off.data_ptr() % 32 == 16
+    m_off.copy_(torch.from_numpy(master))
+    s = torch.from_numpy(scales).cuda()
+    agoq.agoq_wgrad_gemm_int4_accum_fp8(G.dev_bf16(dy), G.dev(xc), G.dev(xs), M, N, K, m_off, s)
+    agoq.agoq_device_status()
+    _assert_same((m_off.cpu().numpy(), s.cpu().numpy()), want)
+    assert not room[:16].any() and not room[16 + M * N:].any()
