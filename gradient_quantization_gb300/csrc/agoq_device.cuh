@@ -150,6 +150,34 @@ __device__ __forceinline__ uint2 e4m3_codes8(const float t[8], float s) {
     return make_uint2(0u, 0u);
 }
 
+// The same codes when every t is a BF16 value (and so is the block absmax that
+// gave s): the binary32 quotient by Markstein's correction of the reciprocal
+// product (P. Markstein, IBM J. Res. Dev. 34(1), 1990), with no bracket and no
+// division.  It is formed negated, -q' = fma(rho, -r, -q) with r = fl(1/s),
+// -q = fl(t * -r) and rho = fma(-q, s, t), and the codes' sign bits are
+// flipped at the end (E4M3 is sign-magnitude): that is q' = fma(rho, r, q)
+// for every t except a zero t, where rho is +0 and only the negated form keeps
+// the sign of -0/s = -0.  For s >= 2^-96, q' = fl(t/s) for every such t: the
+// library's tests run every pair of BF16 values (t, absmax), |t| <= absmax,
+// signed zeros included, through it and through e4m3_codes8 and compare the
+// codes.  Below 2^-96 the residual can fall into the subnormal range, so those
+// blocks take e4m3_codes8.
+__device__ __forceinline__ uint2 e4m3_codes8_bf16(const float t[8], float s) {
+    if (!(s >= 0x1p-96f)) return e4m3_codes8(t, s);
+    const float nr = -__frcp_rn(s);
+    const uint64_t nr2 = f32x2(nr, nr), s2 = f32x2(s, s);
+    uint32_t c[4];
+#pragma unroll
+    for (int p = 0; p < 4; ++p) {
+        const uint64_t tt = f32x2(t[2 * p], t[2 * p + 1]);
+        const uint64_t nq = mul_f32x2(tt, nr2);
+        const uint64_t rho = fma_f32x2(nq, s2, tt);
+        const uint64_t nq1 = fma_f32x2(rho, nr2, nq);
+        c[p] = e4m3x2_from_f32(lo_f32(nq1), hi_f32(nq1));
+    }
+    return make_uint2((c[0] | (c[1] << 16)) ^ 0x80808080u, (c[2] | (c[3] << 16)) ^ 0x80808080u);
+}
+
 // Largest |value| of the BF16 pairs in w[0..N-1], as a binary32 (exact: the
 // maximum of BF16 magnitudes is a BF16 value).  max.xorsign.abs compares
 // magnitudes directly; its sign bit, the XOR of the inputs', is masked once at
