@@ -62,23 +62,6 @@ __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-__device__ __forceinline__ void umma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
-                                          uint32_t idesc, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-__device__ __forceinline__ void umma_commit(uint64_t *bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_u32(bar))
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
     asm volatile(
         "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
@@ -90,17 +73,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t (&v)[32]) {
           "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
           "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]),
           "=r"(v[31])
-        : "r"(taddr));
-    asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&v)[16]) {
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15}, [%16];"
-        : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]),
-          "=r"(v[7]), "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]),
-          "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
         : "r"(taddr));
     asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
@@ -211,18 +183,6 @@ __device__ __forceinline__ void umma_commit_pair(uint64_t *bar) {
             smem_u32(bar))
         : "memory");
 }
-// mbarrier phase test with cluster-scope acquire (arrivals come from other CTAs).
-__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-        "selp.u32 %0, 1, 0, p;\n\t}"
-        : "=r"(ok)
-        : "r"(smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
 // All threads of all CTAs of the cluster.
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
@@ -263,23 +223,6 @@ __device__ __forceinline__ bool wait_bar(uint64_t *bar, uint32_t parity, volatil
     }
 }
 
-// wait_bar with cluster-scope acquire, for barriers other CTAs arrive on.
-__device__ __forceinline__ bool wait_bar_cluster(uint64_t *bar, uint32_t parity,
-                                                 volatile int *abort, unsigned *status,
-                                                 bool ignore_abort = false) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    const long long t0 = clock64();
-    for (;;) {
-        if (mbar_try_wait_cluster(bar, parity)) return true;
-        if (!ignore_abort && *abort) return false;
-        if (clock64() - t0 > kWaitLimitCycles) {
-            *abort = 1;
-            atomicExch(status, kStatusTimeout);
-            return false;
-        }
-    }
-}
-
 // The same wait for a whole warp: lane 0 polls, the outcome is broadcast, and
 // the warp leaves converged (the tcgen05 .sync.aligned instructions need that).
 __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volatile int *abort,
@@ -287,18 +230,6 @@ __device__ __forceinline__ bool warp_wait(uint64_t *bar, uint32_t parity, volati
     const int lane = threadIdx.x & 31;
     bool ok = true;
     if (lane == 0) ok = wait_bar(bar, parity, abort, status, false, hint_ns);
-    ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
-    __syncwarp();
-    return ok;
-}
-
-
-// warp_wait with cluster-scope acquire.
-__device__ __forceinline__ bool warp_wait_cluster(uint64_t *bar, uint32_t parity,
-                                                  volatile int *abort, unsigned *status) {
-    const int lane = threadIdx.x & 31;
-    bool ok = true;
-    if (lane == 0) ok = wait_bar_cluster(bar, parity, abort, status);
     ok = __shfl_sync(0xFFFFFFFFu, ok ? 1 : 0, 0) != 0;
     __syncwarp();
     return ok;
