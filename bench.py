@@ -29,7 +29,9 @@ Also reported:
                 with the kernels left out (the host link's share);
   cpu_baseline  the CPU oracle on the host cores: its all-core (OpenMP) build on
                 the full workload where it fits the time budget, and the
-                single-threaded build on a bounded sample;
+                single-threaded build on a bounded sample; `oracle_rows` times
+                the all-core oracle on the other workloads (full size or a
+                stated sample);
   rows          each other kernel of the path on its own workload, L2 flushed
                 before each timed launch (a 256 MB buffer written, then another
                 256 MB read, so the launch starts from a cold L2 holding no dirty
@@ -363,6 +365,9 @@ def gpu_arm(args):
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         cpu = cpu_baseline(args.cpu_seconds)
+        from oracle import oracle as O
+        if O.parallel_available():
+            cpu["oracle_rows"] = oracle_rows(device)
 
     if rank == 0:
         line = {
@@ -944,6 +949,81 @@ def cpu_baseline(target_s):
     line["cpu_model"] = cpu_model()
     line["host_cores"] = len(os.sched_getaffinity(0))
     return line
+
+
+def oracle_rows(device):
+    """The all-core oracle on the other workloads, each at full size or on a
+    stated sample (a reported baseline, like the step's): the 2048x4096 4-bit
+    round trip, one QuanGrad step of 2^30 elements, the shard reduce with its
+    count (W=8 at 2^25, W=64 on 2^22 elements per shard) and the binary64
+    weight-gradient product on the first 16 rows of dW.  The inputs for the
+    larger ones are drawn and quantized on the GPU and copied to the host."""
+    import numpy as np
+    import torch
+    from gradient_quantization_gb300 import agoq, synthetic
+    from oracle import oracle as O
+    par = True
+    rows = {}
+
+    def timed(fn):
+        t0 = time.perf_counter()
+        out = fn()
+        return time.perf_counter() - t0, out
+
+    def host_u16(t):
+        return t.contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+    x = synthetic.laaq_activation_np(seed=0).reshape(-1)
+    n = x.size
+    dt, (c, sc) = timed(lambda: O.quant_act(x, 4, parallel=par))
+    rows["laaq_int4_quant_2048x4096"] = {"us": round(dt * 1e6, 1),
+                                         "GB/s": round(act_bytes(n, 4) / dt / 1e9, 3),
+                                         "Gelem/s": round(n / dt / 1e9, 4), "sample": "full size"}
+    dt, _ = timed(lambda: O.dequant_act(c, sc, n, 4, parallel=par))
+    rows["laaq_int4_dequant_2048x4096"] = {"us": round(dt * 1e6, 1),
+                                           "GB/s": round(act_bytes(n, 4) / dt / 1e9, 3),
+                                           "Gelem/s": round(n / dt / 1e9, 4), "sample": "full size"}
+    del x, c, sc
+
+    nq = synthetic.QUANGRAD_N
+    g = host_u16(synthetic.quangrad_grad_torch(seed=2, step=0, device=device))
+    m = np.zeros(nq, np.uint8)
+    ms = np.zeros(nq // 128, np.float32)
+    dt, _ = timed(lambda: O.grad_accum_fp8(m, ms, g, parallel=par, in_place=True))
+    nbytes = nq * 4 + (nq // 128) * 8
+    rows["quangrad_accum_2^30"] = {"us": round(dt * 1e6, 1), "GB/s": round(nbytes / dt / 1e9, 3),
+                                   "Gelem/s": round(nq / dt / 1e9, 4),
+                                   "sample": "one step (micro-batch 0 onto a zeroed master), full size"}
+    del g, m, ms
+
+    for W, nr in ((8, synthetic.REDUCE_N), (64, 1 << 22)):
+        sh, ss = reduce_shards_torch(W, nr, device)
+        shh, ssh = sh.cpu().numpy(), ss.cpu().numpy()
+        del sh, ss
+        dt, _ = timed(lambda: O.reduce_fp8_shards(shh, ssh, W, nr, count_naive=True, parallel=par))
+        nbytes = (W + 1) * (nr + (nr // 128) * 4)
+        rows["reduce_W%d_count" % W] = {
+            "us": round(dt * 1e6, 1), "GB/s": round(nbytes / dt / 1e9, 3),
+            "Gelem/s": round(W * nr / dt / 1e9, 4),
+            "sample": "full size (2^25 per shard)" if nr == synthetic.REDUCE_N
+                      else "2^22 elements per shard (the workload has 2^25)"}
+        del shh, ssh
+
+    M, N, K = synthetic.WGRAD_M, synthetic.WGRAD_N, synthetic.WGRAD_K
+    dy, xg = synthetic.wgrad_inputs_torch(seed=4, device=device)
+    xc, xs = agoq.agoq_quant_act(xg, 4)
+    dyh, xch, xsh = host_u16(dy), xc.cpu().numpy(), xs.cpu().numpy()
+    del dy, xg, xc, xs
+    nr = 16
+    r = np.repeat(np.arange(nr, dtype=np.int32), N)
+    cc = np.tile(np.arange(N, dtype=np.int32), nr)
+    dt, _ = timed(lambda: O.wgrad_gemm_int4_f64_entries(dyh, xch, xsh, M, N, K, r, cc,
+                                                         parallel=par))
+    rows["wgrad_gemm_int4_f64"] = {"us": round(dt * 1e6, 1),
+                                   "GFLOP/s": round(2.0 * nr * N * K / dt / 1e9, 3),
+                                   "sample": "the first %d of %d rows of dW (binary64 sums)" % (nr, M)}
+    torch.cuda.synchronize()
+    return rows
 
 
 def reference_arm(args):

@@ -96,10 +96,12 @@ __device__ __forceinline__ uint2 accum_block(const uint2 &mc, const uint4 &g, fl
     for (int i = 0; i < 8; ++i) am = fmaxf(am, fabsf(t[i]));
     am = halfwarp_max(am);
     snew = __fdiv_rn(am, kE4M3Max);
-    // BF16-valued sums (the BF16 intermediate, or a binary32 sum onto an
-    // all-zero master block, t = 0 + g) take the corrected quotient; a
-    // bracket near an E4M3 rounding boundary is common for them.
-    if (MID == kMidBf16 || (MID == kMidF32 && s == 0.0f)) return e4m3_codes8_bf16(t, snew);
+    // BF16-valued sums take the corrected quotient (a bracket near an E4M3
+    // rounding boundary is common for them): the BF16 intermediate, and any
+    // sum onto an all-zero master block, t = 0 + g in binary32 or
+    // t = fp16(g) in FP16 (a BF16 value rounded to the FP16 grid keeps at
+    // most 8 significant bits; an FP16 overflow is outside the contract).
+    if (MID == kMidBf16 || s == 0.0f) return e4m3_codes8_bf16(t, snew);
     return e4m3_codes8(t, snew);
 }
 

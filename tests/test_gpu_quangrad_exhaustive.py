@@ -17,7 +17,11 @@ bracketed path, which the parity tests pin to the oracle); codes and scales
 must agree bit for bit.  A sum onto a zero master is never -0 (+0 + -0 = +0),
 so the BF16 intermediate also runs onto a master of -0 codes (0x80) and scale
 1, where t = -0 + g keeps a -0 gradient, against the bracketed binary32 path
-on the same master.
+on the same master.  The FP16 intermediate takes the corrected quotient onto a
+zero master, where t = fp16(g), a value with at most 8 significant bits; it is
+compared with the same FP16 sums onto a master of zero codes and scale 1 (the
+bracketed path), for every absmax within the FP16 range (an FP16 overflow is
+outside the contract).
 """
 import pytest
 import torch
@@ -27,6 +31,7 @@ from gradient_quantization_gb300 import agoq
 pytestmark = pytest.mark.gpu
 
 SLOTS = 127   # t values per block besides the absmax element
+FP16_TOP = 0x4780   # BF16 patterns below this are at most 65280, within the FP16 range
 
 
 def _blocks(a_lo, a_hi, device="cuda"):
@@ -61,20 +66,23 @@ def _accum(g, scale, mid=None, code=0):
 
 def test_corrected_quotient_equals_bracketed_path_for_every_bf16_pair():
     top = 0x7F80                                   # patterns 1 .. 0x7F7F: positive finite
-    edges = [1, 0x3000, 0x3C00, 0x4400, 0x4C00, 0x5400, 0x6000, 0x6C00, top]
+    edges = [1, 0x3000, 0x3C00, 0x4400, FP16_TOP, 0x4C00, 0x5400, 0x6000, 0x6C00, top]
     total = 0
     for lo, hi in zip(edges[:-1], edges[1:]):
         g = _blocks(lo, hi)
         total += g.numel()
         want_m, want_s = _accum(g, 1.0)              # bracketed requantization
         neg_m, neg_s = _accum(g, 1.0, code=0x80)     # bracketed, t = -0 + g
-        for mid, code, ref in ((None, 0, (want_m, want_s)), (agoq.MID_BF16, 0, (want_m, want_s)),
-                               (agoq.MID_BF16, 0x80, (neg_m, neg_s))):
+        cases = [(None, 0, (want_m, want_s)), (agoq.MID_BF16, 0, (want_m, want_s)),
+                 (agoq.MID_BF16, 0x80, (neg_m, neg_s))]
+        if hi <= FP16_TOP:
+            cases.append((agoq.MID_FP16, 0, _accum(g, 1.0, agoq.MID_FP16)))   # bracketed FP16 sums
+        for mid, code, ref in cases:
             m, s = _accum(g, 0.0 if code == 0 else 1.0, mid, code)   # corrected quotient
             assert torch.equal(s.view(torch.int32), ref[1].view(torch.int32)), (lo, hi, mid, code)
             bad = (m != ref[0]).nonzero()
             assert bad.numel() == 0, (lo, hi, mid, code, bad[:4].flatten().tolist())
             del m, s
-        del g, want_m, want_s, neg_m, neg_s
+        del g, want_m, want_s, neg_m, neg_s, cases
     agoq.agoq_device_status()
     assert total > 1_000_000_000                     # every pair was there
