@@ -16,6 +16,8 @@
 // (used whenever the scale rows allow 16-byte bulk copies) has a producer warp
 // stream (tile, shard group) stages into a shared-memory ring with bulk async
 // copies, so that far more bytes are in flight per SM than registers can hold.
+#include <type_traits>
+
 #include "agoq_device.cuh"
 #include "agoq_launch.h"
 #include "gemm_common.cuh"
@@ -553,39 +555,72 @@ reduce_shards_staged_kernel(
             mbar_try_wait(&full[stage], phase, 0);   // each lane observes the completed phase
             const uint8_t *cs = codes + (size_t)stage * kStCodeBytes + (size_t)(warp * 32 + lane) * 16;
             const float *ss = scl + (size_t)stage * kStShards * kStTile + lb;
+            auto ld = [&](int j) { return *reinterpret_cast<const uint4 *>(cs + (size_t)j * kStTile * 128); };
             // Shards are read from the stage two at a time, the next pair's
             // loads issued before the current pair is added; the stage is
             // released once its last loads are issued (the arrive orders them).
-            uint4 c0 = *reinterpret_cast<const uint4 *>(cs);
-            float s0 = ss[0];
-            uint4 c1 = make_uint4(0u, 0u, 0u, 0u);
-            float s1 = 0.0f;
-            if (k > 1) {
-                c1 = *reinterpret_cast<const uint4 *>(cs + (size_t)kStTile * 128);
-                s1 = ss[kStTile];
-            }
+            if (k == kStShards) {
+                // a full stage: every bound and the rank-0 test are compile-time
+                auto full_stage = [&](auto first_stage) {
+                    constexpr bool kFirst = decltype(first_stage)::value;
+                    uint4 c0 = ld(0), c1 = ld(1);
+                    float s0 = ss[0], s1 = ss[kStTile];
 #pragma unroll
-            for (int j = 0; j < kStShards; j += 2) {
-                if (j >= k) break;
-                uint4 n0 = c0, n1 = c1;
-                float t0 = s0, t1 = s1;
-                if (j + 2 < k) {
-                    n0 = *reinterpret_cast<const uint4 *>(cs + (size_t)(j + 2) * kStTile * 128);
-                    t0 = ss[(j + 2) * kStTile];
-                    if (j + 3 < k) {
-                        n1 = *reinterpret_cast<const uint4 *>(cs + (size_t)(j + 3) * kStTile * 128);
-                        t1 = ss[(j + 3) * kStTile];
+                    for (int j = 0; j < kStShards; j += 2) {
+                        uint4 n0 = c0, n1 = c1;
+                        float t0 = s0, t1 = s1;
+                        if (j + 2 < kStShards) {
+                            n0 = ld(j + 2);
+                            n1 = ld(j + 3);
+                            t0 = ss[(j + 2) * kStTile];
+                            t1 = ss[(j + 3) * kStTile];
+                        } else {
+                            __syncwarp();
+                            if (lane == 0) mbar_arrive(&empty[stage]);
+                        }
+                        st.add2(c0, s0, c1, s1, kFirst && j == 0);
+                        c0 = n0;
+                        c1 = n1;
+                        s0 = t0;
+                        s1 = t1;
                     }
-                } else {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(&empty[stage]);
+                };
+                if (r0 == 0)
+                    full_stage(std::true_type{});
+                else
+                    full_stage(std::false_type{});
+            } else {
+                uint4 c0 = ld(0);
+                float s0 = ss[0];
+                uint4 c1 = make_uint4(0u, 0u, 0u, 0u);
+                float s1 = 0.0f;
+                if (k > 1) {
+                    c1 = ld(1);
+                    s1 = ss[kStTile];
                 }
-                if (j + 1 < k) st.add2(c0, s0, c1, s1, r0 + j == 0);
-                else st.add(c0, s0, r0 + j == 0);
-                c0 = n0;
-                c1 = n1;
-                s0 = t0;
-                s1 = t1;
+#pragma unroll
+                for (int j = 0; j < kStShards; j += 2) {
+                    if (j >= k) break;
+                    uint4 n0 = c0, n1 = c1;
+                    float t0 = s0, t1 = s1;
+                    if (j + 2 < k) {
+                        n0 = ld(j + 2);
+                        t0 = ss[(j + 2) * kStTile];
+                        if (j + 3 < k) {
+                            n1 = ld(j + 3);
+                            t1 = ss[(j + 3) * kStTile];
+                        }
+                    } else {
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&empty[stage]);
+                    }
+                    if (j + 1 < k) st.add2(c0, s0, c1, s1, r0 + j == 0);
+                    else st.add(c0, s0, r0 + j == 0);
+                    c0 = n0;
+                    c1 = n1;
+                    s0 = t0;
+                    s1 = t1;
+                }
             }
             if (++stage == kStStages) {
                 stage = 0;
