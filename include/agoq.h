@@ -279,8 +279,10 @@ agoq_status agoq_reduce_fp8_shards(const void *shards_e4m3, const float *shard_s
  *   otherwise).  dY, x_codes and dW must be 16-byte aligned, x_scales 4-byte
  *   aligned (AGOQ_ERR_ALIGN).  When N is a multiple of 512 and x_scales is
  *   16-byte aligned the scales are staged by TMA with the codes; otherwise the
- *   kernel reads them directly.  Pipeline waits are time-limited: see
- *   agoq_device_status.
+ *   kernel reads them directly.  A 32-byte-aligned dW (as every torch
+ *   allocation is) is written with 32-byte stores, a 16-byte-aligned one with
+ *   16-byte stores (slower; the same values).  Pipeline waits are
+ *   time-limited: see agoq_device_status.
  */
 agoq_status agoq_wgrad_gemm_int4(const void *dY_bf16, const void *x_codes, const float *x_scales,
                                  int M, int N, int K, void *dW_bf16, void *stream);
@@ -303,7 +305,8 @@ agoq_status agoq_wgrad_gemm_int4_f32out(const void *dY_bf16, const void *x_codes
  *   m_i   = fl32(e4m3(c_i) * scale);  t_i = fl32(m_i + g_i);
  *   scale' = fl32(absmax(t) / 448);   c_i' = e4m3_rne_satfinite(fl32(t_i / scale')),
  * i.e. agoq_grad_accum_fp8 with the accumulator as the gradient.
- *   master_e4m3   : in/out, [M][N] E4M3 codes, 16-byte aligned.
+ *   master_e4m3   : in/out, [M][N] E4M3 codes, 16-byte aligned (32-byte aligned:
+ *                   read and written in 32-byte accesses).
  *   master_scales : in/out, [M][N/128] FP32 scales.
  * Shape rules and the other arguments as agoq_wgrad_gemm_int4; the master must
  * not overlap the operands.  The FP32 accumulation order is the tensor cores'
