@@ -76,6 +76,13 @@ __device__ __forceinline__ uint64_t fma_f32x2(uint64_t a, uint64_t b, uint64_t c
     return d;
 }
 
+// max(|a|, |b|, |c|) in one instruction.
+__device__ __forceinline__ float max3_abs(float a, float b, float c) {
+    float d;
+    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
 // ---- E4M3 ------------------------------------------------------------------
 // Two binary32 values to two E4M3 codes, round to nearest even, saturating to
 // +-448; `lo` in bits 0-7.

@@ -180,13 +180,6 @@ __device__ __forceinline__ void add_f16x2_f32(uint32_t h2, float c0, float c1, f
         : "r"(h2), "f"(c0), "f"(c1));
 }
 
-// max(|a|, |b|, |c|).
-__device__ __forceinline__ float max3_abs(float a, float b, float c) {
-    float d;
-    asm("max.abs.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-
 // One lane's share of the reduce of one block: 16 elements (one 16-byte load
 // of codes per shard), their binary32 running sums over the shards in rank
 // order and, with the naive count, the naive FP8 running sums.
