@@ -1079,7 +1079,7 @@ def reduce_shards_torch(W, n, device):
 
 
 PROFILE_CASES = ("accum", "reduce8", "reduce8_nocount", "reduce64", "gemm", "gemm_accum", "silu",
-                 "rmsnorm", "rmsnorm_ws", "fwd_gemm")
+                 "rmsnorm", "rmsnorm_ws", "fwd_gemm", "laaq4_small")
 
 
 def profile_case(name, launches=3):
@@ -1141,6 +1141,12 @@ def profile_case(name, launches=3):
                 agoq.agoq_rmsnorm_backward(c, s, dy, w, T, H, 4, 1e-6)
             else:
                 agoq.agoq_rmsnorm_backward_ws(c, s, dy, w, T, H, 4, 1e-6, ws)
+    elif name == "laaq4_small":
+        # the 2048 x 4096 4-bit round trip (one activation, 21 MB a call)
+        x = synthetic.laaq_activation_torch(seed=0, device=dev)
+        for _ in range(launches):
+            c, s = agoq.agoq_quant_act(x, 4)
+            agoq.agoq_dequant_act(c, s, x.numel(), 4)
     else:
         raise SystemExit("unknown profile case %r (choose from %s)" % (name, ", ".join(PROFILE_CASES)))
     torch.cuda.synchronize()
