@@ -111,6 +111,28 @@ def test_rmsnorm_backward_validation(L):
     assert fn(*args(4, 256, 4), P(D), P(E), P(A), None) == ALIAS         # dw on codes
 
 
+def test_rmsnorm_workspace_bytes_and_ws_validation(L):
+    """The single-read backward's scratch size and its argument checks, which
+    return before any launch."""
+    wb = L.agoq_rmsnorm_backward_workspace_bytes
+    assert wb(4096) == 304 * 4096 * 4 and wb(256) == 304 * 256 * 4
+    assert wb(4352) == 0 and wb(8192) == 0                    # H > 4096: the two-pass path
+    assert wb(100) == -1 and wb(0) == -1 and wb(8448) == -1
+    fn = L.agoq_rmsnorm_backward_ws
+    f = ctypes.c_float
+    D, E, F, W = C + (1 << 20), C + (1 << 22), C + (1 << 23), C + (1 << 26)
+    need = wb(256)
+    args = lambda T, H, bits, eps=1e-6: (P(A), P(B), P(C), P(C + (1 << 19)), T, H, bits, f(eps))
+    assert fn(*args(4, 256, 7), P(D), P(E), P(F), P(W), need, None) == BITS
+    assert fn(*args(4, 384, 4), P(D), P(E), P(F), P(W), need, None) == SHAPE   # H % 256
+    assert fn(*args(4, 256, 4), P(D), P(E), P(F), P(W), need - 4, None) == SHAPE
+    assert fn(*args(4, 256, 4), P(D), P(E), None, P(W), need, None) == NULL    # dw required
+    assert fn(*args(4, 256, 4), P(D), P(E), P(F), None, need, None) == NULL
+    assert fn(*args(4, 256, 4), P(D), P(E), P(F), P(W + 8), need, None) == ALIGN
+    assert fn(*args(4, 256, 4), P(D), P(E), P(F), P(D), need, None) == ALIAS    # scratch on dx
+    assert fn(*args(4, 256, 4), P(D), P(E), P(F), P(A), need, None) == ALIAS    # scratch on codes
+
+
 def test_grad_accum_mid_validation(L):
     FORMAT = 8
     fn = L.agoq_grad_accum_fp8_mid
