@@ -1079,7 +1079,8 @@ def reduce_shards_torch(W, n, device):
 
 
 PROFILE_CASES = ("accum", "reduce8", "reduce8_nocount", "reduce64", "gemm", "gemm_accum", "silu",
-                 "rmsnorm", "rmsnorm_ws", "fwd_gemm", "laaq4_small")
+                 "rmsnorm", "rmsnorm_ws", "fwd_gemm", "laaq4_small", "dequant4_silu",
+                 "dequant8_silu", "quant5_dbca")
 
 
 def profile_case(name, launches=3):
@@ -1141,6 +1142,19 @@ def profile_case(name, launches=3):
                 agoq.agoq_rmsnorm_backward(c, s, dy, w, T, H, 4, 1e-6)
             else:
                 agoq.agoq_rmsnorm_backward_ws(c, s, dy, w, T, H, 4, 1e-6, ws)
+    elif name in ("dequant4_silu", "dequant8_silu"):
+        # the SiLU/gate input of the DBCA-PP step, quantized once, then dequantized
+        bits = 4 if name == "dequant4_silu" else 8
+        x = synthetic.dbca_activations_torch(seed=1, device=dev)[1]
+        c, s = agoq.agoq_quant_act(x, bits)
+        y = torch.empty_like(x)
+        for _ in range(launches):
+            agoq.agoq_dequant_act(c, s, x.numel(), bits, y)
+    elif name == "quant5_dbca":
+        # both DBCA-PP tensors quantized at 5 bits (RMSNorm input, then SiLU input)
+        for x in synthetic.dbca_activations_torch(seed=1, device=dev):
+            for _ in range(launches):
+                agoq.agoq_quant_act(x, 5)
     elif name == "laaq4_small":
         # the 2048 x 4096 4-bit round trip (one activation, 21 MB a call)
         x = synthetic.laaq_activation_torch(seed=0, device=dev)
